@@ -1,0 +1,66 @@
+"""Byte accounting for the decode step's bandwidth metric (host-side only).
+
+The KV size of one token is ``2 * layers * kv_heads * head_dim * elem_bytes``
+(K and V), the formula of "Capítulo 2 — KV cache, jerarquía de memoria,
+continuous batching y PagedAttention", section "Una fórmula útil para estimar
+memoria", and of "KV cache: la memoria de trabajo que sostiene la inferencia
+LLM", section "El precio: cuánto pesa la mochila".  The kernels here serve one
+layer, so a step reads ``layers = 1`` worth of it per cached token.
+
+Algorithmic bytes of one decode call (what the kernel must move at minimum)::
+
+    sum_i L_i * 2 * Hkv * d * e_cache      K and V of every valid token
+  + B * Hq * d * e_q                       q
+  + B * Hq * d * e_q                       out
+  + sum_i ceil(L_i / bs) * 4               block-table entries used
+  + 4 * B                                  seq_lens
+
+and of one cache write of T tokens::
+
+    2 * T * Hkv * d * (e_src + e_cache) + 8 * T
+"""
+from __future__ import annotations
+
+from typing import Iterable
+
+ELEM_BYTES = {"f32": 4, "bf16": 2, "fp8_e4m3": 1}
+
+
+def kv_bytes_per_token(layers: int, kv_heads: int, head_dim: int, elem_bytes: int) -> int:
+    return 2 * layers * kv_heads * head_dim * elem_bytes
+
+
+def block_bytes(block_tokens: int, layers: int, kv_heads: int, head_dim: int,
+                elem_bytes: int) -> int:
+    return block_tokens * kv_bytes_per_token(layers, kv_heads, head_dim, elem_bytes)
+
+
+def blocks_for_tokens(tokens: int, block_size: int) -> int:
+    return -(-int(tokens) // int(block_size))
+
+
+def decode_bytes(seq_lens: Iterable[int], num_q_heads: int, num_kv_heads: int, head_dim: int,
+                 cache_dtype: str, q_dtype: str, block_size: int) -> int:
+    lens = [int(x) for x in seq_lens]
+    e_c, e_q = ELEM_BYTES[cache_dtype], ELEM_BYTES[q_dtype]
+    kv = sum(lens) * kv_bytes_per_token(1, num_kv_heads, head_dim, e_c)
+    qo = 2 * len(lens) * num_q_heads * head_dim * e_q
+    tables = 4 * sum(blocks_for_tokens(L, block_size) for L in lens)
+    return kv + qo + tables + 4 * len(lens)
+
+
+def reshape_bytes(num_tokens: int, num_kv_heads: int, head_dim: int, src_dtype: str,
+                  cache_dtype: str) -> int:
+    per = num_kv_heads * head_dim * (ELEM_BYTES[src_dtype] + ELEM_BYTES[cache_dtype])
+    return 2 * num_tokens * per + 8 * num_tokens
+
+
+def unique_kv_bytes(seq_lens: Iterable[int], shared_prefix_tokens: int, num_kv_heads: int,
+                    head_dim: int, cache_dtype: str) -> int:
+    """KV bytes counting a prefix shared by every sequence once."""
+    lens = [int(x) for x in seq_lens]
+    per = kv_bytes_per_token(1, num_kv_heads, head_dim, ELEM_BYTES[cache_dtype])
+    if not lens:
+        return 0
+    uniq = shared_prefix_tokens + sum(L - shared_prefix_tokens for L in lens)
+    return uniq * per
