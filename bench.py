@@ -1,0 +1,454 @@
+"""Benchmark of one paged-decode step on GB300.
+
+A step is the whole hot path for one decode iteration of one attention layer:
+``kv_reshape_and_cache`` of the step's new K/V tokens (one per sequence), then
+``paged_attention_decode`` over every sequence's paged cache.  The default
+workload is the Llama-3-8B-shaped decode layer: 64 sequences with lengths
+uniform in [128, 2048], 32 query / 8 kv heads, head_dim 128, bf16 cache,
+block_size 16, a shuffled 16384-block pool.
+
+Metric: effective HBM GB/s of the step -- algorithmic bytes (K/V of every
+valid token, q, out, the block-table entries used, seq_lens, plus the cache
+write's bytes) divided by the device time of the step -- with decode tokens/s
+per layer beside it.  L2 is flushed (a 256 MiB write) between timed steps.
+
+``--impl reference`` times the CPU oracle on the same workload instead (a
+bounded sample of sequences per step) and prints the same JSON line.
+
+Multi-GPU (torchrun): every rank runs its own replica of the workload with a
+different seed (the sequences of a decode batch are independent; no
+collective sits on the data path); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+from paged_kv_cache_22_gb300 import metrics  # noqa: E402
+
+METRIC = ("paged decode attention effective HBM GB/s (% of GB300 peak); decode tok/s/layer")
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+# DRAM traffic of one decode launch on the default workload, from an ncu
+# capture, valid only for the kernel sources it was taken on.
+TRAFFIC = {"sources_sha256": None, "bytes_per_launch": None}
+
+WORKLOAD_TEXT = {
+    "llama3_8b": "Llama-3-8B-shaped decode layer: 64 seqs, L~U[128,2048], 32 q / 8 kv heads, "
+                 "head_dim 128, bf16 KV, block 16, 16384-block shuffled pool",
+    "llama70b_128": "Llama-70B-shaped decode layer: 128 seqs, L lognormal(median 800, sigma 1) "
+                    "in [16,8192], 64 q / 8 kv heads, head_dim 128, bf16 KV, block 16",
+    "long_split_kv": "long-context split-KV: 8 seqs x 32768 tokens, 32 q / 8 kv heads, head_dim "
+                     "128, bf16 KV, block 16, 512-token partitions",
+    "prefix_fp8": "prefix sharing + fp8 KV: 256 seqs = 2048 shared prefix + U[1,512] suffix, "
+                  "32 q / 8 kv heads, head_dim 128, fp8-e4m3 KV, bf16 q/out",
+    "tiny_mha": "tiny MHA: 4 seqs {1,17,33,100}, 4 heads, head_dim 64, fp32",
+}
+
+
+def kernel_sources_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_22_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def step_bytes(w: workloads.Workload):
+    lens = w.seq_lens.tolist()
+    dec = metrics.decode_bytes(lens, w.num_q_heads, w.num_kv_heads, w.head_dim, w.cache_dtype,
+                               w.q_dtype, w.block_size)
+    rc = metrics.reshape_bytes(int(w.new_slots.numel()), w.num_kv_heads, w.head_dim, w.src_dtype,
+                               w.cache_dtype)
+    return dec, rc
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed loop runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            target = f"GPU-{uuid}" if not uuid.startswith("GPU-") else uuid
+        except Exception:
+            target = str(device_index)
+        self.target = target
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.target, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args):
+    import paged_kv_cache_22_gb300 as pkv
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pkv.library()
+
+    w = workloads.CONFIGS[args.config](seed=1234 + list(workloads.CONFIGS).index(args.config)
+                                       + 1000 * rank)
+    pt = args.partition_tokens
+    shape = workloads.cache_shape(w)
+    cdt = workloads.cache_torch_dtype(w.cache_dtype)
+    kc = torch.zeros(shape, dtype=cdt, device=dev)
+    vc = torch.zeros(shape, dtype=cdt, device=dev)
+    # history tokens are state carried from earlier steps: written once, untimed
+    if w.hist_slots.numel():
+        pkv.kv_reshape_and_cache(w.hist_k.to(dev), w.hist_v.to(dev), kc, vc, w.hist_slots.to(dev),
+                                 w.kv_scale)
+    q = w.q.to(dev)
+    new_k, new_v, new_slots = w.new_k.to(dev), w.new_v.to(dev), w.new_slots.to(dev)
+    tables, lens = w.block_tables.to(dev), w.seq_lens.to(dev)
+    out = torch.empty_like(q)
+    max_len = w.max_seq_len
+    workspace = pkv.DecodeWorkspace(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        pkv.kv_reshape_and_cache(new_k, new_v, kc, vc, new_slots, w.kv_scale)
+        pkv.paged_attention_decode(out, q, kc, vc, tables, lens, w.scale, w.kv_scale,
+                                   max_seq_len=max_len, partition_tokens=pt, workspace=workspace)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    if pkv.get_device_error():
+        raise RuntimeError("device error during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.fill_(float(i))  # untimed: evicts the previous step's lines from L2
+        ev[i][0].record(stream)
+        pkv.kv_reshape_and_cache(new_k, new_v, kc, vc, new_slots, w.kv_scale)
+        ev[i][1].record(stream)
+        pkv.paged_attention_decode(out, q, kc, vc, tables, lens, w.scale, w.kv_scale,
+                                   max_seq_len=max_len, partition_tokens=pt, workspace=workspace)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    tot_ms = sum(step_ms)
+    if ws > 1:
+        t = torch.tensor([tot_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        tot_ms = float(t.item())
+    if pkv.get_device_error():
+        raise RuntimeError("device error during the timed steps")
+
+    dec_b, rc_b = step_bytes(w)
+    ms_per_step = tot_ms / K
+    value = ws * (dec_b + rc_b) / (ms_per_step * 1e-3) / 1e9
+    dec_avg_ms = sum(dec_ms) / K
+    achieved = dec_b / (dec_avg_ms * 1e-3) / 1e9
+    peak, peak_src = measured_peak()
+
+    # ---- end to end through the public API with host buffers
+    e2e = run_e2e(pkv, w, kc, vc, dev, pt, max(10, min(K, 200)), flush)
+    if ws > 1:
+        t = torch.tensor([e2e["ms_per_step"]], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e["ms_per_step"] = float(t.item())
+    e2e_value = ws * (dec_b + rc_b) / (e2e["ms_per_step"] * 1e-3) / 1e9
+
+    traffic = None
+    if TRAFFIC["sources_sha256"] == kernel_sources_sha() and args.config == "llama3_8b" and pt == 0:
+        traffic = TRAFFIC["bytes_per_launch"]
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.cache_dtype == "bf16" else w.cache_dtype,
+        "data": "synthetic (seeded N(0,1) q/k/v, shuffled block pool)",
+        "config": {
+            "workload": WORKLOAD_TEXT.get(args.config, args.config),
+            "name": args.config,
+            "num_seqs": w.num_seqs, "sum_seq_len": int(w.seq_lens.sum()),
+            "max_seq_len": max_len, "num_q_heads": w.num_q_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+            "block_size": w.block_size, "cache_dtype": w.cache_dtype,
+            "split": "balanced (1 launch)" if pt == 0 else f"fixed {pt}-token partitions + reduce",
+            "l2": "flushed between timed steps (256 MiB write, outside the timed events)",
+            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+        },
+        "decode_tok_s_per_layer": round(ws * w.num_seqs / (ms_per_step * 1e-3), 1),
+        "decode_only": {"ms": round(dec_avg_ms, 6), "gbs": round(achieved, 1),
+                        "frac_of_8TBs": round(achieved / NOMINAL_HBM_GBS, 4),
+                        "bytes": dec_b},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_source": peak_src, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "decode_kernel (balanced split)" if pt == 0 else "decode_kernel (partitions)"},
+        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                "ms_per_step": round(e2e["ms_per_step"], 6)},
+        "gpu_launches": K * (2 if pt == 0 else 3),
+        "clocks": clocks,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e(pkv, w, kc, vc, dev, pt, steps, flush):
+    """Per step: host->device copies of the step's inputs from pinned memory,
+    the two calls, and a device->host read of the output, all timed."""
+    host = {
+        "q": w.q.pin_memory(), "k": w.new_k.pin_memory(), "v": w.new_v.pin_memory(),
+        "slots": w.new_slots.pin_memory(), "tables": w.block_tables.pin_memory(),
+        "lens": w.seq_lens.pin_memory(),
+    }
+    dbuf = {k: torch.empty_like(t, device=dev) for k, t in host.items()}
+    out = torch.empty_like(dbuf["q"])
+    out_host = torch.empty_like(w.q).pin_memory()
+    workspace = pkv.DecodeWorkspace(dev)
+    stream = torch.cuda.current_stream()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def one():
+        for k, t in host.items():
+            dbuf[k].copy_(t, non_blocking=True)
+        pkv.kv_reshape_and_cache(dbuf["k"], dbuf["v"], kc, vc, dbuf["slots"], w.kv_scale)
+        pkv.paged_attention_decode(out, dbuf["q"], kc, vc, dbuf["tables"], dbuf["lens"], w.scale,
+                                   w.kv_scale, max_seq_len=w.max_seq_len, partition_tokens=pt,
+                                   workspace=workspace)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    tot = 0.0
+    for _ in range(steps):
+        flush.fill_(0.5)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        one()
+        b.record(stream)
+        b.synchronize()
+        tot += a.elapsed_time(b)
+    return {"ms_per_step": tot / steps, "h2d": h2d, "d2h": d2h}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_sample(w, max_seqs=None):
+    """(q, caches, tables, lens) numpy inputs for the oracle over the first
+    sequences of the workload, caches filled by the oracle's own cache write."""
+    import oracle
+
+    def np_of(t):
+        t = t.contiguous()
+        if t.dtype == torch.bfloat16:
+            return t.view(torch.int16).numpy().view(np.uint16).copy()
+        return t.numpy().copy()
+
+    B = w.num_seqs if max_seqs is None else min(max_seqs, w.num_seqs)
+    shape = workloads.cache_shape(w)
+    dt = {"f32": np.float32, "bf16": np.uint16, "fp8_e4m3": np.uint8}[w.cache_dtype]
+    kc = np.zeros(shape, dtype=dt)
+    vc = np.zeros(shape, dtype=dt)
+    k, v, slots = w.all_tokens()
+    oracle.reshape_and_cache(np_of(k), np_of(v), kc, vc, slots.numpy().copy(), w.kv_scale)
+    return (np_of(w.q[:B]), kc, vc, w.block_tables[:B].numpy().copy(),
+            w.seq_lens[:B].numpy().copy(), np_of(w.new_k), np_of(w.new_v),
+            w.new_slots.numpy().copy(), B)
+
+
+def cpu_baseline(w, seconds: float):
+    """The oracle, as it stands, timed on this host's cores: repeated full
+    decode steps (cache write of the new tokens + attention) for ~`seconds`."""
+    import oracle
+    q, kc, vc, tables, lens, nk, nv, ns, B = oracle_sample(w)
+    threads = os.cpu_count() or 1
+    dec_b, rc_b = step_bytes(w)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.reshape_and_cache(nk, nv, kc, vc, ns, w.kv_scale)
+        oracle.paged_attention_decode(q, kc, vc, tables, lens, w.scale, w.kv_scale, threads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or reps >= 1000:
+            break
+    return {"value": round(reps * (dec_b + rc_b) / el / 1e9, 3), "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{reps} full decode steps of the same workload ({B} seqs), fp64 C loops, "
+                      f"{el:.1f} s wall"}
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step is a bounded sample
+    (the first few sequences of the workload), scaled to GB/s."""
+    ws, rank, _ = dist_env()
+    if ws > 1 and rank != 0:
+        return
+    import oracle
+    w = workloads.CONFIGS[args.config](seed=1234 + list(workloads.CONFIGS).index(args.config))
+    sample = max(1, min(w.num_seqs, args.ref_seqs))
+    q, kc, vc, tables, lens, nk, nv, ns, B = oracle_sample(w, sample)
+    threads = os.cpu_count() or 1
+    lens_l = lens.tolist()
+    dec_b = metrics.decode_bytes(lens_l, w.num_q_heads, w.num_kv_heads, w.head_dim, w.cache_dtype,
+                                 w.q_dtype, w.block_size)
+    rc_b = metrics.reshape_bytes(B, w.num_kv_heads, w.head_dim, w.src_dtype, w.cache_dtype)
+    nk, nv, ns = nk[:B], nv[:B], ns[:B]
+
+    def step():
+        oracle.reshape_and_cache(nk, nv, kc, vc, ns, w.kv_scale)
+        oracle.paged_attention_decode(q, kc, vc, tables, lens, w.scale, w.kv_scale, threads)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    ms = el * 1e3 / args.steps
+    value = (dec_b + rc_b) / (ms * 1e-3) / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) q/k/v, shuffled block pool)",
+        "config": {"workload": WORKLOAD_TEXT.get(args.config, args.config), "name": args.config,
+                   "sample_seqs": B},
+        "decode_tok_s_per_layer": round(B / (ms * 1e-3), 2),
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"first {B} of {w.num_seqs} sequences per step, fp64 C loops"},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=list(workloads.CONFIGS), default="llama3_8b")
+    ap.add_argument("--partition-tokens", type=int, default=0,
+                    help="0 = balanced split (default); >0 = fixed partitions + reduce")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seqs", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,218 @@
+/*
+ * pkv.h -- C ABI of libpkv.so: paged KV-cache writes and paged decode
+ * attention on one GB300 (sm_103a).
+ *
+ * Every entry point takes plain pointers and sizes.  Device pointers point to
+ * global memory of the current CUDA device; the caller owns every buffer
+ * (the library never allocates or frees device memory).  All calls that
+ * take a stream are asynchronous on that stream and return as soon as the
+ * work is enqueued, except pkv_get_device_error, which synchronises it.
+ *
+ * Layouts (row-major, contiguous):
+ *   q, out           [num_seqs, num_q_heads, head_dim]
+ *   k, v (new)       [num_tokens, num_kv_heads, head_dim]
+ *   k_cache, v_cache [num_blocks, num_kv_heads, block_size, head_dim]
+ *                    one (block, kv head) tile is block_size * head_dim
+ *                    contiguous elements
+ *   block_tables     int32 [num_seqs, max_blocks_per_seq]
+ *   seq_lens         int32 [num_seqs]
+ *   slot_mapping     int64 [num_tokens], slot = block_id * block_size + offset
+ *
+ * Query head qh reads kv head qh / (num_q_heads / num_kv_heads).
+ *
+ * Error behaviour, common to all calls:
+ *   - invalid arguments (null pointers, unsupported sizes or types,
+ *     misaligned buffers) are rejected on the host before anything is
+ *     enqueued: the call returns PKV_ERR_INVALID_ARG or PKV_ERR_UNSUPPORTED;
+ *   - bad data met on the device (a block id outside the pool, a slot outside
+ *     the cache, a sequence longer than its table) is never dereferenced: the
+ *     element is skipped and a bit is set in a per-device error word, read
+ *     and cleared by pkv_get_device_error;
+ *   - a failed kernel launch returns PKV_ERR_CUDA.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* pkv_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,
+  PKV_ERR_UNSUPPORTED = 2,
+  PKV_ERR_CUDA = 3,
+  PKV_ERR_WORKSPACE = 4
+} pkv_status;
+
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2 } pkv_dtype;
+
+/* Device error word bits. */
+#define PKV_DEVERR_BAD_BLOCK_ID 0x1u   /* block table entry outside [0, num_blocks) */
+#define PKV_DEVERR_BAD_SLOT 0x2u       /* slot >= num_blocks * block_size */
+#define PKV_DEVERR_BAD_SEQ_LEN 0x4u    /* seq_len < 0 or beyond the table / hint */
+#define PKV_DEVERR_WAIT_TIMEOUT 0x8u   /* a bounded wait on an async copy gave up */
+
+/* Geometry and element type of one layer's K cache (the V cache is the same).
+ * Supported: head_dim in {64, 128}; block_size in {8, 16, 32}; dtype any of
+ * pkv_dtype. */
+typedef struct {
+  int32_t num_blocks;
+  int32_t block_size;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  pkv_dtype dtype;
+} pkv_cache_desc;
+
+/*
+ * pkv_kv_reshape_and_cache -- write each new token's K and V into its slot.
+ *
+ * "PagedAttention por dentro" (section "La tabla de páginas (block table)"):
+ * a sequence's new token goes to the free position of its last block, or to
+ * position 0 of a freshly appended block.  The host picks the slot; this call
+ * performs the write: for every token t with slot_mapping[t] >= 0 and every
+ * kv head h,
+ *   k_cache[slot / bs][h][slot % bs][:] = convert(k[t][h][:])   (same for v)
+ * convert is a copy (same type), an exact widening (bf16 -> f32), binary32 ->
+ * bf16 round-to-nearest-even, or, for an fp8 cache, e4m3(x / kv_scale) with
+ * the division in binary32, round-to-nearest-even and saturation to +-448.
+ *
+ *   k, v        device, [num_tokens, num_kv_heads, head_dim] of src_dtype
+ *               (PKV_F32 or PKV_BF16), 16-byte aligned
+ *   num_tokens  >= 0 (0 enqueues nothing)
+ *   k_cache, v_cache, cache  destination caches, 16-byte aligned
+ *   slot_mapping device int64 [num_tokens]; negative = skip the token;
+ *               >= num_blocks * block_size sets PKV_DEVERR_BAD_SLOT and skips
+ *   kv_scale    > 0, used only for fp8 caches
+ * Two tokens with the same slot in one call race (the pages' allocator never
+ * hands one slot to two tokens).
+ */
+pkv_status pkv_kv_reshape_and_cache(const void* k, const void* v, pkv_dtype src_dtype,
+                                    int32_t num_tokens, void* k_cache, void* v_cache,
+                                    const pkv_cache_desc* cache, const int64_t* slot_mapping,
+                                    float kv_scale, pkv_stream_t stream);
+
+/*
+ * pkv_decode_workspace_bytes -- device workspace needed by
+ * pkv_paged_attention_decode for this problem on the current device.
+ *
+ * partition_tokens = 0 (balanced split): partial results of the sequences
+ * that are cut between thread blocks, plus one merge counter per
+ * (sequence, kv head); independent of the lengths.  partition_tokens > 0
+ * (fixed partitions): fp32 partials [num_seqs, num_q_heads, P, head_dim] and
+ * [num_seqs, num_q_heads, P] maxima and sums, P = ceil(max_seq_len /
+ * partition_tokens).  Returns 0 for invalid arguments.
+ */
+size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t max_seq_len,
+                                  int32_t partition_tokens);
+
+/*
+ * pkv_paged_attention_decode -- one decode step of attention over paged K/V.
+ *
+ * For every sequence s and query head qh (kv head h = qh / g, g = Hq / Hkv):
+ *   out[s][qh] = softmax_t(scale * q[s][qh] . K_s[t]) . V_s[t],  t < seq_lens[s]
+ * where K_s[t] = k_cache[block_tables[s][t / bs]][h][t % bs] (and V alike):
+ * the decode attention of "Optimización de Inferencia LLM" (section "El
+ * Cuello de Botella de Atención del que Nadie Habla") read through the block
+ * table as in "La despensa por casilleros" (section "El mecanismo: bloques,
+ * block table y el gather del kernel"), with grouped-query sharing as in
+ * "KV cache: la memoria de trabajo" (section "Trucos para que el cuaderno sea
+ * más fino").  seq_lens counts the current token, whose K/V must already be
+ * in the cache.  fp8 caches are read as code * kv_scale.  Accumulation is
+ * binary32; out is rounded once (round-to-nearest-even) to q's type.  A
+ * sequence with seq_len 0 gets a zero row.
+ *
+ *   out, q      device, [num_seqs, num_q_heads, head_dim] of q_dtype:
+ *               PKV_F32 for an f32 cache, PKV_BF16 for bf16 and fp8 caches;
+ *               16-byte aligned
+ *   num_q_heads a multiple of cache->num_kv_heads
+ *   block_tables, max_blocks_per_seq  device int32 table; entries past
+ *               ceil(seq_len / bs) are never read
+ *   seq_lens    device int32 [num_seqs]
+ *   max_seq_len host upper bound of seq_lens (sizes the fixed-partition grid;
+ *               a longer sequence sets PKV_DEVERR_BAD_SEQ_LEN and is clipped)
+ *   partition_tokens  0 = balanced split over all SMs with an in-kernel
+ *               log-sum-exp merge (one launch); > 0 = fixed KV partitions of
+ *               that many tokens (a multiple of block_size), merged by
+ *               pkv_split_kv_reduce inside this call (two launches)
+ *   workspace   device, >= pkv_decode_workspace_bytes(...) bytes, 256-byte
+ *               aligned.  Balanced mode keeps its merge counters at the start
+ *               of the workspace: they must be zero when the call starts, and
+ *               every completed balanced call leaves them at zero again, so a
+ *               workspace zero-filled once can serve any number of balanced
+ *               calls.  A fixed-partition call overwrites that region: re-zero
+ *               the workspace (or use another) before the next balanced call.
+ *               Calls sharing one workspace must not overlap on the GPU.
+ */
+pkv_status pkv_paged_attention_decode(void* out, const void* q, pkv_dtype q_dtype,
+                                      int32_t num_seqs, int32_t num_q_heads, const void* k_cache,
+                                      const void* v_cache, const pkv_cache_desc* cache,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* seq_lens, int32_t max_seq_len, float scale,
+                                      float kv_scale, int32_t partition_tokens, void* workspace,
+                                      size_t workspace_bytes, pkv_stream_t stream);
+
+/*
+ * pkv_split_kv_reduce -- log-sum-exp merge of per-partition partial results.
+ *
+ * The pages do not describe a split of the KV sequence; this is the algebra
+ * of a softmax over disjoint token sets.  For each (s, qh), over the first
+ * n = ceil(seq_lens[s] / partition_tokens) partitions:
+ *   M = max_p m_part[p];  w_p = l_part[p] * exp(m_part[p] - M);
+ *   out = sum_p w_p * o_part[p] / sum_p w_p          (zero row when n = 0)
+ *
+ *   o_part  device fp32 [num_seqs, num_q_heads, max_partitions, head_dim],
+ *           each partition's output already normalised by its own sum
+ *   m_part  device fp32 [num_seqs, num_q_heads, max_partitions]: the largest
+ *           scaled score scale * q . k of the partition (natural-log units)
+ *   l_part  device fp32 [...]: sum over the partition of exp(score - m)
+ *   out     device [num_seqs, num_q_heads, head_dim] of out_dtype (F32/BF16)
+ */
+pkv_status pkv_split_kv_reduce(void* out, pkv_dtype out_dtype, const float* o_part,
+                               const float* m_part, const float* l_part, const int32_t* seq_lens,
+                               int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                               int32_t partition_tokens, int32_t max_partitions,
+                               pkv_stream_t stream);
+
+/*
+ * pkv_gather_kv -- contiguous copy of every sequence's cached tokens (test
+ * and export aid): k_out[cu_seq_lens[s] + t][h][:] =
+ * k_cache[block_tables[s][t / bs]][h][t % bs][:] for t < seq_lens[s], byte
+ * for byte ("La despensa por casilleros", section "El mecanismo: bloques,
+ * block table y el gather del kernel": the blocks read as if contiguous).
+ *
+ *   k_out, v_out  device [sum(seq_lens), num_kv_heads, head_dim] of the
+ *                 cache's type
+ *   cu_seq_lens   device int64 [num_seqs + 1], exclusive prefix of seq_lens
+ *   max_seq_len   host upper bound of seq_lens (sizes the grid)
+ */
+pkv_status pkv_gather_kv(void* k_out, void* v_out, const void* k_cache, const void* v_cache,
+                         const pkv_cache_desc* cache, const int32_t* block_tables,
+                         int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                         const int64_t* cu_seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                         pkv_stream_t stream);
+
+/*
+ * pkv_get_device_error -- synchronise `stream`, then read and clear the
+ * current device's error word (PKV_DEVERR_* bits) into *code_out.
+ */
+pkv_status pkv_get_device_error(uint32_t* code_out, pkv_stream_t stream);
+
+/* Human-readable name of a status; never NULL. */
+const char* pkv_status_string(pkv_status status);
+
+/* Number of SMs of the current device, or 0 on error (the balanced split
+ * sizes its grid from it). */
+int32_t pkv_device_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

@@ -1,0 +1,237 @@
+"""GB300 (sm_103a) paged KV-cache decode: a thin Python binding over libpkv.so.
+
+Every function here only marshals torch tensors into the C ABI declared in
+``include/pkv.h`` (pointers, sizes, the current CUDA stream); all work runs in
+the library's CUDA kernels.  There is no CPU fallback: if ``libpkv.so`` has
+not been built, every call raises.
+
+Entry points (same names as the C ABI, without the ``pkv_`` prefix):
+
+* :func:`kv_reshape_and_cache` -- write new K/V tokens into their slots;
+* :func:`paged_attention_decode` -- one decode step of attention over the
+  paged cache (balanced split with an in-kernel merge, or fixed partitions
+  followed by :func:`split_kv_reduce`);
+* :func:`split_kv_reduce` -- log-sum-exp merge of partition partials;
+* :func:`gather_kv` -- contiguous copy of every sequence's cached tokens;
+* :func:`decode_workspace_bytes`, :func:`get_device_error`.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "PkvError", "CacheDesc", "kv_reshape_and_cache", "paged_attention_decode", "split_kv_reduce",
+    "gather_kv", "decode_workspace_bytes", "get_device_error", "library", "library_path",
+    "DecodeWorkspace", "F32", "BF16", "FP8_E4M3", "DEVERR_BAD_BLOCK_ID", "DEVERR_BAD_SLOT",
+    "DEVERR_BAD_SEQ_LEN", "DEVERR_WAIT_TIMEOUT",
+]
+
+F32, BF16, FP8_E4M3 = 0, 1, 2
+DEVERR_BAD_BLOCK_ID, DEVERR_BAD_SLOT, DEVERR_BAD_SEQ_LEN, DEVERR_WAIT_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "libpkv.so")
+_lib = None
+_lock = threading.Lock()
+
+_STATUS = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED", 3: "PKV_ERR_CUDA",
+           4: "PKV_ERR_WORKSPACE"}
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {_STATUS.get(status, status)}")
+        self.status = status
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("dtype", ctypes.c_int)]
+
+
+def library() -> ctypes.CDLL:
+    """Load libpkv.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(library_path):
+            raise RuntimeError(f"{library_path} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(library_path)
+        vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+        desc = ctypes.POINTER(CacheDesc)
+        sigs = {
+            "pkv_kv_reshape_and_cache": [vp, vp, ctypes.c_int, i32, vp, vp, desc, vp, f32, vp],
+            "pkv_decode_workspace_bytes": [i32, i32, i32, i32, i32, i32],
+            "pkv_paged_attention_decode": [vp, vp, ctypes.c_int, i32, i32, vp, vp, desc, vp, i32, vp,
+                                           i32, f32, f32, i32, vp, sz, vp],
+            "pkv_split_kv_reduce": [vp, ctypes.c_int, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp],
+            "pkv_gather_kv": [vp, vp, vp, vp, desc, vp, i32, vp, vp, i32, i32, vp],
+            "pkv_get_device_error": [ctypes.POINTER(ctypes.c_uint32), vp],
+            "pkv_status_string": [ctypes.c_int],
+            "pkv_device_sm_count": [],
+        }
+        for name, args in sigs.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        lib.pkv_decode_workspace_bytes.restype = sz
+        lib.pkv_status_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+# ------------------------------------------------------------------ marshalling
+_CACHE_DT = {torch.float32: F32, torch.bfloat16: BF16, torch.uint8: FP8_E4M3}
+
+
+def _dt(t: torch.Tensor) -> int:
+    try:
+        return _CACHE_DT[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t.dtype}") from None
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors must live on the CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream: Optional[torch.cuda.Stream]):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _desc(k_cache: torch.Tensor, cache_dtype: Optional[int]) -> CacheDesc:
+    if k_cache.dim() != 4:
+        raise ValueError("caches are [num_blocks, num_kv_heads, block_size, head_dim]")
+    nb, hkv, bs, d = k_cache.shape
+    dt = _dt(k_cache) if cache_dtype is None else cache_dtype
+    return CacheDesc(nb, bs, hkv, d, dt)
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise PkvError(status, what)
+
+
+# ------------------------------------------------------------------ entry points
+def kv_reshape_and_cache(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor,
+                         v_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                         kv_scale: float = 1.0, stream=None) -> None:
+    """Scatter ``k, v [T, Hkv, d]`` into the caches at ``slot_mapping`` (int64).
+
+    A uint8 cache holds fp8-e4m3 codes written as ``e4m3(x / kv_scale)``."""
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    if k.dtype not in (torch.float32, torch.bfloat16) or v.dtype != k.dtype:
+        raise TypeError("k and v must both be float32 or bfloat16")
+    desc = _desc(k_cache, None)
+    _check(library().pkv_kv_reshape_and_cache(
+        _ptr(k), _ptr(v), _dt(k), int(k.shape[0]), _ptr(k_cache), _ptr(v_cache),
+        ctypes.byref(desc), _ptr(slot_mapping), float(kv_scale), _stream(stream)),
+        "kv_reshape_and_cache")
+
+
+def decode_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                           max_seq_len: int, partition_tokens: int = 0) -> int:
+    return int(library().pkv_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                    max_seq_len, partition_tokens))
+
+
+class DecodeWorkspace:
+    """A zero-filled device workspace that grows on demand (torch-allocated)."""
+
+    def __init__(self, device=None):
+        self.device = device
+        self.buf: Optional[torch.Tensor] = None
+
+    def get(self, nbytes: int) -> torch.Tensor:
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=self.device or "cuda")
+        return self.buf
+
+
+_default_ws = {}
+
+
+def paged_attention_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                           v_cache: torch.Tensor, block_tables: torch.Tensor,
+                           seq_lens: torch.Tensor, scale: float, kv_scale: float = 1.0,
+                           max_seq_len: Optional[int] = None, partition_tokens: int = 0,
+                           workspace: Optional[DecodeWorkspace] = None, stream=None) -> torch.Tensor:
+    """One decode step: ``out[s, qh] = softmax(scale * q[s, qh] . K_s^T) . V_s``.
+
+    ``max_seq_len`` is a host upper bound of ``seq_lens`` (the decode never
+    synchronises to read it); by default the table capacity is used."""
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_tables and seq_lens must be int32")
+    B, Hq, d = q.shape
+    desc = _desc(k_cache, None)
+    mbps = int(block_tables.shape[1])
+    if max_seq_len is None:
+        max_seq_len = mbps * desc.block_size
+    nbytes = decode_workspace_bytes(B, Hq, desc.num_kv_heads, d, max_seq_len, partition_tokens)
+    if workspace is None:
+        # one workspace per (device, mode): a fixed-partition call overwrites
+        # the region where the balanced mode keeps its merge counters
+        dev = q.device.index if q.device.index is not None else torch.cuda.current_device()
+        workspace = _default_ws.setdefault((dev, partition_tokens == 0), DecodeWorkspace(q.device))
+    ws = workspace.get(nbytes)
+    qdt = F32 if q.dtype == torch.float32 else BF16
+    _check(library().pkv_paged_attention_decode(
+        _ptr(out), _ptr(q), qdt, B, Hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc),
+        _ptr(block_tables), mbps, _ptr(seq_lens), int(max_seq_len), float(scale), float(kv_scale),
+        int(partition_tokens), _ptr(ws), ws.numel(), _stream(stream)), "paged_attention_decode")
+    return out
+
+
+def split_kv_reduce(out: torch.Tensor, o_part: torch.Tensor, m_part: torch.Tensor,
+                    l_part: torch.Tensor, seq_lens: torch.Tensor, partition_tokens: int,
+                    stream=None) -> torch.Tensor:
+    """Merge ``o_part [B, Hq, P, d]``, ``m_part / l_part [B, Hq, P]`` (fp32)."""
+    B, Hq, P, d = o_part.shape
+    odt = F32 if out.dtype == torch.float32 else BF16
+    _check(library().pkv_split_kv_reduce(
+        _ptr(out), odt, _ptr(o_part), _ptr(m_part), _ptr(l_part), _ptr(seq_lens), B, Hq, d,
+        int(partition_tokens), P, _stream(stream)), "split_kv_reduce")
+    return out
+
+
+def gather_kv(k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+              seq_lens: torch.Tensor, max_seq_len: int, cu_seq_lens: Optional[torch.Tensor] = None,
+              total_tokens: Optional[int] = None, stream=None):
+    """Contiguous ``[sum(seq_lens), Hkv, d]`` copies of K and V."""
+    desc = _desc(k_cache, None)
+    if cu_seq_lens is None:
+        cu_seq_lens = torch.zeros(seq_lens.numel() + 1, dtype=torch.int64, device=seq_lens.device)
+        cu_seq_lens[1:] = torch.cumsum(seq_lens.to(torch.int64), 0)
+    if total_tokens is None:
+        total_tokens = int(cu_seq_lens[-1].item())
+    k_out = torch.empty((total_tokens, desc.num_kv_heads, desc.head_dim), dtype=k_cache.dtype,
+                        device=k_cache.device)
+    v_out = torch.empty_like(k_out)
+    _check(library().pkv_gather_kv(
+        _ptr(k_out), _ptr(v_out), _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc),
+        _ptr(block_tables), int(block_tables.shape[1]), _ptr(seq_lens), _ptr(cu_seq_lens),
+        int(seq_lens.numel()), int(max_seq_len), _stream(stream)), "gather_kv")
+    return k_out, v_out
+
+
+def get_device_error(stream=None) -> int:
+    """Synchronise the stream, then read and clear the device error word."""
+    code = ctypes.c_uint32(0)
+    _check(library().pkv_get_device_error(ctypes.byref(code), _stream(stream)), "get_device_error")
+    return int(code.value)

@@ -1,0 +1,675 @@
+// decode.cuh -- paged decode attention kernels for sm_103a.
+//
+// What is computed (per sequence s, query head qh, kv head h = qh / g):
+//   out[s][qh] = softmax_t(scale * q[s][qh] . K_s[t]) . V_s[t],  t < seq_len[s]
+// with K_s[t] = k_cache[block_tables[s][t / BS]][h][t % BS] -- the decode
+// attention of "Optimización de Inferencia LLM" (section "El Cuello de
+// Botella de Atención del que Nadie Habla"), read block by block through the
+// block table as "La despensa por casilleros" describes (section "El
+// mecanismo: bloques, block table y el gather del kernel") and accumulated
+// with an online softmax, as the kernel pseudo-code of "Optimización de
+// Inferencia LLM" (section "PagedAttention: Conceptos de SO se Encuentran con
+// Memoria GPU") prescribes.
+//
+// Design (GB300):
+//  * Work unit = one (block, kv head) tile of K and one of V, each BS * D
+//    contiguous elements in the [num_blocks, Hkv, BS, D] cache, fetched whole
+//    by one 1-D bulk copy (TMA) into shared memory.  Every tile is read from
+//    HBM exactly once and serves all G query heads of its kv head.
+//  * Each warp owns a private ring of NSW shared-memory stages and its own
+//    mbarriers: it consumes stage k and immediately refills it with its tile
+//    k + NSW.  No warp ever waits for another warp's copies.
+//  * Lane layout inside a tile: C lanes share a token row, each holding
+//    DL = D / C head dimensions for all G heads' queries in registers; R = 32/C
+//    rows run in parallel.  Scores are finished with an xor-shuffle over the C
+//    lanes; the running max is warp-uniform so the accumulator rescale is a
+//    uniform branch.  Dot products and the PV update use packed fp32 FMA.
+//  * Balanced split: the tiles of all (sequence, kv head) segments are laid
+//    end to end and cut into gridDim.x equal ranges, one per CTA, so every SM
+//    streams the same number of bytes whatever the length skew.  A segment cut
+//    between CTAs is merged by the last CTA to finish it (atomic ticket, no
+//    waiting): partial (o, m, l) go through the workspace and are combined by
+//    log-sum-exp.  Fixed-partition mode instead gives each CTA one partition
+//    of one segment and leaves the merge to the reduce kernel.
+#pragma once
+
+#include <math_constants.h>
+
+#include "pkv_device.cuh"
+
+namespace pkv {
+
+struct DecodeArgs {
+  unsigned int* err;  // device error word
+  void* out;
+  const void* q;
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
+  const int32_t* block_tables;
+  int64_t table_stride;  // max_blocks_per_seq
+  const int32_t* seq_lens;
+  int num_seqs;
+  int num_q_heads;
+  int num_kv_heads;
+  int num_blocks;
+  int group;         // g = Hq / Hkv
+  int units_per_kv;  // g / G: query-head chunks per kv head
+  int units;         // num_kv_heads * units_per_kv (segments per sequence)
+  int len_clip;      // longest admissible seq_len
+  float qk_scale;    // scale * log2(e) (* kv_scale for fp8 caches)
+  float out_scale;   // 1 (kv_scale for fp8 caches)
+  // balanced split
+  int* counters;     // [num_seqs * units], zero between calls
+  float* partials;   // [2 * gridDim.x][G * D + 2 * G]
+  // fixed partitions
+  int partition_blocks;
+  int max_partitions;
+  float* o_part;     // [B, Hq, P, D]
+  float* m_part;     // [B, Hq, P]
+  float* l_part;     // [B, Hq, P]
+};
+
+// Compile-time geometry of one kernel instance.
+template <class CT, int D, int BS, int G>
+struct Geo {
+  static constexpr int E = CT::kBytes;
+  static constexpr int TB = BS < 16 ? BS : 16;      // tokens per compute step
+  static constexpr int DL0 = 64 / G;                 // keep G * DL = 64 query registers
+  static constexpr int DLMAX = D * TB / 32;          // at least one token row per lane
+  static constexpr int DL = DL0 < DLMAX ? DL0 : DLMAX;
+  static constexpr int C = D / DL;                   // lanes per token row
+  static constexpr int R = 32 / C;                   // token rows in flight per warp
+  static constexpr int TL = TB / R;                  // tokens per lane per step
+  static constexpr int VB = DL * E >= 16 ? 16 : DL * E;  // bytes per shared-memory vector
+  static constexpr int VE = VB / E;                  // elements per vector
+  static constexpr int NV = DL / VE;                 // vectors per token row per lane
+  static constexpr int PV = VE / 2;                  // fp32 pairs per vector
+  static constexpr int NP = DL / 2;                  // fp32 pairs per lane
+  static constexpr int TILE = BS * D * E;            // bytes of one (block, head) tile
+  static constexpr int STEPS = BS / TB;
+  static constexpr int NSW0 = 16384 / (2 * TILE);
+  static constexpr int NSW = NSW0 < 2 ? 2 : (NSW0 > 8 ? 8 : NSW0);  // stages per warp
+  static_assert(D % DL == 0 && 32 % C == 0 && R <= TB && TB % R == 0, "lane layout");
+  static_assert(DL % VE == 0 && VE % 2 == 0, "vector layout");
+  static_assert(TILE % 16 == 0, "bulk copies move multiples of 16 bytes");
+};
+
+template <class CT, int D, int BS, int G, int W>
+struct Smem {
+  using GE = Geo<CT, D, BS, G>;
+  using QT = typename CT::QType;
+  static constexpr int kStageBytes = 2 * GE::TILE;  // K tile then V tile
+  static constexpr int kMergeFloats = G * D + 2 * G;
+  static constexpr size_t kStages = 0;
+  static constexpr size_t kBars = kStages + (size_t)W * GE::NSW * kStageBytes;
+  static constexpr size_t kQBars = kBars + (size_t)W * GE::NSW * 8;
+  static constexpr size_t kValid = kQBars + 2 * 8;
+  static constexpr size_t kQBuf = (kValid + (size_t)W * GE::NSW * 4 + 127) / 128 * 128;
+  static constexpr size_t kMerge = kQBuf + 2 * (size_t)G * D * sizeof(QT);
+  static constexpr size_t kMisc = kMerge + (size_t)W * kMergeFloats * 4;
+  static constexpr size_t kBytes = kMisc + 64;
+};
+
+// ----------------------------------------------------------------------------
+// Balanced split of T tiles over C CTAs.  With T >= C every CTA gets
+// floor((c+1)T/C) - floor(cT/C) >= 1 tiles; with T < C the first T CTAs get one
+// tile each and the rest none, so a segment's tiles always lie on consecutive
+// non-empty CTAs (the merge counts its pieces as c_last - c_first + 1).
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ int64_t range_start(int64_t c, int64_t T, int64_t C) {
+  return T >= C ? c * T / C : (c < T ? c : T);
+}
+
+// The CTA whose range holds tile u (0 <= u < T).
+__device__ __forceinline__ int cta_of(int64_t u, int64_t T, int64_t C) {
+  return (int)(T >= C ? ((u + 1) * C - 1) / T : u);
+}
+
+// ----------------------------------------------------------------------------
+// Walk over the (sequence, unit) segments that intersect a tile range.  All
+// lanes of a warp hold the same state.
+// ----------------------------------------------------------------------------
+struct Walker {
+  int s, unit, nb;
+  int64_t base;    // linear index of sequence s's first tile
+  int64_t seg_u;   // linear index of segment (s, unit)'s first tile
+  int jb, je;      // piece = blocks [jb, je) of the segment
+  bool done;
+};
+
+template <int BS>
+__device__ __forceinline__ int seq_blocks(const DecodeArgs& a, int s) {
+  int L = __ldg(a.seq_lens + s);
+  if (L < 0 || L > a.len_clip) {
+    raise_error(a.err, PKV_DEVERR_BAD_SEQ_LEN);
+    L = L < 0 ? 0 : a.len_clip;
+  }
+  return (L + BS - 1) / BS;
+}
+
+template <int BS>
+__device__ __forceinline__ int seq_len_clipped(const DecodeArgs& a, int s) {
+  int L = __ldg(a.seq_lens + s);
+  return L < 0 ? 0 : (L > a.len_clip ? a.len_clip : L);
+}
+
+template <int BS>
+__device__ __forceinline__ void walker_settle(Walker& wk, const DecodeArgs& a, int64_t u1) {
+  // Move forward to the first segment with blocks left before u1.
+  while (!wk.done) {
+    if (wk.nb > 0) {
+      wk.seg_u = wk.base + (int64_t)wk.unit * wk.nb;
+      if (wk.seg_u >= u1) { wk.done = true; break; }
+      int64_t left = u1 - wk.seg_u;
+      wk.je = (int64_t)wk.nb < left ? wk.nb : (int)left;
+      if (wk.jb < wk.je) break;
+    }
+    wk.jb = 0;
+    if (wk.nb > 0 && ++wk.unit < a.units) continue;
+    wk.base += (int64_t)wk.nb * a.units;
+    wk.unit = 0;
+    if (++wk.s >= a.num_seqs) { wk.done = true; break; }
+    wk.nb = seq_blocks<BS>(a, wk.s);
+  }
+}
+
+template <int BS>
+__device__ __forceinline__ void walker_next_piece(Walker& wk, const DecodeArgs& a, int64_t u1) {
+  wk.jb = wk.je;  // past the current piece
+  if (wk.je < wk.nb) { wk.done = true; return; }  // the range ended inside this segment
+  wk.jb = 0;
+  if (++wk.unit >= a.units) {
+    wk.unit = 0;
+    wk.base += (int64_t)wk.nb * a.units;
+    if (++wk.s >= a.num_seqs) { wk.done = true; return; }
+    wk.nb = seq_blocks<BS>(a, wk.s);
+  }
+  walker_settle<BS>(wk, a, u1);
+}
+
+// Issue cursor: the warp's own tiles, in the order it will consume them.
+struct Cursor {
+  Walker wk;
+  int j;  // current block index within the piece
+};
+
+template <int BS>
+__device__ __forceinline__ void cursor_fix(Cursor& cu, const DecodeArgs& a, int64_t u1, int w) {
+  while (!cu.wk.done && cu.j >= cu.wk.je) {
+    walker_next_piece<BS>(cu.wk, a, u1);
+    cu.j = cu.wk.jb + w;
+  }
+}
+
+// ----------------------------------------------------------------------------
+// The kernel.
+// ----------------------------------------------------------------------------
+template <class CT, int D, int BS, int G, int W, bool BALANCED>
+__global__ void __launch_bounds__(W * 32, 2)
+    decode_kernel(const DecodeArgs a) {
+  using GE = Geo<CT, D, BS, G>;
+  using SM = Smem<CT, D, BS, G, W>;
+  using QT = typename CT::QType;
+  constexpr int NSW = GE::NSW, C = GE::C, R = GE::R, TL = GE::TL, NV = GE::NV, PV = GE::PV,
+                NP = GE::NP, VE = GE::VE, VB = GE::VB, TB = GE::TB, TILE = GE::TILE;
+  constexpr int E = GE::E;
+
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* stages = smem + SM::kStages;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::kBars);
+  uint64_t* qbars = reinterpret_cast<uint64_t*>(smem + SM::kQBars);
+  int* stage_ok = reinterpret_cast<int*>(smem + SM::kValid);
+  QT* qbuf = reinterpret_cast<QT*>(smem + SM::kQBuf);
+  float* merge = reinterpret_cast<float*>(smem + SM::kMerge);
+  int64_t* misc = reinterpret_cast<int64_t*>(smem + SM::kMisc);
+
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int r = lane / C, c = lane % C;
+
+  // ---------------------------------------------------------------- range
+  int64_t u0, u1, T = 0;
+  Walker wk0;
+  if constexpr (BALANCED) {
+    if (w == 0) {
+      // total tiles, then the sequence that holds this CTA's first tile
+      int64_t mine = 0;
+      for (int s = lane; s < a.num_seqs; s += 32) mine += seq_blocks<BS>(a, s);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, off);
+      T = mine * a.units;
+      u0 = range_start(blockIdx.x, T, gridDim.x);
+      u1 = range_start(blockIdx.x + 1, T, gridDim.x);
+      int s0 = a.num_seqs;
+      int64_t p0 = 0;
+      if (u0 < u1) {
+        int64_t run = 0;  // tiles before this chunk
+        for (int s = 0; s < a.num_seqs; s += 32) {
+          int64_t n = (s + lane < a.num_seqs) ? (int64_t)seq_blocks<BS>(a, s + lane) * a.units : 0;
+          int64_t incl = n;
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) {
+            int64_t t = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += t;
+          }
+          int64_t excl = incl - n;
+          unsigned hit = __ballot_sync(0xffffffffu, n > 0 && run + excl <= u0 && u0 < run + incl);
+          if (hit) {
+            int src = __ffs(hit) - 1;
+            s0 = s + src;
+            p0 = __shfl_sync(0xffffffffu, run + excl, src);
+            break;
+          }
+          run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+      }
+      if (lane == 0) {
+        misc[0] = u0;
+        misc[1] = u1;
+        misc[2] = T;
+        misc[3] = s0;
+        misc[4] = p0;
+      }
+    }
+    // mbarriers
+    if (tid < W * NSW) mbar_init(&bars[tid], 1);
+    if (tid < 2) mbar_init(&qbars[tid], 1);
+    fence_mbar_init();
+    __syncthreads();
+    u0 = misc[0];
+    u1 = misc[1];
+    T = misc[2];
+    // sequences of length 0 get a zero row (spread over the CTAs)
+    for (int s = blockIdx.x; s < a.num_seqs; s += gridDim.x) {
+      if (seq_len_clipped<BS>(a, s) == 0) {
+        QT* o = reinterpret_cast<QT*>(a.out) + (size_t)s * a.num_q_heads * D;
+        for (int i = tid; i < a.num_q_heads * D; i += W * 32) o[i] = from_f32<QT>(0.f);
+      }
+    }
+    if (u0 >= u1 || misc[3] >= a.num_seqs) return;
+    wk0.s = (int)misc[3];
+    wk0.base = misc[4];
+    wk0.nb = seq_blocks<BS>(a, wk0.s);
+    int64_t off = u0 - wk0.base;
+    wk0.unit = (int)(off / wk0.nb);
+    wk0.jb = (int)(off % wk0.nb);
+    wk0.done = false;
+    walker_settle<BS>(wk0, a, u1);
+  } else {
+    // fixed partition blockIdx.y of segment blockIdx.x
+    const int s = blockIdx.x / a.units, unit = blockIdx.x % a.units;
+    const int nb = seq_blocks<BS>(a, s);
+    const int jb = blockIdx.y * a.partition_blocks;
+    const int je = min(nb, jb + a.partition_blocks);
+    if (jb >= je) return;
+    if (tid < W * NSW) mbar_init(&bars[tid], 1);
+    if (tid < 2) mbar_init(&qbars[tid], 1);
+    fence_mbar_init();
+    __syncthreads();
+    wk0.s = s;
+    wk0.unit = unit;
+    wk0.nb = nb;
+    wk0.base = 0;
+    wk0.seg_u = (int64_t)unit * nb;
+    wk0.jb = jb;
+    wk0.je = je;
+    wk0.done = false;
+    u0 = wk0.seg_u + jb;
+    u1 = wk0.seg_u + je;
+  }
+
+  const size_t head_stride = (size_t)BS * D * E;               // one kv head's tile
+  const size_t block_stride = (size_t)a.num_kv_heads * head_stride;
+
+  // ---------------------------------------------------------------- issue side
+  Cursor cur;
+  cur.wk = wk0;
+  cur.j = wk0.jb + w;
+  cursor_fix<BS>(cur, a, u1, w);
+  int issued = 0;
+
+  auto issue_next = [&]() {
+    if (cur.wk.done) return;
+    const int st = issued % NSW;
+    if (lane == 0) {
+      const int32_t id = __ldg(a.block_tables + (size_t)cur.wk.s * a.table_stride + cur.j);
+      const int kvh = cur.wk.unit / a.units_per_kv;
+      uint8_t* dst = stages + ((size_t)w * NSW + st) * SM::kStageBytes;
+      uint64_t* bar = &bars[w * NSW + st];
+      if (id >= 0 && id < a.num_blocks) {
+        stage_ok[w * NSW + st] = 1;
+        const size_t off = (size_t)id * block_stride + (size_t)kvh * head_stride;
+        mbar_arrive_expect_tx(bar, 2 * TILE);
+        bulk_g2s(dst, a.k_cache + off, TILE, bar);
+        bulk_g2s(dst + TILE, a.v_cache + off, TILE, bar);
+      } else {
+        raise_error(a.err, PKV_DEVERR_BAD_BLOCK_ID);
+        stage_ok[w * NSW + st] = 0;
+        mbar_arrive(bar);
+      }
+    }
+    ++issued;
+    cur.j += W;
+    cursor_fix<BS>(cur, a, u1, w);
+  };
+
+  // q of the piece a walker stands on: bulk copy into qbuf[slot]
+  auto issue_q = [&](const Walker& pw, int slot) {
+    const int kvh = pw.unit / a.units_per_kv, chunk = pw.unit % a.units_per_kv;
+    const int qh0 = kvh * a.group + chunk * G;
+    const QT* src = reinterpret_cast<const QT*>(a.q) + ((size_t)pw.s * a.num_q_heads + qh0) * D;
+    mbar_arrive_expect_tx(&qbars[slot], G * D * sizeof(QT));
+    bulk_g2s(qbuf + (size_t)slot * G * D, src, G * D * sizeof(QT), &qbars[slot]);
+  };
+
+  // prologue: q of the first piece, then the first NSW tiles of every warp
+  Walker qlook = wk0;  // warp 0's look-ahead for q prefetch
+  if (w == 0 && lane == 0) issue_q(wk0, 0);
+#pragma unroll 1
+  for (int i = 0; i < NSW; ++i) issue_next();
+
+  // ---------------------------------------------------------------- consume side
+  Walker wk = wk0;
+  int consumed = 0, waited = 0, piece = 0;
+  bool alive = true;
+  float2 q2[G][NP];
+  float2 acc[G][NP];
+  float m_run[G], l_run[G];
+
+#pragma unroll 1
+  while (!wk.done) {
+    const int qslot = piece & 1;
+    if (w == 0) {  // prefetch the next piece's q while this one runs
+      Walker nx = qlook;
+      walker_next_piece<BS>(nx, a, u1);
+      if (!nx.done && lane == 0) {
+        fence_proxy_async_smem();
+        issue_q(nx, qslot ^ 1);
+      }
+      qlook = nx;
+    }
+    if (!mbar_wait_bounded(&qbars[qslot], (piece >> 1) & 1, a.err)) alive = false;
+    {
+      const QT* qs = qbuf + (size_t)qslot * G * D;
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int j = 0; j < NV; ++j)
+#pragma unroll
+          for (int pv = 0; pv < PV; ++pv) {
+            const int dim = (c + C * j) * VE + 2 * pv;
+            q2[h][j * PV + pv] = make_float2(to_f32(qs[h * D + dim]) * a.qk_scale,
+                                             to_f32(qs[h * D + dim + 1]) * a.qk_scale);
+          }
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      m_run[h] = -CUDART_INF_F;
+      l_run[h] = 0.f;
+#pragma unroll
+      for (int i = 0; i < NP; ++i) acc[h][i] = make_float2(0.f, 0.f);
+    }
+    const int L = seq_len_clipped<BS>(a, wk.s);
+
+#pragma unroll 1
+    for (int j = wk.jb + w; j < wk.je; j += W) {
+      const int st = consumed % NSW;
+      const uint8_t* ktile = stages + ((size_t)w * NSW + st) * SM::kStageBytes;
+      const uint8_t* vtile = ktile + TILE;
+      bool ok = false;
+      if (alive && consumed < issued) {
+        ok = mbar_wait_bounded(&bars[w * NSW + st], (consumed / NSW) & 1, a.err);
+        waited = consumed + 1;
+        if (!ok) alive = false;
+      }
+      ok = ok && stage_ok[w * NSW + st];
+      const int valid = ok ? min(BS, L - j * BS) : 0;
+
+#pragma unroll 1
+      for (int step = 0; step < GE::STEPS; ++step) {
+        const int tbase = step * TB;
+        float sc[TL][G];
+        // ---- scores: this lane's DL dimensions of TL token rows
+#pragma unroll
+        for (int k = 0; k < TL; ++k) {
+          const int t = tbase + r + R * k;
+          float2 part[G];
+#pragma unroll
+          for (int h = 0; h < G; ++h) part[h] = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int jv = 0; jv < NV; ++jv) {
+            float2 kv[PV];
+            VecLoad<CT, VB>::run(ktile + (size_t)t * D * E + (c + C * jv) * VB, kv);
+#pragma unroll
+            for (int pv = 0; pv < PV; ++pv)
+#pragma unroll
+              for (int h = 0; h < G; ++h) part[h] = ffma2(q2[h][jv * PV + pv], kv[pv], part[h]);
+          }
+#pragma unroll
+          for (int h = 0; h < G; ++h) sc[k][h] = part[h].x + part[h].y;
+        }
+#pragma unroll
+        for (int off = 1; off < C; off <<= 1)
+#pragma unroll
+          for (int k = 0; k < TL; ++k)
+#pragma unroll
+            for (int h = 0; h < G; ++h) sc[k][h] += __shfl_xor_sync(0xffffffffu, sc[k][h], off);
+        // ---- mask tokens past the sequence end (and whole bad tiles)
+#pragma unroll
+        for (int k = 0; k < TL; ++k)
+          if (tbase + r + R * k >= valid)
+#pragma unroll
+            for (int h = 0; h < G; ++h) sc[k][h] = -CUDART_INF_F;
+        // ---- online softmax, max shared by the whole warp
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          float mx = sc[0][h];
+#pragma unroll
+          for (int k = 1; k < TL; ++k) mx = fmaxf(mx, sc[k][h]);
+#pragma unroll
+          for (int off = C; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+          const float m_new = fmaxf(m_run[h], mx);
+          const float m_use = (m_new == -CUDART_INF_F) ? 0.f : m_new;
+          float lsum = 0.f;
+#pragma unroll
+          for (int k = 0; k < TL; ++k) {
+            sc[k][h] = fast_exp2(sc[k][h] - m_use);
+            lsum += sc[k][h];
+          }
+          if (m_new > m_run[h]) {  // warp-uniform
+            const float alpha = fast_exp2(m_run[h] - m_use);
+            l_run[h] *= alpha;
+            const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+            for (int i = 0; i < NP; ++i) acc[h][i] = __fmul2_rn(acc[h][i], a2);
+            m_run[h] = m_new;
+          }
+          l_run[h] += lsum;
+        }
+        // ---- P . V
+#pragma unroll
+        for (int k = 0; k < TL; ++k) {
+          const int t = tbase + r + R * k;
+          if (t < valid) {
+#pragma unroll
+            for (int jv = 0; jv < NV; ++jv) {
+              float2 vv[PV];
+              VecLoad<CT, VB>::run(vtile + (size_t)t * D * E + (c + C * jv) * VB, vv);
+#pragma unroll
+              for (int h = 0; h < G; ++h) {
+                const float2 p2 = make_float2(sc[k][h], sc[k][h]);
+#pragma unroll
+                for (int pv = 0; pv < PV; ++pv) acc[h][jv * PV + pv] = ffma2(p2, vv[pv], acc[h][jv * PV + pv]);
+              }
+            }
+          }
+        }
+      }
+      ++consumed;
+      __syncwarp();
+      if (lane == 0) fence_proxy_async_smem();
+      __syncwarp();
+      if (alive) issue_next();
+    }
+
+    // ------------------------------------------------------------ merge warps
+    // sum over the R token rows (lanes that share c), then park in shared memory
+#pragma unroll
+    for (int off = C; off < 32; off <<= 1) {
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], off);
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+          acc[h][i].x += __shfl_xor_sync(0xffffffffu, acc[h][i].x, off);
+          acc[h][i].y += __shfl_xor_sync(0xffffffffu, acc[h][i].y, off);
+        }
+      }
+    }
+    float* mw = merge + (size_t)w * SM::kMergeFloats;
+    if (r == 0) {
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int jv = 0; jv < NV; ++jv)
+#pragma unroll
+          for (int pv = 0; pv < PV; ++pv) {
+            const int dim = (c + C * jv) * VE + 2 * pv;
+            mw[h * D + dim] = acc[h][jv * PV + pv].x;
+            mw[h * D + dim + 1] = acc[h][jv * PV + pv].y;
+          }
+      if (c == 0)
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          mw[G * D + h] = m_run[h];
+          mw[G * D + G + h] = l_run[h];
+        }
+    }
+    __syncthreads();
+
+    const int kvh = wk.unit / a.units_per_kv, chunk = wk.unit % a.units_per_kv;
+    const int qh0 = kvh * a.group + chunk * G;
+    const int64_t piece_start = wk.seg_u + wk.jb;
+    const bool whole = (wk.jb == 0 && wk.je == wk.nb);
+    bool final_here = BALANCED && whole;
+    int64_t seg_id = (int64_t)wk.s * a.units + wk.unit;
+
+    // combine the W warps: (num, den, M) per (head, dim)
+    constexpr int kItems = G * D;
+    constexpr int kPer = (kItems + W * 32 - 1) / (W * 32);
+    float res_o[kPer], res_m[kPer], res_l[kPer];
+#pragma unroll
+    for (int it = 0; it < kPer; ++it) {
+      const int idx = tid + it * W * 32;
+      res_o[it] = 0.f;
+      res_m[it] = -CUDART_INF_F;
+      res_l[it] = 0.f;
+      if (idx < kItems) {
+        const int h = idx / D;
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int ww = 0; ww < W; ++ww) M = fmaxf(M, merge[ww * SM::kMergeFloats + G * D + h]);
+        const float Mu = (M == -CUDART_INF_F) ? 0.f : M;
+        float num = 0.f, den = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < W; ++ww) {
+          const float* mm = merge + ww * SM::kMergeFloats;
+          const float f = fast_exp2(mm[G * D + h] - Mu);
+          num += f * mm[idx];
+          den += f * mm[G * D + G + h];
+        }
+        res_o[it] = den > 0.f ? num / den : 0.f;
+        res_m[it] = M;
+        res_l[it] = den;
+      }
+    }
+
+    if (final_here) {
+      QT* o = reinterpret_cast<QT*>(a.out) + ((size_t)wk.s * a.num_q_heads + qh0) * D;
+#pragma unroll
+      for (int it = 0; it < kPer; ++it) {
+        const int idx = tid + it * W * 32;
+        if (idx < kItems) o[idx] = from_f32<QT>(res_o[it] * a.out_scale);
+      }
+    } else if constexpr (!BALANCED) {
+      // fixed partition: natural-log maxima for the reduce kernel
+      const int p = blockIdx.y;
+#pragma unroll
+      for (int it = 0; it < kPer; ++it) {
+        const int idx = tid + it * W * 32;
+        if (idx < kItems) {
+          const int h = idx / D, dd = idx % D;
+          const size_t row = ((size_t)wk.s * a.num_q_heads + qh0 + h) * a.max_partitions + p;
+          a.o_part[row * D + dd] = res_o[it] * a.out_scale;
+          if (dd == 0) {
+            a.m_part[row] = res_m[it] * 0.69314718055994531f;
+            a.l_part[row] = res_l[it];
+          }
+        }
+      }
+    } else {
+      // balanced split, segment cut between CTAs: publish, take a ticket
+      const int64_t C_ = gridDim.x;
+      const int cta = blockIdx.x;
+      const int slot = (piece_start == u0) ? 2 * cta : 2 * cta + 1;
+      float* pslot = a.partials + (size_t)slot * SM::kMergeFloats;
+#pragma unroll
+      for (int it = 0; it < kPer; ++it) {
+        const int idx = tid + it * W * 32;
+        if (idx < kItems) {
+          pslot[idx] = res_o[it];
+          if (idx % D == 0) {
+            pslot[G * D + idx / D] = res_m[it];
+            pslot[G * D + G + idx / D] = res_l[it];
+          }
+        }
+      }
+      __threadfence();
+      __syncthreads();
+      const int c_first = cta_of(wk.seg_u, T, C_), c_last = cta_of(wk.seg_u + wk.nb - 1, T, C_);
+      if (tid == 0) {
+        const int ticket = atomicAdd(a.counters + seg_id, 1);
+        const bool last = (ticket == c_last - c_first);
+        if (last) a.counters[seg_id] = 0;  // ready for the next call
+        misc[5] = last ? 1 : 0;
+        __threadfence();
+      }
+      __syncthreads();
+      if (misc[5]) {
+        QT* o = reinterpret_cast<QT*>(a.out) + ((size_t)wk.s * a.num_q_heads + qh0) * D;
+#pragma unroll
+        for (int it = 0; it < kPer; ++it) {
+          const int idx = tid + it * W * 32;
+          if (idx < kItems) {
+            const int h = idx / D;
+            float M = -CUDART_INF_F;
+            for (int cc = c_first; cc <= c_last; ++cc) {
+              const int64_t u0c = range_start(cc, T, C_);
+              const int sl = (cc == c_first && wk.seg_u != u0c) ? 2 * cc + 1 : 2 * cc;
+              M = fmaxf(M, ld_cg(a.partials + (size_t)sl * SM::kMergeFloats + G * D + h));
+            }
+            const float Mu = (M == -CUDART_INF_F) ? 0.f : M;
+            float num = 0.f, den = 0.f;
+            for (int cc = c_first; cc <= c_last; ++cc) {
+              const int64_t u0c = range_start(cc, T, C_);
+              const int sl = (cc == c_first && wk.seg_u != u0c) ? 2 * cc + 1 : 2 * cc;
+              const float* ps = a.partials + (size_t)sl * SM::kMergeFloats;
+              const float f = ld_cg(ps + G * D + G + h) * fast_exp2(ld_cg(ps + G * D + h) - Mu);
+              num += f * ld_cg(ps + idx);
+              den += f;
+            }
+            o[idx] = from_f32<QT>(den > 0.f ? num / den * a.out_scale : 0.f);
+          }
+        }
+      }
+    }
+    __syncthreads();  // merge area free again
+    ++piece;
+    walker_next_piece<BS>(wk, a, u1);
+  }
+
+  // Leave no copy in flight: wait (bounded) for every stage this warp filled
+  // but did not wait for (only possible after a timeout).
+  for (int k = waited; k < issued; ++k) mbar_wait_bounded(&bars[w * NSW + k % NSW], (k / NSW) & 1, a.err);
+}
+
+}  // namespace pkv

@@ -1,0 +1,47 @@
+// decode_launch.cuh -- registry of the compiled decode kernel instances.
+#pragma once
+
+#include "decode.cuh"
+
+namespace pkv {
+
+constexpr int kDecodeWarps = 4;  // consumer warps per CTA
+
+struct DecodeKernel {
+  const void* fn = nullptr;  // __global__ entry
+  int threads = 0;
+  size_t smem = 0;           // dynamic shared memory bytes
+  int heads_per_unit = 0;    // G
+};
+
+template <class CT, int D, int BS, int G, bool BAL>
+DecodeKernel decode_kernel_info() {
+  DecodeKernel k;
+  k.fn = reinterpret_cast<const void*>(&decode_kernel<CT, D, BS, G, kDecodeWarps, BAL>);
+  k.threads = kDecodeWarps * 32;
+  k.smem = Smem<CT, D, BS, G, kDecodeWarps>::kBytes;
+  k.heads_per_unit = G;
+  return k;
+}
+
+// Fill `out` with the instance for (D, BS, G, balanced); false if not built.
+#define PKV_DECLARE_FINDER(NAME) \
+  bool NAME(int head_dim, int block_size, int heads, bool balanced, DecodeKernel* out);
+
+PKV_DECLARE_FINDER(find_decode_f32)
+PKV_DECLARE_FINDER(find_decode_bf16)
+PKV_DECLARE_FINDER(find_decode_fp8)
+
+// Shared body of the finders: the compiled (D, BS) set is passed as a list.
+template <class CT, int D, int BS>
+bool find_for(int heads, bool balanced, DecodeKernel* out) {
+  switch (heads) {
+    case 1: *out = balanced ? decode_kernel_info<CT, D, BS, 1, true>() : decode_kernel_info<CT, D, BS, 1, false>(); return true;
+    case 2: *out = balanced ? decode_kernel_info<CT, D, BS, 2, true>() : decode_kernel_info<CT, D, BS, 2, false>(); return true;
+    case 4: *out = balanced ? decode_kernel_info<CT, D, BS, 4, true>() : decode_kernel_info<CT, D, BS, 4, false>(); return true;
+    case 8: *out = balanced ? decode_kernel_info<CT, D, BS, 8, true>() : decode_kernel_info<CT, D, BS, 8, false>(); return true;
+    default: return false;
+  }
+}
+
+}  // namespace pkv

@@ -1,0 +1,188 @@
+// kernels.cu -- the cache write, the block-table gather and the split-KV
+// reduce.  All three are short, bandwidth-bound element loops.
+#include <math_constants.h>
+
+#include "kernels.h"
+#include "pkv_device.cuh"
+
+namespace pkv {
+
+// ----------------------------------------------------------------------------
+// reshape_and_cache: "PagedAttention por dentro" (section "La tabla de páginas
+// (block table)") -- the new token of a sequence goes to the free position of
+// its last block.  One thread writes 8 consecutive elements of one (token,
+// kv head) row of K or V into slot_mapping[token].
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void load8(const float* s, float (&x)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(s);
+  const float4 b = *reinterpret_cast<const float4*>(s + 4);
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16* s, float (&x)[8]) {
+  const uint4 v = *reinterpret_cast<const uint4*>(s);
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = bf16x2_to_f2(w[i]);
+    x[2 * i] = f.x;
+    x[2 * i + 1] = f.y;
+  }
+}
+
+template <class Src>
+__device__ __forceinline__ void store8(const Src* s, uint8_t* d, pkv_dtype dt, float kv_scale) {
+  if (dt == PKV_BF16 && sizeof(Src) == 2) {  // bit copy
+    *reinterpret_cast<uint4*>(d) = *reinterpret_cast<const uint4*>(s);
+    return;
+  }
+  float x[8];
+  load8(s, x);
+  if (dt == PKV_F32) {
+    *reinterpret_cast<float4*>(d) = make_float4(x[0], x[1], x[2], x[3]);
+    *reinterpret_cast<float4*>(d + 16) = make_float4(x[4], x[5], x[6], x[7]);
+  } else if (dt == PKV_BF16) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(d) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else {  // fp8 e4m3: x / kv_scale in binary32, round to nearest even, saturate
+    uint32_t w[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = make_float2(__fdiv_rn(x[2 * i], kv_scale), __fdiv_rn(x[2 * i + 1], kv_scale));
+      const uint32_t two = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+      w[i / 2] |= (two & 0xFFFFu) << (16 * (i % 2));
+    }
+    *reinterpret_cast<uint2*>(d) = make_uint2(w[0], w[1]);
+  }
+}
+
+template <class Src>
+__global__ void reshape_and_cache_kernel(ReshapeArgs a) {
+  const int chunks = a.head_dim / 8;
+  const int64_t per_token = (int64_t)a.num_kv_heads * chunks * 2;
+  const int64_t total = (int64_t)a.num_tokens * per_token;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / per_token);
+    int rem = (int)(i % per_token);
+    const int kv = rem / (a.num_kv_heads * chunks);
+    rem %= a.num_kv_heads * chunks;
+    const int h = rem / chunks, ch = rem % chunks;
+    const int64_t slot = a.slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= (int64_t)a.num_blocks * a.block_size) {
+      raise_error(a.err, PKV_DEVERR_BAD_SLOT);
+      continue;
+    }
+    const int64_t blk = slot / a.block_size, off = slot % a.block_size;
+    const Src* src = reinterpret_cast<const Src*>(kv ? a.v : a.k) +
+                     ((int64_t)t * a.num_kv_heads + h) * a.head_dim + ch * 8;
+    const int64_t elem = ((blk * a.num_kv_heads + h) * a.block_size + off) * a.head_dim + ch * 8;
+    uint8_t* dst = reinterpret_cast<uint8_t*>(kv ? a.v_cache : a.k_cache) + elem * a.cache_bytes;
+    store8<Src>(src, dst, a.cache_dtype, a.kv_scale);
+  }
+}
+
+cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, int src_is_bf16, cudaStream_t stream) {
+  const int64_t total = (int64_t)a.num_tokens * a.num_kv_heads * (a.head_dim / 8) * 2;
+  if (total == 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t blocks64 = (total + threads - 1) / threads;
+  const int blocks = (int)(blocks64 < 65535 * 8 ? blocks64 : 65535 * 8);
+  if (src_is_bf16)
+    reshape_and_cache_kernel<__nv_bfloat16><<<blocks, threads, 0, stream>>>(a);
+  else
+    reshape_and_cache_kernel<float><<<blocks, threads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------
+// gather: "La despensa por casilleros" (section "El mecanismo: bloques, block
+// table y el gather del kernel") -- walk a sequence's physical blocks in
+// logical order and read them as if contiguous.  One thread moves 16 bytes.
+// ----------------------------------------------------------------------------
+__global__ void gather_kv_kernel(GatherArgs a) {
+  const int s = blockIdx.y;
+  const int L = a.seq_lens[s];
+  const int row16 = a.head_dim * a.cache_bytes / 16;  // 16-byte units per (token, head)
+  const int64_t per_token = (int64_t)a.num_kv_heads * row16;
+  const int64_t total = (int64_t)(L < 0 ? 0 : L) * per_token;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int p = (int)(i / per_token);
+    const int rem = (int)(i % per_token);
+    const int h = rem / row16, u = rem % row16;
+    const int j = p / a.block_size, off = p % a.block_size;
+    if (j >= a.max_blocks_per_seq) {
+      raise_error(a.err, PKV_DEVERR_BAD_SEQ_LEN);
+      continue;
+    }
+    const int32_t blk = a.block_tables[(int64_t)s * a.max_blocks_per_seq + j];
+    if (blk < 0 || blk >= a.num_blocks) {
+      raise_error(a.err, PKV_DEVERR_BAD_BLOCK_ID);
+      continue;
+    }
+    const int64_t src = (((int64_t)blk * a.num_kv_heads + h) * a.block_size + off) * row16 + u;
+    const int64_t dst = ((a.cu_seq_lens[s] + p) * a.num_kv_heads + h) * row16 + u;
+    reinterpret_cast<uint4*>(a.k_out)[dst] = reinterpret_cast<const uint4*>(a.k_cache)[src];
+    reinterpret_cast<uint4*>(a.v_out)[dst] = reinterpret_cast<const uint4*>(a.v_cache)[src];
+  }
+}
+
+cudaError_t launch_gather_kv(const GatherArgs& a, int max_seq_len, cudaStream_t stream) {
+  if (a.num_seqs == 0 || max_seq_len <= 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t per_seq = (int64_t)max_seq_len * a.num_kv_heads * (a.head_dim * a.cache_bytes / 16);
+  int64_t bx = (per_seq + threads - 1) / threads;
+  if (bx > 4096) bx = 4096;
+  dim3 grid((unsigned)bx, (unsigned)a.num_seqs);
+  gather_kv_kernel<<<grid, threads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------
+// split-KV reduce: log-sum-exp merge of per-partition partials.  One CTA per
+// (sequence, query head), one thread per head dimension.
+// ----------------------------------------------------------------------------
+template <class OT>
+__global__ void split_kv_reduce_kernel(ReduceArgs a) {
+  const int row = blockIdx.x;  // s * Hq + qh
+  const int s = row / a.num_q_heads;
+  const int d = threadIdx.x;
+  const int L = a.seq_lens[s];
+  const int np = L <= 0 ? 0 : (L + a.partition_tokens - 1) / a.partition_tokens;
+  OT* out = reinterpret_cast<OT*>(a.out) + (int64_t)row * a.head_dim;
+  if (np > a.max_partitions) {
+    if (d == 0) raise_error(a.err, PKV_DEVERR_BAD_SEQ_LEN);
+  }
+  const int n = np < a.max_partitions ? np : a.max_partitions;
+  const float* m = a.m_part + (int64_t)row * a.max_partitions;
+  const float* l = a.l_part + (int64_t)row * a.max_partitions;
+  const float* o = a.o_part + (int64_t)row * a.max_partitions * a.head_dim;
+  float M = -CUDART_INF_F;
+  for (int p = 0; p < n; ++p) M = fmaxf(M, m[p]);
+  float num = 0.f, den = 0.f;
+  for (int p = 0; p < n; ++p) {
+    const float wgt = l[p] * expf(m[p] - M);
+    den += wgt;
+    num += wgt * o[(int64_t)p * a.head_dim + d];
+  }
+  if (d < a.head_dim) out[d] = from_f32<OT>(den > 0.f ? num / den : 0.f);
+}
+
+cudaError_t launch_split_kv_reduce(const ReduceArgs& a, int out_is_bf16, cudaStream_t stream) {
+  if (a.num_seqs == 0) return cudaSuccess;
+  const unsigned rows = (unsigned)a.num_seqs * a.num_q_heads;
+  if (out_is_bf16)
+    split_kv_reduce_kernel<__nv_bfloat16><<<rows, a.head_dim, 0, stream>>>(a);
+  else
+    split_kv_reduce_kernel<float><<<rows, a.head_dim, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,366 @@
+// pkv_api.cu -- host side of libpkv.so: argument validation, workspace
+// layout and kernel dispatch for the entry points declared in pkv.h.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "../../include/pkv.h"
+#include "decode_launch.cuh"
+#include "kernels.h"
+
+namespace pkv {
+
+// One error word per device (a __device__ variable exists once per device
+// that loads the module).
+__device__ unsigned int g_device_error_word;
+
+namespace {
+
+constexpr int kMaxCtasPerSm = 4;  // upper bound of the balanced grid, per SM
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_bytes(pkv_dtype d) {
+  switch (d) {
+    case PKV_F32: return 4;
+    case PKV_BF16: return 2;
+    case PKV_FP8_E4M3: return 1;
+  }
+  return 0;
+}
+
+std::mutex g_mu;
+std::map<int, unsigned int*> g_err_addr;                 // device -> error word
+std::map<int, int> g_sm_count;                           // device -> SMs
+std::map<std::pair<const void*, int>, int> g_occupancy;  // (kernel, device) -> CTAs/SM
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return dev;
+}
+
+unsigned int* error_word(int dev) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_err_addr.find(dev);
+  if (it != g_err_addr.end()) return it->second;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_device_error_word) != cudaSuccess) return nullptr;
+  g_err_addr[dev] = static_cast<unsigned int*>(p);
+  return static_cast<unsigned int*>(p);
+}
+
+int sm_count(int dev) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_sm_count.find(dev);
+  if (it != g_sm_count.end()) return it->second;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  g_sm_count[dev] = n;
+  return n;
+}
+
+// Opt the kernel into its dynamic shared memory and report CTAs per SM.
+int prepare_kernel(const DecodeKernel& k, int dev) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto key = std::make_pair(k.fn, dev);
+  auto it = g_occupancy.find(key);
+  if (it != g_occupancy.end()) return it->second;
+  if (cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)k.smem) != cudaSuccess)
+    return 0;
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k.fn, k.threads, k.smem) != cudaSuccess) return 0;
+  g_occupancy[key] = occ;
+  return occ;
+}
+
+// Query heads served per kernel unit: the largest of 8, 4, 2, 1 dividing g.
+int heads_per_unit(int g) {
+  for (int G : {8, 4, 2, 1})
+    if (g % G == 0) return G;
+  return 1;
+}
+
+bool find_decode(pkv_dtype dt, int D, int BS, int G, bool balanced, DecodeKernel* k) {
+  switch (dt) {
+    case PKV_F32: return find_decode_f32(D, BS, G, balanced, k);
+    case PKV_BF16: return find_decode_bf16(D, BS, G, balanced, k);
+    case PKV_FP8_E4M3: return find_decode_fp8(D, BS, G, balanced, k);
+  }
+  return false;
+}
+
+bool valid_cache_desc(const pkv_cache_desc* c) {
+  if (!c) return false;
+  if (c->num_blocks <= 0 || c->num_kv_heads <= 0) return false;
+  if (c->head_dim != 64 && c->head_dim != 128) return false;
+  if (c->block_size != 8 && c->block_size != 16 && c->block_size != 32) return false;
+  return elem_bytes(c->dtype) != 0;
+}
+
+pkv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
+
+size_t balanced_workspace(int B, int units, int G, int D, int grid_max) {
+  return align_up((size_t)B * units * sizeof(int)) + (size_t)2 * grid_max * (G * D + 2 * G) * sizeof(float);
+}
+
+size_t partition_workspace(int B, int Hq, int D, int P) {
+  const size_t rows = (size_t)B * Hq * P;
+  return align_up(rows * D * sizeof(float)) + 2 * align_up(rows * sizeof(float));
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char* pkv_status_string(pkv_status s) {
+  switch (s) {
+    case PKV_OK: return "PKV_OK";
+    case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG";
+    case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+    case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+    case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE";
+  }
+  return "PKV_ERR_UNKNOWN";
+}
+
+int32_t pkv_device_sm_count(void) {
+  const int dev = current_device();
+  return dev < 0 ? 0 : sm_count(dev);
+}
+
+pkv_status pkv_kv_reshape_and_cache(const void* k, const void* v, pkv_dtype src_dtype, int32_t num_tokens,
+                                    void* k_cache, void* v_cache, const pkv_cache_desc* cache,
+                                    const int64_t* slot_mapping, float kv_scale, pkv_stream_t stream) {
+  if (num_tokens < 0 || !valid_cache_desc(cache)) return PKV_ERR_INVALID_ARG;
+  if (src_dtype != PKV_F32 && src_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_INVALID_ARG;
+  if (cache->dtype == PKV_FP8_E4M3 && !(kv_scale > 0.f && std::isfinite(kv_scale))) return PKV_ERR_INVALID_ARG;
+  const int dev = current_device();
+  unsigned int* err = dev < 0 ? nullptr : error_word(dev);
+  if (!err) return PKV_ERR_CUDA;
+  ReshapeArgs a;
+  a.err = err;
+  a.k = k;
+  a.v = v;
+  a.num_tokens = num_tokens;
+  a.num_kv_heads = cache->num_kv_heads;
+  a.head_dim = cache->head_dim;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.num_blocks = cache->num_blocks;
+  a.block_size = cache->block_size;
+  a.cache_dtype = cache->dtype;
+  a.cache_bytes = elem_bytes(cache->dtype);
+  a.slot_mapping = slot_mapping;
+  a.kv_scale = kv_scale;
+  return from_cuda(launch_reshape_and_cache(a, src_dtype == PKV_BF16, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t max_seq_len, int32_t partition_tokens) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return 0;
+  if (head_dim != 64 && head_dim != 128) return 0;
+  if (max_seq_len < 0 || partition_tokens < 0) return 0;
+  const int g = num_q_heads / num_kv_heads;
+  const int G = heads_per_unit(g);
+  const int units = num_kv_heads * (g / G);
+  if (partition_tokens == 0) {
+    const int dev = current_device();
+    const int sms = dev < 0 ? 0 : sm_count(dev);
+    if (sms <= 0) return 0;
+    return balanced_workspace(num_seqs, units, G, head_dim, sms * kMaxCtasPerSm);
+  }
+  const int P = max_seq_len == 0 ? 1 : (max_seq_len + partition_tokens - 1) / partition_tokens;
+  return partition_workspace(num_seqs, num_q_heads, head_dim, P);
+}
+
+pkv_status pkv_split_kv_reduce(void* out, pkv_dtype out_dtype, const float* o_part, const float* m_part,
+                               const float* l_part, const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                               int32_t head_dim, int32_t partition_tokens, int32_t max_partitions,
+                               pkv_stream_t stream) {
+  if (num_seqs < 0 || num_q_heads <= 0 || partition_tokens <= 0 || max_partitions <= 0) return PKV_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (out_dtype != PKV_F32 && out_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PKV_OK;
+  if (!out || !o_part || !m_part || !l_part || !seq_lens) return PKV_ERR_INVALID_ARG;
+  const int dev = current_device();
+  unsigned int* err = dev < 0 ? nullptr : error_word(dev);
+  if (!err) return PKV_ERR_CUDA;
+  ReduceArgs a;
+  a.err = err;
+  a.out = out;
+  a.o_part = o_part;
+  a.m_part = m_part;
+  a.l_part = l_part;
+  a.seq_lens = seq_lens;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.head_dim = head_dim;
+  a.partition_tokens = partition_tokens;
+  a.max_partitions = max_partitions;
+  return from_cuda(launch_split_kv_reduce(a, out_dtype == PKV_BF16, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_paged_attention_decode(void* out, const void* q, pkv_dtype q_dtype, int32_t num_seqs,
+                                      int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                                      const pkv_cache_desc* cache, const int32_t* block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t max_seq_len,
+                                      float scale, float kv_scale, int32_t partition_tokens, void* workspace,
+                                      size_t workspace_bytes, pkv_stream_t stream) {
+  if (num_seqs < 0 || !valid_cache_desc(cache)) return PKV_ERR_INVALID_ARG;
+  if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return PKV_ERR_INVALID_ARG;
+  if (max_blocks_per_seq <= 0 || max_seq_len < 0 || partition_tokens < 0) return PKV_ERR_INVALID_ARG;
+  if (partition_tokens % cache->block_size) return PKV_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (cache->dtype == PKV_FP8_E4M3 && !(kv_scale > 0.f && std::isfinite(kv_scale))) return PKV_ERR_INVALID_ARG;
+  const pkv_dtype want_q = cache->dtype == PKV_F32 ? PKV_F32 : PKV_BF16;
+  if (q_dtype != want_q) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_INVALID_ARG;
+
+  const int D = cache->head_dim, BS = cache->block_size;
+  const int g = num_q_heads / cache->num_kv_heads;
+  const int G = heads_per_unit(g);
+  const bool balanced = partition_tokens == 0;
+  DecodeKernel k;
+  if (!find_decode(cache->dtype, D, BS, G, balanced, &k)) return PKV_ERR_UNSUPPORTED;
+
+  const int dev = current_device();
+  if (dev < 0) return PKV_ERR_CUDA;
+  unsigned int* err = error_word(dev);
+  const int sms = sm_count(dev);
+  const int occ = prepare_kernel(k, dev);
+  if (!err || sms <= 0 || occ <= 0) return PKV_ERR_CUDA;
+
+  DecodeArgs a{};
+  a.err = err;
+  a.out = out;
+  a.q = q;
+  a.k_cache = static_cast<const uint8_t*>(k_cache);
+  a.v_cache = static_cast<const uint8_t*>(v_cache);
+  a.block_tables = block_tables;
+  a.table_stride = max_blocks_per_seq;
+  a.seq_lens = seq_lens;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = cache->num_kv_heads;
+  a.num_blocks = cache->num_blocks;
+  a.group = g;
+  a.units_per_kv = g / G;
+  a.units = cache->num_kv_heads * a.units_per_kv;
+  const int64_t table_tokens = (int64_t)max_blocks_per_seq * BS;
+  a.len_clip = (int)(table_tokens < max_seq_len ? table_tokens : max_seq_len);
+  const bool fp8 = cache->dtype == PKV_FP8_E4M3;
+  a.qk_scale = scale * 1.4426950408889634f * (fp8 ? kv_scale : 1.f);
+  a.out_scale = fp8 ? kv_scale : 1.f;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  void* args[] = {&a};
+  if (balanced) {
+    const int grid_max = sms * kMaxCtasPerSm;
+    const size_t need = balanced_workspace(num_seqs, a.units, G, D, grid_max);
+    if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return PKV_ERR_INVALID_ARG;
+    a.counters = static_cast<int*>(workspace);
+    a.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                          align_up((size_t)num_seqs * a.units * sizeof(int)));
+    int64_t grid = (int64_t)sms * (occ < kMaxCtasPerSm ? occ : kMaxCtasPerSm);
+    // never more CTAs than tiles (upper bound from the host hint)
+    const int64_t tiles_hint = (int64_t)num_seqs * a.units * ((a.len_clip + BS - 1) / BS);
+    if (tiles_hint < grid) grid = tiles_hint > 0 ? tiles_hint : 1;
+    return from_cuda(cudaLaunchKernel(k.fn, dim3((unsigned)grid), dim3(k.threads), args, k.smem, st));
+  }
+  // fixed partitions, then the log-sum-exp reduce
+  const int P = max_seq_len == 0 ? 1 : (max_seq_len + partition_tokens - 1) / partition_tokens;
+  if (P > 65535) return PKV_ERR_UNSUPPORTED;
+  const size_t need = partition_workspace(num_seqs, num_q_heads, D, P);
+  if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return PKV_ERR_INVALID_ARG;
+  const size_t rows = (size_t)num_seqs * num_q_heads * P;
+  char* ws = static_cast<char*>(workspace);
+  a.o_part = reinterpret_cast<float*>(ws);
+  a.m_part = reinterpret_cast<float*>(ws + align_up(rows * D * sizeof(float)));
+  a.l_part = reinterpret_cast<float*>(ws + align_up(rows * D * sizeof(float)) + align_up(rows * sizeof(float)));
+  a.partition_blocks = partition_tokens / BS;
+  a.max_partitions = P;
+  const int64_t segs = (int64_t)num_seqs * a.units;
+  if (segs > 0x7FFFFFFF) return PKV_ERR_UNSUPPORTED;
+  cudaError_t e = cudaLaunchKernel(k.fn, dim3((unsigned)segs, (unsigned)P), dim3(k.threads), args, k.smem, st);
+  if (e != cudaSuccess) return PKV_ERR_CUDA;
+  ReduceArgs r;
+  r.err = err;
+  r.out = out;
+  r.o_part = a.o_part;
+  r.m_part = a.m_part;
+  r.l_part = a.l_part;
+  r.seq_lens = seq_lens;
+  r.num_seqs = num_seqs;
+  r.num_q_heads = num_q_heads;
+  r.head_dim = D;
+  r.partition_tokens = partition_tokens;
+  r.max_partitions = P;
+  return from_cuda(launch_split_kv_reduce(r, q_dtype == PKV_BF16, st));
+}
+
+pkv_status pkv_gather_kv(void* k_out, void* v_out, const void* k_cache, const void* v_cache,
+                         const pkv_cache_desc* cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                         const int32_t* seq_lens, const int64_t* cu_seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                         pkv_stream_t stream) {
+  if (num_seqs < 0 || max_seq_len < 0 || max_blocks_per_seq <= 0 || !valid_cache_desc(cache))
+    return PKV_ERR_INVALID_ARG;
+  if (num_seqs == 0 || max_seq_len == 0) return PKV_OK;
+  if (!k_out || !v_out || !k_cache || !v_cache || !block_tables || !seq_lens || !cu_seq_lens)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned16(k_out) || !aligned16(v_out) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_INVALID_ARG;
+  const int dev = current_device();
+  unsigned int* err = dev < 0 ? nullptr : error_word(dev);
+  if (!err) return PKV_ERR_CUDA;
+  GatherArgs a;
+  a.err = err;
+  a.k_out = k_out;
+  a.v_out = v_out;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.num_blocks = cache->num_blocks;
+  a.block_size = cache->block_size;
+  a.num_kv_heads = cache->num_kv_heads;
+  a.head_dim = cache->head_dim;
+  a.cache_bytes = elem_bytes(cache->dtype);
+  a.block_tables = block_tables;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.seq_lens = seq_lens;
+  a.cu_seq_lens = cu_seq_lens;
+  a.num_seqs = num_seqs;
+  return from_cuda(launch_gather_kv(a, max_seq_len, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_get_device_error(uint32_t* code_out, pkv_stream_t stream) {
+  if (!code_out) return PKV_ERR_INVALID_ARG;
+  const int dev = current_device();
+  unsigned int* err = dev < 0 ? nullptr : error_word(dev);
+  if (!err) return PKV_ERR_CUDA;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return PKV_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpy(&v, err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return PKV_ERR_CUDA;
+  if (cudaMemset(err, 0, sizeof v) != cudaSuccess) return PKV_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return PKV_ERR_CUDA;
+  *code_out = v;
+  return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,98 @@
+"""The C ABI without a GPU: the library loads, exports every entry point
+that include/pkv.h declares, and rejects invalid arguments on the host before
+touching the device."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_22_gb300 import build
+    build.build()
+    import paged_kv_cache_22_gb300 as pkv
+    return pkv.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("pkv_kv_reshape_and_cache", "pkv_paged_attention_decode", "pkv_split_kv_reduce",
+                     "pkv_gather_kv", "pkv_decode_workspace_bytes", "pkv_get_device_error"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in pkv.h but not exported"
+
+
+def test_status_strings(lib):
+    assert lib.pkv_status_string(0) == b"PKV_OK"
+    assert lib.pkv_status_string(4) == b"PKV_ERR_WORKSPACE"
+    assert lib.pkv_status_string(99) == b"PKV_ERR_UNKNOWN"
+
+
+def _desc(nb=8, bs=16, hkv=2, d=128, dt=1):
+    import paged_kv_cache_22_gb300 as pkv
+    return pkv.CacheDesc(nb, bs, hkv, d, dt)
+
+
+def test_host_validation_rejects_before_launch(lib):
+    INVALID, UNSUPPORTED = 1, 2
+    p = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+    d = _desc()
+    # head_dim 96 is outside the supported set
+    bad = _desc(d=96)
+    assert lib.pkv_paged_attention_decode(p, p, 1, 4, 8, p, p, ctypes.byref(bad), p, 4, p, 64,
+                                          1.0, 1.0, 0, p, 1 << 20, None) == INVALID
+    # Hq not a multiple of Hkv
+    assert lib.pkv_paged_attention_decode(p, p, 1, 4, 3, p, p, ctypes.byref(d), p, 4, p, 64,
+                                          1.0, 1.0, 0, p, 1 << 20, None) == INVALID
+    # partition not a multiple of the block size
+    assert lib.pkv_paged_attention_decode(p, p, 1, 4, 8, p, p, ctypes.byref(d), p, 4, p, 64,
+                                          1.0, 1.0, 24, p, 1 << 20, None) == INVALID
+    # q type must match the cache (bf16 cache -> bf16 q)
+    assert lib.pkv_paged_attention_decode(p, p, 0, 4, 8, p, p, ctypes.byref(d), p, 4, p, 64,
+                                          1.0, 1.0, 0, p, 1 << 20, None) == UNSUPPORTED
+    # null cache descriptor, negative counts
+    assert lib.pkv_paged_attention_decode(p, p, 1, 4, 8, p, p, None, p, 4, p, 64, 1.0, 1.0, 0, p,
+                                          1 << 20, None) == INVALID
+    assert lib.pkv_kv_reshape_and_cache(p, p, 1, -1, p, p, ctypes.byref(d), p, 1.0, None) == INVALID
+    # fp8 needs a positive scale
+    f8 = _desc(dt=2)
+    assert lib.pkv_kv_reshape_and_cache(p, p, 1, 4, p, p, ctypes.byref(f8), p, 0.0, None) == INVALID
+    # misaligned buffers
+    odd = ctypes.c_void_p(0x1004)
+    assert lib.pkv_kv_reshape_and_cache(odd, p, 1, 4, p, p, ctypes.byref(d), p, 1.0, None) == INVALID
+    # empty work is a no-op
+    assert lib.pkv_paged_attention_decode(None, None, 1, 0, 8, None, None, ctypes.byref(d), None, 4,
+                                          None, 0, 1.0, 1.0, 0, None, 0, None) == 0
+    assert lib.pkv_kv_reshape_and_cache(None, None, 1, 0, None, None, ctypes.byref(d), None, 1.0,
+                                        None) == 0
+    assert lib.pkv_split_kv_reduce(p, 1, p, p, p, p, 2, 8, 96, 64, 4, None) == UNSUPPORTED
+
+
+def test_partition_workspace_size_formula(lib):
+    # fp32 partials [B, Hq, P, d] + m and l [B, Hq, P], each region 256-byte aligned
+    B, Hq, Hkv, d, L, pt = 8, 32, 8, 128, 32768, 512
+    P = L // pt
+    rows = B * Hq * P
+
+    def up(x):
+        return (x + 255) // 256 * 256
+    want = up(rows * d * 4) + 2 * up(rows * 4)
+    assert lib.pkv_decode_workspace_bytes(B, Hq, Hkv, d, L, pt) == want
+    assert lib.pkv_decode_workspace_bytes(B, Hq, 3, d, L, pt) == 0  # invalid GQA split
