@@ -101,10 +101,12 @@ pkv_status pkv_kv_reshape_and_cache(const void* k, const void* v, pkv_dtype src_
  * pkv_decode_workspace_bytes -- device workspace needed by
  * pkv_paged_attention_decode for this problem on the current device.
  *
- * partition_tokens = 0 (balanced split): partial results of the sequences
- * that are cut between thread blocks, plus one merge counter per
- * (sequence, kv head); independent of the lengths.  partition_tokens > 0
- * (fixed partitions): fp32 partials [num_seqs, num_q_heads, P, head_dim] and
+ * Layout, both modes: a counter region of max(1 MiB, num_seqs * units * 4
+ * bytes rounded up to 256) holding one merge counter per (sequence, kv-head
+ * unit), then the mode's partials.  partition_tokens = 0 (balanced split):
+ * the partial results of segments cut between thread blocks, two slots per
+ * thread block; independent of the lengths.  partition_tokens > 0 (fixed
+ * partitions): fp32 partials [num_seqs, num_q_heads, P, head_dim] and
  * [num_seqs, num_q_heads, P] maxima and sums, P = ceil(max_seq_len /
  * partition_tokens).  Returns 0 for invalid arguments.
  */
@@ -142,13 +144,13 @@ size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
  *               that many tokens (a multiple of block_size), merged by
  *               pkv_split_kv_reduce inside this call (two launches)
  *   workspace   device, >= pkv_decode_workspace_bytes(...) bytes, 256-byte
- *               aligned.  Balanced mode keeps its merge counters at the start
- *               of the workspace: they must be zero when the call starts, and
- *               every completed balanced call leaves them at zero again, so a
- *               workspace zero-filled once can serve any number of balanced
- *               calls.  A fixed-partition call overwrites that region: re-zero
- *               the workspace (or use another) before the next balanced call.
- *               Calls sharing one workspace must not overlap on the GPU.
+ *               aligned.  The merge counters at its start must be zero when a
+ *               balanced call starts; every completed call leaves them zero
+ *               and no call writes partials into the counter region, so a
+ *               workspace zero-filled once serves any sequence of calls of
+ *               either mode while num_seqs * units stays <= 262144 (a larger
+ *               batch grows the region: zero it again then).  Calls sharing
+ *               one workspace must not overlap on the GPU.
  */
 pkv_status pkv_paged_attention_decode(void* out, const void* q, pkv_dtype q_dtype,
                                       int32_t num_seqs, int32_t num_q_heads, const void* k_cache,

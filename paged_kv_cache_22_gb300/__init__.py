@@ -152,14 +152,24 @@ def decode_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, h
 
 
 class DecodeWorkspace:
-    """A zero-filled device workspace that grows on demand (torch-allocated)."""
+    """A device workspace (torch-allocated) that grows on demand.
+
+    It is zero-filled when (re)allocated; the library keeps its merge counters
+    zero between calls.  A batch whose counter region outgrows every earlier
+    one gets a fresh zeroed buffer, since the larger region may cover bytes
+    that held partials."""
+
+    COUNTER_REGION_MIN = 1 << 20
 
     def __init__(self, device=None):
         self.device = device
         self.buf: Optional[torch.Tensor] = None
+        self.counter_bytes = self.COUNTER_REGION_MIN
 
-    def get(self, nbytes: int) -> torch.Tensor:
-        if self.buf is None or self.buf.numel() < nbytes:
+    def get(self, nbytes: int, counter_bytes: int = 0) -> torch.Tensor:
+        grow = self.buf is None or self.buf.numel() < nbytes or counter_bytes > self.counter_bytes
+        if grow:
+            self.counter_bytes = max(self.counter_bytes, counter_bytes)
             self.buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=self.device or "cuda")
         return self.buf
 
@@ -185,11 +195,12 @@ def paged_attention_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Te
         max_seq_len = mbps * desc.block_size
     nbytes = decode_workspace_bytes(B, Hq, desc.num_kv_heads, d, max_seq_len, partition_tokens)
     if workspace is None:
-        # one workspace per (device, mode): a fixed-partition call overwrites
-        # the region where the balanced mode keeps its merge counters
         dev = q.device.index if q.device.index is not None else torch.cuda.current_device()
-        workspace = _default_ws.setdefault((dev, partition_tokens == 0), DecodeWorkspace(q.device))
-    ws = workspace.get(nbytes)
+        workspace = _default_ws.setdefault(dev, DecodeWorkspace(q.device))
+    g = Hq // desc.num_kv_heads
+    heads = next(G for G in (8, 4, 2, 1) if g % G == 0)
+    units = desc.num_kv_heads * (g // heads)
+    ws = workspace.get(nbytes, (B * units * 4 + 255) // 256 * 256)
     qdt = F32 if q.dtype == torch.float32 else BF16
     _check(library().pkv_paged_attention_decode(
         _ptr(out), _ptr(q), qdt, B, Hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc),

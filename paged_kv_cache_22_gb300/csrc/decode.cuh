@@ -87,6 +87,20 @@ struct Geo {
   static constexpr int NP = DL / 2;                  // fp32 pairs per lane
   static constexpr int TILE = BS * D * E;            // bytes of one (block, head) tile
   static constexpr int STEPS = BS / TB;
+  // score reduction: N0 partial scores per lane, halved NT times over the C lanes
+  static constexpr int N0 = TL * G;
+  static constexpr int LC = C == 1 ? 0 : C == 2 ? 1 : C == 4 ? 2 : C == 8 ? 3 : C == 16 ? 4 : 5;
+  static constexpr int LN = N0 == 1 ? 0 : N0 == 2 ? 1 : N0 == 4 ? 2 : N0 == 8 ? 3 : N0 == 16 ? 4 : N0 == 32 ? 5 : N0 == 64 ? 6 : 7;
+  static constexpr int NT = LC < LN ? LC : LN;
+  static constexpr int NF = N0 >> NT;                   // scores owned per lane
+  static constexpr int DUP = NT < LC ? (C >> NT) : 1;   // lanes holding the same score
+  // P.V: each lane owns DV consecutive dims; SL dim slices, TG token groups
+  static constexpr int DV = 4;
+  static constexpr int SL = D / DV;
+  static constexpr int TG = 32 / SL;
+  static constexpr int PPL = (TB / 2) / TG;            // token pairs per lane per step
+  static_assert(SL <= 32 && 32 % SL == 0 && (TB / 2) % TG == 0 && PPL >= 1, "P.V layout");
+  static_assert(C >= G && NF <= TL, "each lane owns scores of one head");
   static constexpr int NSW0 = 16384 / (2 * TILE);
   static constexpr int NSW = NSW0 < 2 ? 2 : (NSW0 > 8 ? 8 : NSW0);  // stages per warp
   static_assert(D % DL == 0 && 32 % C == 0 && R <= TB && TB % R == 0, "lane layout");
@@ -107,6 +121,7 @@ struct Smem {
   static constexpr size_t kQBuf = (kValid + (size_t)W * GE::NSW * 4 + 127) / 128 * 128;
   static constexpr size_t kMerge = kQBuf + 2 * (size_t)G * D * sizeof(QT);
   static constexpr size_t kMisc = kMerge + (size_t)W * kMergeFloats * 4;
+  static_assert(G * GE::TB <= G * D, "probabilities fit in the warp's merge slot");
   static constexpr size_t kBytes = kMisc + 64;
 };
 
@@ -205,7 +220,7 @@ __device__ __forceinline__ void cursor_fix(Cursor& cu, const DecodeArgs& a, int6
 // The kernel.
 // ----------------------------------------------------------------------------
 template <class CT, int D, int BS, int G, int W, bool BALANCED>
-__global__ void __launch_bounds__(W * 32, 2)
+__global__ void __launch_bounds__(W * 32, (G >= 8 ? 2 : 3))
     decode_kernel(const DecodeArgs a) {
   using GE = Geo<CT, D, BS, G>;
   using SM = Smem<CT, D, BS, G, W>;
@@ -371,9 +386,16 @@ __global__ void __launch_bounds__(W * 32, 2)
   Walker wk = wk0;
   int consumed = 0, waited = 0, piece = 0;
   bool alive = true;
-  float2 q2[G][NP];
-  float2 acc[G][NP];
-  float m_run[G], l_run[G];
+  float2 q2[G][NP];          // this lane's query dims, pre-scaled by scale*log2(e)
+  float2 acc[G][GE::DV];     // P.V accumulators: this lane's DV dims, even/odd token halves
+  float m_run[G];            // running max per head (log2 units), warp-uniform
+  float m_own, l_own;        // the owned head's running max and this lane's share of its sum
+  // per-warp probabilities [G][TB]: they live in the warp's own merge slot,
+  // which is dead while the warp walks its tiles (it is written only after
+  // the warp's last tile of a piece and read before the piece's last barrier)
+  float* ps = merge + (size_t)w * SM::kMergeFloats;
+  const int h_own = c / (C / G);          // head of the scores this lane owns after the reduction
+  const bool l_counts = (c % GE::DUP) == 0;  // one copy of each duplicated score counts
 
 #pragma unroll 1
   while (!wk.done) {
@@ -404,10 +426,11 @@ __global__ void __launch_bounds__(W * 32, 2)
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       m_run[h] = -CUDART_INF_F;
-      l_run[h] = 0.f;
 #pragma unroll
-      for (int i = 0; i < NP; ++i) acc[h][i] = make_float2(0.f, 0.f);
+      for (int i = 0; i < GE::DV; ++i) acc[h][i] = make_float2(0.f, 0.f);
     }
+    m_own = -CUDART_INF_F;
+    l_own = 0.f;
     const int L = seq_len_clipped<BS>(a, wk.s);
 
 #pragma unroll 1
@@ -427,8 +450,9 @@ __global__ void __launch_bounds__(W * 32, 2)
 #pragma unroll 1
       for (int step = 0; step < GE::STEPS; ++step) {
         const int tbase = step * TB;
-        float sc[TL][G];
-        // ---- scores: this lane's DL dimensions of TL token rows
+        const int vstep = valid - tbase;  // valid tokens in this step (may be <= 0 or > TB)
+        // ---- partial scores over this lane's DL dims: sc[h * TL + k], token r + R k
+        float sc[GE::N0];
 #pragma unroll
         for (int k = 0; k < TL; ++k) {
           const int t = tbase + r + R * k;
@@ -445,104 +469,119 @@ __global__ void __launch_bounds__(W * 32, 2)
               for (int h = 0; h < G; ++h) part[h] = ffma2(q2[h][jv * PV + pv], kv[pv], part[h]);
           }
 #pragma unroll
-          for (int h = 0; h < G; ++h) sc[k][h] = part[h].x + part[h].y;
+          for (int h = 0; h < G; ++h) sc[h * TL + k] = part[h].x + part[h].y;
         }
+        // ---- recursive halving over the C lanes of the row: each round a lane
+        //      keeps half of its values (by its lane bit) and adds the partner's
+        //      copy of that half; afterwards it owns NF complete scores.
 #pragma unroll
-        for (int off = 1; off < C; off <<= 1)
+        for (int i = 0; i < GE::NT; ++i) {
+          const int msk = C >> (i + 1);
+          const bool hi = (c & msk) != 0;
+          const int half = GE::N0 >> (i + 1);
 #pragma unroll
-          for (int k = 0; k < TL; ++k)
-#pragma unroll
-            for (int h = 0; h < G; ++h) sc[k][h] += __shfl_xor_sync(0xffffffffu, sc[k][h], off);
-        // ---- mask tokens past the sequence end (and whole bad tiles)
-#pragma unroll
-        for (int k = 0; k < TL; ++k)
-          if (tbase + r + R * k >= valid)
-#pragma unroll
-            for (int h = 0; h < G; ++h) sc[k][h] = -CUDART_INF_F;
-        // ---- online softmax, max shared by the whole warp
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float mx = sc[0][h];
-#pragma unroll
-          for (int k = 1; k < TL; ++k) mx = fmaxf(mx, sc[k][h]);
-#pragma unroll
-          for (int off = C; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-          const float m_new = fmaxf(m_run[h], mx);
-          const float m_use = (m_new == -CUDART_INF_F) ? 0.f : m_new;
-          float lsum = 0.f;
-#pragma unroll
-          for (int k = 0; k < TL; ++k) {
-            sc[k][h] = fast_exp2(sc[k][h] - m_use);
-            lsum += sc[k][h];
-          }
-          if (m_new > m_run[h]) {  // warp-uniform
-            const float alpha = fast_exp2(m_run[h] - m_use);
-            l_run[h] *= alpha;
-            const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll
-            for (int i = 0; i < NP; ++i) acc[h][i] = __fmul2_rn(acc[h][i], a2);
-            m_run[h] = m_new;
-          }
-          l_run[h] += lsum;
-        }
-        // ---- P . V
-#pragma unroll
-        for (int k = 0; k < TL; ++k) {
-          const int t = tbase + r + R * k;
-          if (t < valid) {
-#pragma unroll
-            for (int jv = 0; jv < NV; ++jv) {
-              float2 vv[PV];
-              VecLoad<CT, VB>::run(vtile + (size_t)t * D * E + (c + C * jv) * VB, vv);
-#pragma unroll
-              for (int h = 0; h < G; ++h) {
-                const float2 p2 = make_float2(sc[k][h], sc[k][h]);
-#pragma unroll
-                for (int pv = 0; pv < PV; ++pv) acc[h][jv * PV + pv] = ffma2(p2, vv[pv], acc[h][jv * PV + pv]);
-              }
+          for (int jj = 0; jj < (GE::N0 >> 1); ++jj) {
+            if (jj < half) {
+              const float lo_v = sc[jj], hi_v = sc[jj + half];
+              const float send = hi ? lo_v : hi_v;
+              const float keep = hi ? hi_v : lo_v;
+              sc[jj] = keep + __shfl_xor_sync(0xffffffffu, send, msk);
             }
           }
         }
+#pragma unroll
+        for (int i = GE::NT; i < GE::LC; ++i) sc[0] += __shfl_xor_sync(0xffffffffu, sc[0], C >> (i + 1));
+        // ---- owned scores: value v = vbase + jj -> head h_own, token r + R (v % TL)
+        const int vbase = (c >> (GE::LC - GE::NT)) << (GE::LN - GE::NT);
+        float mx = -CUDART_INF_F;
+#pragma unroll
+        for (int jj = 0; jj < GE::NF; ++jj) {
+          const int t = r + R * ((vbase + jj) % TL);
+          if (t >= vstep) sc[jj] = -CUDART_INF_F;
+          mx = fmaxf(mx, sc[jj]);
+        }
+        // max over the lanes that own the same head, then every head's max to all
+#pragma unroll
+        for (int off = 1; off < C / G; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+#pragma unroll
+        for (int off = C; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const float m_new_own = fmaxf(m_own, mx);
+        const float m_use_own = (m_new_own == -CUDART_INF_F) ? 0.f : m_new_own;
+        float lsum = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < GE::NF; ++jj) {
+          const float pj = fast_exp2(sc[jj] - m_use_own);
+          lsum += pj;
+          ps[h_own * TB + r + R * ((vbase + jj) % TL)] = pj;
+        }
+        l_own = l_own * fast_exp2(m_own - m_use_own) + (l_counts ? lsum : 0.f);
+        m_own = m_new_own;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float m_new = fmaxf(m_run[h], __shfl_sync(0xffffffffu, mx, h * (C / G)));
+          if (m_new > m_run[h]) {  // warp-uniform
+            const float alpha = fast_exp2(m_run[h] - m_new);
+            const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+            for (int i = 0; i < GE::DV; ++i) acc[h][i] = __fmul2_rn(acc[h][i], a2);
+            m_run[h] = m_new;
+          }
+        }
+        __syncwarp();
+        // ---- P . V: lane owns DV dims for the token pairs of its group
+        const int tg = lane / GE::SL, d0 = (lane % GE::SL) * GE::DV;
+        const bool full = vstep >= TB;
+#pragma unroll
+        for (int i = 0; i < GE::PPL; ++i) {
+          const int pr = tg + GE::TG * i;  // token pair index within the step
+          const int t0 = 2 * pr;
+          float v0[GE::DV], v1[GE::DV];
+          Vec4Load<CT>::run(vtile + (size_t)(tbase + t0) * D * E + d0 * E, v0);
+          Vec4Load<CT>::run(vtile + (size_t)(tbase + t0 + 1) * D * E + d0 * E, v1);
+          if (!full) {  // tokens past the end may hold NaN: their weight is 0, drop the value too
+#pragma unroll
+            for (int d = 0; d < GE::DV; ++d) {
+              v0[d] = t0 < vstep ? v0[d] : 0.f;
+              v1[d] = t0 + 1 < vstep ? v1[d] : 0.f;
+            }
+          }
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float2 p2 = *reinterpret_cast<const float2*>(ps + h * TB + t0);
+#pragma unroll
+            for (int d = 0; d < GE::DV; ++d) acc[h][d] = ffma2(p2, make_float2(v0[d], v1[d]), acc[h][d]);
+          }
+        }
+        __syncwarp();
       }
       ++consumed;
-      __syncwarp();
-      if (lane == 0) fence_proxy_async_smem();
       __syncwarp();
       if (alive) issue_next();
     }
 
     // ------------------------------------------------------------ merge warps
-    // sum over the R token rows (lanes that share c), then park in shared memory
-#pragma unroll
-    for (int off = C; off < 32; off <<= 1) {
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], off);
-#pragma unroll
-        for (int i = 0; i < NP; ++i) {
-          acc[h][i].x += __shfl_xor_sync(0xffffffffu, acc[h][i].x, off);
-          acc[h][i].y += __shfl_xor_sync(0xffffffffu, acc[h][i].y, off);
-        }
-      }
-    }
+    // P.V: fold token halves and token groups; l: sum over the lanes of a head
     float* mw = merge + (size_t)w * SM::kMergeFloats;
-    if (r == 0) {
+    {
+      const int d0 = (lane % GE::SL) * GE::DV;
 #pragma unroll
       for (int h = 0; h < G; ++h)
 #pragma unroll
-        for (int jv = 0; jv < NV; ++jv)
+        for (int d = 0; d < GE::DV; ++d) {
+          float v = acc[h][d].x + acc[h][d].y;
 #pragma unroll
-          for (int pv = 0; pv < PV; ++pv) {
-            const int dim = (c + C * jv) * VE + 2 * pv;
-            mw[h * D + dim] = acc[h][jv * PV + pv].x;
-            mw[h * D + dim + 1] = acc[h][jv * PV + pv].y;
-          }
-      if (c == 0)
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          mw[G * D + h] = m_run[h];
-          mw[G * D + G + h] = l_run[h];
+          for (int off = GE::SL; off < 32; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+          if (lane < GE::SL) mw[h * D + d0 + d] = v;
         }
+      float l = l_own;
+#pragma unroll
+      for (int off = 1; off < C / G; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+#pragma unroll
+      for (int off = C; off < 32; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+      if (r == 0 && (c % (C / G)) == 0) {
+        mw[G * D + h_own] = m_own;
+        mw[G * D + G + h_own] = l;
+      }
     }
     __syncthreads();
 

@@ -107,13 +107,23 @@ bool valid_cache_desc(const pkv_cache_desc* c) {
 
 pkv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
 
-size_t balanced_workspace(int B, int units, int G, int D, int grid_max) {
-  return align_up((size_t)B * units * sizeof(int)) + (size_t)2 * grid_max * (G * D + 2 * G) * sizeof(float);
+// Workspace layout, both modes: [merge counters][mode-specific partials].
+// The counter region has a fixed minimum size, so partials of any call never
+// land where another (smaller or larger) balanced call keeps its counters.
+constexpr size_t kCounterRegionMin = size_t(1) << 20;  // 262144 segments
+
+size_t counter_region(int B, int units) {
+  const size_t need = align_up((size_t)B * units * sizeof(int));
+  return need > kCounterRegionMin ? need : kCounterRegionMin;
 }
 
-size_t partition_workspace(int B, int Hq, int D, int P) {
+size_t balanced_workspace(int B, int units, int G, int D, int grid_max) {
+  return counter_region(B, units) + (size_t)2 * grid_max * (G * D + 2 * G) * sizeof(float);
+}
+
+size_t partition_workspace(int B, int Hq, int units, int D, int P) {
   const size_t rows = (size_t)B * Hq * P;
-  return align_up(rows * D * sizeof(float)) + 2 * align_up(rows * sizeof(float));
+  return counter_region(B, units) + align_up(rows * D * sizeof(float)) + 2 * align_up(rows * sizeof(float));
 }
 
 }  // namespace
@@ -184,7 +194,7 @@ size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
     return balanced_workspace(num_seqs, units, G, head_dim, sms * kMaxCtasPerSm);
   }
   const int P = max_seq_len == 0 ? 1 : (max_seq_len + partition_tokens - 1) / partition_tokens;
-  return partition_workspace(num_seqs, num_q_heads, head_dim, P);
+  return partition_workspace(num_seqs, num_q_heads, units, head_dim, P);
 }
 
 pkv_status pkv_split_kv_reduce(void* out, pkv_dtype out_dtype, const float* o_part, const float* m_part,
@@ -276,8 +286,7 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, pkv_dtype q_dtyp
     if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return PKV_ERR_INVALID_ARG;
     a.counters = static_cast<int*>(workspace);
-    a.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                          align_up((size_t)num_seqs * a.units * sizeof(int)));
+    a.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + counter_region(num_seqs, a.units));
     int64_t grid = (int64_t)sms * (occ < kMaxCtasPerSm ? occ : kMaxCtasPerSm);
     // never more CTAs than tiles (upper bound from the host hint)
     const int64_t tiles_hint = (int64_t)num_seqs * a.units * ((a.len_clip + BS - 1) / BS);
@@ -287,11 +296,11 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, pkv_dtype q_dtyp
   // fixed partitions, then the log-sum-exp reduce
   const int P = max_seq_len == 0 ? 1 : (max_seq_len + partition_tokens - 1) / partition_tokens;
   if (P > 65535) return PKV_ERR_UNSUPPORTED;
-  const size_t need = partition_workspace(num_seqs, num_q_heads, D, P);
+  const size_t need = partition_workspace(num_seqs, num_q_heads, a.units, D, P);
   if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return PKV_ERR_INVALID_ARG;
   const size_t rows = (size_t)num_seqs * num_q_heads * P;
-  char* ws = static_cast<char*>(workspace);
+  char* ws = static_cast<char*>(workspace) + counter_region(num_seqs, a.units);
   a.o_part = reinterpret_cast<float*>(ws);
   a.m_part = reinterpret_cast<float*>(ws + align_up(rows * D * sizeof(float)));
   a.l_part = reinterpret_cast<float*>(ws + align_up(rows * D * sizeof(float)) + align_up(rows * sizeof(float)));

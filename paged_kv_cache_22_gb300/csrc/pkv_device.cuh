@@ -98,6 +98,33 @@ struct VecLoad<CacheFP8, 8> {
   }
 };
 
+// Widen 4 consecutive elements at `p` (shared memory, aligned to 4 elements).
+template <class CT>
+struct Vec4Load;
+template <>
+struct Vec4Load<CacheF32> {
+  __device__ __forceinline__ static void run(const uint8_t* p, float (&o)[4]) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+  }
+};
+template <>
+struct Vec4Load<CacheBF16> {
+  __device__ __forceinline__ static void run(const uint8_t* p, float (&o)[4]) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    const float2 a = bf16x2_to_f2(v.x), b = bf16x2_to_f2(v.y);
+    o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
+  }
+};
+template <>
+struct Vec4Load<CacheFP8> {
+  __device__ __forceinline__ static void run(const uint8_t* p, float (&o)[4]) {
+    const uint32_t v = *reinterpret_cast<const uint32_t*>(p);
+    const float2 a = e4m3x2_to_f2(v), b = e4m3x2_to_f2(v >> 16);
+    o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
+  }
+};
+
 // q / out element access.
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -173,7 +200,13 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, u
       : "memory");
 }
 
-__device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
+// 2^x on the SFU (flushes subnormal results to zero; 2^-inf = +0).  Relative
+// error is a few ulp, far below every tolerance the outputs are held to.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 

@@ -93,6 +93,6 @@ def test_partition_workspace_size_formula(lib):
 
     def up(x):
         return (x + 255) // 256 * 256
-    want = up(rows * d * 4) + 2 * up(rows * 4)
+    want = (1 << 20) + up(rows * d * 4) + 2 * up(rows * 4)  # counters first
     assert lib.pkv_decode_workspace_bytes(B, Hq, Hkv, d, L, pt) == want
     assert lib.pkv_decode_workspace_bytes(B, Hq, 3, d, L, pt) == 0  # invalid GQA split
