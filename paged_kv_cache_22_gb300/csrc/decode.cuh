@@ -16,21 +16,28 @@
 //    contiguous elements in the [num_blocks, Hkv, BS, D] cache, fetched whole
 //    by one 1-D bulk copy (TMA) into shared memory.  Every tile is read from
 //    HBM exactly once and serves all G query heads of its kv head.
-//  * Each warp owns a private ring of NSW shared-memory stages and its own
-//    mbarriers: it consumes stage k and immediately refills it with its tile
-//    k + NSW.  No warp ever waits for another warp's copies.
-//  * Lane layout inside a tile: C lanes share a token row, each holding
-//    DL = D / C head dimensions for all G heads' queries in registers; R = 32/C
-//    rows run in parallel.  Scores are finished with an xor-shuffle over the C
-//    lanes; the running max is warp-uniform so the accumulator rescale is a
-//    uniform branch.  Dot products and the PV update use packed fp32 FMA.
-//  * Balanced split: the tiles of all (sequence, kv head) segments are laid
-//    end to end and cut into gridDim.x equal ranges, one per CTA, so every SM
-//    streams the same number of bytes whatever the length skew.  A segment cut
-//    between CTAs is merged by the last CTA to finish it (atomic ticket, no
-//    waiting): partial (o, m, l) go through the workspace and are combined by
-//    log-sum-exp.  Fixed-partition mode instead gives each CTA one partition
-//    of one segment and leaves the merge to the reduce kernel.
+//  * Every warp is an independent worker: its own ring of NSW shared-memory
+//    stages with their mbarriers, its own double-buffered query, its own
+//    online-softmax state.  It consumes stage k and refills it with its tile
+//    k + NSW; the block id of the next tile is loaded one tile ahead.  After
+//    the one barrier that publishes the mbarrier inits, warps never wait for
+//    each other.
+//  * Inside a tile: C lanes share a token row, each holding DL = D / C head
+//    dims of all G queries in registers; R = 32 / C rows run in parallel.  The
+//    partial dot products are finished by recursive halving over the C lanes,
+//    after which each lane owns distinct (head, token) scores; the running max
+//    is warp-uniform per head, so accumulator rescales are uniform branches.
+//    Probabilities go through a small shared buffer to the P.V layout, where
+//    each lane owns DV = 4 dims of every token and accumulates token pairs
+//    with packed fp32 FMA.
+//  * Balanced split: the tiles of all (sequence, kv-head unit) segments are
+//    laid end to end and cut into one equal range per warp of the grid, so
+//    every SM streams the same bytes whatever the length skew.  A segment cut
+//    between warps is merged by the last warp to finish a piece of it (atomic
+//    ticket, no waiting): unnormalised partials (acc, m, l) go through the
+//    workspace and are combined by log-sum-exp.  Fixed-partition mode gives
+//    each warp one partition of one segment and leaves the merge to the
+//    reduce kernel.
 #pragma once
 
 #include <math_constants.h>
@@ -60,7 +67,7 @@ struct DecodeArgs {
   float out_scale;   // 1 (kv_scale for fp8 caches)
   // balanced split
   int* counters;     // [num_seqs * units], zero between calls
-  float* partials;   // [2 * gridDim.x][G * D + 2 * G]
+  float* partials;   // [2 * warps][G * D + 2 * G]
   // fixed partitions
   int partition_blocks;
   int max_partitions;
@@ -99,45 +106,45 @@ struct Geo {
   static constexpr int SL = D / DV;
   static constexpr int TG = 32 / SL;
   static constexpr int PPL = (TB / 2) / TG;            // token pairs per lane per step
-  static_assert(SL <= 32 && 32 % SL == 0 && (TB / 2) % TG == 0 && PPL >= 1, "P.V layout");
-  static_assert(C >= G && NF <= TL, "each lane owns scores of one head");
   static constexpr int NSW0 = 16384 / (2 * TILE);
   static constexpr int NSW = NSW0 < 2 ? 2 : (NSW0 > 8 ? 8 : NSW0);  // stages per warp
+  static constexpr int SLOT = G * D + 2 * G;           // floats of one partial result
   static_assert(D % DL == 0 && 32 % C == 0 && R <= TB && TB % R == 0, "lane layout");
   static_assert(DL % VE == 0 && VE % 2 == 0, "vector layout");
   static_assert(TILE % 16 == 0, "bulk copies move multiples of 16 bytes");
+  static_assert(SL <= 32 && 32 % SL == 0 && (TB / 2) % TG == 0 && PPL >= 1, "P.V layout");
+  static_assert(C >= G && NF <= TL, "each lane owns scores of one head");
 };
 
+// Shared memory: per-warp regions, laid out type by type.
 template <class CT, int D, int BS, int G, int W>
 struct Smem {
   using GE = Geo<CT, D, BS, G>;
   using QT = typename CT::QType;
   static constexpr int kStageBytes = 2 * GE::TILE;  // K tile then V tile
-  static constexpr int kMergeFloats = G * D + 2 * G;
   static constexpr size_t kStages = 0;
-  static constexpr size_t kBars = kStages + (size_t)W * GE::NSW * kStageBytes;
+  static constexpr size_t kQBuf = kStages + (size_t)W * GE::NSW * kStageBytes;
+  static constexpr size_t kP = kQBuf + (size_t)W * 2 * G * D * sizeof(QT);
+  static constexpr size_t kBars = (kP + (size_t)W * G * GE::TB * 4 + 7) / 8 * 8;
   static constexpr size_t kQBars = kBars + (size_t)W * GE::NSW * 8;
-  static constexpr size_t kValid = kQBars + 2 * 8;
-  static constexpr size_t kQBuf = (kValid + (size_t)W * GE::NSW * 4 + 127) / 128 * 128;
-  static constexpr size_t kMerge = kQBuf + 2 * (size_t)G * D * sizeof(QT);
-  static constexpr size_t kMisc = kMerge + (size_t)W * kMergeFloats * 4;
-  static_assert(G * GE::TB <= G * D, "probabilities fit in the warp's merge slot");
-  static constexpr size_t kBytes = kMisc + 64;
+  static constexpr size_t kOk = kQBars + (size_t)W * 2 * 8;
+  static constexpr size_t kBytes = kOk + (size_t)W * GE::NSW * 4;
 };
 
 // ----------------------------------------------------------------------------
-// Balanced split of T tiles over C CTAs.  With T >= C every CTA gets
-// floor((c+1)T/C) - floor(cT/C) >= 1 tiles; with T < C the first T CTAs get one
-// tile each and the rest none, so a segment's tiles always lie on consecutive
-// non-empty CTAs (the merge counts its pieces as c_last - c_first + 1).
+// Balanced split of T tiles over N workers.  With T >= N every worker gets
+// floor((c+1)T/N) - floor(cT/N) >= 1 tiles; with T < N the first T workers
+// get one tile each and the rest none, so a segment's tiles always lie on
+// consecutive non-empty workers (the merge counts its pieces as
+// last - first + 1).
 // ----------------------------------------------------------------------------
-__device__ __forceinline__ int64_t range_start(int64_t c, int64_t T, int64_t C) {
-  return T >= C ? c * T / C : (c < T ? c : T);
+__device__ __forceinline__ int64_t range_start(int64_t c, int64_t T, int64_t N) {
+  return T >= N ? c * T / N : (c < T ? c : T);
 }
 
-// The CTA whose range holds tile u (0 <= u < T).
-__device__ __forceinline__ int cta_of(int64_t u, int64_t T, int64_t C) {
-  return (int)(T >= C ? ((u + 1) * C - 1) / T : u);
+// The worker whose range holds tile u (0 <= u < T).
+__device__ __forceinline__ int64_t owner_of(int64_t u, int64_t T, int64_t N) {
+  return T >= N ? ((u + 1) * N - 1) / T : u;
 }
 
 // ----------------------------------------------------------------------------
@@ -162,7 +169,6 @@ __device__ __forceinline__ int seq_blocks(const DecodeArgs& a, int s) {
   return (L + BS - 1) / BS;
 }
 
-template <int BS>
 __device__ __forceinline__ int seq_len_clipped(const DecodeArgs& a, int s) {
   int L = __ldg(a.seq_lens + s);
   return L < 0 ? 0 : (L > a.len_clip ? a.len_clip : L);
@@ -202,20 +208,6 @@ __device__ __forceinline__ void walker_next_piece(Walker& wk, const DecodeArgs& 
   walker_settle<BS>(wk, a, u1);
 }
 
-// Issue cursor: the warp's own tiles, in the order it will consume them.
-struct Cursor {
-  Walker wk;
-  int j;  // current block index within the piece
-};
-
-template <int BS>
-__device__ __forceinline__ void cursor_fix(Cursor& cu, const DecodeArgs& a, int64_t u1, int w) {
-  while (!cu.wk.done && cu.j >= cu.wk.je) {
-    walker_next_piece<BS>(cu.wk, a, u1);
-    cu.j = cu.wk.jb + w;
-  }
-}
-
 // ----------------------------------------------------------------------------
 // The kernel.
 // ----------------------------------------------------------------------------
@@ -226,100 +218,90 @@ __global__ void __launch_bounds__(W * 32, (G >= 8 ? 2 : 3))
   using SM = Smem<CT, D, BS, G, W>;
   using QT = typename CT::QType;
   constexpr int NSW = GE::NSW, C = GE::C, R = GE::R, TL = GE::TL, NV = GE::NV, PV = GE::PV,
-                NP = GE::NP, VE = GE::VE, VB = GE::VB, TB = GE::TB, TILE = GE::TILE;
+                NP = GE::NP, VE = GE::VE, VB = GE::VB, TB = GE::TB, TILE = GE::TILE, DV = GE::DV,
+                SL = GE::SL, SLOT = GE::SLOT;
   constexpr int E = GE::E;
 
   extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* stages = smem + SM::kStages;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::kBars);
-  uint64_t* qbars = reinterpret_cast<uint64_t*>(smem + SM::kQBars);
-  int* stage_ok = reinterpret_cast<int*>(smem + SM::kValid);
-  QT* qbuf = reinterpret_cast<QT*>(smem + SM::kQBuf);
-  float* merge = reinterpret_cast<float*>(smem + SM::kMerge);
-  int64_t* misc = reinterpret_cast<int64_t*>(smem + SM::kMisc);
-
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int r = lane / C, c = lane % C;
+  uint8_t* stages = smem + SM::kStages + (size_t)w * NSW * SM::kStageBytes;
+  QT* qbuf = reinterpret_cast<QT*>(smem + SM::kQBuf) + (size_t)w * 2 * G * D;
+  float* ps = reinterpret_cast<float*>(smem + SM::kP) + (size_t)w * G * TB;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::kBars) + w * NSW;
+  uint64_t* qbars = reinterpret_cast<uint64_t*>(smem + SM::kQBars) + w * 2;
+  int* stage_ok = reinterpret_cast<int*>(smem + SM::kOk) + w * NSW;
 
-  // ---------------------------------------------------------------- range
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < NSW; ++i) mbar_init(&bars[i], 1);
+    mbar_init(&qbars[0], 1);
+    mbar_init(&qbars[1], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();  // the only block-wide barrier: warps are independent from here on
+
+  const int64_t gw = (int64_t)blockIdx.x * W + w;  // this warp's index in the grid
+  const int64_t NW = (int64_t)gridDim.x * W;
   int64_t u0, u1, T = 0;
   Walker wk0;
   if constexpr (BALANCED) {
-    if (w == 0) {
-      // total tiles, then the sequence that holds this CTA's first tile
-      int64_t mine = 0;
-      for (int s = lane; s < a.num_seqs; s += 32) mine += seq_blocks<BS>(a, s);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, off);
-      T = mine * a.units;
-      u0 = range_start(blockIdx.x, T, gridDim.x);
-      u1 = range_start(blockIdx.x + 1, T, gridDim.x);
-      int s0 = a.num_seqs;
-      int64_t p0 = 0;
-      if (u0 < u1) {
-        int64_t run = 0;  // tiles before this chunk
-        for (int s = 0; s < a.num_seqs; s += 32) {
-          int64_t n = (s + lane < a.num_seqs) ? (int64_t)seq_blocks<BS>(a, s + lane) * a.units : 0;
-          int64_t incl = n;
-#pragma unroll
-          for (int off = 1; off < 32; off <<= 1) {
-            int64_t t = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += t;
-          }
-          int64_t excl = incl - n;
-          unsigned hit = __ballot_sync(0xffffffffu, n > 0 && run + excl <= u0 && u0 < run + incl);
-          if (hit) {
-            int src = __ffs(hit) - 1;
-            s0 = s + src;
-            p0 = __shfl_sync(0xffffffffu, run + excl, src);
-            break;
-          }
-          run += __shfl_sync(0xffffffffu, incl, 31);
-        }
-      }
-      if (lane == 0) {
-        misc[0] = u0;
-        misc[1] = u1;
-        misc[2] = T;
-        misc[3] = s0;
-        misc[4] = p0;
-      }
-    }
-    // mbarriers
-    if (tid < W * NSW) mbar_init(&bars[tid], 1);
-    if (tid < 2) mbar_init(&qbars[tid], 1);
-    fence_mbar_init();
-    __syncthreads();
-    u0 = misc[0];
-    u1 = misc[1];
-    T = misc[2];
-    // sequences of length 0 get a zero row (spread over the CTAs)
-    for (int s = blockIdx.x; s < a.num_seqs; s += gridDim.x) {
-      if (seq_len_clipped<BS>(a, s) == 0) {
+    // sequences of length 0 get a zero row (spread over the warps)
+    for (int64_t s = gw; s < a.num_seqs; s += NW) {
+      if (seq_len_clipped(a, (int)s) == 0) {
         QT* o = reinterpret_cast<QT*>(a.out) + (size_t)s * a.num_q_heads * D;
-        for (int i = tid; i < a.num_q_heads * D; i += W * 32) o[i] = from_f32<QT>(0.f);
+        for (int i = lane; i < a.num_q_heads * D; i += 32) o[i] = from_f32<QT>(0.f);
       }
     }
-    if (u0 >= u1 || misc[3] >= a.num_seqs) return;
-    wk0.s = (int)misc[3];
-    wk0.base = misc[4];
-    wk0.nb = seq_blocks<BS>(a, wk0.s);
-    int64_t off = u0 - wk0.base;
+    // total tiles, this warp's range, and the sequence holding its first tile
+    int64_t mine = 0;
+    for (int s = lane; s < a.num_seqs; s += 32) mine += seq_blocks<BS>(a, s);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, off);
+    T = mine * a.units;
+    u0 = range_start(gw, T, NW);
+    u1 = range_start(gw + 1, T, NW);
+    if (u0 >= u1) return;
+    int s0 = a.num_seqs;
+    int64_t p0 = 0, run = 0;  // tiles before the current chunk of 32 sequences
+    for (int s = 0; s < a.num_seqs; s += 32) {
+      const int64_t n = (s + lane < a.num_seqs) ? (int64_t)seq_blocks<BS>(a, s + lane) * a.units : 0;
+      int64_t incl = n;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int64_t t = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += t;
+      }
+      const int64_t excl = incl - n;
+      const unsigned hit = __ballot_sync(0xffffffffu, n > 0 && run + excl <= u0 && u0 < run + incl);
+      if (hit) {
+        const int src = __ffs(hit) - 1;
+        s0 = s + src;
+        p0 = __shfl_sync(0xffffffffu, run + excl, src);
+        break;
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (s0 >= a.num_seqs) return;  // cannot happen for u0 < T
+    wk0.s = s0;
+    wk0.base = p0;
+    wk0.nb = seq_blocks<BS>(a, s0);
+    const int64_t off = u0 - p0;
     wk0.unit = (int)(off / wk0.nb);
     wk0.jb = (int)(off % wk0.nb);
     wk0.done = false;
     walker_settle<BS>(wk0, a, u1);
   } else {
-    // fixed partition blockIdx.y of segment blockIdx.x
-    const int s = blockIdx.x / a.units, unit = blockIdx.x % a.units;
+    // fixed partition p of segment seg, one per warp
+    const int64_t segs = (int64_t)a.num_seqs * a.units;
+    if (gw >= segs * a.max_partitions) return;
+    const int64_t seg = gw / a.max_partitions;
+    const int p = (int)(gw % a.max_partitions);
+    const int s = (int)(seg / a.units), unit = (int)(seg % a.units);
     const int nb = seq_blocks<BS>(a, s);
-    const int jb = blockIdx.y * a.partition_blocks;
+    const int jb = p * a.partition_blocks;
     const int je = min(nb, jb + a.partition_blocks);
     if (jb >= je) return;
-    if (tid < W * NSW) mbar_init(&bars[tid], 1);
-    if (tid < 2) mbar_init(&qbars[tid], 1);
-    fence_mbar_init();
-    __syncthreads();
     wk0.s = s;
     wk0.unit = unit;
     wk0.nb = nb;
@@ -332,42 +314,44 @@ __global__ void __launch_bounds__(W * 32, (G >= 8 ? 2 : 3))
     u1 = wk0.seg_u + je;
   }
 
-  const size_t head_stride = (size_t)BS * D * E;               // one kv head's tile
+  const size_t head_stride = (size_t)BS * D * E;  // one kv head's tile
   const size_t block_stride = (size_t)a.num_kv_heads * head_stride;
 
   // ---------------------------------------------------------------- issue side
-  Cursor cur;
-  cur.wk = wk0;
-  cur.j = wk0.jb + w;
-  cursor_fix<BS>(cur, a, u1, w);
+  Walker cw = wk0;  // issue cursor: segment of the next tile to fetch
+  int cj = wk0.jb;  // its block index
+  int32_t next_id = __ldg(a.block_tables + (size_t)cw.s * a.table_stride + cj);
   int issued = 0;
 
   auto issue_next = [&]() {
-    if (cur.wk.done) return;
+    if (cw.done) return;
     const int st = issued % NSW;
     if (lane == 0) {
-      const int32_t id = __ldg(a.block_tables + (size_t)cur.wk.s * a.table_stride + cur.j);
-      const int kvh = cur.wk.unit / a.units_per_kv;
-      uint8_t* dst = stages + ((size_t)w * NSW + st) * SM::kStageBytes;
-      uint64_t* bar = &bars[w * NSW + st];
-      if (id >= 0 && id < a.num_blocks) {
-        stage_ok[w * NSW + st] = 1;
-        const size_t off = (size_t)id * block_stride + (size_t)kvh * head_stride;
+      const int kvh = cw.unit / a.units_per_kv;
+      uint8_t* dst = stages + (size_t)st * SM::kStageBytes;
+      uint64_t* bar = &bars[st];
+      if (next_id >= 0 && next_id < a.num_blocks) {
+        stage_ok[st] = 1;
+        const size_t off = (size_t)next_id * block_stride + (size_t)kvh * head_stride;
         mbar_arrive_expect_tx(bar, 2 * TILE);
         bulk_g2s(dst, a.k_cache + off, TILE, bar);
         bulk_g2s(dst + TILE, a.v_cache + off, TILE, bar);
       } else {
         raise_error(a.err, PKV_DEVERR_BAD_BLOCK_ID);
-        stage_ok[w * NSW + st] = 0;
+        stage_ok[st] = 0;
         mbar_arrive(bar);
       }
     }
     ++issued;
-    cur.j += W;
-    cursor_fix<BS>(cur, a, u1, w);
+    if (++cj >= cw.je) {
+      walker_next_piece<BS>(cw, a, u1);
+      cj = cw.jb;
+    }
+    // one tile ahead: the id is needed only at the next issue
+    if (!cw.done) next_id = __ldg(a.block_tables + (size_t)cw.s * a.table_stride + cj);
   };
 
-  // q of the piece a walker stands on: bulk copy into qbuf[slot]
+  // q of the piece a walker stands on: bulk copy into this warp's q slot
   auto issue_q = [&](const Walker& pw, int slot) {
     const int kvh = pw.unit / a.units_per_kv, chunk = pw.unit % a.units_per_kv;
     const int qh0 = kvh * a.group + chunk * G;
@@ -376,9 +360,8 @@ __global__ void __launch_bounds__(W * 32, (G >= 8 ? 2 : 3))
     bulk_g2s(qbuf + (size_t)slot * G * D, src, G * D * sizeof(QT), &qbars[slot]);
   };
 
-  // prologue: q of the first piece, then the first NSW tiles of every warp
-  Walker qlook = wk0;  // warp 0's look-ahead for q prefetch
-  if (w == 0 && lane == 0) issue_q(wk0, 0);
+  Walker qlook = wk0;  // look-ahead for the q prefetch
+  if (lane == 0) issue_q(wk0, 0);
 #pragma unroll 1
   for (int i = 0; i < NSW; ++i) issue_next();
 
@@ -387,20 +370,17 @@ __global__ void __launch_bounds__(W * 32, (G >= 8 ? 2 : 3))
   int consumed = 0, waited = 0, piece = 0;
   bool alive = true;
   float2 q2[G][NP];          // this lane's query dims, pre-scaled by scale*log2(e)
-  float2 acc[G][GE::DV];     // P.V accumulators: this lane's DV dims, even/odd token halves
+  float2 acc[G][DV];         // P.V accumulators: this lane's DV dims, even/odd token halves
   float m_run[G];            // running max per head (log2 units), warp-uniform
   float m_own, l_own;        // the owned head's running max and this lane's share of its sum
-  // per-warp probabilities [G][TB]: they live in the warp's own merge slot,
-  // which is dead while the warp walks its tiles (it is written only after
-  // the warp's last tile of a piece and read before the piece's last barrier)
-  float* ps = merge + (size_t)w * SM::kMergeFloats;
-  const int h_own = c / (C / G);          // head of the scores this lane owns after the reduction
-  const bool l_counts = (c % GE::DUP) == 0;  // one copy of each duplicated score counts
+  const int h_own = c / (C / G);              // head of the scores this lane owns
+  const bool l_counts = (c % GE::DUP) == 0;   // one copy of each duplicated score counts
+  const int tg = lane / SL, d0 = (lane % SL) * DV;
 
 #pragma unroll 1
   while (!wk.done) {
     const int qslot = piece & 1;
-    if (w == 0) {  // prefetch the next piece's q while this one runs
+    {  // prefetch the next piece's q while this one runs
       Walker nx = qlook;
       walker_next_piece<BS>(nx, a, u1);
       if (!nx.done && lane == 0) {
@@ -427,24 +407,24 @@ __global__ void __launch_bounds__(W * 32, (G >= 8 ? 2 : 3))
     for (int h = 0; h < G; ++h) {
       m_run[h] = -CUDART_INF_F;
 #pragma unroll
-      for (int i = 0; i < GE::DV; ++i) acc[h][i] = make_float2(0.f, 0.f);
+      for (int i = 0; i < DV; ++i) acc[h][i] = make_float2(0.f, 0.f);
     }
     m_own = -CUDART_INF_F;
     l_own = 0.f;
-    const int L = seq_len_clipped<BS>(a, wk.s);
+    const int L = seq_len_clipped(a, wk.s);
 
 #pragma unroll 1
-    for (int j = wk.jb + w; j < wk.je; j += W) {
+    for (int j = wk.jb; j < wk.je; ++j) {
       const int st = consumed % NSW;
-      const uint8_t* ktile = stages + ((size_t)w * NSW + st) * SM::kStageBytes;
+      const uint8_t* ktile = stages + (size_t)st * SM::kStageBytes;
       const uint8_t* vtile = ktile + TILE;
       bool ok = false;
       if (alive && consumed < issued) {
-        ok = mbar_wait_bounded(&bars[w * NSW + st], (consumed / NSW) & 1, a.err);
+        ok = mbar_wait_bounded(&bars[st], (consumed / NSW) & 1, a.err);
         waited = consumed + 1;
         if (!ok) alive = false;
       }
-      ok = ok && stage_ok[w * NSW + st];
+      ok = ok && stage_ok[st];
       const int valid = ok ? min(BS, L - j * BS) : 0;
 
 #pragma unroll 1
@@ -523,24 +503,22 @@ __global__ void __launch_bounds__(W * 32, (G >= 8 ? 2 : 3))
             const float alpha = fast_exp2(m_run[h] - m_new);
             const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-            for (int i = 0; i < GE::DV; ++i) acc[h][i] = __fmul2_rn(acc[h][i], a2);
+            for (int i = 0; i < DV; ++i) acc[h][i] = __fmul2_rn(acc[h][i], a2);
             m_run[h] = m_new;
           }
         }
         __syncwarp();
         // ---- P . V: lane owns DV dims for the token pairs of its group
-        const int tg = lane / GE::SL, d0 = (lane % GE::SL) * GE::DV;
         const bool full = vstep >= TB;
 #pragma unroll
         for (int i = 0; i < GE::PPL; ++i) {
-          const int pr = tg + GE::TG * i;  // token pair index within the step
-          const int t0 = 2 * pr;
-          float v0[GE::DV], v1[GE::DV];
+          const int t0 = 2 * (tg + GE::TG * i);  // first token of the pair, within the step
+          float v0[DV], v1[DV];
           Vec4Load<CT>::run(vtile + (size_t)(tbase + t0) * D * E + d0 * E, v0);
           Vec4Load<CT>::run(vtile + (size_t)(tbase + t0 + 1) * D * E + d0 * E, v1);
           if (!full) {  // tokens past the end may hold NaN: their weight is 0, drop the value too
 #pragma unroll
-            for (int d = 0; d < GE::DV; ++d) {
+            for (int d = 0; d < DV; ++d) {
               v0[d] = t0 < vstep ? v0[d] : 0.f;
               v1[d] = t0 + 1 < vstep ? v1[d] : 0.f;
             }
@@ -549,166 +527,175 @@ __global__ void __launch_bounds__(W * 32, (G >= 8 ? 2 : 3))
           for (int h = 0; h < G; ++h) {
             const float2 p2 = *reinterpret_cast<const float2*>(ps + h * TB + t0);
 #pragma unroll
-            for (int d = 0; d < GE::DV; ++d) acc[h][d] = ffma2(p2, make_float2(v0[d], v1[d]), acc[h][d]);
+            for (int d = 0; d < DV; ++d) acc[h][d] = ffma2(p2, make_float2(v0[d], v1[d]), acc[h][d]);
           }
         }
         __syncwarp();
       }
       ++consumed;
-      __syncwarp();
       if (alive) issue_next();
     }
 
-    // ------------------------------------------------------------ merge warps
-    // P.V: fold token halves and token groups; l: sum over the lanes of a head
-    float* mw = merge + (size_t)w * SM::kMergeFloats;
-    {
-      const int d0 = (lane % GE::SL) * GE::DV;
+    // ------------------------------------------------------------ piece end
+    // fold the token halves and token groups; l: sum over the lanes of a head
+    float o[G][DV];
 #pragma unroll
-      for (int h = 0; h < G; ++h)
+    for (int h = 0; h < G; ++h)
 #pragma unroll
-        for (int d = 0; d < GE::DV; ++d) {
-          float v = acc[h][d].x + acc[h][d].y;
+      for (int d = 0; d < DV; ++d) {
+        float v = acc[h][d].x + acc[h][d].y;
 #pragma unroll
-          for (int off = GE::SL; off < 32; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-          if (lane < GE::SL) mw[h * D + d0 + d] = v;
-        }
-      float l = l_own;
-#pragma unroll
-      for (int off = 1; off < C / G; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-#pragma unroll
-      for (int off = C; off < 32; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-      if (r == 0 && (c % (C / G)) == 0) {
-        mw[G * D + h_own] = m_own;
-        mw[G * D + G + h_own] = l;
+        for (int off = SL; off < 32; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        o[h][d] = v;
       }
-    }
-    __syncthreads();
+    float l_h = l_own;
+#pragma unroll
+    for (int off = 1; off < C / G; off <<= 1) l_h += __shfl_xor_sync(0xffffffffu, l_h, off);
+#pragma unroll
+    for (int off = C; off < 32; off <<= 1) l_h += __shfl_xor_sync(0xffffffffu, l_h, off);
+    float l_all[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) l_all[h] = __shfl_sync(0xffffffffu, l_h, h * (C / G));
 
     const int kvh = wk.unit / a.units_per_kv, chunk = wk.unit % a.units_per_kv;
     const int qh0 = kvh * a.group + chunk * G;
-    const int64_t piece_start = wk.seg_u + wk.jb;
     const bool whole = (wk.jb == 0 && wk.je == wk.nb);
-    bool final_here = BALANCED && whole;
-    int64_t seg_id = (int64_t)wk.s * a.units + wk.unit;
 
-    // combine the W warps: (num, den, M) per (head, dim)
-    constexpr int kItems = G * D;
-    constexpr int kPer = (kItems + W * 32 - 1) / (W * 32);
-    float res_o[kPer], res_m[kPer], res_l[kPer];
+    if constexpr (!BALANCED) {
+      // fixed partition: normalised output, natural-log max, sum
+      const int p = (int)(gw % a.max_partitions);
+      if (lane < SL) {
 #pragma unroll
-    for (int it = 0; it < kPer; ++it) {
-      const int idx = tid + it * W * 32;
-      res_o[it] = 0.f;
-      res_m[it] = -CUDART_INF_F;
-      res_l[it] = 0.f;
-      if (idx < kItems) {
-        const int h = idx / D;
-        float M = -CUDART_INF_F;
-#pragma unroll
-        for (int ww = 0; ww < W; ++ww) M = fmaxf(M, merge[ww * SM::kMergeFloats + G * D + h]);
-        const float Mu = (M == -CUDART_INF_F) ? 0.f : M;
-        float num = 0.f, den = 0.f;
-#pragma unroll
-        for (int ww = 0; ww < W; ++ww) {
-          const float* mm = merge + ww * SM::kMergeFloats;
-          const float f = fast_exp2(mm[G * D + h] - Mu);
-          num += f * mm[idx];
-          den += f * mm[G * D + G + h];
-        }
-        res_o[it] = den > 0.f ? num / den : 0.f;
-        res_m[it] = M;
-        res_l[it] = den;
-      }
-    }
-
-    if (final_here) {
-      QT* o = reinterpret_cast<QT*>(a.out) + ((size_t)wk.s * a.num_q_heads + qh0) * D;
-#pragma unroll
-      for (int it = 0; it < kPer; ++it) {
-        const int idx = tid + it * W * 32;
-        if (idx < kItems) o[idx] = from_f32<QT>(res_o[it] * a.out_scale);
-      }
-    } else if constexpr (!BALANCED) {
-      // fixed partition: natural-log maxima for the reduce kernel
-      const int p = blockIdx.y;
-#pragma unroll
-      for (int it = 0; it < kPer; ++it) {
-        const int idx = tid + it * W * 32;
-        if (idx < kItems) {
-          const int h = idx / D, dd = idx % D;
+        for (int h = 0; h < G; ++h) {
           const size_t row = ((size_t)wk.s * a.num_q_heads + qh0 + h) * a.max_partitions + p;
-          a.o_part[row * D + dd] = res_o[it] * a.out_scale;
-          if (dd == 0) {
-            a.m_part[row] = res_m[it] * 0.69314718055994531f;
-            a.l_part[row] = res_l[it];
+          const float inv = l_all[h] > 0.f ? a.out_scale / l_all[h] : 0.f;
+          *reinterpret_cast<float4*>(a.o_part + row * D + d0) =
+              make_float4(o[h][0] * inv, o[h][1] * inv, o[h][2] * inv, o[h][3] * inv);
+          if (lane == 0) {
+            a.m_part[row] = m_run[h] * 0.69314718055994531f;
+            a.l_part[row] = l_all[h];
           }
+        }
+      }
+    } else if (whole) {
+      QT* out = reinterpret_cast<QT*>(a.out) + ((size_t)wk.s * a.num_q_heads + qh0) * D;
+      if (lane < SL) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float inv = l_all[h] > 0.f ? a.out_scale / l_all[h] : 0.f;
+#pragma unroll
+          for (int d = 0; d < DV; ++d) out[h * D + d0 + d] = from_f32<QT>(o[h][d] * inv);
         }
       }
     } else {
-      // balanced split, segment cut between CTAs: publish, take a ticket
-      const int64_t C_ = gridDim.x;
-      const int cta = blockIdx.x;
-      const int slot = (piece_start == u0) ? 2 * cta : 2 * cta + 1;
-      float* pslot = a.partials + (size_t)slot * SM::kMergeFloats;
+      // segment cut between warps: publish (acc, m, l), take a ticket; the
+      // last warp to arrive combines every piece and writes the output
+      const int64_t slot = (wk.seg_u + wk.jb == u0) ? 2 * gw : 2 * gw + 1;
+      float* pslot = a.partials + (size_t)slot * SLOT;
+      if (lane < SL) {
 #pragma unroll
-      for (int it = 0; it < kPer; ++it) {
-        const int idx = tid + it * W * 32;
-        if (idx < kItems) {
-          pslot[idx] = res_o[it];
-          if (idx % D == 0) {
-            pslot[G * D + idx / D] = res_m[it];
-            pslot[G * D + G + idx / D] = res_l[it];
+        for (int h = 0; h < G; ++h)
+          *reinterpret_cast<float4*>(pslot + h * D + d0) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+        if (lane == h) {
+          pslot[G * D + h] = m_run[h];
+          pslot[G * D + G + h] = l_all[h];
+        }
+      __syncwarp();
+      __threadfence();
+      const int64_t seg_id = (int64_t)wk.s * a.units + wk.unit;
+      const int64_t w_first = owner_of(wk.seg_u, T, NW), w_last = owner_of(wk.seg_u + wk.nb - 1, T, NW);
+      int last = 0;
+      if (lane == 0) {
+        const int ticket = atomicAdd(a.counters + seg_id, 1);
+        last = (ticket == (int)(w_last - w_first));
+        if (last) a.counters[seg_id] = 0;  // ready for the next call
+      }
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
+        __threadfence();
+        // pieces sit on warps w_first..w_last; the first one's slot depends on
+        // whether the segment starts exactly at that warp's range
+        const int64_t n = w_last - w_first + 1;
+        const int64_t first_slot = (wk.seg_u != range_start(w_first, T, NW)) ? 2 * w_first + 1 : 2 * w_first;
+        auto slot_of = [&](int64_t i) -> const float* {
+          return a.partials + (size_t)(i == 0 ? first_slot : 2 * (w_first + i)) * SLOT;
+        };
+        // maxima: lanes take slots in parallel
+        float M[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) M[h] = -CUDART_INF_F;
+        for (int64_t i = lane; i < n; i += 32) {
+          const float* pp = slot_of(i);
+#pragma unroll
+          for (int h = 0; h < G; ++h) M[h] = fmaxf(M[h], ld_cg(pp + G * D + h));
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) M[h] = fmaxf(M[h], __shfl_xor_sync(0xffffffffu, M[h], off));
+          if (M[h] == -CUDART_INF_F) M[h] = 0.f;
+        }
+        float den[G], num[G][DV];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          den[h] = 0.f;
+#pragma unroll
+          for (int d = 0; d < DV; ++d) num[h][d] = 0.f;
+        }
+        for (int64_t base = 0; base < n; base += 32) {
+          // lane i holds the weights of slot base + i
+          float f[G];
+          if (base + lane < n) {
+            const float* pp = slot_of(base + lane);
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              f[h] = fast_exp2(ld_cg(pp + G * D + h) - M[h]);
+              den[h] += f[h] * ld_cg(pp + G * D + G + h);
+            }
+          } else {
+#pragma unroll
+            for (int h = 0; h < G; ++h) f[h] = 0.f;
+          }
+          const int cnt = (int)(n - base < 32 ? n - base : 32);
+#pragma unroll 4
+          for (int jj = 0; jj < cnt; ++jj) {
+            const float* pp = slot_of(base + jj);
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              const float fj = __shfl_sync(0xffffffffu, f[h], jj);
+              if (lane < SL) {
+                const float4 v = ld_cg(reinterpret_cast<const float4*>(pp + h * D + d0));
+                num[h][0] += fj * v.x;
+                num[h][1] += fj * v.y;
+                num[h][2] += fj * v.z;
+                num[h][3] += fj * v.w;
+              }
+            }
           }
         }
-      }
-      __threadfence();
-      __syncthreads();
-      const int c_first = cta_of(wk.seg_u, T, C_), c_last = cta_of(wk.seg_u + wk.nb - 1, T, C_);
-      if (tid == 0) {
-        const int ticket = atomicAdd(a.counters + seg_id, 1);
-        const bool last = (ticket == c_last - c_first);
-        if (last) a.counters[seg_id] = 0;  // ready for the next call
-        misc[5] = last ? 1 : 0;
-        __threadfence();
-      }
-      __syncthreads();
-      if (misc[5]) {
-        QT* o = reinterpret_cast<QT*>(a.out) + ((size_t)wk.s * a.num_q_heads + qh0) * D;
+        QT* out = reinterpret_cast<QT*>(a.out) + ((size_t)wk.s * a.num_q_heads + qh0) * D;
 #pragma unroll
-        for (int it = 0; it < kPer; ++it) {
-          const int idx = tid + it * W * 32;
-          if (idx < kItems) {
-            const int h = idx / D;
-            float M = -CUDART_INF_F;
-            for (int cc = c_first; cc <= c_last; ++cc) {
-              const int64_t u0c = range_start(cc, T, C_);
-              const int sl = (cc == c_first && wk.seg_u != u0c) ? 2 * cc + 1 : 2 * cc;
-              M = fmaxf(M, ld_cg(a.partials + (size_t)sl * SM::kMergeFloats + G * D + h));
-            }
-            const float Mu = (M == -CUDART_INF_F) ? 0.f : M;
-            float num = 0.f, den = 0.f;
-            for (int cc = c_first; cc <= c_last; ++cc) {
-              const int64_t u0c = range_start(cc, T, C_);
-              const int sl = (cc == c_first && wk.seg_u != u0c) ? 2 * cc + 1 : 2 * cc;
-              const float* ps = a.partials + (size_t)sl * SM::kMergeFloats;
-              const float f = ld_cg(ps + G * D + G + h) * fast_exp2(ld_cg(ps + G * D + h) - Mu);
-              num += f * ld_cg(ps + idx);
-              den += f;
-            }
-            o[idx] = from_f32<QT>(den > 0.f ? num / den * a.out_scale : 0.f);
+        for (int h = 0; h < G; ++h) {
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) den[h] += __shfl_xor_sync(0xffffffffu, den[h], off);
+          if (lane < SL) {
+            const float inv = den[h] > 0.f ? a.out_scale / den[h] : 0.f;
+#pragma unroll
+            for (int d = 0; d < DV; ++d) out[h * D + d0 + d] = from_f32<QT>(num[h][d] * inv);
           }
         }
       }
     }
-    __syncthreads();  // merge area free again
     ++piece;
     walker_next_piece<BS>(wk, a, u1);
   }
 
   // Leave no copy in flight: wait (bounded) for every stage this warp filled
   // but did not wait for (only possible after a timeout).
-  for (int k = waited; k < issued; ++k) mbar_wait_bounded(&bars[w * NSW + k % NSW], (k / NSW) & 1, a.err);
+  for (int k = waited; k < issued; ++k) mbar_wait_bounded(&bars[k % NSW], (k / NSW) & 1, a.err);
 }
 
 }  // namespace pkv

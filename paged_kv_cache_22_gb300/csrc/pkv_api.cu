@@ -117,8 +117,9 @@ size_t counter_region(int B, int units) {
   return need > kCounterRegionMin ? need : kCounterRegionMin;
 }
 
+// Two partial-result slots per warp of the largest balanced grid.
 size_t balanced_workspace(int B, int units, int G, int D, int grid_max) {
-  return counter_region(B, units) + (size_t)2 * grid_max * (G * D + 2 * G) * sizeof(float);
+  return counter_region(B, units) + (size_t)2 * grid_max * kDecodeWarps * (G * D + 2 * G) * sizeof(float);
 }
 
 size_t partition_workspace(int B, int Hq, int units, int D, int P) {
@@ -295,7 +296,6 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, pkv_dtype q_dtyp
   }
   // fixed partitions, then the log-sum-exp reduce
   const int P = max_seq_len == 0 ? 1 : (max_seq_len + partition_tokens - 1) / partition_tokens;
-  if (P > 65535) return PKV_ERR_UNSUPPORTED;
   const size_t need = partition_workspace(num_seqs, num_q_heads, a.units, D, P);
   if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return PKV_ERR_INVALID_ARG;
@@ -306,9 +306,11 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, pkv_dtype q_dtyp
   a.l_part = reinterpret_cast<float*>(ws + align_up(rows * D * sizeof(float)) + align_up(rows * sizeof(float)));
   a.partition_blocks = partition_tokens / BS;
   a.max_partitions = P;
-  const int64_t segs = (int64_t)num_seqs * a.units;
-  if (segs > 0x7FFFFFFF) return PKV_ERR_UNSUPPORTED;
-  cudaError_t e = cudaLaunchKernel(k.fn, dim3((unsigned)segs, (unsigned)P), dim3(k.threads), args, k.smem, st);
+  // one warp per (segment, partition)
+  const int64_t pieces = (int64_t)num_seqs * a.units * P;
+  const int64_t ctas = (pieces + kDecodeWarps - 1) / kDecodeWarps;
+  if (ctas > 0x7FFFFFFF) return PKV_ERR_UNSUPPORTED;
+  cudaError_t e = cudaLaunchKernel(k.fn, dim3((unsigned)ctas), dim3(k.threads), args, k.smem, st);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   ReduceArgs r;
   r.err = err;
