@@ -161,6 +161,44 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, pkv_dtype q_dtyp
                                       size_t workspace_bytes, pkv_stream_t stream);
 
 /*
+ * pkv_paged_attention_decode_noalloc -- pkv_paged_attention_decode
+ * (balanced split) for callers that cannot allocate device memory.
+ *
+ * The source pages have no counterpart: this is a library convenience.
+ * Some callers cannot supply the workspace the balanced split needs -- a
+ * plugin inside a runtime that has reserved all device memory for its own
+ * pool, plain C code that only receives tensor pointers, or a loop that must
+ * not touch an allocator.  This call computes exactly what
+ * pkv_paged_attention_decode computes with partition_tokens = 0, but keeps
+ * its merge counters and partial results in a fixed 16 MiB scratch array in
+ * device global memory that the library reserves on every GPU that loads it,
+ * until the process exits.  It allocates nothing (no cudaMalloc, cudaFree or
+ * allocating library routine).
+ *
+ * Arguments are those of pkv_paged_attention_decode without
+ * partition_tokens, workspace and workspace_bytes; layouts, supported shapes
+ * and error behaviour are the same.  A problem whose counters and partials
+ * need more than the fixed scratch (many (sequence, kv-head) segments, or an
+ * unusually large grid) is refused with PKV_ERR_WORKSPACE before anything
+ * is enqueued.
+ *
+ * The first call on a device looks up the scratch array's device address
+ * (once per device, with that device current); make that first call before
+ * any stream capture.  Every call shares the one scratch array and clears
+ * its counters at the start (an asynchronous memset on `stream`): calls that
+ * overlap on the GPU -- on different streams, or from different threads --
+ * race on it and must be serialised by the caller.
+ */
+pkv_status pkv_paged_attention_decode_noalloc(void* out, const void* q, pkv_dtype q_dtype,
+                                              int32_t num_seqs, int32_t num_q_heads,
+                                              const void* k_cache, const void* v_cache,
+                                              const pkv_cache_desc* cache,
+                                              const int32_t* block_tables,
+                                              int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                              int32_t max_seq_len, float scale, float kv_scale,
+                                              pkv_stream_t stream);
+
+/*
  * pkv_split_kv_reduce -- log-sum-exp merge of per-partition partial results.
  *
  * The pages do not describe a split of the KV sequence; this is the algebra

@@ -128,6 +128,11 @@ size_t partition_workspace(int B, int Hq, int units, int D, int P) {
 }
 
 }  // namespace
+
+// The current device's error word, for entry points defined in other
+// translation units of this library.
+unsigned int* device_error_word(int dev) { return error_word(dev); }
+
 }  // namespace pkv
 
 using namespace pkv;
