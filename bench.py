@@ -90,6 +90,22 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest `value` over all ranks (the identity without a process group)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world_size: int, bytes_per_rank_step: int, ms_per_step: float) -> float:
+    """Whole-job GB/s: every rank moves the same bytes per step (weak
+    scaling); the step time is the slowest rank's."""
+    return world_size * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 def step_bytes(w: workloads.Workload):
     lens = w.seq_lens.tolist()
     dec = metrics.decode_bytes(lens, w.num_q_heads, w.num_kv_heads, w.head_dim, w.cache_dtype,
@@ -225,28 +241,21 @@ def run_gpu(args):
     clocks = sampler.stop()
     step_ms = [e[0].elapsed_time(e[2]) for e in ev]
     dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    tot_ms = sum(step_ms)
-    if ws > 1:
-        t = torch.tensor([tot_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        tot_ms = float(t.item())
+    tot_ms = max_over_ranks(sum(step_ms), dev)
     if pkv.get_device_error():
         raise RuntimeError("device error during the timed steps")
 
     dec_b, rc_b = step_bytes(w)
     ms_per_step = tot_ms / K
-    value = ws * (dec_b + rc_b) / (ms_per_step * 1e-3) / 1e9
+    value = job_throughput(ws, dec_b + rc_b, ms_per_step)
     dec_avg_ms = sum(dec_ms) / K
     achieved = dec_b / (dec_avg_ms * 1e-3) / 1e9
     peak, peak_src = measured_peak()
 
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(pkv, w, kc, vc, dev, pt, max(10, min(K, 200)), flush)
-    if ws > 1:
-        t = torch.tensor([e2e["ms_per_step"]], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e["ms_per_step"] = float(t.item())
-    e2e_value = ws * (dec_b + rc_b) / (e2e["ms_per_step"] * 1e-3) / 1e9
+    e2e["ms_per_step"] = max_over_ranks(e2e["ms_per_step"], dev)
+    e2e_value = job_throughput(ws, dec_b + rc_b, e2e["ms_per_step"])
 
     traffic = None
     if TRAFFIC["sources_sha256"] == kernel_sources_sha() and args.config == "llama3_8b" and pt == 0:
