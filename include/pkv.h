@@ -199,6 +199,36 @@ pkv_status pkv_paged_attention_decode_noalloc(void* out, const void* q, pkv_dtyp
                                               pkv_stream_t stream);
 
 /*
+ * pkv_decode_step -- one decode step of one layer: pkv_kv_reshape_and_cache of
+ * the step's new tokens, then pkv_paged_attention_decode, on `stream`.
+ *
+ * This is the iteration of "vLLM en Kubernetes" (section "Continuous
+ * batching: dejar de esperar al más lento": every step produces one token
+ * per live session) restricted to
+ * one attention layer: the new tokens' K/V enter the cache ("PagedAttention
+ * por dentro", section "La tabla de páginas (block table)"), then each
+ * sequence attends over all its cached tokens.  The result is identical to the
+ * two calls made one after the other.  The decode grid is launched as a
+ * programmatic dependent of the cache-write grid: it reads lengths, block
+ * tables and q while the cache write runs, and waits for the write to finish
+ * before it reads any K/V.  So q, out, block_tables and seq_lens must not be
+ * produced by the cache write, which is always the case here.
+ *
+ * Arguments: those of pkv_kv_reshape_and_cache (k, v, src_dtype,
+ * num_new_tokens, slot_mapping, caches, kv_scale) and of
+ * pkv_paged_attention_decode (the rest).  All arguments are validated before
+ * anything is enqueued.
+ */
+pkv_status pkv_decode_step(const void* k, const void* v, pkv_dtype src_dtype, int32_t num_new_tokens,
+                           const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                           const pkv_cache_desc* cache, void* out, const void* q, pkv_dtype q_dtype,
+                           int32_t num_seqs, int32_t num_q_heads, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                           int32_t max_seq_len, float scale, float kv_scale,
+                           int32_t partition_tokens, void* workspace, size_t workspace_bytes,
+                           pkv_stream_t stream);
+
+/*
  * pkv_split_kv_reduce -- log-sum-exp merge of per-partition partial results.
  *
  * The pages do not describe a split of the KV sequence; this is the algebra

@@ -11,6 +11,8 @@ Entry points (same names as the C ABI, without the ``pkv_`` prefix):
 * :func:`paged_attention_decode` -- one decode step of attention over the
   paged cache (balanced split with an in-kernel merge, or fixed partitions
   followed by :func:`split_kv_reduce`);
+* :func:`decode_step` -- both of the above for one decode step, the decode
+  overlapping its prologue with the cache write;
 * :func:`split_kv_reduce` -- log-sum-exp merge of partition partials;
 * :func:`gather_kv` -- contiguous copy of every sequence's cached tokens;
 * :func:`decode_workspace_bytes`, :func:`get_device_error`.
@@ -25,7 +27,8 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "PkvError", "CacheDesc", "kv_reshape_and_cache", "paged_attention_decode", "split_kv_reduce",
+    "PkvError", "CacheDesc", "kv_reshape_and_cache", "paged_attention_decode", "decode_step",
+    "split_kv_reduce",
     "gather_kv", "decode_workspace_bytes", "get_device_error", "library", "library_path",
     "DecodeWorkspace", "F32", "BF16", "FP8_E4M3", "DEVERR_BAD_BLOCK_ID", "DEVERR_BAD_SLOT",
     "DEVERR_BAD_SEQ_LEN", "DEVERR_WAIT_TIMEOUT",
@@ -74,6 +77,8 @@ def library() -> ctypes.CDLL:
                                            i32, f32, f32, i32, vp, sz, vp],
             "pkv_split_kv_reduce": [vp, ctypes.c_int, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp],
             "pkv_gather_kv": [vp, vp, vp, vp, desc, vp, i32, vp, vp, i32, i32, vp],
+            "pkv_decode_step": [vp, vp, ctypes.c_int, i32, vp, vp, vp, desc, vp, vp, ctypes.c_int, i32,
+                                i32, vp, i32, vp, i32, f32, f32, i32, vp, sz, vp],
             "pkv_get_device_error": [ctypes.POINTER(ctypes.c_uint32), vp],
             "pkv_status_string": [ctypes.c_int],
             "pkv_device_sm_count": [],
@@ -206,6 +211,42 @@ def paged_attention_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Te
         _ptr(out), _ptr(q), qdt, B, Hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc),
         _ptr(block_tables), mbps, _ptr(seq_lens), int(max_seq_len), float(scale), float(kv_scale),
         int(partition_tokens), _ptr(ws), ws.numel(), _stream(stream)), "paged_attention_decode")
+    return out
+
+
+def decode_step(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, out: torch.Tensor,
+                q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                kv_scale: float = 1.0, max_seq_len: Optional[int] = None,
+                partition_tokens: int = 0, workspace: Optional[DecodeWorkspace] = None,
+                stream=None) -> torch.Tensor:
+    """One decode step: write the new tokens ``k, v [T, Hkv, d]`` into their
+    slots, then attend (the decode overlaps its prologue with the write)."""
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    if k.dtype not in (torch.float32, torch.bfloat16) or v.dtype != k.dtype:
+        raise TypeError("k and v must both be float32 or bfloat16")
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_tables and seq_lens must be int32")
+    B, Hq, d = q.shape
+    desc = _desc(k_cache, None)
+    mbps = int(block_tables.shape[1])
+    if max_seq_len is None:
+        max_seq_len = mbps * desc.block_size
+    nbytes = decode_workspace_bytes(B, Hq, desc.num_kv_heads, d, max_seq_len, partition_tokens)
+    if workspace is None:
+        dev = q.device.index if q.device.index is not None else torch.cuda.current_device()
+        workspace = _default_ws.setdefault(dev, DecodeWorkspace(q.device))
+    g = Hq // desc.num_kv_heads
+    heads = next(G for G in (8, 4, 2, 1) if g % G == 0)
+    units = desc.num_kv_heads * (g // heads)
+    ws = workspace.get(nbytes, (B * units * 4 + 255) // 256 * 256)
+    qdt = F32 if q.dtype == torch.float32 else BF16
+    _check(library().pkv_decode_step(
+        _ptr(k), _ptr(v), _dt(k), int(k.shape[0]), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
+        ctypes.byref(desc), _ptr(out), _ptr(q), qdt, B, Hq, _ptr(block_tables), mbps, _ptr(seq_lens),
+        int(max_seq_len), float(scale), float(kv_scale), int(partition_tokens), _ptr(ws), ws.numel(),
+        _stream(stream)), "decode_step")
     return out
 
 

@@ -362,6 +362,10 @@ __global__ void __launch_bounds__(W * 32, (G >= 8 ? 2 : 3))
 
   Walker qlook = wk0;  // look-ahead for the q prefetch
   if (lane == 0) issue_q(wk0, 0);
+  // Everything above reads only the step's inputs (lengths, tables, q).  When
+  // this grid is the programmatic dependent of the cache write, the K/V tiles
+  // must wait for that grid; on an ordinary launch this returns at once.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 #pragma unroll 1
   for (int i = 0; i < NSW; ++i) issue_next();
 

@@ -63,6 +63,9 @@ __device__ __forceinline__ void store8(const Src* s, uint8_t* d, pkv_dtype dt, f
 
 template <class Src>
 __global__ void reshape_and_cache_kernel(ReshapeArgs a) {
+  // A decode launched as this grid's programmatic dependent may start its
+  // prologue now; it waits for this grid's writes before reading any K/V.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int chunks = a.head_dim / 8;
   const int64_t per_token = (int64_t)a.num_kv_heads * chunks * 2;
   const int64_t total = (int64_t)a.num_tokens * per_token;

@@ -230,12 +230,33 @@ pkv_status pkv_split_kv_reduce(void* out, pkv_dtype out_dtype, const float* o_pa
   return from_cuda(launch_split_kv_reduce(a, out_dtype == PKV_BF16, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-pkv_status pkv_paged_attention_decode(void* out, const void* q, pkv_dtype q_dtype, int32_t num_seqs,
-                                      int32_t num_q_heads, const void* k_cache, const void* v_cache,
-                                      const pkv_cache_desc* cache, const int32_t* block_tables,
-                                      int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t max_seq_len,
-                                      float scale, float kv_scale, int32_t partition_tokens, void* workspace,
-                                      size_t workspace_bytes, pkv_stream_t stream) {
+}  // extern "C"
+
+namespace pkv {
+namespace {
+
+// Launch one decode grid; as a programmatic dependent of the previous grid on
+// the stream when `programmatic` is set (its prologue then overlaps that grid).
+cudaError_t launch_decode_grid(const DecodeKernel& k, dim3 grid, void** args, cudaStream_t st, bool programmatic) {
+  if (!programmatic) return cudaLaunchKernel(k.fn, grid, dim3(k.threads), args, k.smem, st);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(k.threads);
+  cfg.dynamicSmemBytes = k.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, k.fn, args);
+}
+
+pkv_status decode_impl(void* out, const void* q, pkv_dtype q_dtype, int32_t num_seqs, int32_t num_q_heads,
+                       const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                       int32_t max_seq_len, float scale, float kv_scale, int32_t partition_tokens, void* workspace,
+                       size_t workspace_bytes, pkv_stream_t stream, bool programmatic, bool dry_run = false) {
   if (num_seqs < 0 || !valid_cache_desc(cache)) return PKV_ERR_INVALID_ARG;
   if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return PKV_ERR_INVALID_ARG;
   if (max_blocks_per_seq <= 0 || max_seq_len < 0 || partition_tokens < 0) return PKV_ERR_INVALID_ARG;
@@ -297,7 +318,8 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, pkv_dtype q_dtyp
     // never more CTAs than tiles (upper bound from the host hint)
     const int64_t tiles_hint = (int64_t)num_seqs * a.units * ((a.len_clip + BS - 1) / BS);
     if (tiles_hint < grid) grid = tiles_hint > 0 ? tiles_hint : 1;
-    return from_cuda(cudaLaunchKernel(k.fn, dim3((unsigned)grid), dim3(k.threads), args, k.smem, st));
+    if (dry_run) return PKV_OK;
+    return from_cuda(launch_decode_grid(k, dim3((unsigned)grid), args, st, programmatic));
   }
   // fixed partitions, then the log-sum-exp reduce
   const int P = max_seq_len == 0 ? 1 : (max_seq_len + partition_tokens - 1) / partition_tokens;
@@ -315,7 +337,8 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, pkv_dtype q_dtyp
   const int64_t pieces = (int64_t)num_seqs * a.units * P;
   const int64_t ctas = (pieces + kDecodeWarps - 1) / kDecodeWarps;
   if (ctas > 0x7FFFFFFF) return PKV_ERR_UNSUPPORTED;
-  cudaError_t e = cudaLaunchKernel(k.fn, dim3((unsigned)ctas), dim3(k.threads), args, k.smem, st);
+  if (dry_run) return PKV_OK;
+  cudaError_t e = launch_decode_grid(k, dim3((unsigned)ctas), args, st, programmatic);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   ReduceArgs r;
   r.err = err;
@@ -330,6 +353,43 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, pkv_dtype q_dtyp
   r.partition_tokens = partition_tokens;
   r.max_partitions = P;
   return from_cuda(launch_split_kv_reduce(r, q_dtype == PKV_BF16, st));
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" {
+
+pkv_status pkv_paged_attention_decode(void* out, const void* q, pkv_dtype q_dtype, int32_t num_seqs,
+                                      int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                                      const pkv_cache_desc* cache, const int32_t* block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t max_seq_len,
+                                      float scale, float kv_scale, int32_t partition_tokens, void* workspace,
+                                      size_t workspace_bytes, pkv_stream_t stream) {
+  return decode_impl(out, q, q_dtype, num_seqs, num_q_heads, k_cache, v_cache, cache, block_tables,
+                     max_blocks_per_seq, seq_lens, max_seq_len, scale, kv_scale, partition_tokens, workspace,
+                     workspace_bytes, stream, false);
+}
+
+pkv_status pkv_decode_step(const void* k, const void* v, pkv_dtype src_dtype, int32_t num_new_tokens,
+                           const int64_t* slot_mapping, void* k_cache, void* v_cache, const pkv_cache_desc* cache,
+                           void* out, const void* q, pkv_dtype q_dtype, int32_t num_seqs, int32_t num_q_heads,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                           int32_t max_seq_len, float scale, float kv_scale, int32_t partition_tokens,
+                           void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+  // every argument is checked before anything is enqueued
+  pkv_status st = decode_impl(out, q, q_dtype, num_seqs, num_q_heads, k_cache, v_cache, cache, block_tables,
+                              max_blocks_per_seq, seq_lens, max_seq_len, scale, kv_scale, partition_tokens,
+                              workspace, workspace_bytes, stream, false, /*dry_run=*/true);
+  if (st != PKV_OK) return st;
+  st = pkv_kv_reshape_and_cache(k, v, src_dtype, num_new_tokens, k_cache, v_cache, cache, slot_mapping, kv_scale,
+                                stream);
+  if (st != PKV_OK) return st;
+  // the decode is the cache write's programmatic dependent only if that grid
+  // was launched (an empty write enqueues nothing)
+  return decode_impl(out, q, q_dtype, num_seqs, num_q_heads, k_cache, v_cache, cache, block_tables,
+                     max_blocks_per_seq, seq_lens, max_seq_len, scale, kv_scale, partition_tokens, workspace,
+                     workspace_bytes, stream, num_new_tokens > 0);
 }
 
 pkv_status pkv_gather_kv(void* k_out, void* v_out, const void* k_cache, const void* v_cache,

@@ -234,6 +234,68 @@ def test_seq_len_beyond_hint_sets_error(pkv):
     assert pkv.get_device_error() & pkv.DEVERR_BAD_SEQ_LEN
 
 
+# ------------------------------------------------------------------ dynamic item schedule
+# Batches with at least two tiles per warp of the balanced grid hand their last
+# tiles out dynamically; segments then end in items, cross the static/dynamic
+# boundary, or fit inside one item.
+MEDIUM = [
+    ("many_short", [37, 5, 16, 1, 90, 17] * 40, 32, 8, 128, "bf16"),
+    ("skewed", [3000, 20, 1, 700, 4096, 33, 2500, 64] * 4, 32, 8, 128, "bf16"),
+    ("g8_mixed", [16, 512, 1500, 3, 800, 2047] * 6, 64, 8, 128, "bf16"),
+    ("fp8_mixed", [300, 1200, 17, 2100] * 10, 32, 8, 128, "fp8_e4m3"),
+]
+
+
+@pytest.mark.parametrize("case", MEDIUM, ids=[c[0] for c in MEDIUM])
+def test_decode_medium_dynamic_schedule(pkv, case):
+    name, lens, Hq, Hkv, d, dt = case
+    w = workloads.make_workload(name, lens, Hq, Hkv, d, 16, dt, seed=len(lens) + Hq)
+    tiles = sum(-(-L // 16) for L in lens) * Hkv * ((Hq // Hkv) // min(8, Hq // Hkv))
+    kc, vc = gpu_caches(pkv, w)
+    ref = oracle_decode(w, threads=8)
+    for rep in range(3):  # counters must come back to zero call after call
+        got = run_decode(pkv, w, kc, vc, 0)
+        assert_close(got, ref, TOL[dt], f"{name} rep {rep} ({tiles} tiles)")
+    assert pkv.get_device_error() == 0
+
+
+# ------------------------------------------------------------------ fused step
+@pytest.mark.parametrize("pt", [0, 64])
+def test_decode_step_equals_write_then_decode(pkv, pt):
+    w = workloads.make_workload("step", [1, 40, 700, 2000, 0, 333] * 6, 32, 8, 128, 16, "bf16",
+                                seed=61)
+    kc1, vc1 = gpu_caches(pkv, w, include_new=False)
+    kc2, vc2 = kc1.clone(), vc1.clone()
+    q, tb, ln = w.q.to(DEV), w.block_tables.to(DEV), w.seq_lens.to(DEV)
+    nk, nv, ns = w.new_k.to(DEV), w.new_v.to(DEV), w.new_slots.to(DEV)
+    o1 = torch.full_like(q, float("nan"))
+    pkv.kv_reshape_and_cache(nk, nv, kc1, vc1, ns)
+    pkv.paged_attention_decode(o1, q, kc1, vc1, tb, ln, w.scale, max_seq_len=w.max_seq_len,
+                               partition_tokens=pt)
+    o2 = torch.full_like(q, float("nan"))
+    for _ in range(2):
+        pkv.decode_step(nk, nv, ns, o2, q, kc2, vc2, tb, ln, w.scale, max_seq_len=w.max_seq_len,
+                        partition_tokens=pt)
+    torch.cuda.synchronize()
+    assert torch.equal(kc1.view(torch.int16), kc2.view(torch.int16))
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert_close(o2.float().cpu().numpy().astype(np.float64), oracle_decode(w), TOL["bf16"])
+    assert pkv.get_device_error() == 0
+
+
+def test_decode_step_validates_everything_before_enqueueing(pkv):
+    w = workloads.make_workload("stepbad", [5, 9], 8, 2, 128, 16, "bf16", seed=62)
+    kc, vc = gpu_caches(pkv, w, include_new=False)
+    before = kc.clone()
+    q = w.q.to(DEV)
+    out = torch.zeros_like(q)
+    with pytest.raises(pkv.PkvError):  # partition not a multiple of the block size
+        pkv.decode_step(w.new_k.to(DEV), w.new_v.to(DEV), w.new_slots.to(DEV), out, q, kc, vc,
+                        w.block_tables.to(DEV), w.seq_lens.to(DEV), w.scale, partition_tokens=24)
+    torch.cuda.synchronize()
+    assert torch.equal(before.view(torch.int16), kc.view(torch.int16))
+
+
 # ------------------------------------------------------------------ split-KV reduce alone
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 def test_split_kv_reduce_matches_oracle(pkv, out_dtype):
