@@ -212,7 +212,7 @@ __device__ __forceinline__ void walker_next_piece(Walker& wk, const DecodeArgs& 
 // The kernel.
 // ----------------------------------------------------------------------------
 template <class CT, int D, int BS, int G, int W, bool BALANCED>
-__global__ void __launch_bounds__(W * 32, (G >= 8 ? 2 : 3))
+__global__ void __launch_bounds__(W * 32, (G >= 8 ? 8 : 12) / W)
     decode_kernel(const DecodeArgs a) {
   using GE = Geo<CT, D, BS, G>;
   using SM = Smem<CT, D, BS, G, W>;

@@ -5,7 +5,7 @@
 
 namespace pkv {
 
-constexpr int kDecodeWarps = 4;  // consumer warps per CTA
+constexpr int kDecodeWarps = 1;  // warps per CTA: each warp is an independent worker
 
 struct DecodeKernel {
   const void* fn = nullptr;  // __global__ entry

@@ -20,7 +20,7 @@ __device__ unsigned int g_device_error_word;
 
 namespace {
 
-constexpr int kMaxCtasPerSm = 4;  // upper bound of the balanced grid, per SM
+constexpr int kMaxCtasPerSm = 16;  // upper bound of the balanced grid, per SM
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }

@@ -25,7 +25,7 @@
 // 16 MiB holds the merge counters (4 bytes per (sequence, kv-head unit)
 // segment) and two partial-result slots per warp of the balanced grid.  On a
 // 152-SM GB300 the grids these kernels run at need at most ~10 MB of slots
-// (8 query heads per unit, head_dim 128: 304 CTAs x 4 warps x 2 x 4160 bytes),
+// (8 query heads per unit, head_dim 128: 1216 one-warp CTAs x 2 x 4160 bytes),
 // which leaves room for about a million segments.  A call that needs more is
 // refused.
 #define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)
@@ -37,7 +37,7 @@ unsigned int* device_error_word(int dev);  // pkv_api.cu
 
 namespace {
 
-constexpr int kMaxCtasPerSmNoAlloc = 4;
+constexpr int kMaxCtasPerSmNoAlloc = 16;
 
 std::mutex g_mu;
 std::map<int, unsigned char*> g_scratch;             // device -> scratch address
