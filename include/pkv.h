@@ -57,6 +57,8 @@ typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2 } pkv_dtype;
 #define PKV_DEVERR_BAD_SLOT 0x2u       /* slot >= num_blocks * block_size */
 #define PKV_DEVERR_BAD_SEQ_LEN 0x4u    /* seq_len < 0 or beyond the table / hint */
 #define PKV_DEVERR_WAIT_TIMEOUT 0x8u   /* a bounded wait on an async copy gave up */
+#define PKV_DEVERR_SMEM_ALIGN 0x10u    /* shared memory not 1024-byte aligned for the swizzled
+                                          tiles: the decode kernel returned without work */
 
 /* Geometry and element type of one layer's K cache (the V cache is the same).
  * Supported: head_dim in {64, 128}; block_size in {8, 16, 32}; dtype any of

@@ -31,11 +31,12 @@ __all__ = [
     "split_kv_reduce",
     "gather_kv", "decode_workspace_bytes", "get_device_error", "library", "library_path",
     "DecodeWorkspace", "F32", "BF16", "FP8_E4M3", "DEVERR_BAD_BLOCK_ID", "DEVERR_BAD_SLOT",
-    "DEVERR_BAD_SEQ_LEN", "DEVERR_WAIT_TIMEOUT",
+    "DEVERR_BAD_SEQ_LEN", "DEVERR_WAIT_TIMEOUT", "DEVERR_SMEM_ALIGN",
 ]
 
 F32, BF16, FP8_E4M3 = 0, 1, 2
 DEVERR_BAD_BLOCK_ID, DEVERR_BAD_SLOT, DEVERR_BAD_SEQ_LEN, DEVERR_WAIT_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+DEVERR_SMEM_ALIGN = 0x10
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libpkv.so")

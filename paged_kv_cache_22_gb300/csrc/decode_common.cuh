@@ -1,0 +1,343 @@
+// decode_common.cuh -- what both paged decode kernels share: the argument
+// block, the tensor-map pair, the balanced split of the tile stream over the
+// warps of the grid, the walk over (sequence, kv-head unit) segments, and the
+// log-sum-exp merge of a segment that was cut between warps.
+//
+// The operation (per sequence s, query head qh, kv head h = qh / g):
+//   out[s][qh] = softmax_t(scale * q[s][qh] . K_s[t]) . V_s[t],  t < seq_len[s]
+// with K_s[t] = k_cache[block_tables[s][t / BS]][h][t % BS] -- the decode
+// attention of "Optimización de Inferencia LLM" (section "El Cuello de
+// Botella de Atención del que Nadie Habla"), read block by block through the
+// block table as "La despensa por casilleros" describes (section "El
+// mecanismo: bloques, block table y el gather del kernel"), accumulated with
+// an online softmax as the kernel sketch of "Optimización de Inferencia LLM"
+// (section "PagedAttention: Conceptos de SO se Encuentran con Memoria GPU")
+// prescribes, and split over the key axis with a log-sum-exp merge of the
+// partial results.
+#pragma once
+
+#include <math_constants.h>
+
+#include "pkv_device.cuh"
+
+namespace pkv {
+
+struct DecodeArgs {
+  unsigned int* err;  // device error word
+  void* out;
+  const void* q;
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
+  const int32_t* block_tables;
+  int64_t table_stride;  // max_blocks_per_seq
+  const int32_t* seq_lens;
+  int num_seqs;
+  int num_q_heads;
+  int num_kv_heads;
+  int num_blocks;
+  int group;         // g = Hq / Hkv
+  int units_per_kv;  // g / G: query-head chunks per kv head
+  int units;         // num_kv_heads * units_per_kv (segments per sequence)
+  int len_clip;      // longest admissible seq_len
+  float qk_scale;    // scale * log2(e) (* kv_scale for fp8 caches)
+  float out_scale;   // 1 (kv_scale for fp8 caches)
+  // balanced split
+  int* counters;     // [num_seqs * units], zero between calls
+  float* partials;   // [2 * warps][G * D + 2 * G]
+  // fixed partitions
+  int partition_blocks;
+  int max_partitions;
+  float* o_part;     // [B, Hq, P, D]
+  float* m_part;     // [B, Hq, P]
+  float* l_part;     // [B, Hq, P]
+};
+
+// Opaque TMA tensor maps of the K and V caches (the layout of CUtensorMap:
+// 128 bytes, 64-byte aligned), filled on the host by cuTensorMapEncodeTiled.
+// Each views a cache [num_blocks, Hkv, BS, D] as the 3-D tensor
+// (D, Hkv * BS, num_blocks), innermost first, with a box of one
+// (block, kv head) tile: (tma_box_bytes(D * E) / E, BS, 1).
+struct alignas(64) TmaMap {
+  uint64_t opaque[16];
+};
+struct TmaMaps {
+  TmaMap k, v;
+};
+
+// Bytes of the innermost box extent for cache rows of `row_bytes`: the
+// 128-byte swizzle span when the row is at least that long, else the row.
+__host__ __device__ constexpr int tma_box_bytes(int row_bytes) { return row_bytes >= 128 ? 128 : row_bytes; }
+
+// ----------------------------------------------------------------------------
+// Balanced split of T tiles over N workers.  With T >= N every worker gets
+// floor((c+1)T/N) - floor(cT/N) >= 1 tiles; with T < N the first T workers
+// get one tile each and the rest none, so a segment's tiles always lie on
+// consecutive non-empty workers (the merge counts its pieces as
+// last - first + 1).
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ int64_t range_start(int64_t c, int64_t T, int64_t N) {
+  return T >= N ? c * T / N : (c < T ? c : T);
+}
+
+// The worker whose range holds tile u (0 <= u < T).
+__device__ __forceinline__ int64_t owner_of(int64_t u, int64_t T, int64_t N) {
+  return T >= N ? ((u + 1) * N - 1) / T : u;
+}
+
+// ----------------------------------------------------------------------------
+// Walk over the (sequence, unit) segments that intersect a tile range.  All
+// lanes of a warp hold the same state.
+// ----------------------------------------------------------------------------
+struct Walker {
+  int s, unit, nb;
+  int64_t base;    // linear index of sequence s's first tile
+  int64_t seg_u;   // linear index of segment (s, unit)'s first tile
+  int jb, je;      // piece = blocks [jb, je) of the segment
+  bool done;
+};
+
+template <int BS>
+__device__ __forceinline__ int seq_blocks(const DecodeArgs& a, int s) {
+  int L = __ldg(a.seq_lens + s);
+  if (L < 0 || L > a.len_clip) {
+    raise_error(a.err, PKV_DEVERR_BAD_SEQ_LEN);
+    L = L < 0 ? 0 : a.len_clip;
+  }
+  return (L + BS - 1) / BS;
+}
+
+__device__ __forceinline__ int seq_len_clipped(const DecodeArgs& a, int s) {
+  int L = __ldg(a.seq_lens + s);
+  return L < 0 ? 0 : (L > a.len_clip ? a.len_clip : L);
+}
+
+template <int BS>
+__device__ __forceinline__ void walker_settle(Walker& wk, const DecodeArgs& a, int64_t u1) {
+  // Move forward to the first segment with blocks left before u1.
+  while (!wk.done) {
+    if (wk.nb > 0) {
+      wk.seg_u = wk.base + (int64_t)wk.unit * wk.nb;
+      if (wk.seg_u >= u1) { wk.done = true; break; }
+      int64_t left = u1 - wk.seg_u;
+      wk.je = (int64_t)wk.nb < left ? wk.nb : (int)left;
+      if (wk.jb < wk.je) break;
+    }
+    wk.jb = 0;
+    if (wk.nb > 0 && ++wk.unit < a.units) continue;
+    wk.base += (int64_t)wk.nb * a.units;
+    wk.unit = 0;
+    if (++wk.s >= a.num_seqs) { wk.done = true; break; }
+    wk.nb = seq_blocks<BS>(a, wk.s);
+  }
+}
+
+template <int BS>
+__device__ __forceinline__ void walker_next_piece(Walker& wk, const DecodeArgs& a, int64_t u1) {
+  wk.jb = wk.je;  // past the current piece
+  if (wk.je < wk.nb) { wk.done = true; return; }  // the range ended inside this segment
+  wk.jb = 0;
+  if (++wk.unit >= a.units) {
+    wk.unit = 0;
+    wk.base += (int64_t)wk.nb * a.units;
+    if (++wk.s >= a.num_seqs) { wk.done = true; return; }
+    wk.nb = seq_blocks<BS>(a, wk.s);
+  }
+  walker_settle<BS>(wk, a, u1);
+}
+
+// ----------------------------------------------------------------------------
+// This warp's work.  Balanced mode: the warp's range [u0, u1) of the linear
+// tile stream (T tiles in all) and the walker on its first piece; rows of
+// empty sequences are zeroed on the way.  Fixed-partition mode: warp gw takes
+// partition gw % P of segment gw / P.  False when the warp has nothing to do.
+// ----------------------------------------------------------------------------
+template <class QT, int D, int BS, bool BALANCED>
+__device__ __forceinline__ bool plan_warp(const DecodeArgs& a, int64_t gw, int64_t NW, int lane, Walker& wk0,
+                                          int64_t& u0, int64_t& u1, int64_t& T) {
+  T = 0;
+  if constexpr (BALANCED) {
+    // sequences of length 0 get a zero row (spread over the warps)
+    for (int64_t s = gw; s < a.num_seqs; s += NW) {
+      if (seq_len_clipped(a, (int)s) == 0) {
+        QT* o = reinterpret_cast<QT*>(a.out) + (size_t)s * a.num_q_heads * D;
+        for (int i = lane; i < a.num_q_heads * D; i += 32) o[i] = from_f32<QT>(0.f);
+      }
+    }
+    // total tiles, this warp's range, and the sequence holding its first tile
+    int64_t mine = 0;
+    for (int s = lane; s < a.num_seqs; s += 32) mine += seq_blocks<BS>(a, s);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, off);
+    T = mine * a.units;
+    u0 = range_start(gw, T, NW);
+    u1 = range_start(gw + 1, T, NW);
+    if (u0 >= u1) return false;
+    int s0 = a.num_seqs;
+    int64_t p0 = 0, run = 0;  // tiles before the current chunk of 32 sequences
+    for (int s = 0; s < a.num_seqs; s += 32) {
+      const int64_t n = (s + lane < a.num_seqs) ? (int64_t)seq_blocks<BS>(a, s + lane) * a.units : 0;
+      int64_t incl = n;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int64_t t = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += t;
+      }
+      const int64_t excl = incl - n;
+      const unsigned hit = __ballot_sync(0xffffffffu, n > 0 && run + excl <= u0 && u0 < run + incl);
+      if (hit) {
+        const int src = __ffs(hit) - 1;
+        s0 = s + src;
+        p0 = __shfl_sync(0xffffffffu, run + excl, src);
+        break;
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (s0 >= a.num_seqs) return false;  // cannot happen for u0 < T
+    wk0.s = s0;
+    wk0.base = p0;
+    wk0.nb = seq_blocks<BS>(a, s0);
+    const int64_t off = u0 - p0;
+    wk0.unit = (int)(off / wk0.nb);
+    wk0.jb = (int)(off % wk0.nb);
+    wk0.done = false;
+    walker_settle<BS>(wk0, a, u1);
+    return true;
+  } else {
+    // fixed partition p of segment seg, one per warp
+    const int64_t segs = (int64_t)a.num_seqs * a.units;
+    if (gw >= segs * a.max_partitions) return false;
+    const int64_t seg = gw / a.max_partitions;
+    const int p = (int)(gw % a.max_partitions);
+    const int s = (int)(seg / a.units), unit = (int)(seg % a.units);
+    const int nb = seq_blocks<BS>(a, s);
+    const int jb = p * a.partition_blocks;
+    const int je = min(nb, jb + a.partition_blocks);
+    if (jb >= je) return false;
+    wk0.s = s;
+    wk0.unit = unit;
+    wk0.nb = nb;
+    wk0.base = 0;
+    wk0.seg_u = (int64_t)unit * nb;
+    wk0.jb = jb;
+    wk0.je = je;
+    wk0.done = false;
+    u0 = wk0.seg_u + jb;
+    u1 = wk0.seg_u + je;
+    return true;
+  }
+}
+
+// First query head of the unit a walker stands on.
+__device__ __forceinline__ int unit_first_head(const DecodeArgs& a, const Walker& wk, int G) {
+  const int kvh = wk.unit / a.units_per_kv, chunk = wk.unit % a.units_per_kv;
+  return kvh * a.group + chunk * G;
+}
+
+// The partial-result slot of the piece a walker stands on: two per warp, the
+// first for a piece that starts exactly at the warp's range (the tail of a
+// segment begun by earlier warps), the second for any later piece.
+template <int G, int D>
+__device__ __forceinline__ float* partial_slot(const DecodeArgs& a, const Walker& wk, int64_t gw, int64_t u0) {
+  const int64_t slot = (wk.seg_u + wk.jb == u0) ? 2 * gw : 2 * gw + 1;
+  return a.partials + (size_t)slot * (G * D + 2 * G);
+}
+
+// ----------------------------------------------------------------------------
+// A segment cut between warps.  The caller has written its piece's
+// unnormalised (acc[G][D], m[G] in log2 units, l[G]) to its slot.  Take the
+// segment's ticket; the last of its pieces to arrive combines all of them by
+// log-sum-exp and writes the output rows (lane-parallel: lanes take slots for
+// the maxima and weights, then lanes < D / 4 own 4 dims each).
+// ----------------------------------------------------------------------------
+template <class QT, int G, int D>
+__device__ __forceinline__ void ticket_and_merge(const DecodeArgs& a, const Walker& wk, int64_t T, int64_t NW,
+                                                 int lane) {
+  constexpr int SLOT = G * D + 2 * G, DV = 4, SL = D / DV;
+  const int d0 = (lane % SL) * DV;
+  __syncwarp();
+  __threadfence();
+  const int64_t seg_id = (int64_t)wk.s * a.units + wk.unit;
+  const int64_t w_first = owner_of(wk.seg_u, T, NW), w_last = owner_of(wk.seg_u + wk.nb - 1, T, NW);
+  int last = 0;
+  if (lane == 0) {
+    const int ticket = atomicAdd(a.counters + seg_id, 1);
+    last = (ticket == (int)(w_last - w_first));
+    if (last) a.counters[seg_id] = 0;  // ready for the next call
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return;
+  __threadfence();
+  // pieces sit on warps w_first..w_last; the first one's slot depends on
+  // whether the segment starts exactly at that warp's range
+  const int64_t n = w_last - w_first + 1;
+  const int64_t first_slot = (wk.seg_u != range_start(w_first, T, NW)) ? 2 * w_first + 1 : 2 * w_first;
+  auto slot_of = [&](int64_t i) -> const float* {
+    return a.partials + (size_t)(i == 0 ? first_slot : 2 * (w_first + i)) * SLOT;
+  };
+  // maxima: lanes take slots in parallel
+  float M[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) M[h] = -CUDART_INF_F;
+  for (int64_t i = lane; i < n; i += 32) {
+    const float* pp = slot_of(i);
+#pragma unroll
+    for (int h = 0; h < G; ++h) M[h] = fmaxf(M[h], ld_cg(pp + G * D + h));
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M[h] = fmaxf(M[h], __shfl_xor_sync(0xffffffffu, M[h], off));
+    if (M[h] == -CUDART_INF_F) M[h] = 0.f;
+  }
+  float den[G], num[G][DV];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    den[h] = 0.f;
+#pragma unroll
+    for (int d = 0; d < DV; ++d) num[h][d] = 0.f;
+  }
+  for (int64_t base = 0; base < n; base += 32) {
+    // lane i holds the weights of slot base + i
+    float f[G];
+    if (base + lane < n) {
+      const float* pp = slot_of(base + lane);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        f[h] = fast_exp2(ld_cg(pp + G * D + h) - M[h]);
+        den[h] += f[h] * ld_cg(pp + G * D + G + h);
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < G; ++h) f[h] = 0.f;
+    }
+    const int cnt = (int)(n - base < 32 ? n - base : 32);
+#pragma unroll 4
+    for (int jj = 0; jj < cnt; ++jj) {
+      const float* pp = slot_of(base + jj);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float fj = __shfl_sync(0xffffffffu, f[h], jj);
+        if (lane < SL) {
+          const float4 v = ld_cg(reinterpret_cast<const float4*>(pp + h * D + d0));
+          num[h][0] += fj * v.x;
+          num[h][1] += fj * v.y;
+          num[h][2] += fj * v.z;
+          num[h][3] += fj * v.w;
+        }
+      }
+    }
+  }
+  QT* out = reinterpret_cast<QT*>(a.out) + ((size_t)wk.s * a.num_q_heads + unit_first_head(a, wk, G)) * D;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) den[h] += __shfl_xor_sync(0xffffffffu, den[h], off);
+    if (lane < SL) {
+      const float inv = den[h] > 0.f ? a.out_scale / den[h] : 0.f;
+#pragma unroll
+      for (int d = 0; d < DV; ++d) out[h * D + d0 + d] = from_f32<QT>(num[h][d] * inv);
+    }
+  }
+}
+
+}  // namespace pkv

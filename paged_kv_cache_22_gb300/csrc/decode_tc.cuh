@@ -1,0 +1,613 @@
+// decode_tc.cuh -- paged decode attention on the tensor cores (bf16 and
+// fp8-e4m3 caches).
+//
+// Computes what decode_common.cuh states.  The two contractions of a decode
+// step are dense once grouped-query heads are stacked: the G query heads of a
+// kv head against one tile of K (G x D times D x 16 tokens) and their
+// probabilities against the tile of V (G x 16 times 16 x D).  On the CUDA
+// cores each element of K and V costs a widening and a fused multiply-add per
+// query head, which makes decode issue-bound long before HBM is saturated;
+// here both contractions run as mma.sync m16n8k16 with fp32 accumulation, so
+// a 16-token tile costs about a hundred warp instructions.
+//
+// Design (GB300):
+//  * Tiles arrive by TMA tensor copies (cp.async.bulk.tensor.3d) of one
+//    (block, kv head) tile of K and of V, the cache viewed as the tensor
+//    (D, Hkv * BS, num_blocks) with a 128-byte (64-byte for 64-byte rows)
+//    swizzle, so that the 8 rows an ldmatrix phase reads fall in 8 distinct
+//    bank groups.  Each warp is an independent worker with its own ring of
+//    NSW stages and mbarriers, exactly as in the CUDA-core kernel; the
+//    balanced split and the ticket merge are shared with it.
+//  * Rows of the m16 operand are the G query heads (G <= 8; rows G..15 are
+//    zero and their results dropped).  Lane (g, t) = (lane / 4, lane % 4)
+//    owns row g: its running max, its share of the row sum and its 2 x D / 8
+//    accumulators.
+//  * q.K: A = q (registers, loaded once per piece), B = K tile through
+//    ldmatrix (K rows are the n index, head dims the k index).  Scores are
+//    scaled in fp32, masked past the sequence end, and enter an online
+//    softmax in log2 units; the rescale of the accumulators is a warp-uniform
+//    branch taken only when some row's max grew.
+//  * P.V: the probabilities leave the q.K accumulators already in the A
+//    operand layout of the next contraction (row g, tokens 2t, 2t+1, 2t+8,
+//    2t+9).  bf16: P is split into a bf16 head and a bf16 remainder, two MMAs
+//    per n-tile, so P keeps ~16 significant bits; V arrives through
+//    ldmatrix.trans.  fp8: K and V codes widen exactly to fp16 (cvt
+//    e4m3x2 -> f16x2) and P is fp16; q is fp16, pre-scaled by a power of two
+//    chosen per piece so that it cannot overflow, the factor moved to the
+//    fp32 score scale.  For fp8 V the n index is permuted so that a lane's
+//    four token rows are read as 16 contiguous bytes each: output column n of
+//    n-tile j is head dim (D / 8) * n + j.
+#pragma once
+
+#include "decode_common.cuh"
+
+namespace pkv {
+
+// ----------------------------------------------------------------------------
+// Instruction wrappers.
+// ----------------------------------------------------------------------------
+
+// One box of a 3-D tensor map into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(void* dst, const TmaMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+// c[16x8] += A[16x16] . B[16x8] with rows 8..15 of A zero: a0 / a2 are the
+// row-g halves (k 2t..2t+1 / 2t+8..2t+9), c0 / c1 columns 2t, 2t+1 of row g.
+template <bool F16>
+__device__ __forceinline__ void mma_k16(float& c0, float& c1, uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  float x2, x3;
+  if constexpr (F16) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %5}, {%7, %8}, "
+        "{%0, %1, %9, %9};"
+        : "+f"(c0), "+f"(c1), "=f"(x2), "=f"(x3)
+        : "r"(a0), "r"(0u), "r"(a2), "r"(b0), "r"(b1), "f"(0.f));
+  } else {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %5}, {%7, %8}, "
+        "{%0, %1, %9, %9};"
+        : "+f"(c0), "+f"(c1), "=f"(x2), "=f"(x3)
+        : "r"(a0), "r"(0u), "r"(a2), "r"(b0), "r"(b1), "f"(0.f));
+  }
+}
+
+// c[16x8] += A[16x8] . B[8x8] (bf16), rows 8..15 of A zero.
+__device__ __forceinline__ void mma_k8_bf16(float& c0, float& c1, uint32_t a0, uint32_t b0) {
+  float x2, x3;
+  asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5}, {%6}, {%0, %1, %7, %7};"
+      : "+f"(c0), "+f"(c1), "=f"(x2), "=f"(x3)
+      : "r"(a0), "r"(0u), "r"(b0), "f"(0.f));
+}
+
+// (lo, hi) -> packed pair, lo in bits 0..15.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Four e4m3 codes -> two exact fp16 pairs: bytes (0, 1) -> lo, (2, 3) -> hi.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+// ----------------------------------------------------------------------------
+// Geometry.
+// ----------------------------------------------------------------------------
+template <class CT, int D, int BS, int G>
+struct TcGeo {
+  static constexpr bool F8 = CT::kBytes == 1;
+  static constexpr int E = CT::kBytes;
+  static constexpr int ROW = D * E;              // bytes of one token row
+  static constexpr int IB = tma_box_bytes(ROW);  // bytes of a box row = swizzle span
+  static constexpr int NBX = ROW / IB;           // boxes per tile
+  static constexpr int BOX = BS * IB;            // bytes of one box
+  static constexpr int TILE = BS * ROW;          // bytes of one (block, kv head) tile
+  static constexpr int STAGE = 2 * TILE;         // K tile then V tile
+  static constexpr int TB = BS < 16 ? BS : 16;   // tokens per compute step
+  static constexpr int STEPS = BS / TB;
+  static constexpr int NTS = TB / 8;             // score n-tiles per step
+  static constexpr int KS = D / 16;              // k-steps of q.K
+  static constexpr int NTO = D / 8;              // output n-tiles
+  static constexpr int VPL = D / 8;              // fp8 V: bytes of a token row per lane
+  static constexpr int NSW0 = 16384 / STAGE;
+  static constexpr int NSW = NSW0 < 2 ? 2 : (NSW0 > 8 ? 8 : NSW0);  // stages per warp
+  static_assert(G >= 1 && G <= 8, "at most 8 query heads per m16 row block");
+  static_assert(IB == 128 || IB == 64, "swizzle span");
+  static_assert(ROW % IB == 0 && KS % 2 == 0, "tile shape");
+  static_assert(!F8 || TB == 16, "fp8 caches: 16-token steps");
+  static_assert(TB == 8 || TB == 16, "compute step");
+  static_assert(STAGE % 1024 == 0 && BOX % 512 == 0, "stages and boxes keep the swizzle phase");
+};
+
+template <class CT, int D, int BS, int G, int W>
+struct TcSmem {
+  using GE = TcGeo<CT, D, BS, G>;
+  static constexpr size_t kStages = 0;  // 1024-byte aligned
+  static constexpr size_t kQBuf = kStages + (size_t)W * GE::NSW * GE::STAGE;
+  static constexpr size_t kBars = (kQBuf + (size_t)W * 2 * G * D * sizeof(__nv_bfloat16) + 7) / 8 * 8;
+  static constexpr size_t kQBars = kBars + (size_t)W * GE::NSW * 8;
+  static constexpr size_t kOk = kQBars + (size_t)W * 2 * 8;
+  static constexpr size_t kBytes = kOk + (size_t)W * GE::NSW * 4;
+};
+
+// Byte offset, within a tile, of 16-byte chunk c of token row `row` as the
+// swizzled tensor copy lays it out: chunk index XOR the 128-byte line index
+// (bits 4..6 ^= bits 7..9; for 64-byte spans bits 4..5 ^= bits 7..8).
+template <class GE>
+__device__ __forceinline__ uint32_t swz(int row, int c) {
+  constexpr int CPB = GE::IB / 16;
+  const uint32_t off = (uint32_t)((c / CPB) * GE::BOX + row * GE::IB + (c % CPB) * 16);
+  constexpr uint32_t M = GE::IB == 128 ? 7u : 3u;
+  return off ^ (((off >> 7) & M) << 4);
+}
+
+// ----------------------------------------------------------------------------
+// The kernel.
+// ----------------------------------------------------------------------------
+template <class CT, int D, int BS, int G, int W, bool BALANCED>
+__global__ void __launch_bounds__(W * 32, 8 / W)
+    decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ TmaMaps maps) {
+  using GE = TcGeo<CT, D, BS, G>;
+  using SM = TcSmem<CT, D, BS, G, W>;
+  using QT = typename CT::QType;
+  constexpr bool F8 = GE::F8;
+  constexpr int NSW = GE::NSW, TB = GE::TB, KS = GE::KS, NTO = GE::NTO, TILE = GE::TILE, STAGE = GE::STAGE;
+
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  if (smem_addr(smem) & 1023u) {  // the swizzle phase needs 1024-byte aligned stages
+    if (threadIdx.x == 0) raise_error(a.err, PKV_DEVERR_SMEM_ALIGN);
+    return;
+  }
+  uint8_t* stages = smem + SM::kStages + (size_t)w * NSW * STAGE;
+  const uint32_t stages_s = smem_addr(stages);
+  QT* qbuf = reinterpret_cast<QT*>(smem + SM::kQBuf) + (size_t)w * 2 * G * D;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::kBars) + w * NSW;
+  uint64_t* qbars = reinterpret_cast<uint64_t*>(smem + SM::kQBars) + w * 2;
+  int* stage_ok = reinterpret_cast<int*>(smem + SM::kOk) + w * NSW;
+
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < NSW; ++i) mbar_init(&bars[i], 1);
+    mbar_init(&qbars[0], 1);
+    mbar_init(&qbars[1], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();  // the only block-wide barrier: warps are independent from here on
+
+  const int64_t gw = (int64_t)blockIdx.x * W + w;
+  const int64_t NW = (int64_t)gridDim.x * W;
+  int64_t u0 = 0, u1 = 0, T = 0;
+  Walker wk0;
+  if (!plan_warp<QT, D, BS, BALANCED>(a, gw, NW, lane, wk0, u0, u1, T)) return;
+
+  // ---------------------------------------------------------------- issue side
+  Walker cw = wk0;
+  int cj = wk0.jb;
+  int32_t next_id = __ldg(a.block_tables + (size_t)cw.s * a.table_stride + cj);
+  int issued = 0;
+
+  auto issue_next = [&]() {
+    if (cw.done) return;
+    const int st = issued % NSW;
+    if (lane == 0) {
+      const int kvh = cw.unit / a.units_per_kv;
+      uint8_t* dst = stages + (size_t)st * STAGE;
+      uint64_t* bar = &bars[st];
+      if (next_id >= 0 && next_id < a.num_blocks) {
+        stage_ok[st] = 1;
+        mbar_arrive_expect_tx(bar, STAGE);
+#pragma unroll
+        for (int bx = 0; bx < GE::NBX; ++bx) {
+          tma_load_3d(dst + bx * GE::BOX, &maps.k, bx * (GE::IB / GE::E), kvh * BS, next_id, bar);
+          tma_load_3d(dst + TILE + bx * GE::BOX, &maps.v, bx * (GE::IB / GE::E), kvh * BS, next_id, bar);
+        }
+      } else {
+        raise_error(a.err, PKV_DEVERR_BAD_BLOCK_ID);
+        stage_ok[st] = 0;
+        mbar_arrive(bar);
+      }
+    }
+    ++issued;
+    if (++cj >= cw.je) {
+      walker_next_piece<BS>(cw, a, u1);
+      cj = cw.jb;
+    }
+    if (!cw.done) next_id = __ldg(a.block_tables + (size_t)cw.s * a.table_stride + cj);
+  };
+
+  auto issue_q = [&](const Walker& pw, int slot) {
+    const QT* src = reinterpret_cast<const QT*>(a.q) + ((size_t)pw.s * a.num_q_heads + unit_first_head(a, pw, G)) * D;
+    mbar_arrive_expect_tx(&qbars[slot], G * D * sizeof(QT));
+    bulk_g2s(qbuf + (size_t)slot * G * D, src, G * D * sizeof(QT), &qbars[slot]);
+  };
+
+  Walker qlook = wk0;
+  if (lane == 0) issue_q(wk0, 0);
+  // Everything above reads only the step's inputs (lengths, tables, q).  When
+  // this grid is the programmatic dependent of the cache write, the K/V tiles
+  // must wait for that grid; on an ordinary launch this returns at once.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+#pragma unroll 1
+  for (int i = 0; i < NSW; ++i) issue_next();
+
+  // Per-lane fragment addresses.  A lane reads 16-byte chunk C + h of token
+  // row `row`, C a compile-time multiple of the lane part h's range, so the
+  // swizzled offset is (lane base) XOR ((C % CPB) << 4) plus the box of C:
+  // only the base is kept in a register.
+  //  q.K, bf16, 16-token steps: rows (0-7 | 8-15) x chunks (2kk | 2kk+1);
+  //  q.K, bf16, 8-token steps: rows 0-7 x chunks 4kq..4kq+3;
+  //  q.K, fp8: rows (0-7 | 8-15) x chunks (2kq | 2kq+1), a chunk = 16 dims;
+  //  P.V, bf16 (ldmatrix.trans): rows (0-7 | 8-15) x chunks (2j | 2j+1), or
+  //  rows 0-7 x chunks 4j..4j+3 for 8-token steps;
+  //  P.V, fp8: rows 2t, 2t+1, 2t+8, 2t+9 at this lane's VPL bytes.
+  auto lane_base = [](int row, int h) -> uint32_t { return swz<GE>(row, h); };
+  uint32_t kx, vx = 0;
+  if constexpr (F8) {
+    kx = lane_base((lane & 7) + 8 * ((lane >> 3) & 1), lane >> 4);
+  } else if constexpr (TB == 16) {
+    kx = lane_base((lane & 7) + 8 * (lane >> 4), (lane >> 3) & 1);
+    vx = lane_base((lane & 7) + 8 * ((lane >> 3) & 1), lane >> 4);
+  } else {
+    kx = lane_base(lane & 7, lane >> 3);
+    vx = lane_base(lane & 7, lane >> 3);
+  }
+  constexpr int CPB = GE::IB / 16;  // chunks per box row
+  // address of chunk C (+ the lane part) relative to a 1024-byte aligned tile base
+  auto frag = [](uint32_t base, int C) -> uint32_t {
+    return (base ^ (uint32_t)((C % CPB) << 4)) + (uint32_t)((C / CPB) * GE::BOX);
+  };
+  uint32_t voff8[4] = {0, 0, 0, 0};
+  if constexpr (F8) {
+    const int c = (g * GE::VPL) / 16, b = (g * GE::VPL) % 16;
+    voff8[0] = swz<GE>(2 * t, c) + b;
+    voff8[1] = swz<GE>(2 * t + 1, c) + b;
+    voff8[2] = swz<GE>(2 * t + 8, c) + b;
+    voff8[3] = swz<GE>(2 * t + 9, c) + b;
+  }
+
+  // ---------------------------------------------------------------- consume side
+  Walker wk = wk0;
+  int consumed = 0, waited = 0, piece = 0;
+  bool alive = true;
+  uint32_t qa[KS][2];     // q.K A operand: row g, (a0, a2) per k-step
+  float o[NTO][2];        // accumulators: row g, columns 2t, 2t+1 of each n-tile
+  float m_run, l_run;     // row g's running max (log2 units) and this lane's share of its sum
+
+#pragma unroll 1
+  while (!wk.done) {
+    const int qslot = piece & 1;
+    {  // prefetch the next piece's q while this one runs
+      Walker nx = qlook;
+      walker_next_piece<BS>(nx, a, u1);
+      if (!nx.done && lane == 0) {
+        fence_proxy_async_smem();
+        issue_q(nx, qslot ^ 1);
+      }
+      qlook = nx;
+    }
+    if (!mbar_wait_bounded(&qbars[qslot], (piece >> 1) & 1, a.err)) alive = false;
+    float qk_mul = a.qk_scale;
+    {
+      const QT* qs = qbuf + (size_t)qslot * G * D + (size_t)(g < G ? g : 0) * D;
+      if constexpr (!F8) {
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+          qa[kk][0] = g < G ? *reinterpret_cast<const uint32_t*>(qs + 16 * kk + 2 * t) : 0u;
+          qa[kk][1] = g < G ? *reinterpret_cast<const uint32_t*>(qs + 16 * kk + 2 * t + 8) : 0u;
+        }
+      } else {
+        // k-step kk holds dims 16kk + 4t + (0, 1) in a0 and + (2, 3) in a2,
+        // the order in which a K chunk reaches the lane through ldmatrix
+        float qv[KS][4];
+        float mq = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+          const uint2 raw = *reinterpret_cast<const uint2*>(qs + 16 * kk + 4 * t);
+          const float2 lo = bf16x2_to_f2(raw.x), hi = bf16x2_to_f2(raw.y);
+          qv[kk][0] = g < G ? lo.x : 0.f;
+          qv[kk][1] = g < G ? lo.y : 0.f;
+          qv[kk][2] = g < G ? hi.x : 0.f;
+          qv[kk][3] = g < G ? hi.y : 0.f;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) mq = fmaxf(mq, fabsf(qv[kk][i]));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mq = fmaxf(mq, __shfl_xor_sync(0xffffffffu, mq, off));
+        // fp16 tops out at 65504: scale q by 2^-sh so that |q| < 2^15
+        int e = 0;
+        frexpf(mq, &e);
+        const int sh = e > 15 ? (e - 15 < 100 ? e - 15 : 100) : 0;
+        const float down = ldexpf(1.f, -sh);
+        qk_mul = a.qk_scale * ldexpf(1.f, sh);
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+          qa[kk][0] = pack_f16x2(qv[kk][0] * down, qv[kk][1] * down);
+          qa[kk][1] = pack_f16x2(qv[kk][2] * down, qv[kk][3] * down);
+        }
+      }
+    }
+#pragma unroll
+    for (int n = 0; n < NTO; ++n) o[n][0] = o[n][1] = 0.f;
+    m_run = -CUDART_INF_F;
+    l_run = 0.f;
+    const int L = seq_len_clipped(a, wk.s);
+
+#pragma unroll 1
+    for (int j = wk.jb; j < wk.je; ++j) {
+      const int st = consumed % NSW;
+      bool ok = false;
+      if (alive && consumed < issued) {
+        ok = mbar_wait_bounded(&bars[st], (consumed / NSW) & 1, a.err);
+        waited = consumed + 1;
+        if (!ok) alive = false;
+      }
+      ok = ok && stage_ok[st];
+      const int valid = ok ? min(BS, L - j * BS) : 0;
+
+#pragma unroll
+      for (int step = 0; step < GE::STEPS; ++step) {
+        const uint32_t kt = stages_s + (uint32_t)(st * STAGE + step * TB * GE::IB);
+        const uint32_t vt = kt + TILE;
+        const int vstep = valid - step * TB;  // valid tokens in this step (may be <= 0 or > TB)
+
+        // ---- scores: s[n][e] = q_g . K[8n + 2t + e]
+        float s[GE::NTS][2];
+        if constexpr (TB == 16) {
+          float s2[2][2][2] = {};  // even / odd k-steps, two independent chains
+          if constexpr (F8) {
+#pragma unroll
+            for (int kq = 0; kq < KS / 2; ++kq) {
+              uint32_t r[4];
+              ldsm_x4(frag(kt + kx, 2 * kq), r);
+              uint32_t b[4][2];
+#pragma unroll
+              for (int m = 0; m < 4; ++m) e4m3x4_to_f16x2x2(r[m], b[m][0], b[m][1]);
+              // r[0]: rows 0-7, k-step 2kq; r[1]: rows 8-15, 2kq; r[2], r[3]: k-step 2kq + 1
+              mma_k16<true>(s2[0][0][0], s2[0][0][1], qa[2 * kq][0], qa[2 * kq][1], b[0][0], b[0][1]);
+              mma_k16<true>(s2[0][1][0], s2[0][1][1], qa[2 * kq][0], qa[2 * kq][1], b[1][0], b[1][1]);
+              mma_k16<true>(s2[1][0][0], s2[1][0][1], qa[2 * kq + 1][0], qa[2 * kq + 1][1], b[2][0], b[2][1]);
+              mma_k16<true>(s2[1][1][0], s2[1][1][1], qa[2 * kq + 1][0], qa[2 * kq + 1][1], b[3][0], b[3][1]);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+              uint32_t r[4];
+              ldsm_x4(frag(kt + kx, 2 * kk), r);
+              // r[0], r[1]: rows 0-7 (b0, b1); r[2], r[3]: rows 8-15
+              mma_k16<false>(s2[kk & 1][0][0], s2[kk & 1][0][1], qa[kk][0], qa[kk][1], r[0], r[1]);
+              mma_k16<false>(s2[kk & 1][1][0], s2[kk & 1][1][1], qa[kk][0], qa[kk][1], r[2], r[3]);
+            }
+          }
+#pragma unroll
+          for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) s[n][e] = s2[0][n][e] + s2[1][n][e];
+        } else {
+          float s2[2][2] = {};
+#pragma unroll
+          for (int kq = 0; kq < KS / 2; ++kq) {
+            uint32_t r[4];
+            ldsm_x4(frag(kt + kx, 4 * kq), r);
+            // rows 0-7; r[0], r[1]: k-step 2kq; r[2], r[3]: k-step 2kq + 1
+            mma_k16<false>(s2[0][0], s2[0][1], qa[2 * kq][0], qa[2 * kq][1], r[0], r[1]);
+            mma_k16<false>(s2[1][0], s2[1][1], qa[2 * kq + 1][0], qa[2 * kq + 1][1], r[2], r[3]);
+          }
+          s[0][0] = s2[0][0] + s2[1][0];
+          s[0][1] = s2[0][1] + s2[1][1];
+        }
+
+        // ---- online softmax of row g (log2 units)
+        float mx = -CUDART_INF_F;
+#pragma unroll
+        for (int n = 0; n < GE::NTS; ++n)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int tok = 8 * n + 2 * t + e;
+            s[n][e] = tok < vstep ? s[n][e] * qk_mul : -CUDART_INF_F;
+            mx = fmaxf(mx, s[n][e]);
+          }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m_run, mx);
+        if (__any_sync(0xffffffffu, m_new > m_run)) {
+          const float alpha = m_new > m_run ? fast_exp2(m_run - m_new) : 1.f;
+          const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+          for (int n = 0; n < NTO; ++n) {
+            const float2 v = __fmul2_rn(make_float2(o[n][0], o[n][1]), a2);
+            o[n][0] = v.x;
+            o[n][1] = v.y;
+          }
+          l_run *= alpha;
+          m_run = m_new;
+        }
+        const float m_use = m_run == -CUDART_INF_F ? 0.f : m_run;
+        float p[GE::NTS][2];
+#pragma unroll
+        for (int n = 0; n < GE::NTS; ++n)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            p[n][e] = fast_exp2(s[n][e] - m_use);
+            l_run += p[n][e];
+          }
+
+        // ---- P . V
+        const bool full = vstep >= TB;
+        if constexpr (F8) {
+          const uint32_t pa0 = pack_f16x2(p[0][0], p[0][1]), pa2 = pack_f16x2(p[1][0], p[1][1]);
+          static_assert(GE::VPL == 16 || GE::VPL == 8, "fp8 V slice");
+          uint32_t X[4][GE::VPL / 4];  // rows 2t, 2t+1, 2t+8, 2t+9
+#pragma unroll
+          for (int ri = 0; ri < 4; ++ri) {
+            const uint8_t* src = stages + (vt - stages_s) + voff8[ri];
+            if constexpr (GE::VPL == 16) {
+              const uint4 v = *reinterpret_cast<const uint4*>(src);
+              X[ri][0] = v.x; X[ri][1] = v.y; X[ri][2] = v.z; X[ri][3] = v.w;
+            } else {
+              const uint2 v = *reinterpret_cast<const uint2*>(src);
+              X[ri][0] = v.x; X[ri][1] = v.y;
+            }
+          }
+          if (!full) {  // rows past the end may hold NaN codes: their weight is 0, drop them too
+            const int rows[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+#pragma unroll
+            for (int ri = 0; ri < 4; ++ri)
+#pragma unroll
+              for (int q = 0; q < GE::VPL / 4; ++q) X[ri][q] = rows[ri] < vstep ? X[ri][q] : 0u;
+          }
+#pragma unroll
+          for (int q = 0; q < GE::VPL / 4; ++q) {
+            // byte k of the lane's slice is n-tile k: pair the two rows of each
+            // B register byte by byte, then widen
+            uint32_t b0[4], b1[4];
+            e4m3x4_to_f16x2x2(__byte_perm(X[0][q], X[1][q], 0x5140), b0[0], b0[1]);
+            e4m3x4_to_f16x2x2(__byte_perm(X[0][q], X[1][q], 0x7362), b0[2], b0[3]);
+            e4m3x4_to_f16x2x2(__byte_perm(X[2][q], X[3][q], 0x5140), b1[0], b1[1]);
+            e4m3x4_to_f16x2x2(__byte_perm(X[2][q], X[3][q], 0x7362), b1[2], b1[3]);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mma_k16<true>(o[4 * q + k][0], o[4 * q + k][1], pa0, pa2, b0[k], b1[k]);
+          }
+        } else {
+          // P = head + remainder, both bf16
+          uint32_t ph[GE::NTS], pl[GE::NTS];
+#pragma unroll
+          for (int n = 0; n < GE::NTS; ++n) {
+            ph[n] = pack_bf16x2(p[n][0], p[n][1]);
+            const float2 h = bf16x2_to_f2(ph[n]);
+            pl[n] = pack_bf16x2(p[n][0] - h.x, p[n][1] - h.y);
+          }
+          // keep-masks of this lane's token pairs (2t, 2t+1) and (2t+8, 2t+9)
+          uint32_t keep0 = 0xFFFFFFFFu, keep1 = 0xFFFFFFFFu;
+          if (!full) {
+            keep0 = (2 * t < vstep ? 0x0000FFFFu : 0u) | (2 * t + 1 < vstep ? 0xFFFF0000u : 0u);
+            keep1 = (2 * t + 8 < vstep ? 0x0000FFFFu : 0u) | (2 * t + 9 < vstep ? 0xFFFF0000u : 0u);
+          }
+          if constexpr (TB == 16) {
+#pragma unroll
+            for (int jv = 0; jv < NTO / 2; ++jv) {
+              uint32_t r[4];
+              ldsm_x4_t(frag(vt + vx, 2 * jv), r);
+              // r[0], r[1]: n-tile 2jv (tokens 2t.. | 2t+8..); r[2], r[3]: n-tile 2jv + 1
+              r[0] &= keep0; r[1] &= keep1; r[2] &= keep0; r[3] &= keep1;
+              mma_k16<false>(o[2 * jv][0], o[2 * jv][1], ph[0], ph[1], r[0], r[1]);
+              mma_k16<false>(o[2 * jv + 1][0], o[2 * jv + 1][1], ph[0], ph[1], r[2], r[3]);
+              mma_k16<false>(o[2 * jv][0], o[2 * jv][1], pl[0], pl[1], r[0], r[1]);
+              mma_k16<false>(o[2 * jv + 1][0], o[2 * jv + 1][1], pl[0], pl[1], r[2], r[3]);
+            }
+          } else {
+#pragma unroll
+            for (int jv = 0; jv < NTO / 4; ++jv) {
+              uint32_t r[4];
+              ldsm_x4_t(frag(vt + vx, 4 * jv), r);
+              // r[m]: n-tile 4jv + m, tokens 2t, 2t+1
+#pragma unroll
+              for (int m = 0; m < 4; ++m) {
+                r[m] &= keep0;
+                mma_k8_bf16(o[4 * jv + m][0], o[4 * jv + m][1], ph[0], r[m]);
+                mma_k8_bf16(o[4 * jv + m][0], o[4 * jv + m][1], pl[0], r[m]);
+              }
+            }
+          }
+        }
+      }
+      __syncwarp();  // every lane is done with this stage before it is refilled
+      ++consumed;
+      if (alive) issue_next();
+    }
+
+    // ------------------------------------------------------------ piece end
+    float l_row = l_run + __shfl_xor_sync(0xffffffffu, l_run, 1);
+    l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
+    const int qh0 = unit_first_head(a, wk, G);
+    const bool whole = (wk.jb == 0 && wk.je == wk.nb);
+    // head dim of accumulator o[n][e]
+    auto odim = [&](int n, int e) -> int { return F8 ? GE::VPL * (2 * t + e) + n : 8 * n + 2 * t + e; };
+
+    if constexpr (!BALANCED) {
+      if (g < G) {
+        const int p = (int)(gw % a.max_partitions);
+        const size_t row = ((size_t)wk.s * a.num_q_heads + qh0 + g) * a.max_partitions + p;
+        const float inv = l_row > 0.f ? a.out_scale / l_row : 0.f;
+        float* dst = a.o_part + row * D;
+#pragma unroll
+        for (int n = 0; n < NTO; ++n)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) dst[odim(n, e)] = o[n][e] * inv;
+        if (t == 0) {
+          a.m_part[row] = m_run * 0.69314718055994531f;
+          a.l_part[row] = l_row;
+        }
+      }
+    } else if (whole) {
+      if (g < G) {
+        QT* dst = reinterpret_cast<QT*>(a.out) + ((size_t)wk.s * a.num_q_heads + qh0 + g) * D;
+        const float inv = l_row > 0.f ? a.out_scale / l_row : 0.f;
+        if constexpr (F8) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            uint32_t pk[NTO / 2];
+#pragma unroll
+            for (int n = 0; n < NTO / 2; ++n) pk[n] = pack_bf16x2(o[2 * n][e] * inv, o[2 * n + 1][e] * inv);
+#pragma unroll
+            for (int n = 0; n < NTO / 2; n += 4)
+              *reinterpret_cast<uint4*>(dst + odim(2 * n, e)) = make_uint4(pk[n], pk[n + 1], pk[n + 2], pk[n + 3]);
+          }
+        } else {
+#pragma unroll
+          for (int n = 0; n < NTO; ++n)
+            *reinterpret_cast<uint32_t*>(dst + odim(n, 0)) = pack_bf16x2(o[n][0] * inv, o[n][1] * inv);
+        }
+      }
+    } else {
+      // segment cut between warps: publish (acc, m, l), take a ticket
+      float* pslot = partial_slot<G, D>(a, wk, gw, u0);
+      if (g < G) {
+#pragma unroll
+        for (int n = 0; n < NTO; ++n)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) pslot[g * D + odim(n, e)] = o[n][e];
+        if (t == 0) {
+          pslot[G * D + g] = m_run;
+          pslot[G * D + G + g] = l_row;
+        }
+      }
+      ticket_and_merge<QT, G, D>(a, wk, T, NW, lane);
+    }
+    ++piece;
+    walker_next_piece<BS>(wk, a, u1);
+  }
+
+  // Leave no copy in flight: wait (bounded) for every stage this warp filled
+  // but did not wait for (only possible after a timeout).
+  for (int k = waited; k < issued; ++k) mbar_wait_bounded(&bars[k % NSW], (k / NSW) & 1, a.err);
+}
+
+}  // namespace pkv

@@ -1,8 +1,11 @@
 // pkv_api.cu -- host side of libpkv.so: argument validation, workspace
 // layout and kernel dispatch for the entry points declared in pkv.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstring>
 #include <cstdint>
 #include <map>
 #include <mutex>
@@ -127,11 +130,72 @@ size_t partition_workspace(int B, int Hq, int units, int D, int P) {
   return counter_region(B, units) + align_up(rows * D * sizeof(float)) + 2 * align_up(rows * sizeof(float));
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (the library links only the runtime).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// The cache [num_blocks, Hkv, BS, D] as the 3-D tensor (D, Hkv * BS,
+// num_blocks), one (block, kv head) tile per box, swizzled over the box row.
+bool encode_cache_map(const pkv_cache_desc* c, const void* base, TmaMap* out) {
+  // the last map encoded by this thread, reused while the cache is the same
+  struct Memo {
+    const void* base = nullptr;
+    pkv_cache_desc desc{};
+    TmaMap map{};
+  };
+  thread_local Memo memo[2];
+  thread_local int next = 0;
+  for (Memo& m : memo)
+    if (m.base == base && std::memcmp(&m.desc, c, sizeof *c) == 0) {
+      *out = m.map;
+      return true;
+    }
+  auto fn = tensor_map_encoder();
+  if (!fn) return false;
+  const int E = elem_bytes(c->dtype);
+  const int row = c->head_dim * E;
+  const int ib = tma_box_bytes(row);
+  const cuuint64_t dims[3] = {(cuuint64_t)c->head_dim, (cuuint64_t)c->num_kv_heads * c->block_size,
+                              (cuuint64_t)c->num_blocks};
+  const cuuint64_t strides[2] = {(cuuint64_t)row, (cuuint64_t)row * c->num_kv_heads * c->block_size};
+  const cuuint32_t box[3] = {(cuuint32_t)(ib / E), (cuuint32_t)c->block_size, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt = c->dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const CUtensorMapSwizzle sw = ib == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  static_assert(sizeof(TmaMap) == sizeof(CUtensorMap), "opaque tensor map size");
+  if (fn(reinterpret_cast<CUtensorMap*>(out), dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  Memo& m = memo[next];
+  next ^= 1;
+  m.base = base;
+  m.desc = *c;
+  m.map = *out;
+  return true;
+}
+
 }  // namespace
 
 // The current device's error word, for entry points defined in other
 // translation units of this library.
 unsigned int* device_error_word(int dev) { return error_word(dev); }
+
+bool encode_cache_maps(const DecodeKernel& k, const pkv_cache_desc* cache, const void* k_cache, const void* v_cache,
+                       TmaMaps* maps) {
+  if (!k.tensor_maps) return true;
+  return encode_cache_map(cache, k_cache, &maps->k) && encode_cache_map(cache, v_cache, &maps->v);
+}
 
 }  // namespace pkv
 
@@ -305,8 +369,10 @@ pkv_status decode_impl(void* out, const void* q, pkv_dtype q_dtype, int32_t num_
   a.qk_scale = scale * 1.4426950408889634f * (fp8 ? kv_scale : 1.f);
   a.out_scale = fp8 ? kv_scale : 1.f;
 
+  TmaMaps maps{};
+  if (!encode_cache_maps(k, cache, k_cache, v_cache, &maps)) return PKV_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  void* args[] = {&a};
+  void* args[] = {&a, &maps};
   if (balanced) {
     const int grid_max = sms * kMaxCtasPerSm;
     const size_t need = balanced_workspace(num_seqs, a.units, G, D, grid_max);

@@ -151,13 +151,15 @@ extern "C" pkv_status pkv_paged_attention_decode_noalloc(
   const size_t need = counter_bytes + (size_t)2 * grid * kDecodeWarps * (G * D + 2 * G) * sizeof(float);
   if (need > PKV_NOALLOC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;  // beyond the fixed scratch
 
+  TmaMaps maps{};
+  if (!encode_cache_maps(k, cache, k_cache, v_cache, &maps)) return PKV_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // the scratch keeps whatever the previous call left: the counters must
   // start at zero
   if (cudaMemsetAsync(scratch, 0, counter_bytes, st) != cudaSuccess) return PKV_ERR_CUDA;
   a.counters = reinterpret_cast<int*>(scratch);
   a.partials = reinterpret_cast<float*>(scratch + counter_bytes);
-  void* args[] = {&a};
+  void* args[] = {&a, &maps};
   return cudaLaunchKernel(k.fn, dim3((unsigned)grid), dim3(k.threads), args, k.smem, st) == cudaSuccess
              ? PKV_OK
              : PKV_ERR_CUDA;
