@@ -10,7 +10,9 @@ block_size 16, a shuffled 16384-block pool.
 Metric: effective HBM GB/s of the step -- algorithmic bytes (K/V of every
 valid token, q, out, the block-table entries used, seq_lens, plus the cache
 write's bytes) divided by the device time of the step -- with decode tokens/s
-per layer beside it.  L2 is flushed (a 256 MiB write) between timed steps.
+per layer beside it.  L2 is flushed between timed steps: a 256 MiB write, then a
+256 MiB read of a second buffer, so the timed kernels start on a cold L2 that
+holds no dirty line of the flush.
 
 ``--impl reference`` times the CPU oracle on the same workload instead (a
 bounded sample of sequences per step) and prints the same JSON line.
@@ -178,6 +180,23 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ GPU arm
+class L2Flush:
+    """Cold L2 before a timed step, outside its events: write a buffer larger
+    than L2 (evicts every line), then read a second one, so that the lines
+    left behind are clean and the timed kernels do not pay the write-back of
+    the flush's own data."""
+
+    def __init__(self, dev):
+        n = L2_FLUSH_BYTES // 4
+        self.dirty = torch.empty(n, dtype=torch.float32, device=dev)
+        self.clean = torch.ones(n, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def __call__(self, i: int = 0):
+        self.dirty.fill_(float(i))
+        torch.sum(self.clean, dim=0, out=self.sink)
+
+
 def run_gpu(args):
     import paged_kv_cache_22_gb300 as pkv
 
@@ -206,7 +225,7 @@ def run_gpu(args):
     out = torch.empty_like(q)
     max_len = w.max_seq_len
     workspace = pkv.DecodeWorkspace(dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
 
     def step():
@@ -218,7 +237,7 @@ def run_gpu(args):
                                    max_seq_len=max_len, partition_tokens=pt, workspace=workspace)
 
     for _ in range(args.warmup):
-        flush.fill_(1.0)
+        flush(1)
         step()
     torch.cuda.synchronize()
     if pkv.get_device_error():
@@ -234,7 +253,7 @@ def run_gpu(args):
     # timed region: K steps (cache write + decode), L2 flushed before each
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     for i in range(K):
-        flush.fill_(float(i))  # untimed: evicts the previous step's lines from L2
+        flush(i)  # untimed: evicts the previous step's lines from L2
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
@@ -244,7 +263,7 @@ def run_gpu(args):
     # the dominant kernel alone, same inputs and flushing, for its roofline
     evd = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     for i in range(K):
-        flush.fill_(float(i))
+        flush(i)
         evd[i][0].record(stream)
         decode_only()
         evd[i][1].record(stream)
@@ -293,7 +312,8 @@ def run_gpu(args):
             "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
             "block_size": w.block_size, "cache_dtype": w.cache_dtype,
             "split": "balanced (1 launch)" if pt == 0 else f"fixed {pt}-token partitions + reduce",
-            "l2": "flushed between timed steps (256 MiB write, outside the timed events)",
+            "l2": "flushed between timed steps, outside the timed events: 256 MiB write, then "
+                  "256 MiB read of a second buffer (cold L2 holding no dirty line)",
             "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
         },
         "decode_tok_s_per_layer": round(ws * w.num_seqs / (ms_per_step * 1e-3), 1),
@@ -348,8 +368,8 @@ def run_e2e(pkv, w, kc, vc, dev, pt, steps, flush):
         one()
     torch.cuda.synchronize()
     tot = 0.0
-    for _ in range(steps):
-        flush.fill_(0.5)
+    for i in range(steps):
+        flush(i)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         one()

@@ -18,10 +18,10 @@
 //    bank groups.  Each warp is an independent worker with its own ring of
 //    NSW stages and mbarriers, exactly as in the CUDA-core kernel; the
 //    balanced split and the ticket merge are shared with it.
-//  * Rows of the m16 operand are the G query heads (G <= 8; rows G..15 are
-//    zero and their results dropped).  Lane (g, t) = (lane / 4, lane % 4)
-//    owns row g: its running max, its share of the row sum and its 2 x D / 8
-//    accumulators.
+//  * Rows of the m16 operand of q.K are the G query heads (G <= 8; rows
+//    G..15 are zero and their results dropped).  Lane (g, t) = (lane / 4,
+//    lane % 4) owns head g: its running max, its share of the row sum and
+//    its 4 x D / 8 accumulators.
 //  * q.K: A = q (registers, loaded once per piece), B = K tile through
 //    ldmatrix (K rows are the n index, head dims the k index).  Scores are
 //    scaled in fp32, masked past the sequence end, and enter an online
@@ -29,14 +29,18 @@
 //    branch taken only when some row's max grew.
 //  * P.V: the probabilities leave the q.K accumulators already in the A
 //    operand layout of the next contraction (row g, tokens 2t, 2t+1, 2t+8,
-//    2t+9).  bf16: P is split into a bf16 head and a bf16 remainder, two MMAs
-//    per n-tile, so P keeps ~16 significant bits; V arrives through
-//    ldmatrix.trans.  fp8: K and V codes widen exactly to fp16 (cvt
-//    e4m3x2 -> f16x2) and P is fp16; q is fp16, pre-scaled by a power of two
-//    chosen per piece so that it cannot overflow, the factor moved to the
-//    fp32 score scale.  For fp8 V the n index is permuted so that a lane's
-//    four token rows are read as 16 contiguous bytes each: output column n of
-//    n-tile j is head dim (D / 8) * n + j.
+//    2t+9).  P is split into a head and a remainder of the operand type (bf16
+//    or fp16), so each weight keeps ~16 or more significant bits: the head
+//    fills rows 0..7 of the m16 operand, the remainder rows 8..15, one MMA
+//    per n-tile serves both, and the two row halves of the accumulator are
+//    summed when the piece ends.
+//  * bf16 caches: V arrives through ldmatrix.trans.  fp8 caches: K and V
+//    codes widen exactly to fp16 (cvt e4m3x2 -> f16x2); q is fp16,
+//    pre-scaled by a power of two chosen per piece so that it cannot
+//    overflow, the factor moved to the fp32 score scale.  For fp8 V the n
+//    index is permuted so that a lane's four token rows are read as 16
+//    contiguous bytes each: output column n of n-tile j is head dim
+//    (D / 8) * n + j.
 #pragma once
 
 #include "decode_common.cuh"
@@ -80,20 +84,39 @@ __device__ __forceinline__ void mma_k16(float& c0, float& c1, uint32_t a0, uint3
         "{%0, %1, %9, %9};"
         : "+f"(c0), "+f"(c1), "=f"(x2), "=f"(x3)
         : "r"(a0), "r"(0u), "r"(a2), "r"(b0), "r"(b1), "f"(0.f));
+    (void)x2, (void)x3;
   } else {
     asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %5}, {%7, %8}, "
         "{%0, %1, %9, %9};"
         : "+f"(c0), "+f"(c1), "=f"(x2), "=f"(x3)
         : "r"(a0), "r"(0u), "r"(a2), "r"(b0), "r"(b1), "f"(0.f));
+    (void)x2, (void)x3;
   }
 }
 
-// c[16x8] += A[16x8] . B[8x8] (bf16), rows 8..15 of A zero.
-__device__ __forceinline__ void mma_k8_bf16(float& c0, float& c1, uint32_t a0, uint32_t b0) {
-  float x2, x3;
-  asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5}, {%6}, {%0, %1, %7, %7};"
-      : "+f"(c0), "+f"(c1), "=f"(x2), "=f"(x3)
-      : "r"(a0), "r"(0u), "r"(b0), "f"(0.f));
+// c[16x8] += A[16x16] . B[16x8], all 16 rows: c0 / c1 row g, c2 / c3 row g+8.
+template <bool F16>
+__device__ __forceinline__ void mma_k16_rows16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  if constexpr (F16) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+                 "{%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+                 "{%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+
+// c[16x8] += A[16x8] . B[8x8] (bf16), all 16 rows.
+__device__ __forceinline__ void mma_k8_bf16_rows16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+  asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5}, {%6}, "
+               "{%0, %1, %2, %3};"
+               : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+               : "r"(a0), "r"(a1), "r"(b0));
 }
 
 // (lo, hi) -> packed pair, lo in bits 0..15.
@@ -106,6 +129,10 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+__device__ __forceinline__ float2 f16x2_to_f2(uint32_t w) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&w));
 }
 
 // Four e4m3 codes -> two exact fp16 pairs: bytes (0, 1) -> lo, (2, 3) -> hi.
@@ -179,7 +206,8 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
   constexpr bool F8 = GE::F8;
   constexpr int NSW = GE::NSW, TB = GE::TB, KS = GE::KS, NTO = GE::NTO, TILE = GE::TILE, STAGE = GE::STAGE;
 
-  extern __shared__ __align__(1024) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t tc_smem[];
+  uint8_t* const smem = tc_smem;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
   if (smem_addr(smem) & 1023u) {  // the swizzle phase needs 1024-byte aligned stages
@@ -298,7 +326,8 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
   int consumed = 0, waited = 0, piece = 0;
   bool alive = true;
   uint32_t qa[KS][2];     // q.K A operand: row g, (a0, a2) per k-step
-  float o[NTO][2];        // accumulators: row g, columns 2t, 2t+1 of each n-tile
+  float o[NTO][4];        // accumulators, columns 2t, 2t+1 of each n-tile: [0..1] the
+                          // P-head part (row g), [2..3] the P-remainder part (row g+8)
   float m_run, l_run;     // row g's running max (log2 units) and this lane's share of its sum
 
 #pragma unroll 1
@@ -355,7 +384,7 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
       }
     }
 #pragma unroll
-    for (int n = 0; n < NTO; ++n) o[n][0] = o[n][1] = 0.f;
+    for (int n = 0; n < NTO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     m_run = -CUDART_INF_F;
     l_run = 0.f;
     const int L = seq_len_clipped(a, wk.s);
@@ -443,8 +472,11 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
 #pragma unroll
           for (int n = 0; n < NTO; ++n) {
             const float2 v = __fmul2_rn(make_float2(o[n][0], o[n][1]), a2);
+            const float2 u = __fmul2_rn(make_float2(o[n][2], o[n][3]), a2);
             o[n][0] = v.x;
             o[n][1] = v.y;
+            o[n][2] = u.x;
+            o[n][3] = u.y;
           }
           l_run *= alpha;
           m_run = m_new;
@@ -462,7 +494,14 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
         // ---- P . V
         const bool full = vstep >= TB;
         if constexpr (F8) {
-          const uint32_t pa0 = pack_f16x2(p[0][0], p[0][1]), pa2 = pack_f16x2(p[1][0], p[1][1]);
+          // P = head + remainder, both fp16
+          uint32_t ph[2], pl[2];
+#pragma unroll
+          for (int n = 0; n < 2; ++n) {
+            ph[n] = pack_f16x2(p[n][0], p[n][1]);
+            const float2 h = f16x2_to_f2(ph[n]);
+            pl[n] = pack_f16x2(p[n][0] - h.x, p[n][1] - h.y);
+          }
           static_assert(GE::VPL == 16 || GE::VPL == 8, "fp8 V slice");
           uint32_t X[4][GE::VPL / 4];  // rows 2t, 2t+1, 2t+8, 2t+9
 #pragma unroll
@@ -493,7 +532,7 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
             e4m3x4_to_f16x2x2(__byte_perm(X[2][q], X[3][q], 0x5140), b1[0], b1[1]);
             e4m3x4_to_f16x2x2(__byte_perm(X[2][q], X[3][q], 0x7362), b1[2], b1[3]);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) mma_k16<true>(o[4 * q + k][0], o[4 * q + k][1], pa0, pa2, b0[k], b1[k]);
+            for (int k = 0; k < 4; ++k) mma_k16_rows16<true>(o[4 * q + k], ph[0], pl[0], ph[1], pl[1], b0[k], b1[k]);
           }
         } else {
           // P = head + remainder, both bf16
@@ -517,10 +556,8 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
               ldsm_x4_t(frag(vt + vx, 2 * jv), r);
               // r[0], r[1]: n-tile 2jv (tokens 2t.. | 2t+8..); r[2], r[3]: n-tile 2jv + 1
               r[0] &= keep0; r[1] &= keep1; r[2] &= keep0; r[3] &= keep1;
-              mma_k16<false>(o[2 * jv][0], o[2 * jv][1], ph[0], ph[1], r[0], r[1]);
-              mma_k16<false>(o[2 * jv + 1][0], o[2 * jv + 1][1], ph[0], ph[1], r[2], r[3]);
-              mma_k16<false>(o[2 * jv][0], o[2 * jv][1], pl[0], pl[1], r[0], r[1]);
-              mma_k16<false>(o[2 * jv + 1][0], o[2 * jv + 1][1], pl[0], pl[1], r[2], r[3]);
+              mma_k16_rows16<false>(o[2 * jv], ph[0], pl[0], ph[1], pl[1], r[0], r[1]);
+              mma_k16_rows16<false>(o[2 * jv + 1], ph[0], pl[0], ph[1], pl[1], r[2], r[3]);
             }
           } else {
 #pragma unroll
@@ -531,8 +568,7 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
 #pragma unroll
               for (int m = 0; m < 4; ++m) {
                 r[m] &= keep0;
-                mma_k8_bf16(o[4 * jv + m][0], o[4 * jv + m][1], ph[0], r[m]);
-                mma_k8_bf16(o[4 * jv + m][0], o[4 * jv + m][1], pl[0], r[m]);
+                mma_k8_bf16_rows16(o[4 * jv + m], ph[0], pl[0], r[m]);
               }
             }
           }
@@ -544,6 +580,11 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
     }
 
     // ------------------------------------------------------------ piece end
+#pragma unroll
+    for (int n = 0; n < NTO; ++n) {
+      o[n][0] += o[n][2];
+      o[n][1] += o[n][3];
+    }
     float l_row = l_run + __shfl_xor_sync(0xffffffffu, l_run, 1);
     l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
     const int qh0 = unit_first_head(a, wk, G);

@@ -7,6 +7,8 @@ cache write is checked bit-exact against the GPU's first).
 """
 from __future__ import annotations
 
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -199,11 +201,13 @@ def test_split_invariance(pkv):
         assert np.abs(o - outs[0]).max() <= 2e-2
 
 
-def test_poisoned_tail_and_table_never_read(pkv):
+@pytest.mark.parametrize("dt", ["bf16", "fp8_e4m3"])
+def test_poisoned_tail_and_table_never_read(pkv, dt):
     """Caches start NaN everywhere and unused table entries are out of the
     pool: a read past seq_len or past the last block would show up as a NaN
-    output or a device error."""
-    w = workloads.make_workload("poison", [1, 15, 17, 31, 33, 100], 16, 4, 128, 16, "bf16", seed=44,
+    output or a device error (the tensor-core path masks the V rows past the
+    end in registers: a NaN times a zero weight would still be NaN)."""
+    w = workloads.make_workload("poison", [1, 15, 17, 31, 33, 100], 16, 4, 128, 16, dt, seed=44,
                                 max_blocks_per_seq=20)
     kc, vc = gpu_caches(pkv, w)
     for pt in (0, 16, 64):
@@ -234,10 +238,10 @@ def test_seq_len_beyond_hint_sets_error(pkv):
     assert pkv.get_device_error() & pkv.DEVERR_BAD_SEQ_LEN
 
 
-# ------------------------------------------------------------------ dynamic item schedule
-# Batches with at least two tiles per warp of the balanced grid hand their last
-# tiles out dynamically; segments then end in items, cross the static/dynamic
-# boundary, or fit inside one item.
+# ------------------------------------------------------------------ segments cut between warps
+# Batches with more tiles than warps in the balanced grid: segments are cut
+# between warps at every length, merged by the last piece to finish, and the
+# merge counters must come back to zero call after call.
 MEDIUM = [
     ("many_short", [37, 5, 16, 1, 90, 17] * 40, 32, 8, 128, "bf16"),
     ("skewed", [3000, 20, 1, 700, 4096, 33, 2500, 64] * 4, 32, 8, 128, "bf16"),
@@ -247,7 +251,7 @@ MEDIUM = [
 
 
 @pytest.mark.parametrize("case", MEDIUM, ids=[c[0] for c in MEDIUM])
-def test_decode_medium_dynamic_schedule(pkv, case):
+def test_decode_medium_cut_segments(pkv, case):
     name, lens, Hq, Hkv, d, dt = case
     w = workloads.make_workload(name, lens, Hq, Hkv, d, 16, dt, seed=len(lens) + Hq)
     tiles = sum(-(-L // 16) for L in lens) * Hkv * ((Hq // Hkv) // min(8, Hq // Hkv))
@@ -337,3 +341,57 @@ def test_named_config_full_size(pkv, name, pt):
     ref = oracle_decode(w, okc, ovc, threads=os.cpu_count() or 4)
     assert_close(got, ref, TOL[w.cache_dtype], name)
     assert pkv.get_device_error() == 0
+
+
+# ------------------------------------------------------------------ tensor-core specifics
+@pytest.mark.parametrize("dt", ["bf16", "fp8_e4m3"])
+def test_large_query_entries(pkv, dt):
+    """fp8 caches run q.K with fp16 operands (largest finite 65504): q entries
+    far beyond that must still give the oracle's answer.  q is scaled by 2^19
+    (exact in bf16) and the softmax scale by 2^-19, so the scores are those of
+    an ordinary workload."""
+    base = workloads.make_workload("bigq", [7, 100, 333], 16, 4, 128, 16, dt, seed=47)
+    f = 2.0 ** 19
+    w = dataclasses.replace(base, q=(base.q.float() * f).to(torch.bfloat16), scale=base.scale / f)
+    kc, vc = gpu_caches(pkv, w)
+    ref = oracle_decode(w)
+    for pt in (0, 64):
+        assert_close(run_decode(pkv, w, kc, vc, pt), ref, TOL[dt], f"partition_tokens {pt}")
+    assert pkv.get_device_error() == 0
+
+
+ROUNDING = [
+    ("gqa4", [1, 2, 17, 300, 1000], 32, 8, 128, 16, "bf16"),
+    ("gqa8", [3, 64, 900], 64, 8, 128, 16, "bf16"),
+    ("bs8", [9, 300], 32, 8, 128, 8, "bf16"),
+    ("bs32", [33, 300], 32, 8, 128, 32, "bf16"),
+    ("d64", [5, 129, 400], 8, 2, 64, 16, "bf16"),
+    ("fp8", [4, 77, 600], 32, 8, 128, 16, "fp8_e4m3"),
+]
+
+
+@pytest.mark.parametrize("pt", [0, 64])
+@pytest.mark.parametrize("case", ROUNDING, ids=[c[0] for c in ROUNDING])
+def test_outputs_are_correctly_rounded(pkv, case, pt):
+    """Accuracy of the contractions beyond the max-abs bound: the share of bf16
+    outputs equal to the oracle's exact result rounded to bf16, and the
+    largest distance in bf16 steps.  P reaches P.V as a head plus a remainder
+    (bf16 + bf16 for bf16 caches, fp16 + fp16 for fp8 caches), about 16 or
+    more significant bits per weight, so nearly every output rounds like the
+    exact value."""
+    name, lens, Hq, Hkv, d, bs, dt = case
+    w = workloads.make_workload(name, lens, Hq, Hkv, d, bs, dt, seed=48 + len(lens))
+    kc, vc = gpu_caches(pkv, w)
+    ref = oracle_decode(w)
+    got = run_decode(pkv, w, kc, vc, pt)
+    rounded = oracle.bf16_decode(oracle.bf16_encode(ref))
+    exact_share = float(np.mean(got == rounded))
+    # one bf16 step at |ref|, floored at 2^-16: near zero the fp32 sums keep
+    # an absolute error of a few 1e-8 that no relative bound covers
+    step = np.full_like(ref, 2.0 ** -16)
+    big = np.abs(ref) >= 2.0 ** -9
+    step[big] = 2.0 ** (np.floor(np.log2(np.abs(ref[big]))) - 7)
+    steps = float(np.max(np.abs(got - ref) / step))
+    want = 0.99
+    assert exact_share >= want, f"{name}: {exact_share:.4f} of outputs correctly rounded (< {want})"
+    assert steps <= 1.0, f"{name}: an output is {steps:.2f} bf16 steps from the exact value"
