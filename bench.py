@@ -51,8 +51,8 @@ L2_FLUSH_BYTES = 256 << 20
 
 # DRAM traffic of one decode launch on the default workload, from an ncu
 # capture, valid only for the kernel sources it was taken on.
-TRAFFIC = {"sources_sha256": "be84ac49a3526b4b3e3fd8d4b58e40b06f181862de21068117479d670e6694cb",
-           "bytes_per_launch": 325923840}  # 318.660352 MB read + 7.263488 MB written
+TRAFFIC = {"sources_sha256": "06d46c0b46c51b58b8df518f1d5d1ac808e5199f45e7ed8a22e048fd9a3e1325",
+           "bytes_per_launch": 322043904}  # 317.679104 MB read + 4.364800 MB written
 
 WORKLOAD_TEXT = {
     "llama3_8b": "Llama-3-8B-shaped decode layer: 64 seqs, L~U[128,2048], 32 q / 8 kv heads, "
@@ -325,7 +325,8 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "decode_kernel (balanced split)" if pt == 0 else "decode_kernel (partitions)"},
+                     "kernel": ("decode_tc_kernel" if w.cache_dtype != "f32" else "decode_kernel")
+                     + (" (balanced split)" if pt == 0 else " (partitions)")},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": round(e2e["ms_per_step"], 6)},
