@@ -51,7 +51,7 @@ L2_FLUSH_BYTES = 256 << 20
 
 # DRAM traffic of one decode launch on the default workload, from an ncu
 # capture, valid only for the kernel sources it was taken on.
-TRAFFIC = {"sources_sha256": "06d46c0b46c51b58b8df518f1d5d1ac808e5199f45e7ed8a22e048fd9a3e1325",
+TRAFFIC = {"sources_sha256": "ab6824dfd010f91e6933b420861037cc6d67b42188bd09ff2b376d1650fb51be",
            "bytes_per_launch": 322043904}  # 317.679104 MB read + 4.364800 MB written
 
 WORKLOAD_TEXT = {
@@ -68,12 +68,13 @@ WORKLOAD_TEXT = {
 
 
 def kernel_sources_sha() -> str:
+    """Hash of the files that define the tensor-core decode kernel's device
+    code (host-side launch code does not change its DRAM traffic)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_22_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+    for f in ("pkv_device.cuh", "decode_common.cuh", "decode_tc.cuh"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
     return h.hexdigest()
 
 
@@ -207,6 +208,7 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     pkv.library()
+    pkv.set_decode_engine(args.engine)
 
     w = workloads.CONFIGS[args.config](seed=1234 + list(workloads.CONFIGS).index(args.config)
                                        + 1000 * rank)
@@ -288,7 +290,8 @@ def run_gpu(args):
     e2e_value = job_throughput(ws, dec_b + rc_b, e2e["ms_per_step"])
 
     traffic = None
-    if TRAFFIC["sources_sha256"] == kernel_sources_sha() and args.config == "llama3_8b" and pt == 0:
+    if (TRAFFIC["sources_sha256"] == kernel_sources_sha() and args.config == "llama3_8b" and pt == 0
+            and args.engine == "tensor_cores"):
         traffic = TRAFFIC["bytes_per_launch"]
 
     line = {
@@ -312,6 +315,8 @@ def run_gpu(args):
             "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
             "block_size": w.block_size, "cache_dtype": w.cache_dtype,
             "split": "balanced (1 launch)" if pt == 0 else f"fixed {pt}-token partitions + reduce",
+            "engine": ("cuda_cores" if w.cache_dtype == "f32" else args.engine)
+                      + " (q.K and P.V; softmax and accumulation in fp32)",
             "l2": "flushed between timed steps, outside the timed events: 256 MiB write, then "
                   "256 MiB read of a second buffer (cold L2 holding no dirty line)",
             "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
@@ -325,7 +330,8 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": ("decode_tc_kernel" if w.cache_dtype != "f32" else "decode_kernel")
+                     "kernel": ("decode_tc_kernel" if w.cache_dtype != "f32" and args.engine == "tensor_cores"
+                                else "decode_kernel")
                      + (" (balanced split)" if pt == 0 else " (partitions)")},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
@@ -483,6 +489,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seqs", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--engine", choices=["tensor_cores", "cuda_cores"], default="tensor_cores",
+                    help="units that run q.K and P.V for bf16 / fp8 caches")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

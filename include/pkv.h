@@ -283,6 +283,30 @@ const char* pkv_status_string(pkv_status status);
  * sizes its grid from it). */
 int32_t pkv_device_sm_count(void);
 
+/*
+ * Which units run the two contractions of the decode (q.K and P.V) for bf16
+ * and fp8 caches.  The softmax, its online rescaling and every accumulation
+ * stay in fp32 either way ("Optimización de Inferencia LLM", section
+ * "PagedAttention: Conceptos de SO se Encuentran con Memoria GPU"); fp32
+ * caches always use the CUDA cores.
+ *
+ *   PKV_ENGINE_TENSOR_CORES (default)  the G query heads of a kv head are the
+ *       rows of an m16n8k16 MMA against each K and V tile, fp32 accumulate;
+ *       probabilities enter P.V as a head plus a remainder of the operand
+ *       type (~16 significant bits).  Fewer instructions per KV byte: the
+ *       decode stays bound by HBM at 8 query heads per kv head and for fp8.
+ *   PKV_ENGINE_CUDA_CORES  every product is a packed fp32 FMA on the CUDA
+ *       cores (probabilities in fp32).
+ *
+ * Process-wide; applies to decode calls issued after it returns (calls in
+ * flight keep the engine they were issued with).  PKV_ERR_INVALID_ARG for an
+ * unknown value.
+ */
+typedef enum { PKV_ENGINE_TENSOR_CORES = 0, PKV_ENGINE_CUDA_CORES = 1 } pkv_decode_engine;
+
+pkv_status pkv_set_decode_engine(pkv_decode_engine engine);
+pkv_decode_engine pkv_get_decode_engine(void);
+
 #ifdef __cplusplus
 }
 #endif

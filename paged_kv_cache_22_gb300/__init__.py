@@ -15,10 +15,14 @@ Entry points (same names as the C ABI, without the ``pkv_`` prefix):
   overlapping its prologue with the cache write;
 * :func:`split_kv_reduce` -- log-sum-exp merge of partition partials;
 * :func:`gather_kv` -- contiguous copy of every sequence's cached tokens;
-* :func:`decode_workspace_bytes`, :func:`get_device_error`.
+* :func:`decode_workspace_bytes`, :func:`get_device_error`;
+* :func:`set_decode_engine` / :func:`get_decode_engine` (and the
+  :func:`decode_engine` context manager) -- tensor cores (default) or CUDA
+  cores for the contractions of bf16 and fp8 decodes.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -31,12 +35,15 @@ __all__ = [
     "split_kv_reduce",
     "gather_kv", "decode_workspace_bytes", "get_device_error", "library", "library_path",
     "DecodeWorkspace", "F32", "BF16", "FP8_E4M3", "DEVERR_BAD_BLOCK_ID", "DEVERR_BAD_SLOT",
-    "DEVERR_BAD_SEQ_LEN", "DEVERR_WAIT_TIMEOUT", "DEVERR_SMEM_ALIGN",
+    "DEVERR_BAD_SEQ_LEN", "DEVERR_WAIT_TIMEOUT", "DEVERR_SMEM_ALIGN", "set_decode_engine",
+    "get_decode_engine", "decode_engine", "ENGINE_TENSOR_CORES", "ENGINE_CUDA_CORES",
 ]
 
 F32, BF16, FP8_E4M3 = 0, 1, 2
 DEVERR_BAD_BLOCK_ID, DEVERR_BAD_SLOT, DEVERR_BAD_SEQ_LEN, DEVERR_WAIT_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 DEVERR_SMEM_ALIGN = 0x10
+ENGINE_TENSOR_CORES, ENGINE_CUDA_CORES = 0, 1
+_ENGINES = {"tensor_cores": ENGINE_TENSOR_CORES, "cuda_cores": ENGINE_CUDA_CORES}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libpkv.so")
@@ -83,6 +90,8 @@ def library() -> ctypes.CDLL:
             "pkv_get_device_error": [ctypes.POINTER(ctypes.c_uint32), vp],
             "pkv_status_string": [ctypes.c_int],
             "pkv_device_sm_count": [],
+            "pkv_set_decode_engine": [ctypes.c_int],
+            "pkv_get_decode_engine": [],
         }
         for name, args in sigs.items():
             fn = getattr(lib, name)
@@ -134,6 +143,30 @@ def _check(status: int, what: str) -> None:
 
 
 # ------------------------------------------------------------------ entry points
+def set_decode_engine(engine) -> None:
+    """Run the contractions of bf16 / fp8 decodes on ``"tensor_cores"``
+    (default) or ``"cuda_cores"`` (also accepts the ENGINE_* integers);
+    process-wide, for calls issued afterwards."""
+    code = _ENGINES.get(engine, engine)
+    _check(library().pkv_set_decode_engine(int(code)), "set_decode_engine")
+
+
+def get_decode_engine() -> str:
+    code = library().pkv_get_decode_engine()
+    return {v: k for k, v in _ENGINES.items()}[code]
+
+
+@contextlib.contextmanager
+def decode_engine(engine):
+    """Temporarily select a decode engine (see :func:`set_decode_engine`)."""
+    prev = get_decode_engine()
+    set_decode_engine(engine)
+    try:
+        yield
+    finally:
+        set_decode_engine(prev)
+
+
 def kv_reshape_and_cache(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor,
                          v_cache: torch.Tensor, slot_mapping: torch.Tensor,
                          kv_scale: float = 1.0, stream=None) -> None:

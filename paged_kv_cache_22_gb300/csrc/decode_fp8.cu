@@ -1,11 +1,11 @@
-// fp8-e4m3-cache decode kernel instances (bf16 q and out).
+// fp8-e4m3-cache decode kernel instances (bf16 q and out), tensor cores.
 #include "decode_launch.cuh"
 
 namespace pkv {
-bool find_decode_fp8(int head_dim, int block_size, int heads, bool balanced, DecodeKernel* out) {
+bool find_decode_fp8_tc(int head_dim, int block_size, int heads, bool balanced, DecodeKernel* out) {
   if (block_size != 16) return false;
-  if (head_dim == 64) return find_for<CacheFP8, 64, 16>(heads, balanced, out);
-  if (head_dim == 128) return find_for<CacheFP8, 128, 16>(heads, balanced, out);
+  if (head_dim == 64) return find_for<CacheFP8, 64, 16, true>(heads, balanced, out);
+  if (head_dim == 128) return find_for<CacheFP8, 128, 16, true>(heads, balanced, out);
   return false;
 }
 }  // namespace pkv

@@ -16,17 +16,19 @@ struct DecodeKernel {
   bool tensor_maps = false;  // reads the caches through the TmaMaps parameter
 };
 
-// fp32 caches run on the CUDA cores, bf16 and fp8 caches on the tensor cores.
-template <class CT, int D, int BS, int G, bool BAL>
+// TC: the q.K and P.V contractions on the tensor cores (decode_tc.cuh, bf16
+// and fp8 caches); otherwise on the CUDA cores (decode.cuh, every cache type).
+template <class CT, int D, int BS, int G, bool BAL, bool TC>
 DecodeKernel decode_kernel_info() {
   DecodeKernel k;
-  if constexpr (CT::kBytes == 4) {
-    k.fn = reinterpret_cast<const void*>(&decode_kernel<CT, D, BS, G, kDecodeWarps, BAL>);
-    k.smem = Smem<CT, D, BS, G, kDecodeWarps>::kBytes;
-  } else {
+  if constexpr (TC) {
+    static_assert(CT::kBytes != 4, "fp32 caches run on the CUDA cores");
     k.fn = reinterpret_cast<const void*>(&decode_tc_kernel<CT, D, BS, G, kDecodeWarps, BAL>);
     k.smem = TcSmem<CT, D, BS, G, kDecodeWarps>::kBytes;
     k.tensor_maps = true;
+  } else {
+    k.fn = reinterpret_cast<const void*>(&decode_kernel<CT, D, BS, G, kDecodeWarps, BAL>);
+    k.smem = Smem<CT, D, BS, G, kDecodeWarps>::kBytes;
   }
   k.threads = kDecodeWarps * 32;
   k.heads_per_unit = G;
@@ -39,23 +41,42 @@ bool encode_cache_maps(const DecodeKernel& k, const pkv_cache_desc* cache, const
                        const void* v_cache, TmaMaps* maps);
 
 // Fill `out` with the instance for (D, BS, G, balanced); false if not built.
+// One finder per cache type and engine, each in its own translation unit.
 #define PKV_DECLARE_FINDER(NAME) \
   bool NAME(int head_dim, int block_size, int heads, bool balanced, DecodeKernel* out);
 
 PKV_DECLARE_FINDER(find_decode_f32)
-PKV_DECLARE_FINDER(find_decode_bf16)
-PKV_DECLARE_FINDER(find_decode_fp8)
+PKV_DECLARE_FINDER(find_decode_bf16_tc)
+PKV_DECLARE_FINDER(find_decode_bf16_cc)
+PKV_DECLARE_FINDER(find_decode_fp8_tc)
+PKV_DECLARE_FINDER(find_decode_fp8_cc)
 
 // Shared body of the finders: the compiled (D, BS) set is passed as a list.
-template <class CT, int D, int BS>
+template <class CT, int D, int BS, bool TC>
 bool find_for(int heads, bool balanced, DecodeKernel* out) {
   switch (heads) {
-    case 1: *out = balanced ? decode_kernel_info<CT, D, BS, 1, true>() : decode_kernel_info<CT, D, BS, 1, false>(); return true;
-    case 2: *out = balanced ? decode_kernel_info<CT, D, BS, 2, true>() : decode_kernel_info<CT, D, BS, 2, false>(); return true;
-    case 4: *out = balanced ? decode_kernel_info<CT, D, BS, 4, true>() : decode_kernel_info<CT, D, BS, 4, false>(); return true;
-    case 8: *out = balanced ? decode_kernel_info<CT, D, BS, 8, true>() : decode_kernel_info<CT, D, BS, 8, false>(); return true;
+    case 1: *out = balanced ? decode_kernel_info<CT, D, BS, 1, true, TC>() : decode_kernel_info<CT, D, BS, 1, false, TC>(); return true;
+    case 2: *out = balanced ? decode_kernel_info<CT, D, BS, 2, true, TC>() : decode_kernel_info<CT, D, BS, 2, false, TC>(); return true;
+    case 4: *out = balanced ? decode_kernel_info<CT, D, BS, 4, true, TC>() : decode_kernel_info<CT, D, BS, 4, false, TC>(); return true;
+    case 8: *out = balanced ? decode_kernel_info<CT, D, BS, 8, true, TC>() : decode_kernel_info<CT, D, BS, 8, false, TC>(); return true;
     default: return false;
   }
 }
+
+// The decode kernel for a cache type, shape and engine (fp32 caches always
+// take the CUDA cores).
+inline bool find_decode(pkv_dtype dt, int D, int BS, int G, bool balanced, bool tensor_cores, DecodeKernel* k) {
+  switch (dt) {
+    case PKV_F32: return find_decode_f32(D, BS, G, balanced, k);
+    case PKV_BF16:
+      return tensor_cores ? find_decode_bf16_tc(D, BS, G, balanced, k) : find_decode_bf16_cc(D, BS, G, balanced, k);
+    case PKV_FP8_E4M3:
+      return tensor_cores ? find_decode_fp8_tc(D, BS, G, balanced, k) : find_decode_fp8_cc(D, BS, G, balanced, k);
+  }
+  return false;
+}
+
+// The engine set by pkv_set_decode_engine (pkv_api.cu).
+bool decode_on_tensor_cores();
 
 }  // namespace pkv

@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <cstdint>
@@ -91,14 +92,7 @@ int heads_per_unit(int g) {
   return 1;
 }
 
-bool find_decode(pkv_dtype dt, int D, int BS, int G, bool balanced, DecodeKernel* k) {
-  switch (dt) {
-    case PKV_F32: return find_decode_f32(D, BS, G, balanced, k);
-    case PKV_BF16: return find_decode_bf16(D, BS, G, balanced, k);
-    case PKV_FP8_E4M3: return find_decode_fp8(D, BS, G, balanced, k);
-  }
-  return false;
-}
+std::atomic<int> g_engine{PKV_ENGINE_TENSOR_CORES};
 
 bool valid_cache_desc(const pkv_cache_desc* c) {
   if (!c) return false;
@@ -191,6 +185,8 @@ bool encode_cache_map(const pkv_cache_desc* c, const void* base, TmaMap* out) {
 // translation units of this library.
 unsigned int* device_error_word(int dev) { return error_word(dev); }
 
+bool decode_on_tensor_cores() { return g_engine.load(std::memory_order_relaxed) == PKV_ENGINE_TENSOR_CORES; }
+
 bool encode_cache_maps(const DecodeKernel& k, const pkv_cache_desc* cache, const void* k_cache, const void* v_cache,
                        TmaMaps* maps) {
   if (!k.tensor_maps) return true;
@@ -212,6 +208,16 @@ const char* pkv_status_string(pkv_status s) {
     case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE";
   }
   return "PKV_ERR_UNKNOWN";
+}
+
+pkv_status pkv_set_decode_engine(pkv_decode_engine engine) {
+  if (engine != PKV_ENGINE_TENSOR_CORES && engine != PKV_ENGINE_CUDA_CORES) return PKV_ERR_INVALID_ARG;
+  g_engine.store(engine, std::memory_order_relaxed);
+  return PKV_OK;
+}
+
+pkv_decode_engine pkv_get_decode_engine(void) {
+  return static_cast<pkv_decode_engine>(g_engine.load(std::memory_order_relaxed));
 }
 
 int32_t pkv_device_sm_count(void) {
@@ -338,7 +344,7 @@ pkv_status decode_impl(void* out, const void* q, pkv_dtype q_dtype, int32_t num_
   const int G = heads_per_unit(g);
   const bool balanced = partition_tokens == 0;
   DecodeKernel k;
-  if (!find_decode(cache->dtype, D, BS, G, balanced, &k)) return PKV_ERR_UNSUPPORTED;
+  if (!find_decode(cache->dtype, D, BS, G, balanced, decode_on_tensor_cores(), &k)) return PKV_ERR_UNSUPPORTED;
 
   const int dev = current_device();
   if (dev < 0) return PKV_ERR_CUDA;

@@ -68,14 +68,6 @@ int occupancy(const DecodeKernel& k, int dev) {
   return occ;
 }
 
-bool find_balanced(pkv_dtype dt, int D, int BS, int G, DecodeKernel* k) {
-  switch (dt) {
-    case PKV_F32: return find_decode_f32(D, BS, G, true, k);
-    case PKV_BF16: return find_decode_bf16(D, BS, G, true, k);
-    case PKV_FP8_E4M3: return find_decode_fp8(D, BS, G, true, k);
-  }
-  return false;
-}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -110,7 +102,7 @@ extern "C" pkv_status pkv_paged_attention_decode_noalloc(
   for (int cand : {8, 4, 2, 1})
     if (g % cand == 0) { G = cand; break; }
   DecodeKernel k;
-  if (!find_balanced(cache->dtype, D, BS, G, &k)) return PKV_ERR_UNSUPPORTED;
+  if (!find_decode(cache->dtype, D, BS, G, true, decode_on_tensor_cores(), &k)) return PKV_ERR_UNSUPPORTED;
 
   int dev = -1, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;

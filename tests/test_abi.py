@@ -96,3 +96,14 @@ def test_partition_workspace_size_formula(lib):
     want = (1 << 20) + up(rows * d * 4) + 2 * up(rows * 4)  # counters first
     assert lib.pkv_decode_workspace_bytes(B, Hq, Hkv, d, L, pt) == want
     assert lib.pkv_decode_workspace_bytes(B, Hq, 3, d, L, pt) == 0  # invalid GQA split
+
+
+def test_decode_engine_switch(lib):
+    import paged_kv_cache_22_gb300 as pkv
+    assert pkv.get_decode_engine() == "tensor_cores"  # the default
+    with pkv.decode_engine("cuda_cores"):
+        assert pkv.get_decode_engine() == "cuda_cores"
+        assert lib.pkv_get_decode_engine() == pkv.ENGINE_CUDA_CORES
+    assert pkv.get_decode_engine() == "tensor_cores"
+    assert lib.pkv_set_decode_engine(7) == 1  # unknown engine: invalid argument, no change
+    assert pkv.get_decode_engine() == "tensor_cores"

@@ -30,6 +30,14 @@ def pkv():
     return m
 
 
+@pytest.fixture(params=["tensor_cores", "cuda_cores"])
+def engine(request, pkv):
+    """Runs a test once per decode engine (bf16 and fp8 caches; fp32 caches
+    take the CUDA cores under both)."""
+    with pkv.decode_engine(request.param):
+        yield request.param
+
+
 def gpu_caches(pkv, w: workloads.Workload, include_new: bool = True):
     shape = workloads.cache_shape(w)
     dt = workloads.cache_torch_dtype(w.cache_dtype)
@@ -142,10 +150,12 @@ SMALL = [
 
 @pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
 @pytest.mark.parametrize("partition_tokens", [0, 64, 512])
-def test_decode_small(pkv, case, partition_tokens):
+def test_decode_small(pkv, engine, case, partition_tokens):
     name, lens, Hq, Hkv, d, bs, dt = case
     if partition_tokens % bs:
         pytest.skip("partition must be a multiple of the block size")
+    if dt == "f32" and engine == "cuda_cores":
+        pytest.skip("fp32 caches take the CUDA cores under either engine")
     w = workloads.make_workload(name, lens, Hq, Hkv, d, bs, dt, seed=len(name) * 7 + Hq)
     kc, vc = gpu_caches(pkv, w)
     okc, ovc = oracle_caches(w)
@@ -166,7 +176,7 @@ def test_tiny_mha_config(pkv):
         assert_close(run_decode(pkv, w, kc, vc, pt), ref, TOL["f32"], f"tiny pt={pt}")
 
 
-def test_length_one_and_zero(pkv):
+def test_length_one_and_zero(pkv, engine):
     w = workloads.make_workload("z", [0, 1, 0, 1, 37], 8, 2, 128, 16, "bf16", seed=5)
     kc, vc = gpu_caches(pkv, w)
     for pt in (0, 16):
@@ -190,7 +200,7 @@ def test_block_permutation_invariance(pkv):
         assert np.array_equal(ga, gb), "same tokens, different placement: identical results"
 
 
-def test_split_invariance(pkv):
+def test_split_invariance(pkv, engine):
     w = workloads.make_workload("si", [1, 48, 511, 512, 513, 2000], 32, 8, 128, 16, "bf16", seed=33)
     kc, vc = gpu_caches(pkv, w)
     ref = oracle_decode(w)
@@ -202,7 +212,7 @@ def test_split_invariance(pkv):
 
 
 @pytest.mark.parametrize("dt", ["bf16", "fp8_e4m3"])
-def test_poisoned_tail_and_table_never_read(pkv, dt):
+def test_poisoned_tail_and_table_never_read(pkv, engine, dt):
     """Caches start NaN everywhere and unused table entries are out of the
     pool: a read past seq_len or past the last block would show up as a NaN
     output or a device error (the tensor-core path masks the V rows past the
@@ -251,7 +261,7 @@ MEDIUM = [
 
 
 @pytest.mark.parametrize("case", MEDIUM, ids=[c[0] for c in MEDIUM])
-def test_decode_medium_cut_segments(pkv, case):
+def test_decode_medium_cut_segments(pkv, engine, case):
     name, lens, Hq, Hkv, d, dt = case
     w = workloads.make_workload(name, lens, Hq, Hkv, d, 16, dt, seed=len(lens) + Hq)
     tiles = sum(-(-L // 16) for L in lens) * Hkv * ((Hq // Hkv) // min(8, Hq // Hkv))
@@ -345,7 +355,7 @@ def test_named_config_full_size(pkv, name, pt):
 
 # ------------------------------------------------------------------ tensor-core specifics
 @pytest.mark.parametrize("dt", ["bf16", "fp8_e4m3"])
-def test_large_query_entries(pkv, dt):
+def test_large_query_entries(pkv, engine, dt):
     """fp8 caches run q.K with fp16 operands (largest finite 65504): q entries
     far beyond that must still give the oracle's answer.  q is scaled by 2^19
     (exact in bf16) and the softmax scale by 2^-19, so the scores are those of
@@ -372,7 +382,7 @@ ROUNDING = [
 
 @pytest.mark.parametrize("pt", [0, 64])
 @pytest.mark.parametrize("case", ROUNDING, ids=[c[0] for c in ROUNDING])
-def test_outputs_are_correctly_rounded(pkv, case, pt):
+def test_outputs_are_correctly_rounded(pkv, engine, case, pt):
     """Accuracy of the contractions beyond the max-abs bound: the share of bf16
     outputs equal to the oracle's exact result rounded to bf16, and the
     largest distance in bf16 steps.  P reaches P.V as a head plus a remainder
