@@ -189,6 +189,8 @@ __global__ void __launch_bounds__(W * 32, (G >= 8 ? 8 : 12) / W)
   // ---------------------------------------------------------------- consume side
   Walker wk = wk0;
   int consumed = 0, waited = 0, piece = 0;
+  CutPiece cut0{}, cut1{};  // this warp's cut pieces (its first and last at most)
+  int ncut = 0;
   bool alive = true;
   float2 q2[G][NP];          // this lane's query dims, pre-scaled by scale*log2(e)
   float2 acc[G][DV];         // P.V accumulators: this lane's DV dims, even/odd token halves
@@ -409,7 +411,7 @@ __global__ void __launch_bounds__(W * 32, (G >= 8 ? 8 : 12) / W)
         }
       }
     } else {
-      // segment cut between warps: publish (acc, m, l), take a ticket; the
+      // segment cut between warps: publish (acc, m, l) now; the
       // last warp to arrive combines every piece and writes the output
       float* pslot = partial_slot<G, D>(a, wk, gw, u0);
       if (lane < SL) {
@@ -423,11 +425,15 @@ __global__ void __launch_bounds__(W * 32, (G >= 8 ? 8 : 12) / W)
           pslot[G * D + h] = m_run[h];
           pslot[G * D + G + h] = l_all[h];
         }
-      ticket_and_merge<QT, G, D>(a, wk, T, NW, lane);
+      // the ticket is taken when this warp's whole range is done
+      if (ncut == 0) cut0 = cut_piece_of(wk); else cut1 = cut_piece_of(wk);
+      ++ncut;
     }
     ++piece;
     walker_next_piece<BS>(wk, a, u1);
   }
+
+  if constexpr (BALANCED) finish_cut_pieces<QT, G, D>(a, cut0, cut1, ncut, T, NW, lane);
 
   // Leave no copy in flight: wait (bounded) for every stage this warp filled
   // but did not wait for (only possible after a timeout).

@@ -243,52 +243,37 @@ __device__ __forceinline__ float* partial_slot(const DecodeArgs& a, const Walker
 }
 
 // ----------------------------------------------------------------------------
-// A segment cut between warps.  The caller has written its piece's
-// unnormalised (acc[G][D], m[G] in log2 units, l[G]) to its slot.  Take the
-// segment's ticket; the last of its pieces to arrive combines all of them by
-// log-sum-exp and writes the output rows (lane-parallel: lanes take slots for
-// the maxima and weights, then lanes < D / 4 own 4 dims each).
+// Segments cut between warps.  A warp's cut pieces are at most its first
+// piece (when its range starts inside a segment) and its last (when the range
+// ends inside one).  The warp writes a cut piece's unnormalised
+// (acc[G][D], m[G] in log2 units, l[G]) to its slot as soon as the piece ends
+// -- plain stores, no wait -- and takes the segments' tickets only when its
+// whole range is done, behind one fence; the last piece of a segment to take
+// its ticket merges every piece by log-sum-exp and writes the output rows.
+// Nothing waits for another warp.
 // ----------------------------------------------------------------------------
+struct CutPiece {
+  int s, unit, nb;
+  int64_t seg_u;  // linear index of the segment's first tile
+};
+
+__device__ __forceinline__ CutPiece cut_piece_of(const Walker& wk) { return CutPiece{wk.s, wk.unit, wk.nb, wk.seg_u}; }
+
+// Merge all pieces of segment `cp` (lane-parallel; lanes < D / 4 own 4 dims).
 template <class QT, int G, int D>
-__device__ __forceinline__ void ticket_and_merge(const DecodeArgs& a, const Walker& wk, int64_t T, int64_t NW,
-                                                 int lane) {
+__device__ __forceinline__ void merge_segment(const DecodeArgs& a, const CutPiece& cp, int64_t T, int64_t NW,
+                                              int lane) {
   constexpr int SLOT = G * D + 2 * G, DV = 4, SL = D / DV;
+  constexpr int NB = G <= 2 ? 8 : (G == 4 ? 4 : 2);  // pieces loaded per round trip
   const int d0 = (lane % SL) * DV;
-  __syncwarp();
-  __threadfence();
-  const int64_t seg_id = (int64_t)wk.s * a.units + wk.unit;
-  const int64_t w_first = owner_of(wk.seg_u, T, NW), w_last = owner_of(wk.seg_u + wk.nb - 1, T, NW);
-  int last = 0;
-  if (lane == 0) {
-    const int ticket = atomicAdd(a.counters + seg_id, 1);
-    last = (ticket == (int)(w_last - w_first));
-    if (last) a.counters[seg_id] = 0;  // ready for the next call
-  }
-  last = __shfl_sync(0xffffffffu, last, 0);
-  if (!last) return;
-  __threadfence();
   // pieces sit on warps w_first..w_last; the first one's slot depends on
   // whether the segment starts exactly at that warp's range
+  const int64_t w_first = owner_of(cp.seg_u, T, NW), w_last = owner_of(cp.seg_u + cp.nb - 1, T, NW);
   const int64_t n = w_last - w_first + 1;
-  const int64_t first_slot = (wk.seg_u != range_start(w_first, T, NW)) ? 2 * w_first + 1 : 2 * w_first;
+  const int64_t first_slot = (cp.seg_u != range_start(w_first, T, NW)) ? 2 * w_first + 1 : 2 * w_first;
   auto slot_of = [&](int64_t i) -> const float* {
     return a.partials + (size_t)(i == 0 ? first_slot : 2 * (w_first + i)) * SLOT;
   };
-  // maxima: lanes take slots in parallel
-  float M[G];
-#pragma unroll
-  for (int h = 0; h < G; ++h) M[h] = -CUDART_INF_F;
-  for (int64_t i = lane; i < n; i += 32) {
-    const float* pp = slot_of(i);
-#pragma unroll
-    for (int h = 0; h < G; ++h) M[h] = fmaxf(M[h], ld_cg(pp + G * D + h));
-  }
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M[h] = fmaxf(M[h], __shfl_xor_sync(0xffffffffu, M[h], off));
-    if (M[h] == -CUDART_INF_F) M[h] = 0.f;
-  }
   float den[G], num[G][DV];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
@@ -296,48 +281,139 @@ __device__ __forceinline__ void ticket_and_merge(const DecodeArgs& a, const Walk
 #pragma unroll
     for (int d = 0; d < DV; ++d) num[h][d] = 0.f;
   }
-  for (int64_t base = 0; base < n; base += 32) {
-    // lane i holds the weights of slot base + i
-    float f[G];
-    if (base + lane < n) {
-      const float* pp = slot_of(base + lane);
+  if (n <= NB) {
+    // the common case: every piece's (m, l, acc) in one round of loads
+    float mm[NB][G], ll[NB][G];
+    float4 oo[NB][G];
+#pragma unroll
+    for (int i = 0; i < NB; ++i) {
+      const float* pp = slot_of(i < n ? i : 0);
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        f[h] = fast_exp2(ld_cg(pp + G * D + h) - M[h]);
-        den[h] += f[h] * ld_cg(pp + G * D + G + h);
+        mm[i][h] = i < n ? ld_cg(pp + G * D + h) : -CUDART_INF_F;
+        ll[i][h] = i < n ? ld_cg(pp + G * D + G + h) : 0.f;
+        oo[i][h] = (i < n && lane < SL) ? ld_cg(reinterpret_cast<const float4*>(pp + h * D + d0))
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-    } else {
-#pragma unroll
-      for (int h = 0; h < G; ++h) f[h] = 0.f;
     }
-    const int cnt = (int)(n - base < 32 ? n - base : 32);
-#pragma unroll 4
-    for (int jj = 0; jj < cnt; ++jj) {
-      const float* pp = slot_of(base + jj);
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float fj = __shfl_sync(0xffffffffu, f[h], jj);
-        if (lane < SL) {
-          const float4 v = ld_cg(reinterpret_cast<const float4*>(pp + h * D + d0));
-          num[h][0] += fj * v.x;
-          num[h][1] += fj * v.y;
-          num[h][2] += fj * v.z;
-          num[h][3] += fj * v.w;
+    for (int h = 0; h < G; ++h) {
+      float M = -CUDART_INF_F;
+#pragma unroll
+      for (int i = 0; i < NB; ++i) M = fmaxf(M, mm[i][h]);
+      if (M == -CUDART_INF_F) M = 0.f;
+#pragma unroll
+      for (int i = 0; i < NB; ++i) {
+        const float f = fast_exp2(mm[i][h] - M);
+        den[h] += f * ll[i][h];
+        num[h][0] += f * oo[i][h].x;
+        num[h][1] += f * oo[i][h].y;
+        num[h][2] += f * oo[i][h].z;
+        num[h][3] += f * oo[i][h].w;
+      }
+    }
+  } else {
+    // many pieces: lanes take slots for the maxima and weights, then the
+    // accumulators stream in rounds of NB slots
+    float M[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) M[h] = -CUDART_INF_F;
+    for (int64_t i = lane; i < n; i += 32) {
+      const float* pp = slot_of(i);
+#pragma unroll
+      for (int h = 0; h < G; ++h) M[h] = fmaxf(M[h], ld_cg(pp + G * D + h));
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) M[h] = fmaxf(M[h], __shfl_xor_sync(0xffffffffu, M[h], off));
+      if (M[h] == -CUDART_INF_F) M[h] = 0.f;
+    }
+    for (int64_t base = 0; base < n; base += 32) {
+      // lane i holds the weights of slot base + i
+      float f[G];
+      if (base + lane < n) {
+        const float* pp = slot_of(base + lane);
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          f[h] = fast_exp2(ld_cg(pp + G * D + h) - M[h]);
+          den[h] += f[h] * ld_cg(pp + G * D + G + h);
         }
+      } else {
+#pragma unroll
+        for (int h = 0; h < G; ++h) f[h] = 0.f;
+      }
+      const int cnt = (int)(n - base < 32 ? n - base : 32);
+#pragma unroll 1
+      for (int jj = 0; jj < cnt; jj += NB) {
+        float4 oo[NB][G];
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+          const float* pp = slot_of(base + (jj + i < cnt ? jj + i : jj));
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+            oo[i][h] = (jj + i < cnt && lane < SL) ? ld_cg(reinterpret_cast<const float4*>(pp + h * D + d0))
+                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < NB; ++i)
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float fj = __shfl_sync(0xffffffffu, f[h], (jj + i) & 31);
+            const float w = jj + i < cnt ? fj : 0.f;
+            num[h][0] += w * oo[i][h].x;
+            num[h][1] += w * oo[i][h].y;
+            num[h][2] += w * oo[i][h].z;
+            num[h][3] += w * oo[i][h].w;
+          }
       }
     }
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) den[h] += __shfl_xor_sync(0xffffffffu, den[h], off);
   }
-  QT* out = reinterpret_cast<QT*>(a.out) + ((size_t)wk.s * a.num_q_heads + unit_first_head(a, wk, G)) * D;
+  const int kvh = cp.unit / a.units_per_kv, chunk = cp.unit % a.units_per_kv;
+  QT* out = reinterpret_cast<QT*>(a.out) + ((size_t)cp.s * a.num_q_heads + kvh * a.group + chunk * G) * D;
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) den[h] += __shfl_xor_sync(0xffffffffu, den[h], off);
     if (lane < SL) {
       const float inv = den[h] > 0.f ? a.out_scale / den[h] : 0.f;
 #pragma unroll
       for (int d = 0; d < DV; ++d) out[h * D + d0 + d] = from_f32<QT>(num[h][d] * inv);
     }
   }
+}
+
+// Take the tickets of this warp's cut pieces (n of them, 0..2) behind one
+// fence, then merge the segments whose last ticket this warp drew.
+template <class QT, int G, int D>
+__device__ __forceinline__ void finish_cut_pieces(const DecodeArgs& a, const CutPiece& c0, const CutPiece& c1,
+                                                  int n, int64_t T, int64_t NW, int lane) {
+  if (n == 0) return;
+  __threadfence();  // this warp's partial slots before its tickets
+  __syncwarp();
+  int last0 = 0, last1 = 0;
+  if (lane == 0) {
+    auto take = [&](const CutPiece& cp) -> int* {
+      return a.counters + ((int64_t)cp.s * a.units + cp.unit);
+    };
+    auto pieces = [&](const CutPiece& cp) -> int {
+      return (int)(owner_of(cp.seg_u + cp.nb - 1, T, NW) - owner_of(cp.seg_u, T, NW));
+    };
+    // both atomics in flight before either result is used
+    const int t0 = atomicAdd(take(c0), 1);
+    const int t1 = n > 1 ? atomicAdd(take(c1), 1) : -1;
+    last0 = t0 == pieces(c0);
+    last1 = n > 1 && t1 == pieces(c1);
+    if (last0) *take(c0) = 0;  // ready for the next call
+    if (last1) *take(c1) = 0;
+  }
+  last0 = __shfl_sync(0xffffffffu, last0, 0);
+  last1 = __shfl_sync(0xffffffffu, last1, 0);
+  if (last0 | last1) __threadfence();  // every other piece's slot before the reads
+  if (last0) merge_segment<QT, G, D>(a, c0, T, NW, lane);
+  if (last1) merge_segment<QT, G, D>(a, c1, T, NW, lane);
 }
 
 }  // namespace pkv

@@ -324,6 +324,8 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
   // ---------------------------------------------------------------- consume side
   Walker wk = wk0;
   int consumed = 0, waited = 0, piece = 0;
+  CutPiece cut0{}, cut1{};  // this warp's cut pieces (its first and last at most)
+  int ncut = 0;
   bool alive = true;
   uint32_t qa[KS][2];     // q.K A operand: row g, (a0, a2) per k-step
   float o[NTO][4];        // accumulators, columns 2t, 2t+1 of each n-tile: [0..1] the
@@ -628,7 +630,7 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
         }
       }
     } else {
-      // segment cut between warps: publish (acc, m, l), take a ticket
+      // segment cut between warps: publish (acc, m, l) now
       float* pslot = partial_slot<G, D>(a, wk, gw, u0);
       if (g < G) {
 #pragma unroll
@@ -640,11 +642,15 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
           pslot[G * D + G + g] = l_row;
         }
       }
-      ticket_and_merge<QT, G, D>(a, wk, T, NW, lane);
+      // the ticket is taken when this warp's whole range is done
+      if (ncut == 0) cut0 = cut_piece_of(wk); else cut1 = cut_piece_of(wk);
+      ++ncut;
     }
     ++piece;
     walker_next_piece<BS>(wk, a, u1);
   }
+
+  if constexpr (BALANCED) finish_cut_pieces<QT, G, D>(a, cut0, cut1, ncut, T, NW, lane);
 
   // Leave no copy in flight: wait (bounded) for every stage this warp filled
   // but did not wait for (only possible after a timeout).
