@@ -477,6 +477,82 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_copy(args):
+    """Block copies on the Llama-3-8B-shaped pool (16,384 blocks of 8 kv heads
+    x 16 tokens x 128 dims, bf16): copy-on-write of random block pairs inside
+    the device pool, or swap of blocks to a pinned host pool and back.  One
+    JSON line; GB/s counts every byte read and written."""
+    import paged_kv_cache_22_gb300 as pkv
+    ws, rank, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pkv.library()
+    nb, hkv, bs, d = 16384, 8, 16, 128
+    block_bytes = hkv * bs * d * 2
+    g = torch.Generator().manual_seed(77 + rank)
+    kc = torch.randn((nb, hkv, bs, d), generator=g).to(torch.bfloat16).to(dev)
+    vc = torch.randn((nb, hkv, bs, d), generator=g).to(torch.bfloat16).to(dev)
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream()
+    if args.op == "copy_blocks":
+        n = 4096  # 2 x 4096 x 32 KiB read + written per call
+        perm = torch.randperm(nb, generator=g)
+        pairs = torch.stack([perm[:n], perm[n:2 * n]], 1).to(torch.int64).to(dev)
+        calls = [lambda: pkv.copy_blocks(kc, vc, kc, vc, pairs)]
+        moved = n * 2 * block_bytes * 2
+        what = "copy-on-write of 4096 random block pairs inside one device pool"
+    else:
+        n = 2048
+        hk = torch.empty((n, hkv, bs, d), dtype=torch.bfloat16).pin_memory()
+        hv = torch.empty_like(hk).pin_memory()
+        perm = torch.randperm(nb, generator=g)
+        out_pairs = torch.stack([perm[:n], torch.arange(n)], 1).to(torch.int64).to(dev)
+        in_pairs = torch.stack([torch.arange(n), perm[n:2 * n]], 1).to(torch.int64).to(dev)
+        calls = [lambda: pkv.copy_blocks(hk, hv, kc, vc, out_pairs),
+                 lambda: pkv.copy_blocks(kc, vc, hk, hv, in_pairs)]
+        moved = 2 * n * 2 * block_bytes * 2
+        what = "swap of 2048 blocks device -> pinned host, then 2048 host -> device"
+    for _ in range(args.warmup):
+        flush(1)
+        for c in calls:
+            c()
+    torch.cuda.synchronize()
+    if pkv.get_device_error():
+        raise RuntimeError("device error during warm-up")
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    K = min(args.steps, 200)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for i in range(K):
+        flush(i)
+        ev[i][0].record(stream)
+        for c in calls:
+            c()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if pkv.get_device_error():
+        raise RuntimeError("device error during the timed steps")
+    ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    gbs = moved / (ms * 1e-3) / 1e9
+    peak, peak_src = measured_peak()
+    line = {
+        "metric": f"{args.op} effective GB/s (bytes read + written)", "value": round(gbs, 1),
+        "unit": "GB/s", "n_gpus": 1, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 6),
+        "higher_is_better": True, "dtype": "bf16", "data": "synthetic (seeded N(0,1) pool)",
+        "config": {"workload": what, "block_bytes_per_cache": block_bytes, "pool_blocks": nb,
+                   "l2": "flushed between timed steps, outside the timed events"},
+        "roofline": ({"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "peak_source": peak_src,
+                      "unit": "GB/s", "frac": round(gbs / peak, 4)} if args.op == "copy_blocks" else
+                     {"bound": "host link", "achieved": round(gbs, 1), "peak": None, "unit": "GB/s",
+                      "frac": None}),
+        "gpu_launches": K * len(calls), "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -491,11 +567,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--engine", choices=["tensor_cores", "cuda_cores"], default="tensor_cores",
                     help="units that run q.K and P.V for bf16 / fp8 caches")
+    ap.add_argument("--op", choices=["decode", "copy_blocks", "swap"], default="decode",
+                    help="decode step (default), or the block-copy kernels alone")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.op != "decode":
+        run_copy(args)
     else:
         run_gpu(args)
 

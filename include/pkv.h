@@ -271,6 +271,38 @@ pkv_status pkv_gather_kv(void* k_out, void* v_out, const void* k_cache, const vo
                          pkv_stream_t stream);
 
 /*
+ * pkv_copy_blocks -- copy whole blocks (K and V, every kv head) from one
+ * block pool to another, or within one pool.
+ *
+ * Two uses in the pages: copy-on-write, where sequences that share a
+ * physical block diverge and the branch about to write gets its own copy
+ * first ("PagedAttention por dentro", section "Copy-on-write para sampling
+ * paralelo"; "La despensa por casilleros", section "Prefix caching:
+ * compartir casilleros con copy-on-write"); and swap, where a preempted
+ * sequence's blocks move to host memory and later come back ("PagedAttention
+ * por dentro", section "Evicción y preemption: qué hace cuando el pool se
+ * agota", the swap strategy).
+ *
+ *   k_dst, v_dst  destination pool [dst->num_blocks, Hkv, bs, d]
+ *   k_src, v_src  source pool [src->num_blocks, Hkv, bs, d]: same block_size,
+ *                 num_kv_heads, head_dim and dtype as the destination (the
+ *                 pools may differ in num_blocks)
+ *   block_pairs   int64 [num_pairs][2], (source block, destination block)
+ *
+ * Every pointer is a device address: device memory, or page-locked host
+ * memory mapped into the device's address space (as cudaHostAlloc returns
+ * it), which is how a swap reaches host memory.  The pools are 16-byte
+ * aligned, block_pairs 8-byte aligned.  The copies of one call run
+ * concurrently: a destination block must not be the source or the
+ * destination of another pair of the same call.  The copy is bit-exact.  A
+ * pair with an id outside its pool sets PKV_DEVERR_BAD_BLOCK_ID and is
+ * skipped.  Asynchronous on `stream`.
+ */
+pkv_status pkv_copy_blocks(void* k_dst, void* v_dst, const pkv_cache_desc* dst, const void* k_src,
+                           const void* v_src, const pkv_cache_desc* src, const int64_t* block_pairs,
+                           int32_t num_pairs, pkv_stream_t stream);
+
+/*
  * pkv_get_device_error -- synchronise `stream`, then read and clear the
  * current device's error word (PKV_DEVERR_* bits) into *code_out.
  */

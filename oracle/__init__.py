@@ -67,6 +67,9 @@ def _load():
             lib.orc_reshape_and_cache.restype = c_int
             lib.orc_reshape_and_cache.argtypes = [vp, vp, c_int, c_int, c_int, c_int, vp, vp,
                                                   c_int, c_int, c_int, vp, c_f]
+            lib.orc_copy_blocks.restype = c_int
+            lib.orc_copy_blocks.argtypes = [vp, vp, c_int, vp, vp, c_int, c_int, c_int, c_int, c_int,
+                                            vp, c_int]
             lib.orc_gather_kv.restype = c_int
             lib.orc_gather_kv.argtypes = [vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int,
                                           vp, c_int, vp, vp, c_int]
@@ -166,6 +169,20 @@ def gather_kv(k_cache: np.ndarray, v_cache: np.ndarray, block_tables: np.ndarray
                              dtype_code(k_cache), NB, Hkv, bs, d, _ptr(tables), tables.shape[1],
                              _ptr(lens), _ptr(cu), len(lens)), "gather_kv")
     return k_out, v_out
+
+
+def copy_blocks(k_dst: np.ndarray, v_dst: np.ndarray, k_src: np.ndarray, v_src: np.ndarray,
+                pairs: np.ndarray) -> None:
+    """In place: block ``pairs[i, 0]`` of the source pool replaces block
+    ``pairs[i, 1]`` of the destination pool, K and V, pairs in order."""
+    lib = _load()
+    if k_dst.dtype != k_src.dtype or k_dst.shape[1:] != k_src.shape[1:]:
+        raise ValueError("pools differ in block geometry or element type")
+    NB_d, Hkv, bs, d = k_dst.shape
+    pr = np.ascontiguousarray(pairs, dtype=np.int64).reshape(-1, 2)
+    _check(lib.orc_copy_blocks(_ptr(k_dst), _ptr(v_dst), NB_d, _ptr(k_src), _ptr(v_src),
+                               k_src.shape[0], dtype_code(k_src), Hkv, bs, d, _ptr(pr), pr.shape[0]),
+           "copy_blocks")
 
 
 # ---------------------------------------------------------------- attention

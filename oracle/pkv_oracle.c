@@ -17,6 +17,13 @@
  *    (section "El mecanismo: bloques, block table y el gather del kernel"):
  *    walk a sequence's physical blocks in logical order and read K and V as
  *    if they were contiguous.
+ *  - orc_copy_blocks: whole-block copies between pools.  "PagedAttention
+ *    por dentro" (sections "Copy-on-write para sampling paralelo" and
+ *    "Evicción y preemption: qué hace cuando el pool se agota", the swap
+ *    strategy) and "La despensa por casilleros" (section "Prefix caching:
+ *    compartir casilleros con copy-on-write"): a shared block is copied for
+ *    the branch about to write it; a preempted sequence's blocks move to
+ *    host memory and back.  A plain byte copy per pair.
  *  - orc_paged_attention_decode: the decode attention definition,
  *    softmax(q . K^T * scale) . V over every cached token of the sequence,
  *    the current one included ("Optimización de Inferencia LLM", section
@@ -208,6 +215,27 @@ int orc_gather_kv(void* k_out, void* v_out, const void* k_cache, const void* v_c
         memcpy((char*)v_out + dst, (const char*)v_cache + src, row);
       }
     }
+  }
+  return ORC_OK;
+}
+
+/* Whole-block copies between pools (copy-on-write of a shared block, swap
+ * to host memory and back): for each pair (src, dst), block src of both
+ * source caches replaces block dst of both destination caches.  A block of
+ * one cache is num_kv_heads * block_size * head_dim contiguous elements.
+ * The pairs are applied in order; an id outside its pool stops the call
+ * with ORC_ERR_RANGE before anything of that pair is written. */
+int orc_copy_blocks(void* k_dst, void* v_dst, int dst_blocks, const void* k_src, const void* v_src,
+                    int src_blocks, int cache_dtype, int num_kv_heads, int block_size, int head_dim,
+                    const int64_t* pairs, int num_pairs) {
+  size_t es = elem_size(cache_dtype);
+  if (es == 0) return ORC_ERR_ARG;
+  size_t blk = (size_t)num_kv_heads * block_size * head_dim * es;
+  for (int i = 0; i < num_pairs; ++i) {
+    int64_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+    if (src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks) return ORC_ERR_RANGE;
+    memcpy((char*)k_dst + (size_t)dst * blk, (const char*)k_src + (size_t)src * blk, blk);
+    memcpy((char*)v_dst + (size_t)dst * blk, (const char*)v_src + (size_t)src * blk, blk);
   }
   return ORC_OK;
 }

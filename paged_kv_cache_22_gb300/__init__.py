@@ -15,6 +15,8 @@ Entry points (same names as the C ABI, without the ``pkv_`` prefix):
   overlapping its prologue with the cache write;
 * :func:`split_kv_reduce` -- log-sum-exp merge of partition partials;
 * :func:`gather_kv` -- contiguous copy of every sequence's cached tokens;
+* :func:`copy_blocks` -- whole-block copies between pools (copy-on-write of a
+  shared block, swap to pinned host memory and back);
 * :func:`decode_workspace_bytes`, :func:`get_device_error`;
 * :func:`set_decode_engine` / :func:`get_decode_engine` (and the
   :func:`decode_engine` context manager) -- tensor cores (default) or CUDA
@@ -33,7 +35,7 @@ import torch
 __all__ = [
     "PkvError", "CacheDesc", "kv_reshape_and_cache", "paged_attention_decode", "decode_step",
     "split_kv_reduce",
-    "gather_kv", "decode_workspace_bytes", "get_device_error", "library", "library_path",
+    "gather_kv", "copy_blocks", "decode_workspace_bytes", "get_device_error", "library", "library_path",
     "DecodeWorkspace", "F32", "BF16", "FP8_E4M3", "DEVERR_BAD_BLOCK_ID", "DEVERR_BAD_SLOT",
     "DEVERR_BAD_SEQ_LEN", "DEVERR_WAIT_TIMEOUT", "DEVERR_SMEM_ALIGN", "set_decode_engine",
     "get_decode_engine", "decode_engine", "ENGINE_TENSOR_CORES", "ENGINE_CUDA_CORES",
@@ -88,6 +90,7 @@ def library() -> ctypes.CDLL:
             "pkv_decode_step": [vp, vp, ctypes.c_int, i32, vp, vp, vp, desc, vp, vp, ctypes.c_int, i32,
                                 i32, vp, i32, vp, i32, f32, f32, i32, vp, sz, vp],
             "pkv_get_device_error": [ctypes.POINTER(ctypes.c_uint32), vp],
+            "pkv_copy_blocks": [vp, vp, desc, vp, vp, desc, vp, i32, vp],
             "pkv_status_string": [ctypes.c_int],
             "pkv_device_sm_count": [],
             "pkv_set_decode_engine": [ctypes.c_int],
@@ -314,6 +317,30 @@ def gather_kv(k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.
         _ptr(block_tables), int(block_tables.shape[1]), _ptr(seq_lens), _ptr(cu_seq_lens),
         int(seq_lens.numel()), int(max_seq_len), _stream(stream)), "gather_kv")
     return k_out, v_out
+
+
+def _addr(t: torch.Tensor):
+    """Device address of a CUDA tensor or of a pinned host tensor (pinned
+    host memory is mapped into the device's address space)."""
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError("tensors must live on the CUDA device or in pinned host memory")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def copy_blocks(k_dst: torch.Tensor, v_dst: torch.Tensor, k_src: torch.Tensor, v_src: torch.Tensor,
+                block_pairs: torch.Tensor, stream=None) -> None:
+    """Copy blocks ``block_pairs[i] = (src, dst)`` (int64 ``[n, 2]``) of the
+    pool ``k_src / v_src`` into the pool ``k_dst / v_dst`` (the same pool for
+    copy-on-write; a pinned host pool for swap).  Every tensor may be a CUDA
+    tensor or a pinned host tensor."""
+    if block_pairs.dtype != torch.int64 or block_pairs.dim() != 2 or block_pairs.shape[1] != 2:
+        raise ValueError("block_pairs must be int64 [n, 2]")
+    dd, sd = _desc(k_dst, None), _desc(k_src, None)
+    _check(library().pkv_copy_blocks(_addr(k_dst), _addr(v_dst), ctypes.byref(dd), _addr(k_src), _addr(v_src),
+                                     ctypes.byref(sd), _addr(block_pairs), int(block_pairs.shape[0]),
+                                     _stream(stream)), "copy_blocks")
 
 
 def get_device_error(stream=None) -> int:

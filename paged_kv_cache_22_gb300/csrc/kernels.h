@@ -46,6 +46,19 @@ struct ReduceArgs {
   int num_seqs, num_q_heads, head_dim, partition_tokens, max_partitions;
 };
 
+struct CopyBlocksArgs {
+  unsigned int* err;
+  void* k_dst;
+  void* v_dst;
+  const void* k_src;
+  const void* v_src;
+  int64_t src_blocks, dst_blocks;
+  int64_t block_bytes;   // Hkv * bs * d * e: one block of one cache, a multiple of 16
+  const int64_t* pairs;  // [num_pairs][2] = (source block, destination block)
+  int64_t num_pairs;
+};
+
+cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t stream);
 cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, int src_is_bf16, cudaStream_t stream);
 cudaError_t launch_gather_kv(const GatherArgs& a, int max_seq_len, cudaStream_t stream);
 cudaError_t launch_split_kv_reduce(const ReduceArgs& a, int out_is_bf16, cudaStream_t stream);

@@ -497,6 +497,35 @@ pkv_status pkv_gather_kv(void* k_out, void* v_out, const void* k_cache, const vo
   return from_cuda(launch_gather_kv(a, max_seq_len, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+pkv_status pkv_copy_blocks(void* k_dst, void* v_dst, const pkv_cache_desc* dst, const void* k_src,
+                           const void* v_src, const pkv_cache_desc* src, const int64_t* block_pairs,
+                           int32_t num_pairs, pkv_stream_t stream) {
+  if (num_pairs < 0 || !valid_cache_desc(dst) || !valid_cache_desc(src)) return PKV_ERR_INVALID_ARG;
+  if (dst->block_size != src->block_size || dst->num_kv_heads != src->num_kv_heads ||
+      dst->head_dim != src->head_dim || dst->dtype != src->dtype)
+    return PKV_ERR_INVALID_ARG;
+  if (num_pairs == 0) return PKV_OK;
+  if (!k_dst || !v_dst || !k_src || !v_src || !block_pairs) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(k_dst) || !aligned16(v_dst) || !aligned16(k_src) || !aligned16(v_src) ||
+      (reinterpret_cast<uintptr_t>(block_pairs) & 7u))
+    return PKV_ERR_INVALID_ARG;
+  const int dev = current_device();
+  unsigned int* err = dev < 0 ? nullptr : error_word(dev);
+  if (!err) return PKV_ERR_CUDA;
+  CopyBlocksArgs a;
+  a.err = err;
+  a.k_dst = k_dst;
+  a.v_dst = v_dst;
+  a.k_src = k_src;
+  a.v_src = v_src;
+  a.src_blocks = src->num_blocks;
+  a.dst_blocks = dst->num_blocks;
+  a.block_bytes = (int64_t)src->num_kv_heads * src->block_size * src->head_dim * elem_bytes(src->dtype);
+  a.pairs = block_pairs;
+  a.num_pairs = num_pairs;
+  return from_cuda(launch_copy_blocks(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 pkv_status pkv_get_device_error(uint32_t* code_out, pkv_stream_t stream) {
   if (!code_out) return PKV_ERR_INVALID_ARG;
   const int dev = current_device();

@@ -442,3 +442,61 @@ def test_config_shapes():
     lens = w.seq_lens.numpy()
     assert lens.min() >= 16 and lens.max() <= 8192 and len(lens) == 128
     assert w.num_blocks == math.ceil(1.1 * sum(-(-int(L) // 16) for L in lens))
+
+
+# ---------------------------------------------------------------- block copies
+def _pool(rng, nb, hkv=2, bs=16, d=64):
+    k = rng.integers(0, 1 << 16, size=(nb, hkv, bs, d), dtype=np.uint16)
+    v = rng.integers(0, 1 << 16, size=(nb, hkv, bs, d), dtype=np.uint16)
+    return k, v
+
+
+def test_copy_on_write_keeps_the_shared_block_and_diverges_the_copy():
+    """Two sequences share their first block; the branch about to write gets
+    a copy first.  Through the (independent) gather: right after the copy both
+    sequences read the same tokens; after the write into the copy only the
+    writer's token changes, and the other sequence still reads the original."""
+    rng = np.random.default_rng(7)
+    kc, vc = _pool(rng, 8)
+    tables = np.array([[3, 5], [3, 6]], dtype=np.int32)  # block 3 shared
+    lens = np.array([20, 20], dtype=np.int32)
+    before_k, before_v = oracle.gather_kv(kc, vc, tables, lens)
+    oracle.copy_blocks(kc, vc, kc, vc, np.array([[3, 1]]))  # COW: 3 -> fresh block 1
+    tables_b = tables.copy()
+    tables_b[1, 0] = 1
+    k1, v1 = oracle.gather_kv(kc, vc, tables_b, lens)
+    assert np.array_equal(k1, before_k) and np.array_equal(v1, before_v)
+    # sequence 1 writes token 4 (inside its copy, slot 1*16 + 4)
+    new = rng.standard_normal((1, 2, 64)).astype(np.float32)
+    oracle.reshape_and_cache(new, new, kc, vc, np.array([1 * 16 + 4]), 1.0)
+    k2, v2 = oracle.gather_kv(kc, vc, tables_b, lens)
+    diff = np.nonzero(np.any(k2 != before_k, axis=(1, 2)))[0]
+    assert diff.tolist() == [20 + 4], "only the writer's token changes"
+    k_a, _ = oracle.gather_kv(kc, vc, tables[:1], lens[:1])
+    assert np.array_equal(k_a, before_k[:20]), "the shared block is untouched"
+
+
+def test_swap_out_and_back_to_other_ids_preserves_every_token():
+    """Swap a sequence's blocks to a host pool and back into different device
+    blocks; with the table rewritten to the new ids the gather is unchanged."""
+    rng = np.random.default_rng(8)
+    kc, vc = _pool(rng, 12)
+    host_k, host_v = np.zeros((4, 2, 16, 64), np.uint16), np.zeros((4, 2, 16, 64), np.uint16)
+    table = np.array([[9, 2, 7]], dtype=np.int32)
+    lens = np.array([40], dtype=np.int32)
+    ref_k, ref_v = oracle.gather_kv(kc, vc, table, lens)
+    oracle.copy_blocks(host_k, host_v, kc, vc, np.array([[9, 0], [2, 1], [7, 2]]))
+    oracle.copy_blocks(kc, vc, host_k, host_v, np.array([[0, 4], [1, 10], [2, 0]]))
+    got_k, got_v = oracle.gather_kv(kc, vc, np.array([[4, 10, 0]], dtype=np.int32), lens)
+    assert np.array_equal(got_k, ref_k) and np.array_equal(got_v, ref_v)
+
+
+def test_copy_blocks_rejects_ids_outside_the_pools():
+    rng = np.random.default_rng(9)
+    kc, vc = _pool(rng, 4)
+    snap = kc.copy()
+    with pytest.raises(oracle.OracleError):
+        oracle.copy_blocks(kc, vc, kc, vc, np.array([[0, 4]]))
+    with pytest.raises(oracle.OracleError):
+        oracle.copy_blocks(kc, vc, kc, vc, np.array([[-1, 2]]))
+    assert np.array_equal(kc, snap)
