@@ -405,3 +405,32 @@ def test_outputs_are_correctly_rounded(pkv, engine, case, pt):
     want = 0.99
     assert exact_share >= want, f"{name}: {exact_share:.4f} of outputs correctly rounded (< {want})"
     assert steps <= 1.0, f"{name}: an output is {steps:.2f} bf16 steps from the exact value"
+
+
+# ------------------------------------------------------------------ out-of-pool tables at scale
+@pytest.mark.parametrize("dt", ["bf16", "fp8_e4m3"])
+def test_out_of_pool_tables_in_half_the_batch(pkv, dt):
+    """The first half of a full-size batch has tables pointing outside the
+    pool: those tiles are skipped (flagged, never read), so the warps of the
+    balanced split holding them finish at once while the rest stream.  Every
+    clean row must still match the oracle, call after call (the merge
+    counters come back to zero)."""
+    import os
+    n_bad, n_good = 40, 40
+    w = workloads.make_workload("halfbad", [2048] * (n_bad + n_good), 32, 8, 128, 16, dt, seed=91)
+    kc, vc = gpu_caches(pkv, w)
+    okc, ovc = oracle_caches(w)
+    tables = w.block_tables.clone()
+    used = tables[:n_bad] != workloads.UNUSED_TABLE_ENTRY
+    tables[:n_bad][used] = w.num_blocks + 5
+    ref = oracle.paged_attention_decode(to_np(w.q[n_bad:]), okc, ovc, to_np(w.block_tables[n_bad:]),
+                                        to_np(w.seq_lens[n_bad:]), w.scale, w.kv_scale,
+                                        os.cpu_count() or 4)
+    q = w.q.to(DEV)
+    for rep in range(3):
+        out = torch.full_like(q, float("nan"))
+        pkv.paged_attention_decode(out, q, kc, vc, tables.to(DEV), w.seq_lens.to(DEV), w.scale,
+                                   w.kv_scale, max_seq_len=w.max_seq_len)
+        assert pkv.get_device_error() == pkv.DEVERR_BAD_BLOCK_ID
+        got = out[n_bad:].float().cpu().numpy().astype(np.float64)
+        assert_close(got, ref, TOL[dt], f"clean rows, call {rep}")
