@@ -73,6 +73,11 @@ def _load():
             lib.orc_gather_kv.restype = c_int
             lib.orc_gather_kv.argtypes = [vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int,
                                           vp, c_int, vp, vp, c_int]
+            lib.orc_paged_attention_decode_window.restype = c_int
+            lib.orc_paged_attention_decode_window.argtypes = [vp, vp, c_int, c_int, c_int, vp, vp,
+                                                              c_int, c_int, c_int, c_int, c_int, vp,
+                                                              c_int, vp, c_d, c_d, c_int, c_int,
+                                                              c_int]
             lib.orc_paged_attention_decode.restype = c_int
             lib.orc_paged_attention_decode.argtypes = [vp, vp, c_int, c_int, c_int, vp, vp, c_int,
                                                        c_int, c_int, c_int, c_int, vp, c_int, vp,
@@ -188,8 +193,11 @@ def copy_blocks(k_dst: np.ndarray, v_dst: np.ndarray, k_src: np.ndarray, v_src: 
 # ---------------------------------------------------------------- attention
 def paged_attention_decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
                            block_tables: np.ndarray, seq_lens: np.ndarray, scale: float,
-                           kv_scale: float = 1.0, threads: int = 1) -> np.ndarray:
-    """fp64 ``[B, Hq, d]`` decode attention over each sequence's paged K/V."""
+                           kv_scale: float = 1.0, threads: int = 1, window: int = 0,
+                           sinks: int = 0) -> np.ndarray:
+    """fp64 ``[B, Hq, d]`` decode attention over each sequence's paged K/V.
+    ``window > 0``: a sequence of length L attends only its first ``sinks``
+    and last ``window`` tokens."""
     lib = _load()
     B, Hq, d = q.shape
     NB, Hkv, bs, d2 = k_cache.shape
@@ -198,10 +206,10 @@ def paged_attention_decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarr
     tables = np.ascontiguousarray(block_tables, dtype=np.int32)
     lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
     out = np.zeros((B, Hq, d), dtype=np.float64)
-    _check(lib.orc_paged_attention_decode(_ptr(out), _ptr(q), dtype_code(q), B, Hq, _ptr(k_cache),
-                                          _ptr(v_cache), dtype_code(k_cache), NB, Hkv, bs, d,
-                                          _ptr(tables), tables.shape[1], _ptr(lens), float(scale),
-                                          float(kv_scale), int(threads)), "paged_attention_decode")
+    _check(lib.orc_paged_attention_decode_window(
+        _ptr(out), _ptr(q), dtype_code(q), B, Hq, _ptr(k_cache), _ptr(v_cache), dtype_code(k_cache),
+        NB, Hkv, bs, d, _ptr(tables), tables.shape[1], _ptr(lens), float(scale), float(kv_scale),
+        int(window), int(sinks), int(threads)), "paged_attention_decode")
     return out
 
 

@@ -30,7 +30,11 @@
  *    "El Cuello de Botella de Atención del que Nadie Habla", and "Capítulo 2",
  *    section "Qué guarda realmente el KV cache").  Query head qh reads kv
  *    head qh / (Hq / Hkv) (grouped-query sharing, "KV cache: la memoria de
- *    trabajo", section "Trucos para que el cuaderno sea más fino").
+ *    trabajo", section "Trucos para que el cuaderno sea más fino").  With a
+ *    sliding window the sum runs only over the window's last tokens and the
+ *    attention sinks, the first tokens ("PagedAttention por dentro",
+ *    sections "Sliding window attention" and "StreamingLLM (Xiao et al.,
+ *    2024): los attention sinks").
  *  - orc_partition_attention / orc_split_kv_reduce: the same attention
  *    restricted to fixed token partitions, and the log-sum-exp merge of the
  *    partitions.  The pages do not describe a split; this is the plain
@@ -263,18 +267,38 @@ typedef struct {
   double* o_part; /* [B, Hq, P, d] */
   double* m_part; /* [B, Hq, P] */
   double* l_part; /* [B, Hq, P] */
+  /* sliding window (window > 0): a sequence of length L attends only its
+   * first `sinks` tokens and its last `window` tokens */
+  int window, sinks;
   /* work distribution over (sequence, kv head) pairs */
   int next_unit;
   pthread_mutex_t lock;
   int status;
 } orc_job;
 
+/* Is token p of a sequence of length L attended?  Without a window every
+ * p < L is.  With one, only the first `sinks` tokens (attention sinks) and
+ * the last `window` tokens are ("PagedAttention por dentro", sections
+ * "Sliding window attention" and "StreamingLLM (Xiao et al., 2024): los
+ * attention sinks"). */
+static int attended(const orc_job* jb, int L, int p) {
+  if (p < 0 || p >= L) return 0;
+  if (jb->window <= 0 || L <= jb->window) return 1;
+  return p < jb->sinks || p >= L - jb->window;
+}
+
 /* Copy sequence s, kv head h into contiguous fp64 K and V ([L][d]) through
  * the block table: logical token p lives in physical block table[p / bs] at
- * offset p % bs. */
+ * offset p % bs.  Tokens that are not attended are left zero and their
+ * blocks are never looked at (an engine frees the blocks that fell out of
+ * the window). */
 static int gather_f64(const orc_job* jb, int s, int h, int L, double* K, double* V) {
   const int d = jb->head_dim, bs = jb->block_size;
   for (int p = 0; p < L; ++p) {
+    if (!attended(jb, L, p)) {
+      for (int i = 0; i < d; ++i) K[(size_t)p * d + i] = V[(size_t)p * d + i] = 0.0;
+      continue;
+    }
     int j = p / bs, off = p % bs;
     if (j >= jb->max_blocks_per_seq) return ORC_ERR_RANGE;
     int32_t blk = jb->block_tables[(size_t)s * jb->max_blocks_per_seq + j];
@@ -288,13 +312,16 @@ static int gather_f64(const orc_job* jb, int s, int h, int L, double* K, double*
   return ORC_OK;
 }
 
-/* softmax(scale * q . K[t]) . V over tokens t in [t0, t1); returns the
- * normalised output in o, the largest scaled score in *m_out and the sum of
- * exp(score - max) in *l_out. */
-static void attend_f64(const double* qv, const double* K, const double* V, int t0, int t1, int d,
-                       double scale, double* o, double* m_out, double* l_out, double* w) {
+/* softmax(scale * q . K[t]) . V over the attended tokens t in [t0, t1)
+ * (keep[t] != 0); returns the normalised output in o, the largest scaled
+ * score in *m_out and the sum of exp(score - max) in *l_out.  With no token
+ * attended: o = 0, m = -inf, l = 0. */
+static void attend_f64(const double* qv, const double* K, const double* V, const unsigned char* keep,
+                       int t0, int t1, int d, double scale, double* o, double* m_out, double* l_out,
+                       double* w) {
   double m = -INFINITY;
   for (int t = t0; t < t1; ++t) {
+    if (!keep[t]) continue;
     double dot = 0.0;
     for (int i = 0; i < d; ++i) dot += qv[i] * K[(size_t)t * d + i];
     w[t - t0] = scale * dot;
@@ -302,18 +329,23 @@ static void attend_f64(const double* qv, const double* K, const double* V, int t
   }
   double l = 0.0;
   for (int t = t0; t < t1; ++t) {
+    if (!keep[t]) continue;
     w[t - t0] = exp(w[t - t0] - m);
     l += w[t - t0];
   }
   for (int i = 0; i < d; ++i) o[i] = 0.0;
-  for (int t = t0; t < t1; ++t)
+  for (int t = t0; t < t1; ++t) {
+    if (!keep[t]) continue;
     for (int i = 0; i < d; ++i) o[i] += w[t - t0] * V[(size_t)t * d + i];
-  for (int i = 0; i < d; ++i) o[i] /= l;
+  }
+  if (l > 0.0)
+    for (int i = 0; i < d; ++i) o[i] /= l;
   *m_out = m;
   *l_out = l;
 }
 
-static int run_unit(orc_job* jb, int unit, double* K, double* V, double* qv, double* w) {
+static int run_unit(orc_job* jb, int unit, double* K, double* V, double* qv, double* w,
+                    unsigned char* keep) {
   const int d = jb->head_dim;
   const int g = jb->num_q_heads / jb->num_kv_heads;
   const int s = unit / jb->num_kv_heads, h = unit % jb->num_kv_heads;
@@ -321,6 +353,7 @@ static int run_unit(orc_job* jb, int unit, double* K, double* V, double* qv, dou
   if (L < 0) return ORC_ERR_RANGE;
   int rc = gather_f64(jb, s, h, L, K, V);
   if (rc != ORC_OK) return rc;
+  for (int p = 0; p < L; ++p) keep[p] = (unsigned char)attended(jb, L, p);
   for (int qh = h * g; qh < (h + 1) * g; ++qh) {
     size_t qbase = ((size_t)s * jb->num_q_heads + qh) * d;
     for (int i = 0; i < d; ++i) qv[i] = (double)load_as_f32(jb->q, jb->q_dtype, qbase + i);
@@ -331,7 +364,7 @@ static int run_unit(orc_job* jb, int unit, double* K, double* V, double* qv, dou
         continue;
       }
       double m, l;
-      attend_f64(qv, K, V, 0, L, d, jb->scale, o, &m, &l, w);
+      attend_f64(qv, K, V, keep, 0, L, d, jb->scale, o, &m, &l, w);
     } else {
       const int P = jb->partition_tokens;
       for (int p = 0; p < jb->max_partitions; ++p) {
@@ -344,7 +377,7 @@ static int run_unit(orc_job* jb, int unit, double* K, double* V, double* qv, dou
           jb->l_part[pi] = 0.0;
           continue;
         }
-        attend_f64(qv, K, V, t0, t1, d, jb->scale, o, &jb->m_part[pi], &jb->l_part[pi], w);
+        attend_f64(qv, K, V, keep, t0, t1, d, jb->scale, o, &jb->m_part[pi], &jb->l_part[pi], w);
       }
     }
   }
@@ -366,14 +399,15 @@ static void* worker(void* arg) {
   double* V = (double*)malloc(L * d * sizeof(double));
   double* qv = (double*)malloc((size_t)d * sizeof(double));
   double* w = (double*)malloc(L * sizeof(double));
-  int rc = (K && V && qv && w) ? ORC_OK : ORC_ERR_NOMEM;
+  unsigned char* keep = (unsigned char*)malloc(L);
+  int rc = (K && V && qv && w && keep) ? ORC_OK : ORC_ERR_NOMEM;
   const int units = jb->num_seqs * jb->num_kv_heads;
   while (rc == ORC_OK) {
     pthread_mutex_lock(&jb->lock);
     int u = jb->next_unit++;
     pthread_mutex_unlock(&jb->lock);
     if (u >= units) break;
-    rc = run_unit(jb, u, K, V, qv, w);
+    rc = run_unit(jb, u, K, V, qv, w, keep);
   }
   if (rc != ORC_OK) {
     pthread_mutex_lock(&jb->lock);
@@ -385,6 +419,7 @@ static void* worker(void* arg) {
   free(V);
   free(qv);
   free(w);
+  free(keep);
   return NULL;
 }
 
@@ -409,13 +444,15 @@ static int run_job(orc_job* jb, int num_threads) {
   return jb->status;
 }
 
-/* out: [num_seqs, num_q_heads, head_dim] doubles. */
-int orc_paged_attention_decode(double* out, const void* q, int q_dtype, int num_seqs,
-                               int num_q_heads, const void* k_cache, const void* v_cache,
-                               int cache_dtype, int num_blocks, int num_kv_heads, int block_size,
-                               int head_dim, const int32_t* block_tables, int max_blocks_per_seq,
-                               const int32_t* seq_lens, double scale, double kv_scale,
-                               int num_threads) {
+/* out: [num_seqs, num_q_heads, head_dim] doubles.  window > 0: each
+ * sequence attends only its first `sinks` and last `window` tokens. */
+int orc_paged_attention_decode_window(double* out, const void* q, int q_dtype, int num_seqs,
+                                      int num_q_heads, const void* k_cache, const void* v_cache,
+                                      int cache_dtype, int num_blocks, int num_kv_heads,
+                                      int block_size, int head_dim, const int32_t* block_tables,
+                                      int max_blocks_per_seq, const int32_t* seq_lens, double scale,
+                                      double kv_scale, int window, int sinks, int num_threads) {
+  if (window < 0 || sinks < 0) return ORC_ERR_ARG;
   orc_job jb;
   memset(&jb, 0, sizeof jb);
   jb.q = q;
@@ -434,8 +471,22 @@ int orc_paged_attention_decode(double* out, const void* q, int q_dtype, int num_
   jb.num_q_heads = num_q_heads;
   jb.scale = scale;
   jb.kv_scale = kv_scale;
+  jb.window = window;
+  jb.sinks = sinks;
   jb.out = out;
   return run_job(&jb, num_threads);
+}
+
+int orc_paged_attention_decode(double* out, const void* q, int q_dtype, int num_seqs,
+                               int num_q_heads, const void* k_cache, const void* v_cache,
+                               int cache_dtype, int num_blocks, int num_kv_heads, int block_size,
+                               int head_dim, const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* seq_lens, double scale, double kv_scale,
+                               int num_threads) {
+  return orc_paged_attention_decode_window(out, q, q_dtype, num_seqs, num_q_heads, k_cache, v_cache,
+                                           cache_dtype, num_blocks, num_kv_heads, block_size, head_dim,
+                                           block_tables, max_blocks_per_seq, seq_lens, scale, kv_scale,
+                                           0, 0, num_threads);
 }
 
 /* Per-partition attention: partition p of sequence s covers tokens

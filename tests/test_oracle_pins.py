@@ -500,3 +500,73 @@ def test_copy_blocks_rejects_ids_outside_the_pools():
     with pytest.raises(oracle.OracleError):
         oracle.copy_blocks(kc, vc, kc, vc, np.array([[-1, 2]]))
     assert np.array_equal(kc, snap)
+
+
+# ---------------------------------------------------------------- sliding window and sinks
+def _window_case(seed=31):
+    w = workloads.make_workload("win", [1, 5, 17, 40, 70], 8, 2, 64, 16, "f32", seed=seed)
+    kc, vc = oracle_caches(w)
+    return w, kc, vc
+
+
+def _decode(w, kc, vc, tables=None, **kw):
+    return oracle.paged_attention_decode(to_np(w.q), kc, vc, to_np(w.block_tables if tables is None else tables),
+                                         to_np(w.seq_lens), w.scale, w.kv_scale, 1, **kw)
+
+
+def test_window_covering_every_token_is_plain_attention():
+    w, kc, vc = _window_case()
+    plain = _decode(w, kc, vc)
+    assert np.array_equal(_decode(w, kc, vc, window=70), plain)
+    assert np.array_equal(_decode(w, kc, vc, window=20, sinks=50), plain)  # sinks + window >= L
+
+
+def test_window_of_one_returns_the_last_value():
+    w, kc, vc = _window_case()
+    got = _decode(w, kc, vc, window=1)
+    k_all, v_all = oracle.gather_kv(kc, vc, to_np(w.block_tables), to_np(w.seq_lens))
+    cu = np.concatenate([[0], np.cumsum(w.seq_lens.numpy())])
+    g = w.num_q_heads // w.num_kv_heads
+    for s in range(w.num_seqs):
+        last = v_all[cu[s + 1] - 1].astype(np.float64)  # [Hkv, d]
+        assert np.array_equal(got[s], np.repeat(last, g, axis=0))
+
+
+@pytest.mark.parametrize("window,sinks", [(8, 0), (8, 4), (20, 3), (33, 16)])
+def test_window_equals_brute_force_over_the_kept_tokens(window, sinks):
+    """numpy fp64 softmax over exactly the kept positions (first `sinks`,
+    last `window`) of the gathered sequence; the hole between the sinks and
+    the window lies inside one block for some lengths."""
+    w, kc, vc = _window_case()
+    got = _decode(w, kc, vc, window=window, sinks=sinks)
+    k_all, v_all = oracle.gather_kv(kc, vc, to_np(w.block_tables), to_np(w.seq_lens))
+    lens = w.seq_lens.numpy()
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    q = w.q.numpy().astype(np.float64)
+    g = w.num_q_heads // w.num_kv_heads
+    for s in range(w.num_seqs):
+        L = int(lens[s])
+        keep = [p for p in range(L) if L <= window or p < sinks or p >= L - window]
+        K = k_all[cu[s]:cu[s + 1]].astype(np.float64)[keep]  # [n, Hkv, d]
+        V = v_all[cu[s]:cu[s + 1]].astype(np.float64)[keep]
+        for qh in range(w.num_q_heads):
+            sc = w.scale * (K[:, qh // g] @ q[s, qh])
+            p = np.exp(sc - sc.max())
+            ref = (p[:, None] * V[:, qh // g]).sum(0) / p.sum()
+            assert np.abs(got[s, qh] - ref).max() < 1e-12
+
+
+def test_window_never_reads_blocks_outside_the_kept_tokens():
+    """Blocks holding no kept token may have been freed: their table entries
+    point outside the pool, and the result does not change."""
+    w, kc, vc = _window_case()
+    window, sinks, bs = 16, 4, w.block_size
+    ref = _decode(w, kc, vc, window=window, sinks=sinks)
+    tables = w.block_tables.clone()
+    for s, L in enumerate(w.seq_lens.tolist()):
+        for j in range(-(-L // bs)):
+            toks = range(j * bs, min(L, (j + 1) * bs))
+            if not any(L <= window or p < sinks or p >= L - window for p in toks):
+                tables[s, j] = w.num_blocks + 7
+    assert not torch.equal(tables, w.block_tables)
+    assert np.array_equal(_decode(w, kc, vc, tables=tables, window=window, sinks=sinks), ref)
