@@ -110,10 +110,10 @@ def job_throughput(world_size: int, bytes_per_rank_step: int, ms_per_step: float
     return world_size * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
 
 
-def step_bytes(w: workloads.Workload):
+def step_bytes(w: workloads.Workload, window: int = 0, sinks: int = 0):
     lens = w.seq_lens.tolist()
     dec = metrics.decode_bytes(lens, w.num_q_heads, w.num_kv_heads, w.head_dim, w.cache_dtype,
-                               w.q_dtype, w.block_size)
+                               w.q_dtype, w.block_size, window, sinks)
     rc = metrics.reshape_bytes(int(w.new_slots.numel()), w.num_kv_heads, w.head_dim, w.src_dtype,
                                w.cache_dtype)
     return dec, rc
@@ -230,13 +230,22 @@ def run_gpu(args):
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
 
+    win, sinks = args.window, args.sinks
+
     def step():
+        if win:  # the windowed decode after the cache write (two launches)
+            pkv.kv_reshape_and_cache(new_k, new_v, kc, vc, new_slots, w.kv_scale)
+            pkv.paged_attention_decode(out, q, kc, vc, tables, lens, w.scale, w.kv_scale,
+                                       max_seq_len=max_len, partition_tokens=pt, workspace=workspace,
+                                       window=win, sinks=sinks)
+            return
         pkv.decode_step(new_k, new_v, new_slots, out, q, kc, vc, tables, lens, w.scale, w.kv_scale,
                         max_seq_len=max_len, partition_tokens=pt, workspace=workspace)
 
     def decode_only():
         pkv.paged_attention_decode(out, q, kc, vc, tables, lens, w.scale, w.kv_scale,
-                                   max_seq_len=max_len, partition_tokens=pt, workspace=workspace)
+                                   max_seq_len=max_len, partition_tokens=pt, workspace=workspace,
+                                   window=win, sinks=sinks)
 
     for _ in range(args.warmup):
         flush(1)
@@ -277,7 +286,7 @@ def run_gpu(args):
     if pkv.get_device_error():
         raise RuntimeError("device error during the timed steps")
 
-    dec_b, rc_b = step_bytes(w)
+    dec_b, rc_b = step_bytes(w, win, sinks)
     ms_per_step = tot_ms / K
     value = job_throughput(ws, dec_b + rc_b, ms_per_step)
     dec_avg_ms = sum(dec_ms) / K
@@ -285,13 +294,13 @@ def run_gpu(args):
     peak, peak_src = measured_peak()
 
     # ---- end to end through the public API with host buffers
-    e2e = run_e2e(pkv, w, kc, vc, dev, pt, max(10, min(K, 200)), flush)
+    e2e = run_e2e(pkv, w, kc, vc, dev, pt, max(10, min(K, 200)), flush, win, sinks)
     e2e["ms_per_step"] = max_over_ranks(e2e["ms_per_step"], dev)
     e2e_value = job_throughput(ws, dec_b + rc_b, e2e["ms_per_step"])
 
     traffic = None
     if (TRAFFIC["sources_sha256"] == kernel_sources_sha() and args.config == "llama3_8b" and pt == 0
-            and args.engine == "tensor_cores"):
+            and args.engine == "tensor_cores" and not win):
         traffic = TRAFFIC["bytes_per_launch"]
 
     line = {
@@ -315,6 +324,8 @@ def run_gpu(args):
             "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
             "block_size": w.block_size, "cache_dtype": w.cache_dtype,
             "split": "balanced (1 launch)" if pt == 0 else f"fixed {pt}-token partitions + reduce",
+            **({"window": win, "sinks": sinks,
+                "step_launches": "kv_reshape_and_cache, then the windowed decode"} if win else {}),
             "engine": ("cuda_cores" if w.cache_dtype == "f32" else args.engine)
                       + " (q.K and P.V; softmax and accumulation in fp32)",
             "l2": "flushed between timed steps, outside the timed events: 256 MiB write, then "
@@ -340,14 +351,14 @@ def run_gpu(args):
         "clocks": clocks,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, win, sinks)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
 
 
-def run_e2e(pkv, w, kc, vc, dev, pt, steps, flush):
+def run_e2e(pkv, w, kc, vc, dev, pt, steps, flush, window=0, sinks=0):
     """Per step: host->device copies of the step's inputs from pinned memory,
     the two calls, and a device->host read of the output, all timed."""
     host = {
@@ -366,9 +377,15 @@ def run_e2e(pkv, w, kc, vc, dev, pt, steps, flush):
     def one():
         for k, t in host.items():
             dbuf[k].copy_(t, non_blocking=True)
-        pkv.decode_step(dbuf["k"], dbuf["v"], dbuf["slots"], out, dbuf["q"], kc, vc, dbuf["tables"],
-                        dbuf["lens"], w.scale, w.kv_scale, max_seq_len=w.max_seq_len,
-                        partition_tokens=pt, workspace=workspace)
+        if window:
+            pkv.kv_reshape_and_cache(dbuf["k"], dbuf["v"], kc, vc, dbuf["slots"], w.kv_scale)
+            pkv.paged_attention_decode(out, dbuf["q"], kc, vc, dbuf["tables"], dbuf["lens"], w.scale,
+                                       w.kv_scale, max_seq_len=w.max_seq_len, partition_tokens=pt,
+                                       workspace=workspace, window=window, sinks=sinks)
+        else:
+            pkv.decode_step(dbuf["k"], dbuf["v"], dbuf["slots"], out, dbuf["q"], kc, vc, dbuf["tables"],
+                            dbuf["lens"], w.scale, w.kv_scale, max_seq_len=w.max_seq_len,
+                            partition_tokens=pt, workspace=workspace)
         out_host.copy_(out, non_blocking=True)
 
     for _ in range(3):
@@ -410,17 +427,18 @@ def oracle_sample(w, max_seqs=None):
             w.new_slots.numpy().copy(), B)
 
 
-def cpu_baseline(w, seconds: float):
+def cpu_baseline(w, seconds: float, window: int = 0, sinks: int = 0):
     """The oracle, as it stands, timed on this host's cores: repeated full
     decode steps (cache write of the new tokens + attention) for ~`seconds`."""
     import oracle
     q, kc, vc, tables, lens, nk, nv, ns, B = oracle_sample(w)
     threads = os.cpu_count() or 1
-    dec_b, rc_b = step_bytes(w)
+    dec_b, rc_b = step_bytes(w, window, sinks)
     reps, t0 = 0, time.perf_counter()
     while True:
         oracle.reshape_and_cache(nk, nv, kc, vc, ns, w.kv_scale)
-        oracle.paged_attention_decode(q, kc, vc, tables, lens, w.scale, w.kv_scale, threads)
+        oracle.paged_attention_decode(q, kc, vc, tables, lens, w.scale, w.kv_scale, threads,
+                                      window=window, sinks=sinks)
         reps += 1
         el = time.perf_counter() - t0
         if el >= seconds or reps >= 1000:
@@ -444,13 +462,14 @@ def run_reference(args):
     threads = os.cpu_count() or 1
     lens_l = lens.tolist()
     dec_b = metrics.decode_bytes(lens_l, w.num_q_heads, w.num_kv_heads, w.head_dim, w.cache_dtype,
-                                 w.q_dtype, w.block_size)
+                                 w.q_dtype, w.block_size, args.window, args.sinks)
     rc_b = metrics.reshape_bytes(B, w.num_kv_heads, w.head_dim, w.src_dtype, w.cache_dtype)
     nk, nv, ns = nk[:B], nv[:B], ns[:B]
 
     def step():
         oracle.reshape_and_cache(nk, nv, kc, vc, ns, w.kv_scale)
-        oracle.paged_attention_decode(q, kc, vc, tables, lens, w.scale, w.kv_scale, threads)
+        oracle.paged_attention_decode(q, kc, vc, tables, lens, w.scale, w.kv_scale, threads,
+                                      window=args.window, sinks=args.sinks)
 
     for _ in range(args.warmup):
         step()
@@ -567,6 +586,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--engine", choices=["tensor_cores", "cuda_cores"], default="tensor_cores",
                     help="units that run q.K and P.V for bf16 / fp8 caches")
+    ap.add_argument("--window", type=int, default=0,
+                    help="> 0: sliding-window decode over the last WINDOW tokens (plus --sinks)")
+    ap.add_argument("--sinks", type=int, default=0, help="attention-sink tokens kept with --window")
     ap.add_argument("--op", choices=["decode", "copy_blocks", "swap"], default="decode",
                     help="decode step (default), or the block-copy kernels alone")
     args = ap.parse_args()

@@ -201,6 +201,32 @@ pkv_status pkv_paged_attention_decode_noalloc(void* out, const void* q, pkv_dtyp
                                               pkv_stream_t stream);
 
 /*
+ * pkv_paged_attention_decode_window -- pkv_paged_attention_decode over a
+ * sliding window with attention sinks: a sequence of length L > window_tokens
+ * attends only its first sink_tokens tokens and its last window_tokens tokens
+ * ("PagedAttention por dentro", sections "Sliding window attention" and
+ * "StreamingLLM (Xiao et al., 2024): los attention sinks").  The blocks that
+ * hold no attended token are never read, nor their table entries (an engine
+ * frees the blocks that fell out of the window; the entries may hold
+ * anything).  A sequence with L <= window_tokens attends every token.
+ *
+ *   window_tokens  > 0; 0 makes the call pkv_paged_attention_decode
+ *   sink_tokens    >= 0, ignored without a window
+ *
+ * Every other argument, the workspace (the same size as
+ * pkv_decode_workspace_bytes gives) and the error behaviour are those of
+ * pkv_paged_attention_decode; negative window_tokens or sink_tokens give
+ * PKV_ERR_INVALID_ARG.
+ */
+pkv_status pkv_paged_attention_decode_window(void* out, const void* q, pkv_dtype q_dtype, int32_t num_seqs,
+                                             int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                                             const pkv_cache_desc* cache, const int32_t* block_tables,
+                                             int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                             int32_t max_seq_len, float scale, float kv_scale, int32_t window_tokens,
+                                             int32_t sink_tokens, int32_t partition_tokens, void* workspace,
+                                             size_t workspace_bytes, pkv_stream_t stream);
+
+/*
  * pkv_decode_step -- one decode step of one layer: pkv_kv_reshape_and_cache of
  * the step's new tokens, then pkv_paged_attention_decode, on `stream`.
  *

@@ -85,6 +85,8 @@ def library() -> ctypes.CDLL:
             "pkv_decode_workspace_bytes": [i32, i32, i32, i32, i32, i32],
             "pkv_paged_attention_decode": [vp, vp, ctypes.c_int, i32, i32, vp, vp, desc, vp, i32, vp,
                                            i32, f32, f32, i32, vp, sz, vp],
+            "pkv_paged_attention_decode_window": [vp, vp, ctypes.c_int, i32, i32, vp, vp, desc, vp, i32,
+                                                  vp, i32, f32, f32, i32, i32, i32, vp, sz, vp],
             "pkv_split_kv_reduce": [vp, ctypes.c_int, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp],
             "pkv_gather_kv": [vp, vp, vp, vp, desc, vp, i32, vp, vp, i32, i32, vp],
             "pkv_decode_step": [vp, vp, ctypes.c_int, i32, vp, vp, vp, desc, vp, vp, ctypes.c_int, i32,
@@ -223,11 +225,14 @@ def paged_attention_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Te
                            v_cache: torch.Tensor, block_tables: torch.Tensor,
                            seq_lens: torch.Tensor, scale: float, kv_scale: float = 1.0,
                            max_seq_len: Optional[int] = None, partition_tokens: int = 0,
-                           workspace: Optional[DecodeWorkspace] = None, stream=None) -> torch.Tensor:
+                           workspace: Optional[DecodeWorkspace] = None, stream=None,
+                           window: int = 0, sinks: int = 0) -> torch.Tensor:
     """One decode step: ``out[s, qh] = softmax(scale * q[s, qh] . K_s^T) . V_s``.
 
     ``max_seq_len`` is a host upper bound of ``seq_lens`` (the decode never
-    synchronises to read it); by default the table capacity is used."""
+    synchronises to read it); by default the table capacity is used.
+    ``window > 0``: each sequence attends only its last ``window`` tokens and
+    its first ``sinks`` tokens (blocks outside them are never read)."""
     if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
         raise TypeError("block_tables and seq_lens must be int32")
     B, Hq, d = q.shape
@@ -244,6 +249,13 @@ def paged_attention_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Te
     units = desc.num_kv_heads * (g // heads)
     ws = workspace.get(nbytes, (B * units * 4 + 255) // 256 * 256)
     qdt = F32 if q.dtype == torch.float32 else BF16
+    if window:
+        _check(library().pkv_paged_attention_decode_window(
+            _ptr(out), _ptr(q), qdt, B, Hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc),
+            _ptr(block_tables), mbps, _ptr(seq_lens), int(max_seq_len), float(scale), float(kv_scale),
+            int(window), int(sinks), int(partition_tokens), _ptr(ws), ws.numel(), _stream(stream)),
+            "paged_attention_decode_window")
+        return out
     _check(library().pkv_paged_attention_decode(
         _ptr(out), _ptr(q), qdt, B, Hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc),
         _ptr(block_tables), mbps, _ptr(seq_lens), int(max_seq_len), float(scale), float(kv_scale),

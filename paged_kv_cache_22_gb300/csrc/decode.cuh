@@ -137,7 +137,13 @@ __global__ void __launch_bounds__(W * 32, (G >= 8 ? 8 : 12) / W)
   // ---------------------------------------------------------------- issue side
   Walker cw = wk0;  // issue cursor: segment of the next tile to fetch
   int cj = wk0.jb;  // its block index
-  int32_t next_id = __ldg(a.block_tables + (size_t)cw.s * a.table_stride + cj);
+  // table entry of the j-th block a walker's sequence reads (the logical
+  // block, past the blocks a sliding window leaves out)
+  auto table_id = [&](const Walker& wk_, int j) -> int32_t {
+    const int jl = a.window > 0 ? logical_block<BS>(a, seq_len_clipped(a, wk_.s), j) : j;
+    return __ldg(a.block_tables + (size_t)wk_.s * a.table_stride + jl);
+  };
+  int32_t next_id = table_id(cw, cj);
   int issued = 0;
 
   auto issue_next = [&]() {
@@ -165,7 +171,7 @@ __global__ void __launch_bounds__(W * 32, (G >= 8 ? 8 : 12) / W)
       cj = cw.jb;
     }
     // one tile ahead: the id is needed only at the next issue
-    if (!cw.done) next_id = __ldg(a.block_tables + (size_t)cw.s * a.table_stride + cj);
+    if (!cw.done) next_id = table_id(cw, cj);
   };
 
   // q of the piece a walker stands on: bulk copy into this warp's q slot
@@ -248,12 +254,12 @@ __global__ void __launch_bounds__(W * 32, (G >= 8 ? 8 : 12) / W)
         if (!ok) alive = false;
       }
       ok = ok && stage_ok[st];
-      const int valid = ok ? min(BS, L - j * BS) : 0;
+      TileMask tm = tile_mask<BS>(a, L, a.window > 0 ? logical_block<BS>(a, L, j) : j);
+      if (!ok) tm.hi = 0;  // a skipped tile: nothing is kept
 
 #pragma unroll 1
       for (int step = 0; step < GE::STEPS; ++step) {
         const int tbase = step * TB;
-        const int vstep = valid - tbase;  // valid tokens in this step (may be <= 0 or > TB)
         // ---- partial scores over this lane's DL dims: sc[h * TL + k], token r + R k
         float sc[GE::N0];
 #pragma unroll
@@ -300,7 +306,7 @@ __global__ void __launch_bounds__(W * 32, (G >= 8 ? 8 : 12) / W)
 #pragma unroll
         for (int jj = 0; jj < GE::NF; ++jj) {
           const int t = r + R * ((vbase + jj) % TL);
-          if (t >= vstep) sc[jj] = -CUDART_INF_F;
+          if (!tm.keep(tbase + t)) sc[jj] = -CUDART_INF_F;
           mx = fmaxf(mx, sc[jj]);
         }
         // max over the lanes that own the same head, then every head's max to all
@@ -332,7 +338,7 @@ __global__ void __launch_bounds__(W * 32, (G >= 8 ? 8 : 12) / W)
         }
         __syncwarp();
         // ---- P . V: lane owns DV dims for the token pairs of its group
-        const bool full = vstep >= TB;
+        const bool full = tm.all(tbase, tbase + TB);
 #pragma unroll
         for (int i = 0; i < GE::PPL; ++i) {
           const int t0 = 2 * (tg + GE::TG * i);  // first token of the pair, within the step
@@ -342,8 +348,8 @@ __global__ void __launch_bounds__(W * 32, (G >= 8 ? 8 : 12) / W)
           if (!full) {  // tokens past the end may hold NaN: their weight is 0, drop the value too
 #pragma unroll
             for (int d = 0; d < DV; ++d) {
-              v0[d] = t0 < vstep ? v0[d] : 0.f;
-              v1[d] = t0 + 1 < vstep ? v1[d] : 0.f;
+              v0[d] = tm.keep(tbase + t0) ? v0[d] : 0.f;
+              v1[d] = tm.keep(tbase + t0 + 1) ? v1[d] : 0.f;
             }
           }
 #pragma unroll

@@ -39,6 +39,8 @@ struct DecodeArgs {
   int units_per_kv;  // g / G: query-head chunks per kv head
   int units;         // num_kv_heads * units_per_kv (segments per sequence)
   int len_clip;      // longest admissible seq_len
+  int window;        // > 0: attend only the last `window` tokens and the first `sinks`
+  int sinks;
   float qk_scale;    // scale * log2(e) (* kv_scale for fp8 caches)
   float out_scale;   // 1 (kv_scale for fp8 caches)
   // balanced split
@@ -96,6 +98,66 @@ struct Walker {
   bool done;
 };
 
+// ----------------------------------------------------------------------------
+// Sliding window with attention sinks ("PagedAttention por dentro", sections
+// "Sliding window attention" and "StreamingLLM (Xiao et al., 2024): los
+// attention sinks"): a sequence of length L > window attends only its first
+// `sinks` tokens and its last `window` tokens.  Its blocks are read as the
+// blocks holding sink tokens, then the window's blocks; the whole blocks in
+// between (an engine may have freed them) are never touched.  BlockMap:
+// blocks [0, nsb) and [wsb, nb) are read, nsb == wsb when nothing is left out.
+// ----------------------------------------------------------------------------
+struct BlockMap {
+  int nsb, wsb;
+};
+
+template <int BS>
+__device__ __forceinline__ BlockMap block_map(const DecodeArgs& a, int L) {
+  BlockMap m{0, 0};
+  if (a.window > 0 && L > a.window) {
+    const int ws = L - a.window;                 // first window token
+    const int sk = a.sinks < ws ? a.sinks : ws;  // sink tokens before it
+    const int nsb = (sk + BS - 1) / BS, wsb = ws / BS;
+    if (wsb > nsb) {
+      m.nsb = nsb;
+      m.wsb = wsb;
+    }
+  }
+  return m;
+}
+
+// Logical block of the j-th block a sequence of length L reads.
+template <int BS>
+__device__ __forceinline__ int logical_block(const DecodeArgs& a, int L, int j) {
+  const BlockMap m = block_map<BS>(a, L);
+  return j < m.nsb ? j : j + (m.wsb - m.nsb);
+}
+
+// Tokens of logical block jl that are attended: tok < hi and (tok < s_hi or
+// tok >= w_lo), tok counted from the block's first token.
+struct TileMask {
+  int hi, s_hi, w_lo;
+  __device__ __forceinline__ bool keep(int tok) const { return tok < hi && (tok < s_hi || tok >= w_lo); }
+  // every token of [t0, t1) kept
+  __device__ __forceinline__ bool all(int t0, int t1) const { return t1 <= hi && (w_lo <= t0 || s_hi >= t1); }
+};
+
+template <int BS>
+__device__ __forceinline__ TileMask tile_mask(const DecodeArgs& a, int L, int jl) {
+  const int base = jl * BS;
+  TileMask m;
+  m.hi = L - base < BS ? L - base : BS;
+  m.s_hi = 0;
+  m.w_lo = 0;
+  if (a.window > 0 && L > a.window) {
+    const int sh = a.sinks - base, wl = L - a.window - base;
+    m.s_hi = sh < 0 ? 0 : (sh > BS ? BS : sh);
+    m.w_lo = wl < 0 ? 0 : (wl > BS ? BS : wl);
+  }
+  return m;
+}
+
+// Blocks a sequence reads (all of its blocks unless a window leaves some out).
 template <int BS>
 __device__ __forceinline__ int seq_blocks(const DecodeArgs& a, int s) {
   int L = __ldg(a.seq_lens + s);
@@ -103,7 +165,8 @@ __device__ __forceinline__ int seq_blocks(const DecodeArgs& a, int s) {
     raise_error(a.err, PKV_DEVERR_BAD_SEQ_LEN);
     L = L < 0 ? 0 : a.len_clip;
   }
-  return (L + BS - 1) / BS;
+  const BlockMap m = block_map<BS>(a, L);
+  return (L + BS - 1) / BS - (m.wsb - m.nsb);
 }
 
 __device__ __forceinline__ int seq_len_clipped(const DecodeArgs& a, int s) {

@@ -239,7 +239,13 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
   // ---------------------------------------------------------------- issue side
   Walker cw = wk0;
   int cj = wk0.jb;
-  int32_t next_id = __ldg(a.block_tables + (size_t)cw.s * a.table_stride + cj);
+  // table entry of the j-th block a walker's sequence reads (the logical
+  // block, past the blocks a sliding window leaves out)
+  auto table_id = [&](const Walker& wk_, int j) -> int32_t {
+    const int jl = a.window > 0 ? logical_block<BS>(a, seq_len_clipped(a, wk_.s), j) : j;
+    return __ldg(a.block_tables + (size_t)wk_.s * a.table_stride + jl);
+  };
+  int32_t next_id = table_id(cw, cj);
   int issued = 0;
 
   auto issue_next = [&]() {
@@ -268,7 +274,7 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
       walker_next_piece<BS>(cw, a, u1);
       cj = cw.jb;
     }
-    if (!cw.done) next_id = __ldg(a.block_tables + (size_t)cw.s * a.table_stride + cj);
+    if (!cw.done) next_id = table_id(cw, cj);
   };
 
   auto issue_q = [&](const Walker& pw, int slot) {
@@ -401,13 +407,14 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
         if (!ok) alive = false;
       }
       ok = ok && stage_ok[st];
-      const int valid = ok ? min(BS, L - j * BS) : 0;
+      TileMask tm = tile_mask<BS>(a, L, a.window > 0 ? logical_block<BS>(a, L, j) : j);
+      if (!ok) tm.hi = 0;  // a skipped tile: nothing is kept
 
 #pragma unroll
       for (int step = 0; step < GE::STEPS; ++step) {
         const uint32_t kt = stages_s + (uint32_t)(st * STAGE + step * TB * GE::IB);
         const uint32_t vt = kt + TILE;
-        const int vstep = valid - step * TB;  // valid tokens in this step (may be <= 0 or > TB)
+        const int t0 = step * TB;  // first token of this step within the tile
 
         // ---- scores: s[n][e] = q_g . K[8n + 2t + e]
         float s[GE::NTS][2];
@@ -462,7 +469,7 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int tok = 8 * n + 2 * t + e;
-            s[n][e] = tok < vstep ? s[n][e] * qk_mul : -CUDART_INF_F;
+            s[n][e] = tm.keep(t0 + tok) ? s[n][e] * qk_mul : -CUDART_INF_F;
             mx = fmaxf(mx, s[n][e]);
           }
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
@@ -494,7 +501,7 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
           }
 
         // ---- P . V
-        const bool full = vstep >= TB;
+        const bool full = tm.all(t0, t0 + TB);
         if constexpr (F8) {
           // P = head + remainder, both fp16
           uint32_t ph[2], pl[2];
@@ -517,12 +524,12 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
               X[ri][0] = v.x; X[ri][1] = v.y;
             }
           }
-          if (!full) {  // rows past the end may hold NaN codes: their weight is 0, drop them too
+          if (!full) {  // rows not attended may hold NaN codes: their weight is 0, drop them too
             const int rows[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
 #pragma unroll
             for (int ri = 0; ri < 4; ++ri)
 #pragma unroll
-              for (int q = 0; q < GE::VPL / 4; ++q) X[ri][q] = rows[ri] < vstep ? X[ri][q] : 0u;
+              for (int q = 0; q < GE::VPL / 4; ++q) X[ri][q] = tm.keep(t0 + rows[ri]) ? X[ri][q] : 0u;
           }
 #pragma unroll
           for (int q = 0; q < GE::VPL / 4; ++q) {
@@ -548,8 +555,8 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
           // keep-masks of this lane's token pairs (2t, 2t+1) and (2t+8, 2t+9)
           uint32_t keep0 = 0xFFFFFFFFu, keep1 = 0xFFFFFFFFu;
           if (!full) {
-            keep0 = (2 * t < vstep ? 0x0000FFFFu : 0u) | (2 * t + 1 < vstep ? 0xFFFF0000u : 0u);
-            keep1 = (2 * t + 8 < vstep ? 0x0000FFFFu : 0u) | (2 * t + 9 < vstep ? 0xFFFF0000u : 0u);
+            keep0 = (tm.keep(t0 + 2 * t) ? 0x0000FFFFu : 0u) | (tm.keep(t0 + 2 * t + 1) ? 0xFFFF0000u : 0u);
+            keep1 = (tm.keep(t0 + 2 * t + 8) ? 0x0000FFFFu : 0u) | (tm.keep(t0 + 2 * t + 9) ? 0xFFFF0000u : 0u);
           }
           if constexpr (TB == 16) {
 #pragma unroll

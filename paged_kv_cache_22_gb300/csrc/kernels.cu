@@ -158,7 +158,15 @@ __global__ void split_kv_reduce_kernel(ReduceArgs a) {
   const int s = row / a.num_q_heads;
   const int d = threadIdx.x;
   const int L = a.seq_lens[s];
-  const int np = L <= 0 ? 0 : (L + a.partition_tokens - 1) / a.partition_tokens;
+  int np = L <= 0 ? 0 : (L + a.partition_tokens - 1) / a.partition_tokens;
+  if (a.window > 0 && L > a.window) {
+    // partitions of the blocks read: the sink blocks, then the window's
+    const int bs = a.block_size, ws = L - a.window, sk = a.sinks < ws ? a.sinks : ws;
+    const int nsb = (sk + bs - 1) / bs, wsb = ws / bs;
+    const int nb = (L + bs - 1) / bs - (wsb > nsb ? wsb - nsb : 0);
+    const int pb = a.partition_tokens / bs;
+    np = (nb + pb - 1) / pb;
+  }
   OT* out = reinterpret_cast<OT*>(a.out) + (int64_t)row * a.head_dim;
   if (np > a.max_partitions) {
     if (d == 0) raise_error(a.err, PKV_DEVERR_BAD_SEQ_LEN);

@@ -44,6 +44,8 @@ struct ReduceArgs {
   const float* l_part;
   const int32_t* seq_lens;
   int num_seqs, num_q_heads, head_dim, partition_tokens, max_partitions;
+  // sliding window (window > 0): partitions cover the blocks the decode read
+  int block_size, window, sinks;
 };
 
 struct CopyBlocksArgs {

@@ -285,7 +285,7 @@ pkv_status pkv_split_kv_reduce(void* out, pkv_dtype out_dtype, const float* o_pa
   const int dev = current_device();
   unsigned int* err = dev < 0 ? nullptr : error_word(dev);
   if (!err) return PKV_ERR_CUDA;
-  ReduceArgs a;
+  ReduceArgs a{};
   a.err = err;
   a.out = out;
   a.o_part = o_part;
@@ -326,8 +326,10 @@ pkv_status decode_impl(void* out, const void* q, pkv_dtype q_dtype, int32_t num_
                        const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
                        const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
                        int32_t max_seq_len, float scale, float kv_scale, int32_t partition_tokens, void* workspace,
-                       size_t workspace_bytes, pkv_stream_t stream, bool programmatic, bool dry_run = false) {
+                       size_t workspace_bytes, pkv_stream_t stream, bool programmatic, bool dry_run = false,
+                       int32_t window = 0, int32_t sinks = 0) {
   if (num_seqs < 0 || !valid_cache_desc(cache)) return PKV_ERR_INVALID_ARG;
+  if (window < 0 || sinks < 0) return PKV_ERR_INVALID_ARG;
   if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return PKV_ERR_INVALID_ARG;
   if (max_blocks_per_seq <= 0 || max_seq_len < 0 || partition_tokens < 0) return PKV_ERR_INVALID_ARG;
   if (partition_tokens % cache->block_size) return PKV_ERR_INVALID_ARG;
@@ -371,6 +373,8 @@ pkv_status decode_impl(void* out, const void* q, pkv_dtype q_dtype, int32_t num_
   a.units = cache->num_kv_heads * a.units_per_kv;
   const int64_t table_tokens = (int64_t)max_blocks_per_seq * BS;
   a.len_clip = (int)(table_tokens < max_seq_len ? table_tokens : max_seq_len);
+  a.window = window;
+  a.sinks = window > 0 ? sinks : 0;
   const bool fp8 = cache->dtype == PKV_FP8_E4M3;
   a.qk_scale = scale * 1.4426950408889634f * (fp8 ? kv_scale : 1.f);
   a.out_scale = fp8 ? kv_scale : 1.f;
@@ -412,7 +416,7 @@ pkv_status decode_impl(void* out, const void* q, pkv_dtype q_dtype, int32_t num_
   if (dry_run) return PKV_OK;
   cudaError_t e = launch_decode_grid(k, dim3((unsigned)ctas), args, st, programmatic);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
-  ReduceArgs r;
+  ReduceArgs r{};
   r.err = err;
   r.out = out;
   r.o_part = a.o_part;
@@ -424,6 +428,9 @@ pkv_status decode_impl(void* out, const void* q, pkv_dtype q_dtype, int32_t num_
   r.head_dim = D;
   r.partition_tokens = partition_tokens;
   r.max_partitions = P;
+  r.block_size = BS;
+  r.window = a.window;
+  r.sinks = a.sinks;
   return from_cuda(launch_split_kv_reduce(r, q_dtype == PKV_BF16, st));
 }
 
@@ -441,6 +448,18 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, pkv_dtype q_dtyp
   return decode_impl(out, q, q_dtype, num_seqs, num_q_heads, k_cache, v_cache, cache, block_tables,
                      max_blocks_per_seq, seq_lens, max_seq_len, scale, kv_scale, partition_tokens, workspace,
                      workspace_bytes, stream, false);
+}
+
+pkv_status pkv_paged_attention_decode_window(void* out, const void* q, pkv_dtype q_dtype, int32_t num_seqs,
+                                             int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                                             const pkv_cache_desc* cache, const int32_t* block_tables,
+                                             int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                             int32_t max_seq_len, float scale, float kv_scale, int32_t window_tokens,
+                                             int32_t sink_tokens, int32_t partition_tokens, void* workspace,
+                                             size_t workspace_bytes, pkv_stream_t stream) {
+  return decode_impl(out, q, q_dtype, num_seqs, num_q_heads, k_cache, v_cache, cache, block_tables,
+                     max_blocks_per_seq, seq_lens, max_seq_len, scale, kv_scale, partition_tokens, workspace,
+                     workspace_bytes, stream, false, false, window_tokens, sink_tokens);
 }
 
 pkv_status pkv_decode_step(const void* k, const void* v, pkv_dtype src_dtype, int32_t num_new_tokens,

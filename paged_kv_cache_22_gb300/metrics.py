@@ -39,13 +39,33 @@ def blocks_for_tokens(tokens: int, block_size: int) -> int:
     return -(-int(tokens) // int(block_size))
 
 
+def attended_tokens(L: int, window: int = 0, sinks: int = 0) -> int:
+    """Tokens a sequence of length L attends: all of them, or with a sliding
+    window its first `sinks` and last `window` tokens."""
+    if window <= 0 or L <= window:
+        return L
+    return min(sinks, L - window) + window
+
+
+def blocks_read(L: int, block_size: int, window: int = 0, sinks: int = 0) -> int:
+    """Blocks whose table entry and K/V a decode reads: every block, or with a
+    window the blocks holding sink tokens and the window's blocks."""
+    nb = blocks_for_tokens(L, block_size)
+    if window <= 0 or L <= window:
+        return nb
+    ws = L - window
+    nsb, wsb = blocks_for_tokens(min(sinks, ws), block_size), ws // block_size
+    return nb - (wsb - nsb) if wsb > nsb else nb
+
+
 def decode_bytes(seq_lens: Iterable[int], num_q_heads: int, num_kv_heads: int, head_dim: int,
-                 cache_dtype: str, q_dtype: str, block_size: int) -> int:
+                 cache_dtype: str, q_dtype: str, block_size: int, window: int = 0,
+                 sinks: int = 0) -> int:
     lens = [int(x) for x in seq_lens]
     e_c, e_q = ELEM_BYTES[cache_dtype], ELEM_BYTES[q_dtype]
-    kv = sum(lens) * kv_bytes_per_token(1, num_kv_heads, head_dim, e_c)
+    kv = sum(attended_tokens(L, window, sinks) for L in lens) * kv_bytes_per_token(1, num_kv_heads, head_dim, e_c)
     qo = 2 * len(lens) * num_q_heads * head_dim * e_q
-    tables = 4 * sum(blocks_for_tokens(L, block_size) for L in lens)
+    tables = 4 * sum(blocks_read(L, block_size, window, sinks) for L in lens)
     return kv + qo + tables + 4 * len(lens)
 
 

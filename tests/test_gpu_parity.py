@@ -434,3 +434,64 @@ def test_out_of_pool_tables_in_half_the_batch(pkv, dt):
         assert pkv.get_device_error() == pkv.DEVERR_BAD_BLOCK_ID
         got = out[n_bad:].float().cpu().numpy().astype(np.float64)
         assert_close(got, ref, TOL[dt], f"clean rows, call {rep}")
+
+
+# ------------------------------------------------------------------ sliding window and sinks
+WINDOWS = [(8, 0), (8, 4), (20, 3), (33, 16), (1, 0), (4096, 0), (200, 4)]
+WIN_CASES = [
+    ("w_bf16", [1, 5, 17, 40, 70, 300, 1000], 32, 8, 128, 16, "bf16"),
+    ("w_fp8", [3, 33, 500], 32, 8, 128, 16, "fp8_e4m3"),
+    ("w_f32", [2, 19, 260], 8, 2, 64, 16, "f32"),
+    ("w_bs8_g8", [9, 130], 16, 2, 128, 8, "bf16"),
+]
+
+
+def window_ref(w, window, sinks, tables=None):
+    okc, ovc = oracle_caches(w)
+    return oracle.paged_attention_decode(to_np(w.q), okc, ovc, to_np(w.block_tables if tables is None else tables),
+                                         to_np(w.seq_lens), w.scale, w.kv_scale, 4, window=window, sinks=sinks)
+
+
+@pytest.mark.parametrize("pt", [0, 64])
+@pytest.mark.parametrize("case", WIN_CASES, ids=[c[0] for c in WIN_CASES])
+def test_sliding_window_matches_oracle(pkv, engine, case, pt):
+    name, lens, Hq, Hkv, d, bs, dt = case
+    if dt == "f32" and engine == "cuda_cores":
+        pytest.skip("fp32 caches take the CUDA cores under either engine")
+    if pt % bs:
+        pytest.skip("partition must be a multiple of the block size")
+    w = workloads.make_workload(name, lens, Hq, Hkv, d, bs, dt, seed=61 + len(lens))
+    kc, vc = gpu_caches(pkv, w)
+    q = w.q.to(DEV)
+    for window, sinks in WINDOWS:
+        out = torch.full_like(q, float("nan"))
+        pkv.paged_attention_decode(out, q, kc, vc, w.block_tables.to(DEV), w.seq_lens.to(DEV), w.scale,
+                                   w.kv_scale, max_seq_len=w.max_seq_len, partition_tokens=pt,
+                                   window=window, sinks=sinks)
+        got = out.float().cpu().numpy().astype(np.float64)
+        assert_close(got, window_ref(w, window, sinks), TOL[dt], f"{name} window {window} sinks {sinks}")
+    assert pkv.get_device_error() == 0
+
+
+@pytest.mark.parametrize("pt", [0, 32])
+def test_sliding_window_never_reads_blocks_left_out(pkv, engine, pt):
+    """Blocks holding no attended token may have been freed: their table
+    entries point outside the pool and the caches there are NaN; nothing is
+    flagged and the output is the oracle's."""
+    w = workloads.make_workload("wfree", [100, 333, 1000, 47], 32, 8, 128, 16, "bf16", seed=66,
+                                max_blocks_per_seq=70)
+    kc, vc = gpu_caches(pkv, w)
+    window, sinks, bs = 64, 4, w.block_size
+    tables = w.block_tables.clone()
+    for s, L in enumerate(w.seq_lens.tolist()):
+        for j in range(-(-L // bs)):
+            toks = range(j * bs, min(L, (j + 1) * bs))
+            if not any(L <= window or p < sinks or p >= L - window for p in toks):
+                tables[s, j] = w.num_blocks + 9
+    ref = window_ref(w, window, sinks)
+    q = w.q.to(DEV)
+    out = torch.full_like(q, float("nan"))
+    pkv.paged_attention_decode(out, q, kc, vc, tables.to(DEV), w.seq_lens.to(DEV), w.scale,
+                               max_seq_len=w.max_seq_len, partition_tokens=pt, window=window, sinks=sinks)
+    assert pkv.get_device_error() == 0
+    assert_close(out.float().cpu().numpy().astype(np.float64), ref, TOL["bf16"], "window with freed blocks")
