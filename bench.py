@@ -231,8 +231,16 @@ def run_gpu(args):
     stream = torch.cuda.current_stream()
 
     win, sinks = args.window, args.sinks
+    pblocks = w.shared_prefix_blocks if args.cascade else 0
+    if args.cascade and not pblocks:
+        raise SystemExit("--cascade needs a workload whose tables share a prefix (prefix_fp8)")
 
     def step():
+        if pblocks:  # cache write, then the cascade's prefix pass and decode (three launches)
+            pkv.kv_reshape_and_cache(new_k, new_v, kc, vc, new_slots, w.kv_scale)
+            pkv.cascade_decode(out, q, kc, vc, tables, lens, pblocks, w.scale, w.kv_scale,
+                               max_seq_len=max_len, workspace=workspace)
+            return
         if win:  # the windowed decode after the cache write (two launches)
             pkv.kv_reshape_and_cache(new_k, new_v, kc, vc, new_slots, w.kv_scale)
             pkv.paged_attention_decode(out, q, kc, vc, tables, lens, w.scale, w.kv_scale,
@@ -243,6 +251,10 @@ def run_gpu(args):
                         max_seq_len=max_len, partition_tokens=pt, workspace=workspace)
 
     def decode_only():
+        if pblocks:
+            pkv.cascade_decode(out, q, kc, vc, tables, lens, pblocks, w.scale, w.kv_scale,
+                               max_seq_len=max_len, workspace=workspace)
+            return
         pkv.paged_attention_decode(out, q, kc, vc, tables, lens, w.scale, w.kv_scale,
                                    max_seq_len=max_len, partition_tokens=pt, workspace=workspace,
                                    window=win, sinks=sinks)
@@ -290,17 +302,21 @@ def run_gpu(args):
     ms_per_step = tot_ms / K
     value = job_throughput(ws, dec_b + rc_b, ms_per_step)
     dec_avg_ms = sum(dec_ms) / K
-    achieved = dec_b / (dec_avg_ms * 1e-3) / 1e9
+    # roofline bytes: what the timed call must move (a shared prefix once)
+    roof_b = (metrics.cascade_bytes(w.seq_lens.tolist(), pblocks * w.block_size, w.num_q_heads,
+                                    w.num_kv_heads, w.head_dim, w.cache_dtype, w.q_dtype, w.block_size)
+              if pblocks else dec_b)
+    achieved = roof_b / (dec_avg_ms * 1e-3) / 1e9
     peak, peak_src = measured_peak()
 
     # ---- end to end through the public API with host buffers
-    e2e = run_e2e(pkv, w, kc, vc, dev, pt, max(10, min(K, 200)), flush, win, sinks)
+    e2e = run_e2e(pkv, w, kc, vc, dev, pt, max(10, min(K, 200)), flush, win, sinks, pblocks)
     e2e["ms_per_step"] = max_over_ranks(e2e["ms_per_step"], dev)
     e2e_value = job_throughput(ws, dec_b + rc_b, e2e["ms_per_step"])
 
     traffic = None
     if (TRAFFIC["sources_sha256"] == kernel_sources_sha() and args.config == "llama3_8b" and pt == 0
-            and args.engine == "tensor_cores" and not win):
+            and args.engine == "tensor_cores" and not win and not pblocks):
         traffic = TRAFFIC["bytes_per_launch"]
 
     line = {
@@ -326,6 +342,10 @@ def run_gpu(args):
             "split": "balanced (1 launch)" if pt == 0 else f"fixed {pt}-token partitions + reduce",
             **({"window": win, "sinks": sinks,
                 "step_launches": "kv_reshape_and_cache, then the windowed decode"} if win else {}),
+            **({"cascade": {"prefix_blocks": pblocks,
+                            "step_launches": "kv_reshape_and_cache, prefix_attention_kernel, decode_tc_kernel",
+                            "metric_bytes": "logical: every sequence's prefix counted (as plain decode reads it)",
+                            "roofline_bytes": "unique: the shared prefix once"}} if pblocks else {}),
             "engine": ("cuda_cores" if w.cache_dtype == "f32" else args.engine)
                       + " (q.K and P.V; softmax and accumulation in fp32)",
             "l2": "flushed between timed steps, outside the timed events: 256 MiB write, then "
@@ -333,21 +353,25 @@ def run_gpu(args):
             "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
         },
         "decode_tok_s_per_layer": round(ws * w.num_seqs / (ms_per_step * 1e-3), 1),
-        "step": "kv_reshape_and_cache + paged_attention_decode (pkv_decode_step: the decode "
-                "is the cache write's programmatic dependent)",
-        "decode_only": {"ms": round(dec_avg_ms, 6), "gbs": round(achieved, 1),
-                        "frac_of_8TBs": round(achieved / NOMINAL_HBM_GBS, 4),
-                        "bytes": dec_b},
+        "step": ("kv_reshape_and_cache + cascade_decode (prefix pass, then suffix decode)" if pblocks else
+                 "kv_reshape_and_cache + paged_attention_decode (windowed)" if win else
+                 "kv_reshape_and_cache + paged_attention_decode (pkv_decode_step: the decode "
+                 "is the cache write's programmatic dependent)"),
+        "decode_only": {"ms": round(dec_avg_ms, 6), "gbs": round(dec_b / (dec_avg_ms * 1e-3) / 1e9, 1),
+                        "frac_of_8TBs": round(dec_b / (dec_avg_ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
+                        "bytes": dec_b, **({"unique_bytes": roof_b} if pblocks else {})},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": ("decode_tc_kernel" if w.cache_dtype != "f32" and args.engine == "tensor_cores"
-                                else "decode_kernel")
-                     + (" (balanced split)" if pt == 0 else " (partitions)")},
+                     "kernel": ("prefix_attention_kernel + decode_tc_kernel (cascade, both launches)"
+                                if pblocks else
+                                ("decode_tc_kernel" if w.cache_dtype != "f32" and args.engine == "tensor_cores"
+                                 else "decode_kernel")
+                                + (" (balanced split)" if pt == 0 else " (partitions)"))},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": round(e2e["ms_per_step"], 6)},
-        "gpu_launches": K * (2 if pt == 0 else 3),
+        "gpu_launches": K * (3 if pblocks else (2 if pt == 0 else 3)),
         "clocks": clocks,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -358,7 +382,7 @@ def run_gpu(args):
         torch.distributed.destroy_process_group()
 
 
-def run_e2e(pkv, w, kc, vc, dev, pt, steps, flush, window=0, sinks=0):
+def run_e2e(pkv, w, kc, vc, dev, pt, steps, flush, window=0, sinks=0, prefix_blocks=0):
     """Per step: host->device copies of the step's inputs from pinned memory,
     the two calls, and a device->host read of the output, all timed."""
     host = {
@@ -377,7 +401,11 @@ def run_e2e(pkv, w, kc, vc, dev, pt, steps, flush, window=0, sinks=0):
     def one():
         for k, t in host.items():
             dbuf[k].copy_(t, non_blocking=True)
-        if window:
+        if prefix_blocks:
+            pkv.kv_reshape_and_cache(dbuf["k"], dbuf["v"], kc, vc, dbuf["slots"], w.kv_scale)
+            pkv.cascade_decode(out, dbuf["q"], kc, vc, dbuf["tables"], dbuf["lens"], prefix_blocks, w.scale,
+                               w.kv_scale, max_seq_len=w.max_seq_len, workspace=workspace)
+        elif window:
             pkv.kv_reshape_and_cache(dbuf["k"], dbuf["v"], kc, vc, dbuf["slots"], w.kv_scale)
             pkv.paged_attention_decode(out, dbuf["q"], kc, vc, dbuf["tables"], dbuf["lens"], w.scale,
                                        w.kv_scale, max_seq_len=w.max_seq_len, partition_tokens=pt,
@@ -589,6 +617,8 @@ def main():
     ap.add_argument("--window", type=int, default=0,
                     help="> 0: sliding-window decode over the last WINDOW tokens (plus --sinks)")
     ap.add_argument("--sinks", type=int, default=0, help="attention-sink tokens kept with --window")
+    ap.add_argument("--cascade", action="store_true",
+                    help="decode a shared-prefix workload as prefix pass + suffix decode (prefix_fp8)")
     ap.add_argument("--op", choices=["decode", "copy_blocks", "swap"], default="decode",
                     help="decode step (default), or the block-copy kernels alone")
     args = ap.parse_args()

@@ -227,6 +227,71 @@ pkv_status pkv_paged_attention_decode_window(void* out, const void* q, pkv_dtype
                                              size_t workspace_bytes, pkv_stream_t stream);
 
 /*
+ * pkv_cascade_workspace_bytes -- bytes of device workspace pkv_cascade_decode
+ * needs for this problem (0 for invalid sizes, a batch too large for the
+ * counter region described below, or no current device): the workspace of a
+ * balanced pkv_paged_attention_decode call, then the prefix partial result
+ * (num_seqs * num_q_heads rows of head_dim + 4 fp32 values: the unnormalised
+ * output, the running maximum, the running sum, two of padding), then one
+ * such partial per piece the prefix pass may cut the prefix into (the pieces
+ * fill one wave of the GPU; at most 32).
+ */
+size_t pkv_cascade_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t max_seq_len);
+
+/*
+ * pkv_cascade_decode -- pkv_paged_attention_decode for a batch whose block
+ * tables all begin with the same prefix_blocks physical blocks (requests
+ * that share a system prompt: "PagedAttention por dentro", section "Prefix
+ * caching cross-session"; "La despensa por casilleros", section "Prefix
+ * caching: compartir casilleros con copy-on-write").  The result is the one
+ * pkv_paged_attention_decode gives on the same arguments; only the order of
+ * the work differs:
+ *
+ *   1. one kernel attends every query row of the batch (num_seqs * group rows
+ *      per kv head) over the shared prefix blocks, so each prefix block is
+ *      read once per call instead of once per sequence, and leaves a partial
+ *      result per row (unnormalised output, running maximum, running sum) in
+ *      the workspace;
+ *   2. the decode kernel attends each sequence over its own blocks after the
+ *      prefix and folds the prefix partial in with the log-sum-exp merge of
+ *      split-KV decoding.
+ *
+ * A sequence shorter than the prefix attends only its first seq_lens[i]
+ * tokens of it, as in plain decoding.
+ *
+ *   prefix_blocks  number of leading table entries every sequence shares,
+ *                  0 <= prefix_blocks <= max_blocks_per_seq; 0 makes the call
+ *                  a plain pkv_paged_attention_decode.  The prefix blocks are
+ *                  read through the first sequence's table, which must hold
+ *                  all prefix_blocks entries; every other sequence's entries
+ *                  for the prefix blocks it attends are compared with the
+ *                  first's, and a differing entry raises
+ *                  PKV_DEVERR_BAD_BLOCK_ID
+ *   workspace      at least pkv_cascade_workspace_bytes(...) bytes of device
+ *                  memory, 256-byte aligned, owned by the caller.  Its first
+ *                  1 MiB holds merge counters, as for
+ *                  pkv_paged_attention_decode: the decode's at the bottom,
+ *                  the prefix pass's (num_kv_heads * ceil(num_seqs * group /
+ *                  16) of them) at the top.  They must be zero when a call
+ *                  starts and every completed call leaves them zero, so a
+ *                  workspace zero-filled once serves any sequence of decode
+ *                  and cascade calls.  A batch whose two counter sets do not
+ *                  fit in 1 MiB gets PKV_ERR_UNSUPPORTED
+ *
+ * Every other argument is that of pkv_paged_attention_decode (the
+ * partitioning is always the balanced one).  Caches of PKV_F32 give
+ * PKV_ERR_UNSUPPORTED: the prefix pass runs on the tensor cores, which take
+ * bf16 and fp8 operands.  All arguments are validated before anything is
+ * enqueued; errors as for pkv_paged_attention_decode.
+ */
+pkv_status pkv_cascade_decode(void* out, const void* q, pkv_dtype q_dtype, int32_t num_seqs, int32_t num_q_heads,
+                              const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                              int32_t max_seq_len, int32_t prefix_blocks, float scale, float kv_scale,
+                              void* workspace, size_t workspace_bytes, pkv_stream_t stream);
+
+/*
  * pkv_decode_step -- one decode step of one layer: pkv_kv_reshape_and_cache of
  * the step's new tokens, then pkv_paged_attention_decode, on `stream`.
  *

@@ -34,7 +34,7 @@ import torch
 
 __all__ = [
     "PkvError", "CacheDesc", "kv_reshape_and_cache", "paged_attention_decode", "decode_step",
-    "split_kv_reduce",
+    "split_kv_reduce", "cascade_decode", "cascade_workspace_bytes",
     "gather_kv", "copy_blocks", "decode_workspace_bytes", "get_device_error", "library", "library_path",
     "DecodeWorkspace", "F32", "BF16", "FP8_E4M3", "DEVERR_BAD_BLOCK_ID", "DEVERR_BAD_SLOT",
     "DEVERR_BAD_SEQ_LEN", "DEVERR_WAIT_TIMEOUT", "DEVERR_SMEM_ALIGN", "set_decode_engine",
@@ -91,6 +91,9 @@ def library() -> ctypes.CDLL:
             "pkv_gather_kv": [vp, vp, vp, vp, desc, vp, i32, vp, vp, i32, i32, vp],
             "pkv_decode_step": [vp, vp, ctypes.c_int, i32, vp, vp, vp, desc, vp, vp, ctypes.c_int, i32,
                                 i32, vp, i32, vp, i32, f32, f32, i32, vp, sz, vp],
+            "pkv_cascade_workspace_bytes": [i32, i32, i32, i32, i32],
+            "pkv_cascade_decode": [vp, vp, ctypes.c_int, i32, i32, vp, vp, desc, vp, i32, vp, i32, i32,
+                                   f32, f32, vp, sz, vp],
             "pkv_get_device_error": [ctypes.POINTER(ctypes.c_uint32), vp],
             "pkv_copy_blocks": [vp, vp, desc, vp, vp, desc, vp, i32, vp],
             "pkv_status_string": [ctypes.c_int],
@@ -103,6 +106,7 @@ def library() -> ctypes.CDLL:
             fn.argtypes = args
             fn.restype = ctypes.c_int
         lib.pkv_decode_workspace_bytes.restype = sz
+        lib.pkv_cascade_workspace_bytes.restype = sz
         lib.pkv_status_string.restype = ctypes.c_char_p
         _lib = lib
         return lib
@@ -260,6 +264,43 @@ def paged_attention_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Te
         _ptr(out), _ptr(q), qdt, B, Hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc),
         _ptr(block_tables), mbps, _ptr(seq_lens), int(max_seq_len), float(scale), float(kv_scale),
         int(partition_tokens), _ptr(ws), ws.numel(), _stream(stream)), "paged_attention_decode")
+    return out
+
+
+def cascade_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                            max_seq_len: int) -> int:
+    return int(library().pkv_cascade_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                     max_seq_len))
+
+
+def cascade_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                   block_tables: torch.Tensor, seq_lens: torch.Tensor, prefix_blocks: int, scale: float,
+                   kv_scale: float = 1.0, max_seq_len: Optional[int] = None,
+                   workspace: Optional[DecodeWorkspace] = None, stream=None) -> torch.Tensor:
+    """paged_attention_decode for a batch whose tables all begin with the same
+    ``prefix_blocks`` blocks: the shared prefix is attended once for every
+    query row of the batch, then each sequence's own blocks, and the two
+    partial results are merged (bf16 and fp8 caches)."""
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_tables and seq_lens must be int32")
+    B, Hq, d = q.shape
+    desc = _desc(k_cache, None)
+    mbps = int(block_tables.shape[1])
+    if max_seq_len is None:
+        max_seq_len = mbps * desc.block_size
+    nbytes = cascade_workspace_bytes(B, Hq, desc.num_kv_heads, d, max_seq_len)
+    if workspace is None:
+        dev = q.device.index if q.device.index is not None else torch.cuda.current_device()
+        workspace = _default_ws.setdefault(dev, DecodeWorkspace(q.device))
+    g = Hq // desc.num_kv_heads
+    heads = next(G for G in (8, 4, 2, 1) if g % G == 0)
+    units = desc.num_kv_heads * (g // heads)
+    ws = workspace.get(nbytes, (B * units * 4 + 255) // 256 * 256)
+    qdt = F32 if q.dtype == torch.float32 else BF16
+    _check(library().pkv_cascade_decode(
+        _ptr(out), _ptr(q), qdt, B, Hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc),
+        _ptr(block_tables), mbps, _ptr(seq_lens), int(max_seq_len), int(prefix_blocks), float(scale),
+        float(kv_scale), _ptr(ws), ws.numel(), _stream(stream)), "cascade_decode")
     return out
 
 

@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(W * 32, (G >= 8 ? 8 : 12) / W)
   // table entry of the j-th block a walker's sequence reads (the logical
   // block, past the blocks a sliding window leaves out)
   auto table_id = [&](const Walker& wk_, int j) -> int32_t {
-    const int jl = a.window > 0 ? logical_block<BS>(a, seq_len_clipped(a, wk_.s), j) : j;
+    const int jl = remaps_blocks(a) ? logical_block<BS>(a, seq_len_clipped(a, wk_.s), j) : j;
     return __ldg(a.block_tables + (size_t)wk_.s * a.table_stride + jl);
   };
   int32_t next_id = table_id(cw, cj);
@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(W * 32, (G >= 8 ? 8 : 12) / W)
         if (!ok) alive = false;
       }
       ok = ok && stage_ok[st];
-      TileMask tm = tile_mask<BS>(a, L, a.window > 0 ? logical_block<BS>(a, L, j) : j);
+      TileMask tm = tile_mask<BS>(a, L, remaps_blocks(a) ? logical_block<BS>(a, L, j) : j);
       if (!ok) tm.hi = 0;  // a skipped tile: nothing is kept
 
 #pragma unroll 1

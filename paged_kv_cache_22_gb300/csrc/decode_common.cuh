@@ -41,6 +41,12 @@ struct DecodeArgs {
   int len_clip;      // longest admissible seq_len
   int window;        // > 0: attend only the last `window` tokens and the first `sinks`
   int sinks;
+  // cascade: the first skip_blocks blocks of every sequence are a shared
+  // prefix already attended; its partial result per output row, [B * Hq]
+  // rows of pre_row_floats(D) floats (o unnormalised, then m in log2 units,
+  // then l), is where each segment's online softmax starts
+  int skip_blocks;
+  const float* pre;
   float qk_scale;    // scale * log2(e) (* kv_scale for fp8 caches)
   float out_scale;   // 1 (kv_scale for fp8 caches)
   // balanced split
@@ -114,6 +120,11 @@ struct BlockMap {
 template <int BS>
 __device__ __forceinline__ BlockMap block_map(const DecodeArgs& a, int L) {
   BlockMap m{0, 0};
+  if (a.skip_blocks > 0) {  // cascade: the blocks past the shared prefix
+    const int nb = (L + BS - 1) / BS;
+    m.wsb = a.skip_blocks < nb ? a.skip_blocks : nb;
+    return m;
+  }
   if (a.window > 0 && L > a.window) {
     const int ws = L - a.window;                 // first window token
     const int sk = a.sinks < ws ? a.sinks : ws;  // sink tokens before it
@@ -125,6 +136,14 @@ __device__ __forceinline__ BlockMap block_map(const DecodeArgs& a, int L) {
   }
   return m;
 }
+
+// Whether some sequence may skip blocks (a window, or a cascade's prefix),
+// so that the j-th block read is not logical block j.
+__device__ __forceinline__ bool remaps_blocks(const DecodeArgs& a) { return a.window > 0 || a.skip_blocks > 0; }
+
+// Floats per row of a cascade's prefix partial: D of o, m, l, two of padding
+// (rows stay 16-byte aligned for bulk copies).
+__host__ __device__ constexpr int pre_row_floats(int D) { return D + 4; }
 
 // Logical block of the j-th block a sequence of length L reads.
 template <int BS>
@@ -219,11 +238,20 @@ __device__ __forceinline__ bool plan_warp(const DecodeArgs& a, int64_t gw, int64
                                           int64_t& u0, int64_t& u1, int64_t& T) {
   T = 0;
   if constexpr (BALANCED) {
-    // sequences of length 0 get a zero row (spread over the warps)
+    // sequences with no block to read get their row here (spread over the
+    // warps): zero, or in a cascade the shared prefix's result alone
     for (int64_t s = gw; s < a.num_seqs; s += NW) {
-      if (seq_len_clipped(a, (int)s) == 0) {
+      if (seq_blocks<BS>(a, (int)s) == 0) {
         QT* o = reinterpret_cast<QT*>(a.out) + (size_t)s * a.num_q_heads * D;
-        for (int i = lane; i < a.num_q_heads * D; i += 32) o[i] = from_f32<QT>(0.f);
+        for (int i = lane; i < a.num_q_heads * D; i += 32) {
+          float v = 0.f;
+          if (a.pre) {
+            const float* pr = a.pre + ((size_t)s * a.num_q_heads + i / D) * pre_row_floats(D);
+            const float l = pr[D + 1];
+            v = l > 0.f ? pr[i % D] * (a.out_scale / l) : 0.f;
+          }
+          o[i] = from_f32<QT>(v);
+        }
       }
     }
     // total tiles, this warp's range, and the sequence holding its first tile

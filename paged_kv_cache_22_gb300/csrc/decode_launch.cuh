@@ -3,6 +3,7 @@
 
 #include "decode.cuh"
 #include "decode_tc.cuh"
+#include "decode_prefix.cuh"
 
 namespace pkv {
 
@@ -75,6 +76,23 @@ inline bool find_decode(pkv_dtype dt, int D, int BS, int G, bool balanced, bool 
   }
   return false;
 }
+
+// The shared-prefix kernel of cascade decode (bf16 and fp8 caches).
+struct PrefixKernel {
+  const void* fn = nullptr;  // __global__ entry, parameters (PrefixArgs, TmaMaps)
+  size_t smem = 0;
+};
+
+template <class CT, int D, int BS>
+PrefixKernel prefix_kernel_info() {
+  PrefixKernel k;
+  k.fn = reinterpret_cast<const void*>(&prefix_attention_kernel<CT, D, BS>);
+  k.smem = PrefixSmem<CT, D, BS>::kBytes;
+  return k;
+}
+
+bool find_prefix_bf16(int head_dim, int block_size, PrefixKernel* out);
+bool find_prefix_fp8(int head_dim, int block_size, PrefixKernel* out);
 
 // The engine set by pkv_set_decode_engine (pkv_api.cu).
 bool decode_on_tensor_cores();

@@ -1,0 +1,500 @@
+// decode_prefix.cuh -- the shared-prefix half of cascade decode.
+//
+// When every sequence of a batch starts with the same prefix blocks (a
+// shared system prompt: "La despensa por casilleros", section "Prefix
+// caching: compartir casilleros con copy-on-write"), decode reads the
+// prefix's K and V once per sequence although the tiles are the same.  The
+// cascade splits the work: this kernel attends every query row of the batch
+// to the prefix once per 16 rows, and the decode kernel then walks each
+// sequence's own blocks past the prefix and folds this partial result in by
+// log-sum-exp.  The output is that of plain decode.
+//
+// Design (GB300): one warp per (kv head, block of 16 query rows, piece of
+// the prefix); the 16 rows are (sequence, query head) pairs of that kv head,
+// so all 16 rows of the m16n8k16 operand are real and each prefix tile feeds
+// 16 rows instead of G.  The prefix is cut into pieces so that the grid fills
+// every SM; the last warp of a (kv head, row block) to finish merges the
+// pieces' partials by log-sum-exp into the one partial the decode reads.
+// Tiles come by TMA tensor copies into a per-warp ring, swizzled for
+// ldmatrix, as in the decode kernel; P keeps a head and a remainder of the
+// operand type (two MMAs per n-tile).  Partials are unnormalised:
+// o = sum_t 2^(s_t - m) v_t, m = max_t s_t (log2 units of the scaled score),
+// l = sum_t 2^(s_t - m), over the prefix tokens t < seq_len of the row.
+#pragma once
+
+#include "decode_tc.cuh"
+
+namespace pkv {
+
+struct PrefixArgs {
+  unsigned int* err;
+  const void* q;                 // [B, Hq, D]
+  const int32_t* block_tables;   // the first prefix_blocks entries of every row are the prefix
+  int64_t table_stride;
+  const int32_t* seq_lens;
+  int num_seqs, num_q_heads, num_kv_heads, group, num_blocks, len_clip;
+  int prefix_blocks;
+  int row_blocks;                // ceil(num_seqs * group / 16)
+  int splits;                    // the prefix is cut into this many pieces (<= 32) ...
+  int split_blocks;              // ... of this many blocks (the last may be shorter)
+  float qk_scale;                // scale * log2(e) (* kv_scale for fp8 caches)
+  float* pre;                    // [B * Hq] rows of pre_row_floats(D): o, m, l (the result)
+  float* scratch;                // [splits, B * Hq] rows of the same: one per piece (splits > 1)
+  int* counters;                 // [Hkv * row_blocks], zero between calls (splits > 1)
+};
+
+template <class CT, int D, int BS>
+struct PrefixSmem {
+  using GE = TcGeo<CT, D, BS, 1>;
+  static constexpr size_t kStages = 0;  // 1024-byte aligned
+  static constexpr size_t kBars = (size_t)GE::NSW * GE::STAGE;
+  static constexpr size_t kBytes = kBars + (size_t)GE::NSW * 8;
+};
+
+template <class CT, int D, int BS>
+__global__ void __launch_bounds__(32, 8)
+    prefix_attention_kernel(const __grid_constant__ PrefixArgs a, const __grid_constant__ TmaMaps maps) {
+  using GE = TcGeo<CT, D, BS, 1>;
+  using SM = PrefixSmem<CT, D, BS>;
+  using QT = typename CT::QType;
+  constexpr bool F8 = GE::F8;
+  constexpr int NSW = GE::NSW, TB = GE::TB, KS = GE::KS, NTO = GE::NTO, TILE = GE::TILE, STAGE = GE::STAGE;
+  static_assert(TB == 16 || !F8, "fp8 caches: 16-token steps");
+
+  extern __shared__ __align__(1024) uint8_t pf_smem[];
+  uint8_t* const stages = pf_smem + SM::kStages;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  if (smem_addr(stages) & 1023u) {
+    if (lane == 0) raise_error(a.err, PKV_DEVERR_SMEM_ALIGN);
+    return;
+  }
+  const uint32_t stages_s = smem_addr(stages);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(pf_smem + SM::kBars);
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < NSW; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  // CTA -> (piece of the prefix, kv head, block of 16 rows)
+  const int piece = blockIdx.x % a.splits, hr = blockIdx.x / a.splits;
+  const int h = hr / a.row_blocks, rb = hr % a.row_blocks;
+  const int jb = piece * a.split_blocks;
+  const int je = min(a.prefix_blocks, jb + a.split_blocks);
+  const int ptok = a.prefix_blocks * BS;
+  // the lane's two rows (g, g + 8): sequence, query head, prefix tokens attended
+  int rs[2], rq[2], rlim[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int R = rb * 16 + g + 8 * r;
+    rs[r] = R / a.group;
+    rq[r] = h * a.group + R % a.group;
+    if (rs[r] < a.num_seqs) {
+      int L = __ldg(a.seq_lens + rs[r]);
+      L = L < 0 ? 0 : (L > a.len_clip ? a.len_clip : L);
+      rlim[r] = L < ptok ? L : ptok;
+    } else {
+      rlim[r] = 0;
+    }
+  }
+  // tokens no row of this warp attends are zeroed in V (they may be unwritten)
+  int lim_all = rlim[0] > rlim[1] ? rlim[0] : rlim[1];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) lim_all = max(lim_all, __shfl_xor_sync(0xffffffffu, lim_all, off));
+
+  // the prefix blocks a sequence attends must be those of sequence 0's table
+  // (checked once, by kv head 0; entries past a short sequence's end are not
+  // read by plain decode either, so they are not compared)
+  if (h == 0 && piece == 0) {
+    const int s_lo = rb * 16 / a.group, s_hi = min(a.num_seqs, (rb * 16 + 15) / a.group + 1);
+    for (int s = s_lo; s < s_hi; ++s) {
+      int L = __ldg(a.seq_lens + s);
+      L = L < 0 ? 0 : (L > a.len_clip ? a.len_clip : L);
+      const int nb = min(a.prefix_blocks, (L + BS - 1) / BS);
+      for (int j = lane; j < nb; j += 32)
+        if (__ldg(a.block_tables + (size_t)s * a.table_stride + j) != __ldg(a.block_tables + j))
+          raise_error(a.err, PKV_DEVERR_BAD_BLOCK_ID);
+    }
+  }
+
+  // q.K A operand, all 16 rows: (a0, a1, a2, a3) per k-step
+  uint32_t qa[KS][4];
+  float qk_mul = a.qk_scale;
+  {
+    const QT* qrow[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+      qrow[r] = reinterpret_cast<const QT*>(a.q) + ((size_t)(rs[r] < a.num_seqs ? rs[r] : 0) * a.num_q_heads + rq[r]) * D;
+    if constexpr (!F8) {
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const bool live = rs[r] < a.num_seqs;
+          qa[kk][r] = live ? *reinterpret_cast<const uint32_t*>(qrow[r] + 16 * kk + 2 * t) : 0u;
+          qa[kk][2 + r] = live ? *reinterpret_cast<const uint32_t*>(qrow[r] + 16 * kk + 2 * t + 8) : 0u;
+        }
+    } else {
+      // fp16 operands in the order a K chunk reaches the lane (dims 4t..4t+3
+      // of each 16-dim chunk), scaled by a power of two so that |q| < 2^15
+      float qv[KS][2][4];
+      float mq = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const bool live = rs[r] < a.num_seqs;
+          const uint2 raw = live ? *reinterpret_cast<const uint2*>(qrow[r] + 16 * kk + 4 * t) : make_uint2(0u, 0u);
+          const float2 lo = bf16x2_to_f2(raw.x), hi = bf16x2_to_f2(raw.y);
+          qv[kk][r][0] = lo.x;
+          qv[kk][r][1] = lo.y;
+          qv[kk][r][2] = hi.x;
+          qv[kk][r][3] = hi.y;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) mq = fmaxf(mq, fabsf(qv[kk][r][i]));
+        }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mq = fmaxf(mq, __shfl_xor_sync(0xffffffffu, mq, off));
+      int e = 0;
+      frexpf(mq, &e);
+      const int sh = e > 15 ? (e - 15 < 100 ? e - 15 : 100) : 0;
+      const float down = ldexpf(1.f, -sh);
+      qk_mul = a.qk_scale * ldexpf(1.f, sh);
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          qa[kk][r] = pack_f16x2(qv[kk][r][0] * down, qv[kk][r][1] * down);
+          qa[kk][2 + r] = pack_f16x2(qv[kk][r][2] * down, qv[kk][r][3] * down);
+        }
+    }
+  }
+
+  // ---------------------------------------------------------------- issue side
+  int issued = 0;  // blocks of this piece whose copy was started
+  auto issue_next = [&]() {
+    if (jb + issued >= je) return;
+    const int st = issued % NSW;
+    if (lane == 0) {
+      const int32_t id = __ldg(a.block_tables + jb + issued);
+      uint8_t* dst = stages + (size_t)st * STAGE;
+      if (id >= 0 && id < a.num_blocks) {
+        mbar_arrive_expect_tx(&bars[st], STAGE);
+#pragma unroll
+        for (int bx = 0; bx < GE::NBX; ++bx) {
+          tma_load_3d(dst + bx * GE::BOX, &maps.k, bx * (GE::IB / GE::E), h * BS, id, &bars[st]);
+          tma_load_3d(dst + TILE + bx * GE::BOX, &maps.v, bx * (GE::IB / GE::E), h * BS, id, &bars[st]);
+        }
+      } else {
+        raise_error(a.err, PKV_DEVERR_BAD_BLOCK_ID);
+        mbar_arrive(&bars[st]);
+      }
+    }
+    ++issued;
+  };
+  // the cascade's decode runs after this grid on the stream; the cache write
+  // of the step (if any) ran before both
+#pragma unroll 1
+  for (int i = 0; i < NSW; ++i) issue_next();
+
+  // fragment addresses (as in the decode kernel)
+  auto lane_base = [](int row, int hh) -> uint32_t { return swz<GE>(row, hh); };
+  uint32_t kx, vx = 0;
+  if constexpr (F8) {
+    kx = lane_base((lane & 7) + 8 * ((lane >> 3) & 1), lane >> 4);
+  } else if constexpr (TB == 16) {
+    kx = lane_base((lane & 7) + 8 * (lane >> 4), (lane >> 3) & 1);
+    vx = lane_base((lane & 7) + 8 * ((lane >> 3) & 1), lane >> 4);
+  } else {
+    kx = lane_base(lane & 7, lane >> 3);
+    vx = lane_base(lane & 7, lane >> 3);
+  }
+  constexpr int CPB = GE::IB / 16;
+  auto frag = [](uint32_t base, int C) -> uint32_t {
+    return (base ^ (uint32_t)((C % CPB) << 4)) + (uint32_t)((C / CPB) * GE::BOX);
+  };
+  uint32_t voff8[4] = {0, 0, 0, 0};
+  if constexpr (F8) {
+    const int c = (g * GE::VPL) / 16, b = (g * GE::VPL) % 16;
+    voff8[0] = swz<GE>(2 * t, c) + b;
+    voff8[1] = swz<GE>(2 * t + 1, c) + b;
+    voff8[2] = swz<GE>(2 * t + 8, c) + b;
+    voff8[3] = swz<GE>(2 * t + 9, c) + b;
+  }
+
+  // ---------------------------------------------------------------- consume side
+  float o[NTO][4];  // columns 2t, 2t+1 of each n-tile: [0..1] row g, [2..3] row g + 8
+#pragma unroll
+  for (int n = 0; n < NTO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F}, l_run[2] = {0.f, 0.f};
+  int waited = 0;
+  bool alive = true;
+
+#pragma unroll 1
+  for (int j = jb; j < je; ++j) {
+    const int i = j - jb;  // position in this piece's ring
+    const int st = i % NSW;
+    if (alive) {
+      if (!mbar_wait_bounded(&bars[st], (i / NSW) & 1, a.err)) alive = false;
+      waited = i + 1;
+    }
+    const int32_t id = __ldg(a.block_tables + j);
+    const bool ok = alive && id >= 0 && id < a.num_blocks;
+#pragma unroll
+    for (int step = 0; step < GE::STEPS; ++step) {
+      const uint32_t kt = stages_s + (uint32_t)(st * STAGE + step * TB * GE::IB);
+      const uint32_t vt = kt + TILE;
+      const int p0 = j * BS + step * TB;  // prefix position of the step's first token
+      // ---- scores of both rows: c[n] = (row g: cols 2t, 2t+1 | row g + 8: same)
+      float sc[GE::NTS][4];
+      {
+        float s2[2][GE::NTS][4] = {};
+        if constexpr (F8) {
+#pragma unroll
+          for (int kq = 0; kq < KS / 2; ++kq) {
+            uint32_t r[4];
+            ldsm_x4(frag(kt + kx, 2 * kq), r);
+            uint32_t b[4][2];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) e4m3x4_to_f16x2x2(r[m], b[m][0], b[m][1]);
+            mma_k16_rows16<true>(s2[0][0], qa[2 * kq][0], qa[2 * kq][1], qa[2 * kq][2], qa[2 * kq][3], b[0][0], b[0][1]);
+            mma_k16_rows16<true>(s2[0][1], qa[2 * kq][0], qa[2 * kq][1], qa[2 * kq][2], qa[2 * kq][3], b[1][0], b[1][1]);
+            mma_k16_rows16<true>(s2[1][0], qa[2 * kq + 1][0], qa[2 * kq + 1][1], qa[2 * kq + 1][2], qa[2 * kq + 1][3],
+                                 b[2][0], b[2][1]);
+            mma_k16_rows16<true>(s2[1][1], qa[2 * kq + 1][0], qa[2 * kq + 1][1], qa[2 * kq + 1][2], qa[2 * kq + 1][3],
+                                 b[3][0], b[3][1]);
+          }
+        } else if constexpr (TB == 16) {
+#pragma unroll
+          for (int kk = 0; kk < KS; ++kk) {
+            uint32_t r[4];
+            ldsm_x4(frag(kt + kx, 2 * kk), r);
+            mma_k16_rows16<false>(s2[kk & 1][0], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], r[0], r[1]);
+            mma_k16_rows16<false>(s2[kk & 1][1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], r[2], r[3]);
+          }
+        } else {
+#pragma unroll
+          for (int kq = 0; kq < KS / 2; ++kq) {
+            uint32_t r[4];
+            ldsm_x4(frag(kt + kx, 4 * kq), r);
+            mma_k16_rows16<false>(s2[0][0], qa[2 * kq][0], qa[2 * kq][1], qa[2 * kq][2], qa[2 * kq][3], r[0], r[1]);
+            mma_k16_rows16<false>(s2[1][0], qa[2 * kq + 1][0], qa[2 * kq + 1][1], qa[2 * kq + 1][2],
+                                  qa[2 * kq + 1][3], r[2], r[3]);
+          }
+        }
+#pragma unroll
+        for (int n = 0; n < GE::NTS; ++n)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) sc[n][c] = s2[0][n][c] + s2[1][n][c];
+      }
+      // ---- online softmax, row by row (c = 2r + e: row g + 8r, column 2t + e)
+      float mx[2] = {-CUDART_INF_F, -CUDART_INF_F};
+#pragma unroll
+      for (int n = 0; n < GE::NTS; ++n)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int r = c >> 1, tok = p0 + 8 * n + 2 * t + (c & 1);
+          sc[n][c] = (ok && tok < rlim[r]) ? sc[n][c] * qk_mul : -CUDART_INF_F;
+          mx[r] = fmaxf(mx[r], sc[n][c]);
+        }
+      float alpha[2];
+      bool grow = false;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+        const float m_new = fmaxf(m_run[r], mx[r]);
+        alpha[r] = m_new > m_run[r] ? fast_exp2(m_run[r] - m_new) : 1.f;
+        grow |= m_new > m_run[r];
+        m_run[r] = m_new;
+      }
+      if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+        for (int n = 0; n < NTO; ++n) {
+          o[n][0] *= alpha[0];
+          o[n][1] *= alpha[0];
+          o[n][2] *= alpha[1];
+          o[n][3] *= alpha[1];
+        }
+        l_run[0] *= alpha[0];
+        l_run[1] *= alpha[1];
+      }
+      float p[GE::NTS][4];
+#pragma unroll
+      for (int n = 0; n < GE::NTS; ++n)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int r = c >> 1;
+          const float mu = m_run[r] == -CUDART_INF_F ? 0.f : m_run[r];
+          p[n][c] = fast_exp2(sc[n][c] - mu);
+          l_run[r] += p[n][c];
+        }
+      // ---- P . V: P as a head and a remainder, both rows real
+      const bool full = ok && p0 + TB <= lim_all;
+      uint32_t ph[2][4], pl[2][4];  // [0]: k-step tokens 0-7 (a0 row g, a1 row g+8) ...
+      // A operand (m16 x k16 tokens): a0 = row g, tokens 2t..; a1 = row g+8, tokens 2t..;
+      // a2 = row g, tokens 2t+8..; a3 = row g+8, tokens 2t+8..
+#pragma unroll
+      for (int n = 0; n < GE::NTS; ++n)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const float x0 = p[n][2 * r], x1 = p[n][2 * r + 1];
+          uint32_t hh, ll;
+          if constexpr (F8) {
+            hh = pack_f16x2(x0, x1);
+            const float2 hv = f16x2_to_f2(hh);
+            ll = pack_f16x2(x0 - hv.x, x1 - hv.y);
+          } else {
+            hh = pack_bf16x2(x0, x1);
+            const float2 hv = bf16x2_to_f2(hh);
+            ll = pack_bf16x2(x0 - hv.x, x1 - hv.y);
+          }
+          ph[n][r] = hh;
+          pl[n][r] = ll;
+        }
+      if constexpr (F8) {
+        uint32_t X[4][GE::VPL / 4];
+#pragma unroll
+        for (int ri = 0; ri < 4; ++ri) {
+          const uint8_t* src = stages + (vt - stages_s) + voff8[ri];
+          if constexpr (GE::VPL == 16) {
+            const uint4 v = *reinterpret_cast<const uint4*>(src);
+            X[ri][0] = v.x; X[ri][1] = v.y; X[ri][2] = v.z; X[ri][3] = v.w;
+          } else {
+            const uint2 v = *reinterpret_cast<const uint2*>(src);
+            X[ri][0] = v.x; X[ri][1] = v.y;
+          }
+        }
+        if (!full) {
+          const int rows[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+#pragma unroll
+          for (int ri = 0; ri < 4; ++ri)
+#pragma unroll
+            for (int qq = 0; qq < GE::VPL / 4; ++qq) X[ri][qq] = (ok && p0 + rows[ri] < lim_all) ? X[ri][qq] : 0u;
+        }
+#pragma unroll
+        for (int qq = 0; qq < GE::VPL / 4; ++qq) {
+          uint32_t b0[4], b1[4];
+          e4m3x4_to_f16x2x2(__byte_perm(X[0][qq], X[1][qq], 0x5140), b0[0], b0[1]);
+          e4m3x4_to_f16x2x2(__byte_perm(X[0][qq], X[1][qq], 0x7362), b0[2], b0[3]);
+          e4m3x4_to_f16x2x2(__byte_perm(X[2][qq], X[3][qq], 0x5140), b1[0], b1[1]);
+          e4m3x4_to_f16x2x2(__byte_perm(X[2][qq], X[3][qq], 0x7362), b1[2], b1[3]);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            mma_k16_rows16<true>(o[4 * qq + k], ph[0][0], ph[0][1], ph[1][0], ph[1][1], b0[k], b1[k]);
+            mma_k16_rows16<true>(o[4 * qq + k], pl[0][0], pl[0][1], pl[1][0], pl[1][1], b0[k], b1[k]);
+          }
+        }
+      } else {
+        uint32_t keep0 = 0xFFFFFFFFu, keep1 = 0xFFFFFFFFu;
+        if (!full) {
+          auto kept = [&](int tok) { return ok && p0 + tok < lim_all; };
+          keep0 = (kept(2 * t) ? 0x0000FFFFu : 0u) | (kept(2 * t + 1) ? 0xFFFF0000u : 0u);
+          keep1 = (kept(2 * t + 8) ? 0x0000FFFFu : 0u) | (kept(2 * t + 9) ? 0xFFFF0000u : 0u);
+        }
+        if constexpr (TB == 16) {
+#pragma unroll
+          for (int jv = 0; jv < NTO / 2; ++jv) {
+            uint32_t r[4];
+            ldsm_x4_t(frag(vt + vx, 2 * jv), r);
+            r[0] &= keep0; r[1] &= keep1; r[2] &= keep0; r[3] &= keep1;
+            mma_k16_rows16<false>(o[2 * jv], ph[0][0], ph[0][1], ph[1][0], ph[1][1], r[0], r[1]);
+            mma_k16_rows16<false>(o[2 * jv + 1], ph[0][0], ph[0][1], ph[1][0], ph[1][1], r[2], r[3]);
+            mma_k16_rows16<false>(o[2 * jv], pl[0][0], pl[0][1], pl[1][0], pl[1][1], r[0], r[1]);
+            mma_k16_rows16<false>(o[2 * jv + 1], pl[0][0], pl[0][1], pl[1][0], pl[1][1], r[2], r[3]);
+          }
+        } else {
+#pragma unroll
+          for (int jv = 0; jv < NTO / 4; ++jv) {
+            uint32_t r[4];
+            ldsm_x4_t(frag(vt + vx, 4 * jv), r);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              r[m] &= keep0;
+              mma_k8_bf16_rows16(o[4 * jv + m], ph[0][0], ph[0][1], r[m]);
+              mma_k8_bf16_rows16(o[4 * jv + m], pl[0][0], pl[0][1], r[m]);
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();  // every lane is done with this stage before it is refilled
+    if (alive) issue_next();
+  }
+
+  // ---------------------------------------------------------------- partials
+  constexpr int PRF = pre_row_floats(D);
+  const size_t rows = (size_t)a.num_seqs * a.num_q_heads;
+  float* base = a.splits == 1 ? a.pre : a.scratch + (size_t)piece * rows * PRF;
+  auto odim = [&](int n, int e) -> int { return F8 ? GE::VPL * (2 * t + e) + n : 8 * n + 2 * t + e; };
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    float l_row = l_run[r] + __shfl_xor_sync(0xffffffffu, l_run[r], 1);
+    l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
+    if (rs[r] < a.num_seqs) {
+      float* dst = base + ((size_t)rs[r] * a.num_q_heads + rq[r]) * PRF;
+#pragma unroll
+      for (int n = 0; n < NTO; ++n)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) dst[odim(n, e)] = o[n][2 * r + e];
+      if (t == 0) {
+        dst[D] = m_run[r];
+        dst[D + 1] = l_row;
+      }
+    }
+  }
+  if (a.splits > 1) {
+    // the last piece of this (kv head, row block) to finish merges them all
+    __threadfence();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+      last = atomicAdd(a.counters + hr, 1) == a.splits - 1;
+      if (last) a.counters[hr] = 0;  // ready for the next call
+    }
+    if (__shfl_sync(0xffffffffu, last, 0)) {
+      __threadfence();
+      for (int rr = 0; rr < 16; ++rr) {
+        const int R = rb * 16 + rr, s = R / a.group;
+        if (s >= a.num_seqs) break;
+        const size_t row = (size_t)s * a.num_q_heads + h * a.group + R % a.group;
+        float mk = -CUDART_INF_F, lk = 0.f;
+        if (lane < a.splits) {
+          const float* p = a.scratch + ((size_t)lane * rows + row) * PRF;
+          mk = __ldcg(p + D);
+          lk = __ldcg(p + D + 1);
+        }
+        float M = mk;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        const float Mc = M == -CUDART_INF_F ? 0.f : M;
+        const float wk = lane < a.splits ? fast_exp2(mk - Mc) : 0.f;
+        float den = lk * wk;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < a.splits; ++k) {
+          const float wkk = __shfl_sync(0xffffffffu, wk, k);
+          if (4 * lane < D) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(a.scratch + ((size_t)k * rows + row) * PRF) + lane);
+            acc.x += v.x * wkk;
+            acc.y += v.y * wkk;
+            acc.z += v.z * wkk;
+            acc.w += v.w * wkk;
+          }
+        }
+        float* dst = a.pre + row * PRF;
+        if (4 * lane < D) reinterpret_cast<float4*>(dst)[lane] = acc;
+        if (lane == 0) {
+          dst[D] = M;
+          dst[D + 1] = den;
+        }
+      }
+    }
+  }
+  for (int k = waited; k < issued; ++k) mbar_wait_bounded(&bars[k % NSW], (k / NSW) & 1, a.err);
+}
+
+}  // namespace pkv

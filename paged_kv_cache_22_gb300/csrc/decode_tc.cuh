@@ -180,7 +180,10 @@ struct TcSmem {
   static constexpr size_t kBars = (kQBuf + (size_t)W * 2 * G * D * sizeof(__nv_bfloat16) + 7) / 8 * 8;
   static constexpr size_t kQBars = kBars + (size_t)W * GE::NSW * 8;
   static constexpr size_t kOk = kQBars + (size_t)W * 2 * 8;
-  static constexpr size_t kBytes = kOk + (size_t)W * GE::NSW * 4;
+  // cascade: one warp's next prefix partial (G rows), and its barrier
+  static constexpr size_t kPBuf = (kOk + (size_t)W * GE::NSW * 4 + 15) / 16 * 16;
+  static constexpr size_t kPBar = kPBuf + (size_t)W * G * pre_row_floats(D) * sizeof(float);
+  static constexpr size_t kBytes = kPBar + (size_t)W * 8;
 };
 
 // Byte offset, within a tile, of 16-byte chunk c of token row `row` as the
@@ -220,12 +223,15 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::kBars) + w * NSW;
   uint64_t* qbars = reinterpret_cast<uint64_t*>(smem + SM::kQBars) + w * 2;
   int* stage_ok = reinterpret_cast<int*>(smem + SM::kOk) + w * NSW;
+  float* pbuf = reinterpret_cast<float*>(smem + SM::kPBuf) + (size_t)w * G * pre_row_floats(D);
+  uint64_t* pbar = reinterpret_cast<uint64_t*>(smem + SM::kPBar) + w;
 
   if (lane == 0) {
 #pragma unroll
     for (int i = 0; i < NSW; ++i) mbar_init(&bars[i], 1);
     mbar_init(&qbars[0], 1);
     mbar_init(&qbars[1], 1);
+    mbar_init(pbar, 1);
     fence_mbar_init();
   }
   __syncthreads();  // the only block-wide barrier: warps are independent from here on
@@ -242,7 +248,7 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
   // table entry of the j-th block a walker's sequence reads (the logical
   // block, past the blocks a sliding window leaves out)
   auto table_id = [&](const Walker& wk_, int j) -> int32_t {
-    const int jl = a.window > 0 ? logical_block<BS>(a, seq_len_clipped(a, wk_.s), j) : j;
+    const int jl = remaps_blocks(a) ? logical_block<BS>(a, seq_len_clipped(a, wk_.s), j) : j;
     return __ldg(a.block_tables + (size_t)wk_.s * a.table_stride + jl);
   };
   int32_t next_id = table_id(cw, cj);
@@ -283,8 +289,23 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
     bulk_g2s(qbuf + (size_t)slot * G * D, src, G * D * sizeof(QT), &qbars[slot]);
   };
 
+  // cascade: the prefix partial of the G rows of a piece that starts a
+  // segment (one buffer: the next piece's copy starts once this piece has
+  // read its own)
+  constexpr uint32_t kPreBytes = (uint32_t)(G * pre_row_floats(D) * sizeof(float));
+  auto issue_pre = [&](const Walker& pw) {
+    const float* src = a.pre + ((size_t)pw.s * a.num_q_heads + unit_first_head(a, pw, G)) * pre_row_floats(D);
+    mbar_arrive_expect_tx(pbar, kPreBytes);
+    bulk_g2s(pbuf, src, kPreBytes, pbar);
+  };
+  int pre_issued = 0, pre_waited = 0;
+
   Walker qlook = wk0;
   if (lane == 0) issue_q(wk0, 0);
+  if (a.pre && wk0.jb == 0) {
+    if (lane == 0) issue_pre(wk0);
+    ++pre_issued;
+  }
   // Everything above reads only the step's inputs (lengths, tables, q).  When
   // this grid is the programmatic dependent of the cache write, the K/V tiles
   // must wait for that grid; on an ordinary launch this returns at once.
@@ -313,6 +334,8 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
     kx = lane_base(lane & 7, lane >> 3);
     vx = lane_base(lane & 7, lane >> 3);
   }
+  // head dim of accumulator o[n][e]
+  auto odim = [&](int n, int e) -> int { return F8 ? GE::VPL * (2 * t + e) + n : 8 * n + 2 * t + e; };
   constexpr int CPB = GE::IB / 16;  // chunks per box row
   // address of chunk C (+ the lane part) relative to a 1024-byte aligned tile base
   auto frag = [](uint32_t base, int C) -> uint32_t {
@@ -395,6 +418,27 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
     for (int n = 0; n < NTO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     m_run = -CUDART_INF_F;
     l_run = 0.f;
+    if (a.pre && wk.jb == 0) {
+      // cascade: a segment's online softmax starts from the shared prefix's
+      // partial (o relative to m, l), so no later merge step sees the prefix
+      if (alive && !mbar_wait_bounded(pbar, pre_waited & 1, a.err)) alive = false;
+      ++pre_waited;
+      if (g < G) {
+        const float* pr = pbuf + (size_t)g * pre_row_floats(D);
+#pragma unroll
+        for (int n = 0; n < NTO; ++n)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) o[n][e] = pr[odim(n, e)];
+        m_run = pr[D];
+        l_run = t == 0 ? pr[D + 1] : 0.f;
+      }
+    }
+    if (a.pre && !qlook.done && qlook.jb == 0) {  // the next piece starts a segment
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) issue_pre(qlook);
+      ++pre_issued;
+    }
     const int L = seq_len_clipped(a, wk.s);
 
 #pragma unroll 1
@@ -407,7 +451,7 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
         if (!ok) alive = false;
       }
       ok = ok && stage_ok[st];
-      TileMask tm = tile_mask<BS>(a, L, a.window > 0 ? logical_block<BS>(a, L, j) : j);
+      TileMask tm = tile_mask<BS>(a, L, remaps_blocks(a) ? logical_block<BS>(a, L, j) : j);
       if (!ok) tm.hi = 0;  // a skipped tile: nothing is kept
 
 #pragma unroll
@@ -598,8 +642,6 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
     l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
     const int qh0 = unit_first_head(a, wk, G);
     const bool whole = (wk.jb == 0 && wk.je == wk.nb);
-    // head dim of accumulator o[n][e]
-    auto odim = [&](int n, int e) -> int { return F8 ? GE::VPL * (2 * t + e) + n : 8 * n + 2 * t + e; };
 
     if constexpr (!BALANCED) {
       if (g < G) {
@@ -662,6 +704,7 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
   // Leave no copy in flight: wait (bounded) for every stage this warp filled
   // but did not wait for (only possible after a timeout).
   for (int k = waited; k < issued; ++k) mbar_wait_bounded(&bars[k % NSW], (k / NSW) & 1, a.err);
+  for (int k = pre_waited; k < pre_issued; ++k) mbar_wait_bounded(pbar, k & 1, a.err);
 }
 
 }  // namespace pkv

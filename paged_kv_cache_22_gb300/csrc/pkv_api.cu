@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstring>
@@ -305,6 +306,16 @@ pkv_status pkv_split_kv_reduce(void* out, pkv_dtype out_dtype, const float* o_pa
 namespace pkv {
 namespace {
 
+// Options of a decode beyond the plain call: the sliding window, and the
+// suffix half of cascade decode (blocks past a shared prefix, the prefix's
+// partial folded in, always on the tensor cores).
+struct DecodeExtras {
+  int32_t window = 0, sinks = 0;
+  int32_t skip_blocks = 0;
+  const float* pre = nullptr;
+  bool force_tc = false;
+};
+
 // Launch one decode grid; as a programmatic dependent of the previous grid on
 // the stream when `programmatic` is set (its prologue then overlaps that grid).
 cudaError_t launch_decode_grid(const DecodeKernel& k, dim3 grid, void** args, cudaStream_t st, bool programmatic) {
@@ -327,9 +338,9 @@ pkv_status decode_impl(void* out, const void* q, pkv_dtype q_dtype, int32_t num_
                        const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
                        int32_t max_seq_len, float scale, float kv_scale, int32_t partition_tokens, void* workspace,
                        size_t workspace_bytes, pkv_stream_t stream, bool programmatic, bool dry_run = false,
-                       int32_t window = 0, int32_t sinks = 0) {
+                       const DecodeExtras& ex = DecodeExtras()) {
   if (num_seqs < 0 || !valid_cache_desc(cache)) return PKV_ERR_INVALID_ARG;
-  if (window < 0 || sinks < 0) return PKV_ERR_INVALID_ARG;
+  if (ex.window < 0 || ex.sinks < 0 || ex.skip_blocks < 0) return PKV_ERR_INVALID_ARG;
   if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return PKV_ERR_INVALID_ARG;
   if (max_blocks_per_seq <= 0 || max_seq_len < 0 || partition_tokens < 0) return PKV_ERR_INVALID_ARG;
   if (partition_tokens % cache->block_size) return PKV_ERR_INVALID_ARG;
@@ -346,7 +357,8 @@ pkv_status decode_impl(void* out, const void* q, pkv_dtype q_dtype, int32_t num_
   const int G = heads_per_unit(g);
   const bool balanced = partition_tokens == 0;
   DecodeKernel k;
-  if (!find_decode(cache->dtype, D, BS, G, balanced, decode_on_tensor_cores(), &k)) return PKV_ERR_UNSUPPORTED;
+  if (!find_decode(cache->dtype, D, BS, G, balanced, ex.force_tc || decode_on_tensor_cores(), &k))
+    return PKV_ERR_UNSUPPORTED;
 
   const int dev = current_device();
   if (dev < 0) return PKV_ERR_CUDA;
@@ -373,8 +385,10 @@ pkv_status decode_impl(void* out, const void* q, pkv_dtype q_dtype, int32_t num_
   a.units = cache->num_kv_heads * a.units_per_kv;
   const int64_t table_tokens = (int64_t)max_blocks_per_seq * BS;
   a.len_clip = (int)(table_tokens < max_seq_len ? table_tokens : max_seq_len);
-  a.window = window;
-  a.sinks = window > 0 ? sinks : 0;
+  a.window = ex.window;
+  a.sinks = ex.window > 0 ? ex.sinks : 0;
+  a.skip_blocks = ex.skip_blocks;
+  a.pre = ex.pre;
   const bool fp8 = cache->dtype == PKV_FP8_E4M3;
   a.qk_scale = scale * 1.4426950408889634f * (fp8 ? kv_scale : 1.f);
   a.out_scale = fp8 ? kv_scale : 1.f;
@@ -459,7 +473,140 @@ pkv_status pkv_paged_attention_decode_window(void* out, const void* q, pkv_dtype
                                              size_t workspace_bytes, pkv_stream_t stream) {
   return decode_impl(out, q, q_dtype, num_seqs, num_q_heads, k_cache, v_cache, cache, block_tables,
                      max_blocks_per_seq, seq_lens, max_seq_len, scale, kv_scale, partition_tokens, workspace,
-                     workspace_bytes, stream, false, false, window_tokens, sink_tokens);
+                     workspace_bytes, stream, false, false, DecodeExtras{window_tokens, sink_tokens});
+}
+
+}  // extern "C"
+
+namespace pkv {
+
+// Pieces the cascade's prefix pass cuts the prefix into: enough one-warp CTAs
+// (kv heads x blocks of 16 query rows x pieces) for one resident wave of
+// kPrefixCtasPerSm per SM, each piece at least kMinPieceBlocks blocks long.
+constexpr int kPrefixCtasPerSm = 8, kMinPieceBlocks = 4, kMaxPieces = 32;
+
+int prefix_pieces(int sms, int num_seqs, int group, int num_kv_heads, int prefix_blocks) {
+  const int64_t pairs = (int64_t)num_kv_heads * (((int64_t)num_seqs * group + 15) / 16);
+  int64_t S = pairs > 0 ? (int64_t)sms * kPrefixCtasPerSm / pairs : 1;
+  if (prefix_blocks >= 0) S = std::min<int64_t>(S, prefix_blocks / kMinPieceBlocks);
+  return (int)std::max<int64_t>(1, std::min<int64_t>(S, kMaxPieces));
+}
+
+// Byte offsets of a cascade's workspace: the balanced decode's workspace,
+// then the prefix partial the decode reads, then one partial per piece when
+// the prefix is cut (as many pieces as the longest prefix may get).  The
+// prefix pass's merge counters (one per kv head and 16-row block) sit at the
+// top of the decode's zeroed counter region, whose bottom holds the decode's:
+// both fit while num_seqs * units + pairs <= 262144.
+struct CascadeLayout {
+  size_t counters, pre, scratch, total;
+};
+
+bool cascade_layout(int num_seqs, int num_q_heads, int num_kv_heads, int D, int max_seq_len, CascadeLayout* L) {
+  const size_t dec = pkv_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, D, max_seq_len, 0);
+  if (dec == 0) return false;
+  const int dev = current_device();
+  const int sms = dev < 0 ? 0 : sm_count(dev);
+  if (sms <= 0) return false;
+  const int group = num_q_heads / num_kv_heads;
+  const size_t pairs = (size_t)num_kv_heads * (((size_t)num_seqs * group + 15) / 16);
+  const size_t row_bytes = (size_t)num_seqs * num_q_heads * pre_row_floats(D) * sizeof(float);
+  const int pieces = prefix_pieces(sms, num_seqs, group, num_kv_heads, -1);
+  const size_t units = (size_t)num_kv_heads * (group / heads_per_unit(group));
+  if (((size_t)num_seqs * units + pairs) * sizeof(int) > kCounterRegionMin) return false;
+  L->counters = kCounterRegionMin - pairs * sizeof(int);
+  L->pre = align_up(dec);
+  L->scratch = L->pre + align_up(row_bytes);
+  L->total = L->scratch + (pieces > 1 ? align_up(pieces * row_bytes) : 0);
+  return true;
+}
+
+}  // namespace pkv
+
+extern "C" {
+
+size_t pkv_cascade_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t max_seq_len) {
+  CascadeLayout L;
+  return cascade_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_seq_len, &L) ? L.total : 0;
+}
+
+pkv_status pkv_cascade_decode(void* out, const void* q, pkv_dtype q_dtype, int32_t num_seqs, int32_t num_q_heads,
+                              const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                              int32_t max_seq_len, int32_t prefix_blocks, float scale, float kv_scale,
+                              void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+  if (prefix_blocks < 0 || prefix_blocks > max_blocks_per_seq) return PKV_ERR_INVALID_ARG;
+  if (!valid_cache_desc(cache)) return PKV_ERR_INVALID_ARG;
+  if (cache->dtype == PKV_F32) return PKV_ERR_UNSUPPORTED;  // the prefix kernel runs on the tensor cores
+  const int D = cache->head_dim, BS = cache->block_size;
+  const size_t dec = pkv_decode_workspace_bytes(num_seqs, num_q_heads, cache->num_kv_heads, D, max_seq_len, 0);
+  if (prefix_blocks == 0 || num_seqs == 0)
+    return decode_impl(out, q, q_dtype, num_seqs, num_q_heads, k_cache, v_cache, cache, block_tables,
+                       max_blocks_per_seq, seq_lens, max_seq_len, scale, kv_scale, 0, workspace,
+                       workspace_bytes < dec ? workspace_bytes : dec, stream, false);
+  CascadeLayout lay;
+  if (!cascade_layout(num_seqs, num_q_heads, cache->num_kv_heads, D, max_seq_len, &lay))
+    return dec == 0 ? PKV_ERR_INVALID_ARG : PKV_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < lay.total) return PKV_ERR_WORKSPACE;
+  const int dev = current_device();
+  const int sms = dev < 0 ? 0 : sm_count(dev);
+  unsigned int* err = dev < 0 ? nullptr : error_word(dev);
+  if (!err || sms <= 0) return PKV_ERR_CUDA;
+  const int group = num_q_heads / cache->num_kv_heads;
+  int S = prefix_pieces(sms, num_seqs, group, cache->num_kv_heads, prefix_blocks);
+  const int SB = (prefix_blocks + S - 1) / S;
+  S = (prefix_blocks + SB - 1) / SB;  // no empty piece
+  char* ws = static_cast<char*>(workspace);
+  float* pre = reinterpret_cast<float*>(ws + lay.pre);
+  DecodeExtras ex;
+  ex.skip_blocks = prefix_blocks;
+  ex.pre = pre;
+  ex.force_tc = true;
+  // every argument is checked before anything is enqueued
+  pkv_status st = decode_impl(out, q, q_dtype, num_seqs, num_q_heads, k_cache, v_cache, cache, block_tables,
+                              max_blocks_per_seq, seq_lens, max_seq_len, scale, kv_scale, 0, workspace, dec, stream,
+                              false, /*dry_run=*/true, ex);
+  if (st != PKV_OK) return st;
+  PrefixKernel pk;
+  const bool found = cache->dtype == PKV_BF16 ? find_prefix_bf16(D, BS, &pk) : find_prefix_fp8(D, BS, &pk);
+  if (!found) return PKV_ERR_UNSUPPORTED;
+  if (cudaFuncSetAttribute(pk.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pk.smem) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  DecodeKernel tk;  // the tensor maps both kernels read the caches through
+  tk.tensor_maps = true;
+  TmaMaps maps{};
+  if (!encode_cache_maps(tk, cache, k_cache, v_cache, &maps)) return PKV_ERR_CUDA;
+  PrefixArgs pa{};
+  pa.err = err;
+  pa.q = q;
+  pa.block_tables = block_tables;
+  pa.table_stride = max_blocks_per_seq;
+  pa.seq_lens = seq_lens;
+  pa.num_seqs = num_seqs;
+  pa.num_q_heads = num_q_heads;
+  pa.num_kv_heads = cache->num_kv_heads;
+  pa.group = num_q_heads / cache->num_kv_heads;
+  pa.num_blocks = cache->num_blocks;
+  const int64_t table_tokens = (int64_t)max_blocks_per_seq * BS;
+  pa.len_clip = (int)(table_tokens < max_seq_len ? table_tokens : max_seq_len);
+  pa.prefix_blocks = prefix_blocks;
+  pa.row_blocks = (int)(((int64_t)num_seqs * pa.group + 15) / 16);
+  pa.splits = S;
+  pa.split_blocks = SB;
+  const bool fp8 = cache->dtype == PKV_FP8_E4M3;
+  pa.qk_scale = scale * 1.4426950408889634f * (fp8 ? kv_scale : 1.f);
+  pa.pre = pre;
+  pa.scratch = reinterpret_cast<float*>(ws + lay.scratch);
+  pa.counters = reinterpret_cast<int*>(ws + lay.counters);
+  const int64_t ctas = (int64_t)cache->num_kv_heads * pa.row_blocks * S;
+  if (ctas > 0x7FFFFFFF) return PKV_ERR_UNSUPPORTED;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  void* args[] = {&pa, &maps};
+  if (cudaLaunchKernel(pk.fn, dim3((unsigned)ctas), dim3(32), args, pk.smem, cs) != cudaSuccess) return PKV_ERR_CUDA;
+  return decode_impl(out, q, q_dtype, num_seqs, num_q_heads, k_cache, v_cache, cache, block_tables,
+                     max_blocks_per_seq, seq_lens, max_seq_len, scale, kv_scale, 0, workspace, dec, stream, false,
+                     false, ex);
 }
 
 pkv_status pkv_decode_step(const void* k, const void* v, pkv_dtype src_dtype, int32_t num_new_tokens,

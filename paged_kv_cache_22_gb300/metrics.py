@@ -84,3 +84,24 @@ def unique_kv_bytes(seq_lens: Iterable[int], shared_prefix_tokens: int, num_kv_h
         return 0
     uniq = shared_prefix_tokens + sum(L - shared_prefix_tokens for L in lens)
     return uniq * per
+
+
+def cascade_bytes(seq_lens: Iterable[int], prefix_tokens: int, num_q_heads: int, num_kv_heads: int,
+                  head_dim: int, cache_dtype: str, q_dtype: str, block_size: int) -> int:
+    """Algorithmic bytes of a decode call that reads a prefix shared by every
+    sequence once: the prefix tokens any sequence attends, each sequence's
+    tokens past the prefix, q, out, the table entries read (the prefix's
+    once) and seq_lens.  The prefix partial result the cascade writes and
+    reads back is traffic of the method, not counted here."""
+    lens = [int(x) for x in seq_lens]
+    if not lens:
+        return 0
+    e_c, e_q = ELEM_BYTES[cache_dtype], ELEM_BYTES[q_dtype]
+    per = kv_bytes_per_token(1, num_kv_heads, head_dim, e_c)
+    pre = min(prefix_tokens, max(lens))
+    kv = (pre + sum(max(L - prefix_tokens, 0) for L in lens)) * per
+    qo = 2 * len(lens) * num_q_heads * head_dim * e_q
+    pb = blocks_for_tokens(prefix_tokens, block_size)
+    tables = 4 * (blocks_for_tokens(pre, block_size)
+                  + sum(max(blocks_for_tokens(L, block_size) - pb, 0) for L in lens))
+    return kv + qo + tables + 4 * len(lens)

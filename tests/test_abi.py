@@ -107,3 +107,27 @@ def test_decode_engine_switch(lib):
     assert pkv.get_decode_engine() == "tensor_cores"
     assert lib.pkv_set_decode_engine(7) == 1  # unknown engine: invalid argument, no change
     assert pkv.get_decode_engine() == "tensor_cores"
+
+
+def test_cascade_workspace_size_without_a_device(lib):
+    # the balanced decode's share depends on the device's SM count: without a
+    # device both sizes are 0 (the formula is checked on the GPU)
+    B, Hq, Hkv, d, L = 256, 32, 8, 128, 2560
+    if lib.pkv_decode_workspace_bytes(B, Hq, Hkv, d, L, 0) == 0:
+        assert lib.pkv_cascade_workspace_bytes(B, Hq, Hkv, d, L) == 0
+    assert lib.pkv_cascade_workspace_bytes(B, Hq, 3, d, L) == 0  # invalid GQA split
+
+
+def test_cascade_rejects_bad_prefix_before_launch(lib):
+    from paged_kv_cache_22_gb300 import CacheDesc
+    INVALID, UNSUPPORTED = 1, 2
+    desc = CacheDesc(num_blocks=8, block_size=16, num_kv_heads=2, head_dim=64, dtype=1)
+    p = ctypes.c_void_p(256)
+    for pb in (-1, 5):  # the table has 4 entries per sequence
+        st = lib.pkv_cascade_decode(p, p, 1, 2, 8, p, p, ctypes.byref(desc), p, 4, p, 64, pb, 0.125, 1.0,
+                                    p, 1 << 24, None)
+        assert st == INVALID
+    desc.dtype = 0  # fp32 caches
+    st = lib.pkv_cascade_decode(p, p, 0, 2, 8, p, p, ctypes.byref(desc), p, 4, p, 64, 2, 0.125, 1.0,
+                                p, 1 << 24, None)
+    assert st == UNSUPPORTED
