@@ -95,7 +95,7 @@ struct Smem {
 // ----------------------------------------------------------------------------
 // The kernel.
 // ----------------------------------------------------------------------------
-template <class CT, int D, int BS, int G, int W, bool BALANCED>
+template <class CT, int D, int BS, int G, int W, bool BALANCED, bool REMAP>
 __global__ void __launch_bounds__(W * 32, (G >= 8 ? 8 : 12) / W)
     decode_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ TmaMaps) {
   using GE = Geo<CT, D, BS, G>;
@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(W * 32, (G >= 8 ? 8 : 12) / W)
   // table entry of the j-th block a walker's sequence reads (the logical
   // block, past the blocks a sliding window leaves out)
   auto table_id = [&](const Walker& wk_, int j) -> int32_t {
-    const int jl = remaps_blocks(a) ? logical_block<BS>(a, seq_len_clipped(a, wk_.s), j) : j;
+    const int jl = REMAP ? logical_block<BS>(a, seq_len_clipped(a, wk_.s), j) : j;
     return __ldg(a.block_tables + (size_t)wk_.s * a.table_stride + jl);
   };
   int32_t next_id = table_id(cw, cj);
@@ -254,8 +254,8 @@ __global__ void __launch_bounds__(W * 32, (G >= 8 ? 8 : 12) / W)
         if (!ok) alive = false;
       }
       ok = ok && stage_ok[st];
-      TileMask tm = tile_mask<BS>(a, L, remaps_blocks(a) ? logical_block<BS>(a, L, j) : j);
-      if (!ok) tm.hi = 0;  // a skipped tile: nothing is kept
+      TileMask tm = tile_mask<BS, REMAP>(a, L, REMAP ? logical_block<BS>(a, L, j) : j);
+      if (!ok) tm.clear();  // a skipped tile: nothing is kept
 
 #pragma unroll 1
       for (int step = 0; step < GE::STEPS; ++step) {

@@ -4,12 +4,6 @@
 
 namespace pkv {
 bool find_decode_bf16_cc(int head_dim, int block_size, int heads, bool balanced, DecodeKernel* out) {
-  if (head_dim == 128) {
-    if (block_size == 16) return find_for<CacheBF16, 128, 16, false>(heads, balanced, out);
-    if (block_size == 8) return find_for<CacheBF16, 128, 8, false>(heads, balanced, out);
-    if (block_size == 32) return find_for<CacheBF16, 128, 32, false>(heads, balanced, out);
-  }
-  if (head_dim == 64 && block_size == 16) return find_for<CacheBF16, 64, 16, false>(heads, balanced, out);
-  return false;
+  return find_shape<CacheBF16, false, false>(head_dim, block_size, heads, balanced, out);
 }
 }  // namespace pkv

@@ -138,8 +138,10 @@ __device__ __forceinline__ BlockMap block_map(const DecodeArgs& a, int L) {
 }
 
 // Whether some sequence may skip blocks (a window, or a cascade's prefix),
-// so that the j-th block read is not logical block j.
-__device__ __forceinline__ bool remaps_blocks(const DecodeArgs& a) { return a.window > 0 || a.skip_blocks > 0; }
+// so that the j-th block read is not logical block j.  The decode kernels
+// take this as a compile-time REMAP parameter: a per-tile runtime branch on
+// it costs ~10 % of the fp8 decode, whose tile loop is latency bound.
+inline bool remaps_blocks(int window, int skip_blocks) { return window > 0 || skip_blocks > 0; }
 
 // Floats per row of a cascade's prefix partial: D of o, m, l, two of padding
 // (rows stay 16-byte aligned for bulk copies).
@@ -152,27 +154,31 @@ __device__ __forceinline__ int logical_block(const DecodeArgs& a, int L, int j) 
   return j < m.nsb ? j : j + (m.wsb - m.nsb);
 }
 
-// Tokens of logical block jl that are attended: tok < hi and (tok < s_hi or
-// tok >= w_lo), tok counted from the block's first token.
+// Tokens of logical block jl that are attended, one bit per token (bit t:
+// token t of the block, t < 32): t < hi and, under a window, (t < s_hi or
+// t >= w_lo).  Computed once per tile, so that every per-token test in the
+// score and V masks is a single bit test.
+__device__ __forceinline__ uint32_t low_bits(int n) { return n <= 0 ? 0u : (n >= 32 ? 0xFFFFFFFFu : (1u << n) - 1u); }
+
 struct TileMask {
-  int hi, s_hi, w_lo;
-  __device__ __forceinline__ bool keep(int tok) const { return tok < hi && (tok < s_hi || tok >= w_lo); }
+  uint32_t bits;
+  __device__ __forceinline__ bool keep(int tok) const { return (bits >> tok) & 1u; }
   // every token of [t0, t1) kept
-  __device__ __forceinline__ bool all(int t0, int t1) const { return t1 <= hi && (w_lo <= t0 || s_hi >= t1); }
+  __device__ __forceinline__ bool all(int t0, int t1) const {
+    const uint32_t m = low_bits(t1) & ~low_bits(t0);
+    return (bits & m) == m;
+  }
+  __device__ __forceinline__ void clear() { bits = 0u; }
 };
 
-template <int BS>
+template <int BS, bool REMAP>
 __device__ __forceinline__ TileMask tile_mask(const DecodeArgs& a, int L, int jl) {
+  static_assert(BS <= 32, "one bit per token of a block");
   const int base = jl * BS;
   TileMask m;
-  m.hi = L - base < BS ? L - base : BS;
-  m.s_hi = 0;
-  m.w_lo = 0;
-  if (a.window > 0 && L > a.window) {
-    const int sh = a.sinks - base, wl = L - a.window - base;
-    m.s_hi = sh < 0 ? 0 : (sh > BS ? BS : sh);
-    m.w_lo = wl < 0 ? 0 : (wl > BS ? BS : wl);
-  }
+  m.bits = low_bits(L - base < BS ? L - base : BS);
+  if constexpr (REMAP)
+    if (a.window > 0 && L > a.window) m.bits &= low_bits(a.sinks - base) | ~low_bits(L - a.window - base);
   return m;
 }
 

@@ -3,9 +3,6 @@
 
 namespace pkv {
 bool find_decode_fp8_cc(int head_dim, int block_size, int heads, bool balanced, DecodeKernel* out) {
-  if (block_size != 16) return false;
-  if (head_dim == 64) return find_for<CacheFP8, 64, 16, false>(heads, balanced, out);
-  if (head_dim == 128) return find_for<CacheFP8, 128, 16, false>(heads, balanced, out);
-  return false;
+  return find_shape<CacheFP8, false, false>(head_dim, block_size, heads, balanced, out);
 }
 }  // namespace pkv

@@ -19,16 +19,18 @@ struct DecodeKernel {
 
 // TC: the q.K and P.V contractions on the tensor cores (decode_tc.cuh, bf16
 // and fp8 caches); otherwise on the CUDA cores (decode.cuh, every cache type).
-template <class CT, int D, int BS, int G, bool BAL, bool TC>
+// REMAP: the instance that may skip blocks (a sliding window, a cascade's
+// prefix); plain decode runs the instance without that code.
+template <class CT, int D, int BS, int G, bool BAL, bool TC, bool REMAP>
 DecodeKernel decode_kernel_info() {
   DecodeKernel k;
   if constexpr (TC) {
     static_assert(CT::kBytes != 4, "fp32 caches run on the CUDA cores");
-    k.fn = reinterpret_cast<const void*>(&decode_tc_kernel<CT, D, BS, G, kDecodeWarps, BAL>);
-    k.smem = TcSmem<CT, D, BS, G, kDecodeWarps>::kBytes;
+    k.fn = reinterpret_cast<const void*>(&decode_tc_kernel<CT, D, BS, G, kDecodeWarps, BAL, REMAP>);
+    k.smem = TcSmem<CT, D, BS, G, kDecodeWarps, REMAP>::kBytes;
     k.tensor_maps = true;
   } else {
-    k.fn = reinterpret_cast<const void*>(&decode_kernel<CT, D, BS, G, kDecodeWarps, BAL>);
+    k.fn = reinterpret_cast<const void*>(&decode_kernel<CT, D, BS, G, kDecodeWarps, BAL, REMAP>);
     k.smem = Smem<CT, D, BS, G, kDecodeWarps>::kBytes;
   }
   k.threads = kDecodeWarps * 32;
@@ -42,7 +44,8 @@ bool encode_cache_maps(const DecodeKernel& k, const pkv_cache_desc* cache, const
                        const void* v_cache, TmaMaps* maps);
 
 // Fill `out` with the instance for (D, BS, G, balanced); false if not built.
-// One finder per cache type and engine, each in its own translation unit.
+// One finder per cache type, engine and REMAP, each in its own translation
+// unit (they compile in parallel).
 #define PKV_DECLARE_FINDER(NAME) \
   bool NAME(int head_dim, int block_size, int heads, bool balanced, DecodeKernel* out);
 
@@ -51,28 +54,58 @@ PKV_DECLARE_FINDER(find_decode_bf16_tc)
 PKV_DECLARE_FINDER(find_decode_bf16_cc)
 PKV_DECLARE_FINDER(find_decode_fp8_tc)
 PKV_DECLARE_FINDER(find_decode_fp8_cc)
+PKV_DECLARE_FINDER(find_decode_f32_remap)
+PKV_DECLARE_FINDER(find_decode_bf16_tc_remap)
+PKV_DECLARE_FINDER(find_decode_bf16_cc_remap)
+PKV_DECLARE_FINDER(find_decode_fp8_tc_remap)
+PKV_DECLARE_FINDER(find_decode_fp8_cc_remap)
 
-// Shared body of the finders: the compiled (D, BS) set is passed as a list.
-template <class CT, int D, int BS, bool TC>
+// Shared body of the finders: the heads-per-unit switch for one (D, BS).
+template <class CT, int D, int BS, bool TC, bool REMAP>
 bool find_for(int heads, bool balanced, DecodeKernel* out) {
   switch (heads) {
-    case 1: *out = balanced ? decode_kernel_info<CT, D, BS, 1, true, TC>() : decode_kernel_info<CT, D, BS, 1, false, TC>(); return true;
-    case 2: *out = balanced ? decode_kernel_info<CT, D, BS, 2, true, TC>() : decode_kernel_info<CT, D, BS, 2, false, TC>(); return true;
-    case 4: *out = balanced ? decode_kernel_info<CT, D, BS, 4, true, TC>() : decode_kernel_info<CT, D, BS, 4, false, TC>(); return true;
-    case 8: *out = balanced ? decode_kernel_info<CT, D, BS, 8, true, TC>() : decode_kernel_info<CT, D, BS, 8, false, TC>(); return true;
+    case 1: *out = balanced ? decode_kernel_info<CT, D, BS, 1, true, TC, REMAP>() : decode_kernel_info<CT, D, BS, 1, false, TC, REMAP>(); return true;
+    case 2: *out = balanced ? decode_kernel_info<CT, D, BS, 2, true, TC, REMAP>() : decode_kernel_info<CT, D, BS, 2, false, TC, REMAP>(); return true;
+    case 4: *out = balanced ? decode_kernel_info<CT, D, BS, 4, true, TC, REMAP>() : decode_kernel_info<CT, D, BS, 4, false, TC, REMAP>(); return true;
+    case 8: *out = balanced ? decode_kernel_info<CT, D, BS, 8, true, TC, REMAP>() : decode_kernel_info<CT, D, BS, 8, false, TC, REMAP>(); return true;
     default: return false;
   }
 }
 
-// The decode kernel for a cache type, shape and engine (fp32 caches always
-// take the CUDA cores).
-inline bool find_decode(pkv_dtype dt, int D, int BS, int G, bool balanced, bool tensor_cores, DecodeKernel* k) {
+// The compiled (D, BS) sets: fp32 and fp8 caches block size 16, head dim 64
+// or 128; bf16 caches also block sizes 8 and 32 at head dim 128.
+template <class CT, bool TC, bool REMAP>
+bool find_shape(int head_dim, int block_size, int heads, bool balanced, DecodeKernel* out) {
+  if constexpr (CT::kBytes == 2) {
+    if (head_dim == 128) {
+      if (block_size == 16) return find_for<CT, 128, 16, TC, REMAP>(heads, balanced, out);
+      if (block_size == 8) return find_for<CT, 128, 8, TC, REMAP>(heads, balanced, out);
+      if (block_size == 32) return find_for<CT, 128, 32, TC, REMAP>(heads, balanced, out);
+    }
+    if (head_dim == 64 && block_size == 16) return find_for<CT, 64, 16, TC, REMAP>(heads, balanced, out);
+    return false;
+  } else {
+    if (block_size != 16) return false;
+    if (head_dim == 64) return find_for<CT, 64, 16, TC, REMAP>(heads, balanced, out);
+    if (head_dim == 128) return find_for<CT, 128, 16, TC, REMAP>(heads, balanced, out);
+    return false;
+  }
+}
+
+// The decode kernel for a cache type, shape, engine and REMAP (fp32 caches
+// always take the CUDA cores).
+inline bool find_decode(pkv_dtype dt, int D, int BS, int G, bool balanced, bool tensor_cores, bool remap,
+                        DecodeKernel* k) {
   switch (dt) {
-    case PKV_F32: return find_decode_f32(D, BS, G, balanced, k);
+    case PKV_F32: return remap ? find_decode_f32_remap(D, BS, G, balanced, k) : find_decode_f32(D, BS, G, balanced, k);
     case PKV_BF16:
-      return tensor_cores ? find_decode_bf16_tc(D, BS, G, balanced, k) : find_decode_bf16_cc(D, BS, G, balanced, k);
+      if (tensor_cores)
+        return remap ? find_decode_bf16_tc_remap(D, BS, G, balanced, k) : find_decode_bf16_tc(D, BS, G, balanced, k);
+      return remap ? find_decode_bf16_cc_remap(D, BS, G, balanced, k) : find_decode_bf16_cc(D, BS, G, balanced, k);
     case PKV_FP8_E4M3:
-      return tensor_cores ? find_decode_fp8_tc(D, BS, G, balanced, k) : find_decode_fp8_cc(D, BS, G, balanced, k);
+      if (tensor_cores)
+        return remap ? find_decode_fp8_tc_remap(D, BS, G, balanced, k) : find_decode_fp8_tc(D, BS, G, balanced, k);
+      return remap ? find_decode_fp8_cc_remap(D, BS, G, balanced, k) : find_decode_fp8_cc(D, BS, G, balanced, k);
   }
   return false;
 }

@@ -172,7 +172,7 @@ struct TcGeo {
   static_assert(STAGE % 1024 == 0 && BOX % 512 == 0, "stages and boxes keep the swizzle phase");
 };
 
-template <class CT, int D, int BS, int G, int W>
+template <class CT, int D, int BS, int G, int W, bool REMAP>
 struct TcSmem {
   using GE = TcGeo<CT, D, BS, G>;
   static constexpr size_t kStages = 0;  // 1024-byte aligned
@@ -180,9 +180,9 @@ struct TcSmem {
   static constexpr size_t kBars = (kQBuf + (size_t)W * 2 * G * D * sizeof(__nv_bfloat16) + 7) / 8 * 8;
   static constexpr size_t kQBars = kBars + (size_t)W * GE::NSW * 8;
   static constexpr size_t kOk = kQBars + (size_t)W * 2 * 8;
-  // cascade: one warp's next prefix partial (G rows), and its barrier
+  // cascade (REMAP kernels): one warp's next prefix partial (G rows), and its barrier
   static constexpr size_t kPBuf = (kOk + (size_t)W * GE::NSW * 4 + 15) / 16 * 16;
-  static constexpr size_t kPBar = kPBuf + (size_t)W * G * pre_row_floats(D) * sizeof(float);
+  static constexpr size_t kPBar = kPBuf + (REMAP ? (size_t)W * G * pre_row_floats(D) * sizeof(float) : 0);
   static constexpr size_t kBytes = kPBar + (size_t)W * 8;
 };
 
@@ -200,11 +200,11 @@ __device__ __forceinline__ uint32_t swz(int row, int c) {
 // ----------------------------------------------------------------------------
 // The kernel.
 // ----------------------------------------------------------------------------
-template <class CT, int D, int BS, int G, int W, bool BALANCED>
+template <class CT, int D, int BS, int G, int W, bool BALANCED, bool REMAP>
 __global__ void __launch_bounds__(W * 32, 8 / W)
     decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ TmaMaps maps) {
   using GE = TcGeo<CT, D, BS, G>;
-  using SM = TcSmem<CT, D, BS, G, W>;
+  using SM = TcSmem<CT, D, BS, G, W, REMAP>;
   using QT = typename CT::QType;
   constexpr bool F8 = GE::F8;
   constexpr int NSW = GE::NSW, TB = GE::TB, KS = GE::KS, NTO = GE::NTO, TILE = GE::TILE, STAGE = GE::STAGE;
@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
   // table entry of the j-th block a walker's sequence reads (the logical
   // block, past the blocks a sliding window leaves out)
   auto table_id = [&](const Walker& wk_, int j) -> int32_t {
-    const int jl = remaps_blocks(a) ? logical_block<BS>(a, seq_len_clipped(a, wk_.s), j) : j;
+    const int jl = REMAP ? logical_block<BS>(a, seq_len_clipped(a, wk_.s), j) : j;
     return __ldg(a.block_tables + (size_t)wk_.s * a.table_stride + jl);
   };
   int32_t next_id = table_id(cw, cj);
@@ -302,9 +302,11 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
 
   Walker qlook = wk0;
   if (lane == 0) issue_q(wk0, 0);
-  if (a.pre && wk0.jb == 0) {
-    if (lane == 0) issue_pre(wk0);
-    ++pre_issued;
+  if constexpr (REMAP) {
+    if (a.pre && wk0.jb == 0) {
+      if (lane == 0) issue_pre(wk0);
+      ++pre_issued;
+    }
   }
   // Everything above reads only the step's inputs (lengths, tables, q).  When
   // this grid is the programmatic dependent of the cache write, the K/V tiles
@@ -418,26 +420,28 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
     for (int n = 0; n < NTO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     m_run = -CUDART_INF_F;
     l_run = 0.f;
-    if (a.pre && wk.jb == 0) {
-      // cascade: a segment's online softmax starts from the shared prefix's
-      // partial (o relative to m, l), so no later merge step sees the prefix
-      if (alive && !mbar_wait_bounded(pbar, pre_waited & 1, a.err)) alive = false;
-      ++pre_waited;
-      if (g < G) {
-        const float* pr = pbuf + (size_t)g * pre_row_floats(D);
+    if constexpr (REMAP) {
+      if (a.pre && wk.jb == 0) {
+        // cascade: a segment's online softmax starts from the shared prefix's
+        // partial (o relative to m, l), so no later merge step sees the prefix
+        if (alive && !mbar_wait_bounded(pbar, pre_waited & 1, a.err)) alive = false;
+        ++pre_waited;
+        if (g < G) {
+          const float* pr = pbuf + (size_t)g * pre_row_floats(D);
 #pragma unroll
-        for (int n = 0; n < NTO; ++n)
+          for (int n = 0; n < NTO; ++n)
 #pragma unroll
-          for (int e = 0; e < 2; ++e) o[n][e] = pr[odim(n, e)];
-        m_run = pr[D];
-        l_run = t == 0 ? pr[D + 1] : 0.f;
+            for (int e = 0; e < 2; ++e) o[n][e] = pr[odim(n, e)];
+          m_run = pr[D];
+          l_run = t == 0 ? pr[D + 1] : 0.f;
+        }
       }
-    }
-    if (a.pre && !qlook.done && qlook.jb == 0) {  // the next piece starts a segment
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) issue_pre(qlook);
-      ++pre_issued;
+      if (a.pre && !qlook.done && qlook.jb == 0) {  // the next piece starts a segment
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) issue_pre(qlook);
+        ++pre_issued;
+      }
     }
     const int L = seq_len_clipped(a, wk.s);
 
@@ -451,8 +455,8 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
         if (!ok) alive = false;
       }
       ok = ok && stage_ok[st];
-      TileMask tm = tile_mask<BS>(a, L, remaps_blocks(a) ? logical_block<BS>(a, L, j) : j);
-      if (!ok) tm.hi = 0;  // a skipped tile: nothing is kept
+      TileMask tm = tile_mask<BS, REMAP>(a, L, REMAP ? logical_block<BS>(a, L, j) : j);
+      if (!ok) tm.clear();  // a skipped tile: nothing is kept
 
 #pragma unroll
       for (int step = 0; step < GE::STEPS; ++step) {

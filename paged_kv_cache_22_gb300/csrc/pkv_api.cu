@@ -357,7 +357,8 @@ pkv_status decode_impl(void* out, const void* q, pkv_dtype q_dtype, int32_t num_
   const int G = heads_per_unit(g);
   const bool balanced = partition_tokens == 0;
   DecodeKernel k;
-  if (!find_decode(cache->dtype, D, BS, G, balanced, ex.force_tc || decode_on_tensor_cores(), &k))
+  if (!find_decode(cache->dtype, D, BS, G, balanced, ex.force_tc || decode_on_tensor_cores(),
+                   remaps_blocks(ex.window, ex.skip_blocks), &k))
     return PKV_ERR_UNSUPPORTED;
 
   const int dev = current_device();

@@ -102,7 +102,7 @@ extern "C" pkv_status pkv_paged_attention_decode_noalloc(
   for (int cand : {8, 4, 2, 1})
     if (g % cand == 0) { G = cand; break; }
   DecodeKernel k;
-  if (!find_decode(cache->dtype, D, BS, G, true, decode_on_tensor_cores(), &k)) return PKV_ERR_UNSUPPORTED;
+  if (!find_decode(cache->dtype, D, BS, G, true, decode_on_tensor_cores(), false, &k)) return PKV_ERR_UNSUPPORTED;
 
   int dev = -1, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
