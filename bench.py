@@ -51,8 +51,8 @@ L2_FLUSH_BYTES = 256 << 20
 
 # DRAM traffic of one decode launch on the default workload, from an ncu
 # capture, valid only for the kernel sources it was taken on.
-TRAFFIC = {"sources_sha256": "ab6824dfd010f91e6933b420861037cc6d67b42188bd09ff2b376d1650fb51be",
-           "bytes_per_launch": 322043904}  # 317.679104 MB read + 4.364800 MB written
+TRAFFIC = {"sources_sha256": "e566db48573e366f48c7f27e7c3b59b2cd9bf168f99fc8f860af5da365cf330e",
+           "bytes_per_launch": 322487040}  # 317.651456 MB read + 4.835584 MB written
 
 WORKLOAD_TEXT = {
     "llama3_8b": "Llama-3-8B-shaped decode layer: 64 seqs, L~U[128,2048], 32 q / 8 kv heads, "
