@@ -43,16 +43,22 @@ struct PrefixArgs {
   int* counters;                 // [Hkv * row_blocks], zero between calls (splits > 1)
 };
 
+// Warps per CTA: the PW warps of a CTA take 16 rows each of the same kv head
+// and piece, and share one ring of prefix tiles (one tensor copy per tile
+// for all of them).
+constexpr int kPrefixWarps = 4;
+
 template <class CT, int D, int BS>
 struct PrefixSmem {
   using GE = TcGeo<CT, D, BS, 1>;
   static constexpr size_t kStages = 0;  // 1024-byte aligned
-  static constexpr size_t kBars = (size_t)GE::NSW * GE::STAGE;
-  static constexpr size_t kBytes = kBars + (size_t)GE::NSW * 8;
+  static constexpr size_t kFull = (size_t)GE::NSW * GE::STAGE;  // tile landed
+  static constexpr size_t kEmpty = kFull + (size_t)GE::NSW * 8;  // every warp done with it
+  static constexpr size_t kBytes = kEmpty + (size_t)GE::NSW * 8;
 };
 
 template <class CT, int D, int BS>
-__global__ void __launch_bounds__(32, 8)
+__global__ void __launch_bounds__(32 * kPrefixWarps, 12 / kPrefixWarps)
     prefix_attention_kernel(const __grid_constant__ PrefixArgs a, const __grid_constant__ TmaMaps maps) {
   using GE = TcGeo<CT, D, BS, 1>;
   using SM = PrefixSmem<CT, D, BS>;
@@ -63,24 +69,34 @@ __global__ void __launch_bounds__(32, 8)
 
   extern __shared__ __align__(1024) uint8_t pf_smem[];
   uint8_t* const stages = pf_smem + SM::kStages;
-  const int lane = threadIdx.x & 31;
+  constexpr int PW = kPrefixWarps;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
   if (smem_addr(stages) & 1023u) {
-    if (lane == 0) raise_error(a.err, PKV_DEVERR_SMEM_ALIGN);
+    if (threadIdx.x == 0) raise_error(a.err, PKV_DEVERR_SMEM_ALIGN);
     return;
   }
   const uint32_t stages_s = smem_addr(stages);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(pf_smem + SM::kBars);
-  if (lane == 0) {
+  uint64_t* bars = reinterpret_cast<uint64_t*>(pf_smem + SM::kFull);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(pf_smem + SM::kEmpty);
+  if (threadIdx.x == 0) {
 #pragma unroll
-    for (int i = 0; i < NSW; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < NSW; ++i) {
+      mbar_init(&bars[i], 1);
+      mbar_init(&empty[i], PW);
+    }
     fence_mbar_init();
   }
-  __syncwarp();
+  __syncthreads();
 
-  // CTA -> (piece of the prefix, kv head, block of 16 rows)
-  const int piece = blockIdx.x % a.splits, hr = blockIdx.x / a.splits;
-  const int h = hr / a.row_blocks, rb = hr % a.row_blocks;
+  // CTA -> (piece of the prefix, kv head, PW blocks of 16 rows); warp -> one
+  // of those blocks (past the last one a warp has no rows but still keeps
+  // the ring's pace)
+  const int groups = (a.row_blocks + PW - 1) / PW;
+  const int piece = blockIdx.x % a.splits, cg = blockIdx.x / a.splits;
+  const int h = cg / groups, rb = (cg % groups) * PW + w;
+  const bool has_rows = rb < a.row_blocks;
+  const int hr = h * a.row_blocks + rb;
   const int jb = piece * a.split_blocks;
   const int je = min(a.prefix_blocks, jb + a.split_blocks);
   const int ptok = a.prefix_blocks * BS;
@@ -173,11 +189,12 @@ __global__ void __launch_bounds__(32, 8)
   }
 
   // ---------------------------------------------------------------- issue side
+  // Producer: lane 0 of warp 0 starts every tile copy of the CTA.
   int issued = 0;  // blocks of this piece whose copy was started
   auto issue_next = [&]() {
     if (jb + issued >= je) return;
     const int st = issued % NSW;
-    if (lane == 0) {
+    if (w == 0 && lane == 0) {
       const int32_t id = __ldg(a.block_tables + jb + issued);
       uint8_t* dst = stages + (size_t)st * STAGE;
       if (id >= 0 && id < a.num_blocks) {
@@ -196,8 +213,10 @@ __global__ void __launch_bounds__(32, 8)
   };
   // the cascade's decode runs after this grid on the stream; the cache write
   // of the step (if any) ran before both
+  if (w == 0) {
 #pragma unroll 1
-  for (int i = 0; i < NSW; ++i) issue_next();
+    for (int i = 0; i < NSW; ++i) issue_next();
+  }
 
   // fragment addresses (as in the decode kernel)
   auto lane_base = [](int row, int hh) -> uint32_t { return swz<GE>(row, hh); };
@@ -420,8 +439,15 @@ __global__ void __launch_bounds__(32, 8)
         }
       }
     }
-    __syncwarp();  // every lane is done with this stage before it is refilled
-    if (alive) issue_next();
+    __syncwarp();  // every lane is done with this stage ...
+    if (lane == 0) mbar_arrive(&empty[st]);  // ... and so is this warp
+    // The producer refills the stage of the previous block once every warp
+    // is done with it (a block later, so the wait seldom blocks).
+    if (w == 0 && i >= 1 && jb + issued < je) {
+      const int ip = i - 1;
+      if (alive && !mbar_wait_bounded(&empty[ip % NSW], (ip / NSW) & 1, a.err)) alive = false;
+      if (alive) issue_next();
+    }
   }
 
   // ---------------------------------------------------------------- partials
@@ -445,7 +471,7 @@ __global__ void __launch_bounds__(32, 8)
       }
     }
   }
-  if (a.splits > 1) {
+  if (a.splits > 1 && has_rows) {
     // the last piece of this (kv head, row block) to finish merges them all
     __threadfence();
     __syncwarp();
@@ -456,40 +482,65 @@ __global__ void __launch_bounds__(32, 8)
     }
     if (__shfl_sync(0xffffffffu, last, 0)) {
       __threadfence();
-      for (int rr = 0; rr < 16; ++rr) {
-        const int R = rb * 16 + rr, s = R / a.group;
-        if (s >= a.num_seqs) break;
-        const size_t row = (size_t)s * a.num_q_heads + h * a.group + R % a.group;
-        float mk = -CUDART_INF_F, lk = 0.f;
-        if (lane < a.splits) {
-          const float* p = a.scratch + ((size_t)lane * rows + row) * PRF;
-          mk = __ldcg(p + D);
-          lk = __ldcg(p + D + 1);
-        }
-        float M = mk;
+      // four rows at a time, every load of the four issued before any use:
+      // lane k < splits reads piece k's (m, l); lane i covers dims 4i..4i+3
+#pragma unroll 1
+      for (int r0 = 0; r0 < 16; r0 += 4) {
+        size_t row[4];
+        bool live[4];
+        float mk[4], lk[4];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        const float Mc = M == -CUDART_INF_F ? 0.f : M;
-        const float wk = lane < a.splits ? fast_exp2(mk - Mc) : 0.f;
-        float den = lk * wk;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int k = 0; k < a.splits; ++k) {
-          const float wkk = __shfl_sync(0xffffffffu, wk, k);
-          if (4 * lane < D) {
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(a.scratch + ((size_t)k * rows + row) * PRF) + lane);
-            acc.x += v.x * wkk;
-            acc.y += v.y * wkk;
-            acc.z += v.z * wkk;
-            acc.w += v.w * wkk;
+        for (int u = 0; u < 4; ++u) {
+          const int R = rb * 16 + r0 + u, s = R / a.group;
+          live[u] = s < a.num_seqs;
+          row[u] = live[u] ? (size_t)s * a.num_q_heads + h * a.group + R % a.group : 0;
+          mk[u] = -CUDART_INF_F;
+          lk[u] = 0.f;
+          if (live[u] && lane < a.splits) {
+            const float* p = a.scratch + ((size_t)lane * rows + row[u]) * PRF;
+            mk[u] = __ldcg(p + D);
+            lk[u] = __ldcg(p + D + 1);
           }
         }
-        float* dst = a.pre + row * PRF;
-        if (4 * lane < D) reinterpret_cast<float4*>(dst)[lane] = acc;
-        if (lane == 0) {
-          dst[D] = M;
-          dst[D + 1] = den;
+        float M[4], wk[4], den[4];
+        float4 acc[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          M[u] = mk[u];
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) M[u] = fmaxf(M[u], __shfl_xor_sync(0xffffffffu, M[u], off));
+          const float Mc = M[u] == -CUDART_INF_F ? 0.f : M[u];
+          wk[u] = lane < a.splits ? fast_exp2(mk[u] - Mc) : 0.f;
+          den[u] = lk[u] * wk[u];
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) den[u] += __shfl_xor_sync(0xffffffffu, den[u], off);
+          acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        for (int k = 0; k < a.splits; ++k) {
+          float4 v[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            v[u] = (live[u] && 4 * lane < D)
+                       ? __ldcg(reinterpret_cast<const float4*>(a.scratch + ((size_t)k * rows + row[u]) * PRF) + lane)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float wkk = __shfl_sync(0xffffffffu, wk[u], k);
+            acc[u].x += v[u].x * wkk;
+            acc[u].y += v[u].y * wkk;
+            acc[u].z += v[u].z * wkk;
+            acc[u].w += v[u].w * wkk;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (!live[u]) continue;
+          float* dst = a.pre + row[u] * PRF;
+          if (4 * lane < D) reinterpret_cast<float4*>(dst)[lane] = acc[u];
+          if (lane == 0) {
+            dst[D] = M[u];
+            dst[D + 1] = den[u];
+          }
         }
       }
     }

@@ -481,14 +481,14 @@ pkv_status pkv_paged_attention_decode_window(void* out, const void* q, pkv_dtype
 
 namespace pkv {
 
-// Pieces the cascade's prefix pass cuts the prefix into: enough one-warp CTAs
-// (kv heads x blocks of 16 query rows x pieces) for one resident wave of
-// kPrefixCtasPerSm per SM, each piece at least kMinPieceBlocks blocks long.
-constexpr int kPrefixCtasPerSm = 8, kMinPieceBlocks = 4, kMaxPieces = 32;
+// Pieces the cascade's prefix pass cuts the prefix into: enough warps (kv
+// heads x blocks of 16 query rows x pieces) for one resident wave of
+// kPrefixWarpsPerSm per SM, each piece at least kMinPieceBlocks blocks long.
+constexpr int kPrefixWarpsPerSm = 12, kMinPieceBlocks = 4, kMaxPieces = 32;
 
 int prefix_pieces(int sms, int num_seqs, int group, int num_kv_heads, int prefix_blocks) {
   const int64_t pairs = (int64_t)num_kv_heads * (((int64_t)num_seqs * group + 15) / 16);
-  int64_t S = pairs > 0 ? (int64_t)sms * kPrefixCtasPerSm / pairs : 1;
+  int64_t S = pairs > 0 ? (int64_t)sms * kPrefixWarpsPerSm / pairs : 1;
   if (prefix_blocks >= 0) S = std::min<int64_t>(S, prefix_blocks / kMinPieceBlocks);
   return (int)std::max<int64_t>(1, std::min<int64_t>(S, kMaxPieces));
 }
@@ -600,11 +600,12 @@ pkv_status pkv_cascade_decode(void* out, const void* q, pkv_dtype q_dtype, int32
   pa.pre = pre;
   pa.scratch = reinterpret_cast<float*>(ws + lay.scratch);
   pa.counters = reinterpret_cast<int*>(ws + lay.counters);
-  const int64_t ctas = (int64_t)cache->num_kv_heads * pa.row_blocks * S;
+  const int64_t ctas = (int64_t)cache->num_kv_heads * ((pa.row_blocks + kPrefixWarps - 1) / kPrefixWarps) * S;
   if (ctas > 0x7FFFFFFF) return PKV_ERR_UNSUPPORTED;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   void* args[] = {&pa, &maps};
-  if (cudaLaunchKernel(pk.fn, dim3((unsigned)ctas), dim3(32), args, pk.smem, cs) != cudaSuccess) return PKV_ERR_CUDA;
+  if (cudaLaunchKernel(pk.fn, dim3((unsigned)ctas), dim3(32 * kPrefixWarps), args, pk.smem, cs) != cudaSuccess)
+    return PKV_ERR_CUDA;
   return decode_impl(out, q, q_dtype, num_seqs, num_q_heads, k_cache, v_cache, cache, block_tables,
                      max_blocks_per_seq, seq_lens, max_seq_len, scale, kv_scale, 0, workspace, dec, stream, false,
                      false, ex);

@@ -140,7 +140,7 @@ def test_table_that_disagrees_on_the_prefix_is_flagged(pkv):
 def test_workspace_size_formula(pkv):
     # the balanced decode's workspace, then the prefix partial [B * Hq] rows of
     # d + 4 fp32 values, then one such partial per piece when there are
-    # several (pieces fill one wave of 8 one-warp CTAs per SM over (kv head,
+    # several (pieces fill one wave of 12 warps per SM over (kv head,
     # 16-row block) pairs, at most 32); each region 256-byte aligned
     B, Hq, Hkv, d, L = 256, 32, 8, 128, 2560
 
@@ -149,7 +149,7 @@ def test_workspace_size_formula(pkv):
     dec = pkv.decode_workspace_bytes(B, Hq, Hkv, d, L, 0)
     assert dec > 0
     pairs = Hkv * -(-B * (Hq // Hkv) // 16)
-    pieces = max(1, min(pkv.library().pkv_device_sm_count() * 8 // pairs, 32))
+    pieces = max(1, min(pkv.library().pkv_device_sm_count() * 12 // pairs, 32))
     row_bytes = B * Hq * (d + 4) * 4
     want = up(dec) + up(row_bytes) + (up(pieces * row_bytes) if pieces > 1 else 0)
     assert pkv.cascade_workspace_bytes(B, Hq, Hkv, d, L) == want
