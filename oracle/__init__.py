@@ -83,6 +83,9 @@ def _load():
                                                        c_int, c_int, c_int, c_int, vp, c_int, vp,
                                                        c_d, c_d, c_int]
             lib.orc_partition_attention.restype = c_int
+            lib.orc_paged_attention_multi.argtypes = [vp, vp, c_int, vp, c_int, c_int, vp, vp, c_int,
+                                                      c_int, c_int, c_int, c_int, vp, c_int, vp,
+                                                      c_d, c_d, c_int]
             lib.orc_partition_attention.argtypes = [vp, vp, vp, vp, c_int, c_int, c_int, vp, vp,
                                                     c_int, c_int, c_int, c_int, c_int, vp, c_int,
                                                     vp, c_d, c_d, c_int, c_int, c_int]
@@ -210,6 +213,32 @@ def paged_attention_decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarr
         _ptr(out), _ptr(q), dtype_code(q), B, Hq, _ptr(k_cache), _ptr(v_cache), dtype_code(k_cache),
         NB, Hkv, bs, d, _ptr(tables), tables.shape[1], _ptr(lens), float(scale), float(kv_scale),
         int(window), int(sinks), int(threads)), "paged_attention_decode")
+    return out
+
+
+def paged_attention_multi(q: np.ndarray, q_start: np.ndarray, k_cache: np.ndarray,
+                          v_cache: np.ndarray, block_tables: np.ndarray, seq_lens: np.ndarray,
+                          scale: float, kv_scale: float = 1.0, threads: int = 1) -> np.ndarray:
+    """fp64 ``[total, Hq, d]`` attention of several query tokens per sequence:
+    sequence s owns rows ``q_start[s] .. q_start[s+1]-1`` of ``q [total, Hq,
+    d]``, its last positions; query token i attends positions
+    ``0 .. seq_lens[s] - T + i`` (causal inside the chunk)."""
+    lib = _load()
+    total, Hq, d = q.shape
+    NB, Hkv, bs, d2 = k_cache.shape
+    if d != d2:
+        raise ValueError("head_dim mismatch")
+    starts = np.ascontiguousarray(q_start, dtype=np.int32)
+    tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B = lens.shape[0]
+    if starts.shape[0] != B + 1 or int(starts[-1]) != total:
+        raise ValueError("q_start must have num_seqs + 1 entries ending at the number of query rows")
+    out = np.zeros((total, Hq, d), dtype=np.float64)
+    _check(lib.orc_paged_attention_multi(
+        _ptr(out), _ptr(q), dtype_code(q), _ptr(starts), B, Hq, _ptr(k_cache), _ptr(v_cache),
+        dtype_code(k_cache), NB, Hkv, bs, d, _ptr(tables), tables.shape[1], _ptr(lens), float(scale),
+        float(kv_scale), int(threads)), "paged_attention_multi")
     return out
 
 

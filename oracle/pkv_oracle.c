@@ -35,6 +35,16 @@
  *    attention sinks, the first tokens ("PagedAttention por dentro",
  *    sections "Sliding window attention" and "StreamingLLM (Xiao et al.,
  *    2024): los attention sinks").
+ *  - orc_paged_attention_multi: the same attention for several query tokens
+ *    per sequence, a prefill chunk or the tokens a speculative step
+ *    verifies.  "PagedAttention por dentro" (section "Chunked prefill
+ *    integrado con paged KV": prefill chunks and decode tokens attend the
+ *    same paged cache in one step) and "Componentes Internos de Servicio de
+ *    vLLM" (section "Chunked prefill protege la cola del TTFT": fixed-size
+ *    chunks, 512 tokens by default).  The chunk's tokens are the sequence's
+ *    last positions, written to the cache first, and each attends the
+ *    positions up to its own (prefill attention is causal; the pages do
+ *    not spell out the mask, this is the plain reading).
  *  - orc_partition_attention / orc_split_kv_reduce: the same attention
  *    restricted to fixed token partitions, and the log-sum-exp merge of the
  *    partitions.  The pages do not describe a split; this is the plain
@@ -270,6 +280,9 @@ typedef struct {
   /* sliding window (window > 0): a sequence of length L attends only its
    * first `sinks` tokens and its last `window` tokens */
   int window, sinks;
+  /* multi-token queries (q_start != NULL): sequence s has the query tokens
+   * q_start[s] .. q_start[s+1]-1 of q [total, Hq, d]; out is [total, Hq, d] */
+  const int32_t* q_start;
   /* work distribution over (sequence, kv head) pairs */
   int next_unit;
   pthread_mutex_t lock;
@@ -344,6 +357,29 @@ static void attend_f64(const double* qv, const double* K, const double* V, const
   *l_out = l;
 }
 
+/* Multi-token queries of one (sequence, kv head): the T query tokens of the
+ * sequence are its last T positions; query token i sits at position
+ * L - T + i and attends positions 0 .. L - T + i, itself included (the causal
+ * mask inside the chunk). */
+static int run_unit_multi(orc_job* jb, int s, int h, int L, const double* K, const double* V,
+                          double* qv, double* w, unsigned char* keep) {
+  const int d = jb->head_dim;
+  const int g = jb->num_q_heads / jb->num_kv_heads;
+  const int q0 = jb->q_start[s], T = jb->q_start[s + 1] - q0;
+  if (T < 0 || T > L) return ORC_ERR_RANGE;
+  for (int p = 0; p < L; ++p) keep[p] = 1;
+  for (int i = 0; i < T; ++i) {
+    const int pos = L - T + i;
+    for (int qh = h * g; qh < (h + 1) * g; ++qh) {
+      size_t qbase = ((size_t)(q0 + i) * jb->num_q_heads + qh) * d;
+      for (int c = 0; c < d; ++c) qv[c] = (double)load_as_f32(jb->q, jb->q_dtype, qbase + c);
+      double m, l;
+      attend_f64(qv, K, V, keep, 0, pos + 1, d, jb->scale, jb->out + qbase, &m, &l, w);
+    }
+  }
+  return ORC_OK;
+}
+
 static int run_unit(orc_job* jb, int unit, double* K, double* V, double* qv, double* w,
                     unsigned char* keep) {
   const int d = jb->head_dim;
@@ -353,6 +389,7 @@ static int run_unit(orc_job* jb, int unit, double* K, double* V, double* qv, dou
   if (L < 0) return ORC_ERR_RANGE;
   int rc = gather_f64(jb, s, h, L, K, V);
   if (rc != ORC_OK) return rc;
+  if (jb->q_start) return run_unit_multi(jb, s, h, L, K, V, qv, w, keep);
   for (int p = 0; p < L; ++p) keep[p] = (unsigned char)attended(jb, L, p);
   for (int qh = h * g; qh < (h + 1) * g; ++qh) {
     size_t qbase = ((size_t)s * jb->num_q_heads + qh) * d;
@@ -560,4 +597,42 @@ int orc_split_kv_reduce(double* out, const double* o_part, const double* m_part,
     }
   }
   return ORC_OK;
+}
+
+/* Paged attention of several query tokens per sequence (chunked prefill,
+ * the verification step of speculative decoding).  Sequence s has the
+ * query tokens q_start[s] .. q_start[s+1]-1 of q [total, Hq, d]; they are
+ * the sequence's last T = q_start[s+1] - q_start[s] positions, already in
+ * the cache, and query token i attends positions 0 .. seq_lens[s] - T + i
+ * (causal inside the chunk).  out: [total, Hq, d] doubles.  T = 1 for every
+ * sequence is decode. */
+int orc_paged_attention_multi(double* out, const void* q, int q_dtype, const int32_t* q_start,
+                              int num_seqs, int num_q_heads, const void* k_cache, const void* v_cache,
+                              int cache_dtype, int num_blocks, int num_kv_heads, int block_size,
+                              int head_dim, const int32_t* block_tables, int max_blocks_per_seq,
+                              const int32_t* seq_lens, double scale, double kv_scale, int num_threads) {
+  if (!q_start || q_start[0] != 0) return ORC_ERR_ARG;
+  for (int s = 0; s < num_seqs; ++s)
+    if (q_start[s + 1] < q_start[s]) return ORC_ERR_ARG;
+  orc_job jb;
+  memset(&jb, 0, sizeof jb);
+  jb.q = q;
+  jb.q_dtype = q_dtype;
+  jb.q_start = q_start;
+  jb.k_cache = k_cache;
+  jb.v_cache = v_cache;
+  jb.cache_dtype = cache_dtype;
+  jb.num_blocks = num_blocks;
+  jb.num_kv_heads = num_kv_heads;
+  jb.block_size = block_size;
+  jb.head_dim = head_dim;
+  jb.block_tables = block_tables;
+  jb.max_blocks_per_seq = max_blocks_per_seq;
+  jb.seq_lens = seq_lens;
+  jb.num_seqs = num_seqs;
+  jb.num_q_heads = num_q_heads;
+  jb.scale = scale;
+  jb.kv_scale = kv_scale;
+  jb.out = out;
+  return run_job(&jb, num_threads);
 }

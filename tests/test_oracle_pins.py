@@ -570,3 +570,131 @@ def test_window_never_reads_blocks_outside_the_kept_tokens():
                 tables[s, j] = w.num_blocks + 7
     assert not torch.equal(tables, w.block_tables)
     assert np.array_equal(_decode(w, kc, vc, tables=tables, window=window, sinks=sinks), ref)
+
+
+# ------------------------------------------------------------------ multi-token queries
+def _multi_case(cache_dtype="f32", seed=41, lens=(1, 5, 17, 40, 70), q_lens=(1, 3, 17, 8, 33), Hq=8, Hkv=2,
+                d=64, identity=False):
+    kw = dict(identity_tables=True, num_blocks=sum(-(-L // 16) for L in lens)) if identity else {}
+    w = workloads.make_workload("mq", list(lens), Hq, Hkv, d, 16, cache_dtype, seed=seed, **kw)
+    q, q_start = workloads.chunk_queries(w, list(q_lens), seed=seed + 1)
+    kc, vc = oracle_caches(w)
+    return w, q, q_start, kc, vc
+
+
+def _multi(w, q, q_start, kc, vc, tables=None):
+    return oracle.paged_attention_multi(to_np(q), to_np(q_start), kc, vc,
+                                        to_np(w.block_tables if tables is None else tables),
+                                        to_np(w.seq_lens), w.scale, w.kv_scale, 2)
+
+
+def test_multi_with_one_query_token_is_decode():
+    """T = 1 for every sequence: the query token is the last position, which
+    is exactly decode."""
+    w, _, _, kc, vc = _multi_case()
+    q_start = torch.arange(w.num_seqs + 1, dtype=torch.int32)
+    got = _multi(w, w.q, q_start, kc, vc)
+    assert np.array_equal(got, oracle_decode(w, kc, vc))
+
+
+def test_multi_last_token_of_each_chunk_is_decode_of_its_query():
+    """The last query token of a chunk sits at position L - 1 and sees the
+    whole sequence: the decode of that query row."""
+    w, q, q_start, kc, vc = _multi_case(seed=43)
+    got = _multi(w, q, q_start, kc, vc)
+    last = q[q_start[1:].long() - 1]  # [B, Hq, d]
+    ref = oracle.paged_attention_decode(to_np(last), kc, vc, to_np(w.block_tables), to_np(w.seq_lens),
+                                        w.scale, w.kv_scale, 1)
+    assert np.array_equal(got[q_start[1:].numpy() - 1], ref)
+
+
+@pytest.mark.parametrize("cache_dtype", ["f32", "bf16", "fp8_e4m3"])
+def test_multi_contiguous_case_matches_torch_sdpa_with_bottom_right_causal_mask(cache_dtype):
+    """Identity tables make the paged cache contiguous; torch SDPA in fp64
+    with an explicit mask (query token i of T may see key j iff
+    j <= L - T + i) on the decoded cache must agree."""
+    lens, q_lens = (1, 16, 17, 75), (1, 16, 5, 30)
+    Hq, Hkv, d = 8, 2, 64
+    w, q, q_start, kc, vc = _multi_case(cache_dtype, seed=47, lens=lens, q_lens=q_lens, Hq=Hq, Hkv=Hkv, d=d,
+                                        identity=True)
+    got = _multi(w, q, q_start, kc, vc)
+    if cache_dtype == "f32":
+        Kall, Vall = kc.astype(np.float64), vc.astype(np.float64)
+    elif cache_dtype == "bf16":
+        Kall = torch.from_numpy(kc.view(np.int16)).view(torch.bfloat16).double().numpy()
+        Vall = torch.from_numpy(vc.view(np.int16)).view(torch.bfloat16).double().numpy()
+    else:
+        Kall = torch.from_numpy(kc).view(torch.float8_e4m3fn).double().numpy() * w.kv_scale
+        Vall = torch.from_numpy(vc).view(torch.float8_e4m3fn).double().numpy() * w.kv_scale
+    qd = q.double()
+    start = 0
+    for s, (L, T) in enumerate(zip(lens, q_lens)):
+        nb = -(-L // 16)
+        K = torch.from_numpy(Kall[start:start + nb].transpose(1, 0, 2, 3).reshape(Hkv, nb * 16, d)[:, :L].copy())
+        V = torch.from_numpy(Vall[start:start + nb].transpose(1, 0, 2, 3).reshape(Hkv, nb * 16, d)[:, :L].copy())
+        rows = qd[int(q_start[s]):int(q_start[s + 1])].transpose(0, 1)  # [Hq, T, d]
+        mask = torch.arange(L)[None, :] <= (L - T + torch.arange(T))[:, None]  # [T, L]
+        ref = torch.nn.functional.scaled_dot_product_attention(rows, K, V, attn_mask=mask, scale=w.scale,
+                                                               enable_gqa=True)  # [Hq, T, d]
+        np.testing.assert_allclose(got[int(q_start[s]):int(q_start[s + 1])], ref.transpose(0, 1).numpy(),
+                                   rtol=0, atol=1e-12)
+        start += nb
+
+
+def test_multi_is_causal_inside_the_chunk():
+    """Changing the cache at positions after a query token's own position
+    leaves its output unchanged; changing its own position changes it (the
+    token attends itself)."""
+    w, q, q_start, kc, vc = _multi_case(seed=53, lens=(40,), q_lens=(12,))
+    base = _multi(w, q, q_start, kc, vc)
+    L, T, bs = 40, 12, w.block_size
+    for pos in (L - T + 3, L - 1):  # a position inside the chunk
+        k2, v2 = kc.copy(), vc.copy()
+        blk = int(w.block_tables[0, pos // bs])
+        k2[blk, :, pos % bs, :] += 0.5
+        v2[blk, :, pos % bs, :] -= 0.25
+        got = _multi(w, q, q_start, k2, v2)
+        i_pos = pos - (L - T)  # the query token sitting at `pos`
+        assert np.array_equal(got[:i_pos], base[:i_pos])  # earlier tokens never see it
+        assert not np.allclose(got[i_pos], base[i_pos])   # the token at pos attends itself
+
+
+def test_multi_equal_keys_give_running_means_of_values():
+    """With every key equal the softmax is uniform: query token i of a chunk
+    of T returns the mean of V over positions 0 .. L - T + i."""
+    rng = np.random.default_rng(7)
+    L, T, Hkv, d, Hq = 37, 9, 2, 16, 4
+    K = np.repeat(rng.standard_normal((1, Hkv, d)).astype(np.float32), L, axis=0)
+    V = rng.standard_normal((L, Hkv, d)).astype(np.float32)
+    kc, vc, tables = _cache_with_tokens(K, V)
+    q = rng.standard_normal((T, Hq, d)).astype(np.float32)
+    out = oracle.paged_attention_multi(q, np.array([0, T], np.int32), kc, vc, tables,
+                                       np.array([L], np.int32), 0.3, 1.0, 1)
+    g = Hq // Hkv
+    for i in range(T):
+        mean = V[:L - T + i + 1].astype(np.float64).mean(axis=0)  # [Hkv, d]
+        for qh in range(Hq):
+            np.testing.assert_allclose(out[i, qh], mean[qh // g], rtol=0, atol=1e-12)
+
+
+def test_multi_block_permutation_invariance_and_empty_chunks():
+    """Placement of the blocks does not matter; a sequence with no query
+    token contributes no row."""
+    lens, q_lens = [5, 40, 100, 1], [2, 0, 33, 1]
+    ident = workloads.make_workload("p", lens, 8, 2, 64, 16, "bf16", seed=9, identity_tables=True, num_blocks=20)
+    shuf = workloads.make_workload("p", lens, 8, 2, 64, 16, "bf16", seed=9, num_blocks=20)
+    q, q_start = workloads.chunk_queries(ident, q_lens, seed=3)
+    a = _multi(ident, q, q_start, *oracle_caches(ident))
+    b = _multi(shuf, q, q_start, *oracle_caches(shuf))
+    assert a.shape == (sum(q_lens), 8, 64)
+    assert np.array_equal(a, b)
+
+
+def test_multi_rejects_bad_query_ranges():
+    w, q, q_start, kc, vc = _multi_case()
+    bad = q_start.clone()
+    bad[1] = bad[0] + int(w.seq_lens[0]) + 1  # more query tokens than positions
+    bad[2:] += int(bad[1]) - int(q_start[1])
+    qq = torch.zeros((int(bad[-1]), w.num_q_heads, w.head_dim), dtype=q.dtype)
+    with pytest.raises(Exception):
+        _multi(w, qq, bad, kc, vc)

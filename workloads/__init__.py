@@ -245,6 +245,27 @@ CONFIGS = {
 }
 
 
+def chunk_queries(w: Workload, q_lens: Sequence[int], seed: int = 0):
+    """Query rows for several query tokens per sequence (a prefill chunk, or
+    the tokens a speculative step verifies): sequence s gets ``q_lens[s]``
+    rows, ``1 <= q_lens[s] <= seq_lens[s]`` (0 allowed), seeded N(0, 1) in the
+    workload's query dtype.  Returns ``(q [total, Hq, d], q_start int32
+    [B + 1])``: sequence s owns rows ``q_start[s] .. q_start[s+1]-1``, its last
+    ``q_lens[s]`` positions (the cache already holds their K and V)."""
+    lens = w.seq_lens.tolist()
+    if len(q_lens) != len(lens):
+        raise ValueError("one query count per sequence")
+    for T, L in zip(q_lens, lens):
+        if T < 0 or T > L:
+            raise ValueError("0 <= q_lens[s] <= seq_lens[s]")
+    gen = torch.Generator().manual_seed(seed)
+    total = int(sum(q_lens))
+    q = _normal(gen, (total, w.num_q_heads, w.head_dim), _TORCH_SRC[w.q_dtype])
+    q_start = torch.zeros(len(lens) + 1, dtype=torch.int32)
+    q_start[1:] = torch.cumsum(torch.tensor(q_lens, dtype=torch.int64), 0).to(torch.int32)
+    return q, q_start
+
+
 def poison_bits(cache_dtype: str) -> int:
     """Byte pattern that fills a fresh cache: a NaN in every float type, so a
     reader of a never-written slot poisons its result."""
