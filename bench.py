@@ -600,6 +600,160 @@ def run_copy(args):
         print(json.dumps(line), flush=True)
 
 
+def run_multi(args):
+    """Paged attention for several query tokens per sequence
+    (pkv_paged_attention_multi) on a multi-token workload: speculative
+    verification of 4 tokens on the Llama-3-8B-shaped batch (HBM-bound:
+    GB/s), or 512-token prefill chunks (a contraction: TFLOP/s).  The step is
+    the attention call; the chunk's K/V are in the cache before timing (their
+    write is the decode step's cache-write kernel)."""
+    import paged_kv_cache_22_gb300 as pkv
+    ws, rank, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pkv.library()
+    w, q_cpu, qs_cpu = workloads.MULTI_CONFIGS[args.multi_config](seed=1301 + 1000 * rank
+                                                                  + list(workloads.MULTI_CONFIGS).index(
+                                                                      args.multi_config))
+    shape = workloads.cache_shape(w)
+    cdt = workloads.cache_torch_dtype(w.cache_dtype)
+    kc = torch.zeros(shape, dtype=cdt, device=dev)
+    vc = torch.zeros(shape, dtype=cdt, device=dev)
+    k, v, sl = w.all_tokens()
+    pkv.kv_reshape_and_cache(k.to(dev), v.to(dev), kc, vc, sl.to(dev), w.kv_scale)
+    q, q_start = q_cpu.to(dev), qs_cpu.to(dev)
+    tables, lens = w.block_tables.to(dev), w.seq_lens.to(dev)
+    q_lens = (qs_cpu[1:] - qs_cpu[:-1]).tolist()
+    max_q = max(q_lens)
+    out = torch.empty_like(q)
+    workspace = pkv.DecodeWorkspace(dev)
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream()
+
+    def call(o=out, qq=q, qs=q_start, tb=tables, ln=lens):
+        pkv.paged_attention_multi(o, qq, qs, kc, vc, tb, ln, w.scale, w.kv_scale, max_q=max_q,
+                                  max_seq_len=w.max_seq_len, workspace=workspace)
+
+    for _ in range(args.warmup):
+        flush(1)
+        call()
+    torch.cuda.synchronize()
+    if pkv.get_device_error():
+        raise RuntimeError("device error during warm-up")
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    K = args.steps
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for i in range(K):
+        flush(i)
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if pkv.get_device_error():
+        raise RuntimeError("device error during the timed steps")
+    ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in ev) / K, dev)
+    lens_l = w.seq_lens.tolist()
+    nbytes = metrics.multi_bytes(lens_l, q_lens, w.num_q_heads, w.num_kv_heads, w.head_dim, w.cache_dtype,
+                                 w.q_dtype, w.block_size)
+    flops = metrics.multi_flops(lens_l, q_lens, w.num_q_heads, w.head_dim)
+    gbs = ws * nbytes / (ms * 1e-3) / 1e9
+    tflops = ws * flops / (ms * 1e-3) / 1e12
+    compute = args.multi_config == "prefill_chunk512"
+
+    # end to end: q, offsets, tables and lengths from pinned host memory, out read back
+    host = {"q": q_cpu.pin_memory(), "qs": qs_cpu.pin_memory(), "tb": w.block_tables.pin_memory(),
+            "ln": w.seq_lens.pin_memory()}
+    dbuf = {kk: torch.empty_like(t, device=dev) for kk, t in host.items()}
+    out_host = torch.empty_like(q_cpu).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    tot, n_e2e = 0.0, max(10, min(K, 200))
+    for i in range(n_e2e + 3):
+        flush(i)
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_.record(stream)
+        for kk, t in host.items():
+            dbuf[kk].copy_(t, non_blocking=True)
+        call(out, dbuf["q"], dbuf["qs"], dbuf["tb"], dbuf["ln"])
+        out_host.copy_(out, non_blocking=True)
+        b_.record(stream)
+        b_.synchronize()
+        if i >= 3:
+            tot += a_.elapsed_time(b_)
+    e2e_ms = max_over_ranks(tot / n_e2e, dev)
+
+    hbm_peak, hbm_src = measured_peak()
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tc_peak, tc_src = float(json.load(f)["bf16_tflops"]), "measured (cuBLAS bf16 burst)"
+    except (OSError, KeyError, ValueError):
+        tc_peak, tc_src = 1900.0, "fallback"
+    unit = "TFLOP/s" if compute else "GB/s"
+    value = tflops if compute else gbs
+    e2e_value = (ws * flops / (e2e_ms * 1e-3) / 1e12) if compute else (ws * nbytes / (e2e_ms * 1e-3) / 1e9)
+    line = {
+        "metric": ("multi-token paged attention (prefill chunks) TFLOP/s" if compute else
+                   "multi-token paged attention (speculative verify) effective HBM GB/s"),
+        "value": round(value, 2 if compute else 1), "unit": unit, "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) q/k/v, shuffled block pool)",
+        "config": {"workload": args.multi_config, "num_seqs": w.num_seqs, "query_rows": int(qs_cpu[-1]),
+                   "query_tokens_per_seq": max_q, "sum_seq_len": int(sum(lens_l)),
+                   "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                   "block_size": w.block_size, "cache_dtype": w.cache_dtype,
+                   "step": "pkv_paged_attention_multi (the chunk's K/V already in the cache)",
+                   "l2": "flushed between timed steps, outside the timed events",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "bytes_per_step": nbytes, "flop_per_step": flops,
+        "gbs": round(gbs, 1), "tflops": round(tflops, 3),
+        "roofline": ({"bound": "tensor", "achieved": round(tflops, 2), "peak": tc_peak, "peak_source": tc_src,
+                      "unit": "TFLOP/s", "frac": round(tflops / tc_peak, 4), "traffic": None,
+                      "kernel": "prefix_attention_kernel (MULTI), mma.sync m16n8k16"} if compute else
+                     {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "peak_source": hbm_src,
+                      "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "traffic": None,
+                      "kernel": "prefix_attention_kernel (MULTI)"}),
+        "e2e": {"value": round(e2e_value, 2 if compute else 1), "unit": unit, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 6)},
+        "gpu_launches": K, "clocks": clocks,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_multi(w, q_cpu, qs_cpu, args.cpu_seconds, compute)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def cpu_baseline_multi(w, q_cpu, qs_cpu, seconds: float, compute: bool):
+    """The oracle's multi-token attention, as it stands, on this host's cores:
+    the first sequences of the workload (enough for ~`seconds`), repeated."""
+    import oracle
+    _, kc, vc, tables, lens, _, _, _, _ = oracle_sample(w)
+    threads = os.cpu_count() or 1
+    q_lens = (qs_cpu[1:] - qs_cpu[:-1]).tolist()
+    n = 2 if compute else 8  # sequences in the sample
+    qs = qs_cpu[:n + 1].numpy().copy()
+    qrows = q_cpu[:int(qs[-1])].contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+    nbytes = metrics.multi_bytes(lens[:n], q_lens[:n], w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                 w.cache_dtype, w.q_dtype, w.block_size)
+    flops = metrics.multi_flops(lens[:n], q_lens[:n], w.num_q_heads, w.head_dim)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.paged_attention_multi(qrows, qs, kc, vc, tables[:n], lens[:n], w.scale, w.kv_scale, threads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or reps >= 1000:
+            break
+    value = reps * flops / el / 1e12 if compute else reps * nbytes / el / 1e9
+    return {"value": round(value, 5 if compute else 3), "unit": "TFLOP/s" if compute else "GB/s",
+            "cores": threads, "kind": "oracle",
+            "sample": f"{reps} passes over the first {n} sequences of the workload, fp64 C loops, {el:.1f} s wall"}
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -619,13 +773,17 @@ def main():
     ap.add_argument("--sinks", type=int, default=0, help="attention-sink tokens kept with --window")
     ap.add_argument("--cascade", action="store_true",
                     help="decode a shared-prefix workload as prefix pass + suffix decode (prefix_fp8)")
-    ap.add_argument("--op", choices=["decode", "copy_blocks", "swap"], default="decode",
-                    help="decode step (default), or the block-copy kernels alone")
+    ap.add_argument("--op", choices=["decode", "copy_blocks", "swap", "multi"], default="decode",
+                    help="decode step (default), the block-copy kernels alone, or multi-token attention")
+    ap.add_argument("--multi-config", choices=list(workloads.MULTI_CONFIGS), default="verify4_llama3_8b",
+                    help="workload of --op multi")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.op == "multi":
+        run_multi(args)
     elif args.op != "decode":
         run_copy(args)
     else:

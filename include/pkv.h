@@ -292,6 +292,60 @@ pkv_status pkv_cascade_decode(void* out, const void* q, pkv_dtype q_dtype, int32
                               void* workspace, size_t workspace_bytes, pkv_stream_t stream);
 
 /*
+ * pkv_multi_workspace_bytes -- bytes of device workspace
+ * pkv_paged_attention_multi needs (0 for invalid sizes, a batch too large for
+ * the counter region below, or no current device): the 1 MiB counter region,
+ * then, when the K/V range is cut into pieces, one partial row of head_dim + 4
+ * fp32 values per query row, query head and piece (at most 32 pieces).
+ *   max_q   the largest number of query tokens of one sequence
+ */
+size_t pkv_multi_workspace_bytes(int32_t num_seqs, int32_t total_q, int32_t max_q, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t head_dim);
+
+/*
+ * pkv_paged_attention_multi -- paged attention for several query tokens per
+ * sequence: a chunk of a chunked prefill, or the tokens a speculative step
+ * verifies ("PagedAttention por dentro", section "Chunked prefill integrado
+ * con paged KV"; "Componentes Internos de Servicio de vLLM", section
+ * "Chunked prefill protege la cola del TTFT").  The chunk's K and V are
+ * already in the cache (pkv_kv_reshape_and_cache first, as in decode).
+ *
+ *   out[r][qh] = softmax_t(scale * q[r][qh] . K_s[t]) . V_s[t]
+ *                over t = 0 .. seq_lens[s] - T + i
+ *
+ * for the i-th of the T = q_start[s+1] - q_start[s] query rows of sequence s,
+ * r = q_start[s] + i: the chunk is the sequence's last T positions and each
+ * of its tokens attends every position up to its own (causal inside the
+ * chunk).  T = 1 for every sequence is decode.  The query heads of a kv head
+ * are grouped as in pkv_paged_attention_decode.
+ *
+ *   out, q        device [total_q, num_q_heads, head_dim], bf16 (q_dtype
+ *                 PKV_BF16), 16-byte aligned; out is written only
+ *   q_start       device int32 [num_seqs + 1], q_start[0] = 0, non-decreasing,
+ *                 q_start[num_seqs] = total_q
+ *   max_q         host upper bound of T (sizes the grid); T > max_q, T >
+ *                 seq_lens[s] or a row past total_q sets PKV_DEVERR_BAD_SEQ_LEN
+ *                 and leaves the sequence's rows unwritten
+ *   caches        bf16 or fp8-e4m3 (PKV_F32 gives PKV_ERR_UNSUPPORTED: the
+ *                 products run on the tensor cores); block tables, seq_lens,
+ *                 max_seq_len, scale and kv_scale as for
+ *                 pkv_paged_attention_decode
+ *   workspace     >= pkv_multi_workspace_bytes(...) bytes of device memory,
+ *                 256-byte aligned, its first 1 MiB zero when the call starts
+ *                 (every completed call leaves it zero; the same region as
+ *                 the decode's counters)
+ *
+ * All arguments are validated before anything is enqueued; errors as for
+ * pkv_paged_attention_decode.
+ */
+pkv_status pkv_paged_attention_multi(void* out, const void* q, pkv_dtype q_dtype, const int32_t* q_start,
+                                     int32_t num_seqs, int32_t total_q, int32_t max_q, int32_t num_q_heads,
+                                     const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
+                                     const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                     const int32_t* seq_lens, int32_t max_seq_len, float scale, float kv_scale,
+                                     void* workspace, size_t workspace_bytes, pkv_stream_t stream);
+
+/*
  * pkv_decode_step -- one decode step of one layer: pkv_kv_reshape_and_cache of
  * the step's new tokens, then pkv_paged_attention_decode, on `stream`.
  *

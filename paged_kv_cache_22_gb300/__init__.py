@@ -34,7 +34,8 @@ import torch
 
 __all__ = [
     "PkvError", "CacheDesc", "kv_reshape_and_cache", "paged_attention_decode", "decode_step",
-    "split_kv_reduce", "cascade_decode", "cascade_workspace_bytes",
+    "split_kv_reduce", "cascade_decode", "cascade_workspace_bytes", "paged_attention_multi",
+    "multi_workspace_bytes",
     "gather_kv", "copy_blocks", "decode_workspace_bytes", "get_device_error", "library", "library_path",
     "DecodeWorkspace", "F32", "BF16", "FP8_E4M3", "DEVERR_BAD_BLOCK_ID", "DEVERR_BAD_SLOT",
     "DEVERR_BAD_SEQ_LEN", "DEVERR_WAIT_TIMEOUT", "DEVERR_SMEM_ALIGN", "set_decode_engine",
@@ -94,6 +95,9 @@ def library() -> ctypes.CDLL:
             "pkv_cascade_workspace_bytes": [i32, i32, i32, i32, i32],
             "pkv_cascade_decode": [vp, vp, ctypes.c_int, i32, i32, vp, vp, desc, vp, i32, vp, i32, i32,
                                    f32, f32, vp, sz, vp],
+            "pkv_multi_workspace_bytes": [i32, i32, i32, i32, i32, i32],
+            "pkv_paged_attention_multi": [vp, vp, ctypes.c_int, vp, i32, i32, i32, i32, vp, vp, desc, vp, i32,
+                                          vp, i32, f32, f32, vp, sz, vp],
             "pkv_get_device_error": [ctypes.POINTER(ctypes.c_uint32), vp],
             "pkv_copy_blocks": [vp, vp, desc, vp, vp, desc, vp, i32, vp],
             "pkv_status_string": [ctypes.c_int],
@@ -107,6 +111,7 @@ def library() -> ctypes.CDLL:
             fn.restype = ctypes.c_int
         lib.pkv_decode_workspace_bytes.restype = sz
         lib.pkv_cascade_workspace_bytes.restype = sz
+        lib.pkv_multi_workspace_bytes.restype = sz
         lib.pkv_status_string.restype = ctypes.c_char_p
         _lib = lib
         return lib
@@ -301,6 +306,48 @@ def cascade_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_
         _ptr(out), _ptr(q), qdt, B, Hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc),
         _ptr(block_tables), mbps, _ptr(seq_lens), int(max_seq_len), int(prefix_blocks), float(scale),
         float(kv_scale), _ptr(ws), ws.numel(), _stream(stream)), "cascade_decode")
+    return out
+
+
+def multi_workspace_bytes(num_seqs: int, total_q: int, max_q: int, num_q_heads: int, num_kv_heads: int,
+                          head_dim: int) -> int:
+    return int(library().pkv_multi_workspace_bytes(num_seqs, total_q, max_q, num_q_heads, num_kv_heads,
+                                                   head_dim))
+
+
+def paged_attention_multi(out: torch.Tensor, q: torch.Tensor, q_start: torch.Tensor, k_cache: torch.Tensor,
+                          v_cache: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                          scale: float, kv_scale: float = 1.0, max_q: Optional[int] = None,
+                          max_seq_len: Optional[int] = None, workspace: Optional[DecodeWorkspace] = None,
+                          stream=None) -> torch.Tensor:
+    """Attention of several query tokens per sequence (a prefill chunk, a
+    speculative step's tokens): sequence s owns rows ``q_start[s] ..
+    q_start[s+1]-1`` of ``q [total, Hq, d]``, its last positions, each
+    attending every position up to its own.  ``max_q`` is a host bound of the
+    rows per sequence (read from ``q_start`` with a synchronisation when
+    omitted)."""
+    if q_start.dtype != torch.int32 or block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("q_start, block_tables and seq_lens must be int32")
+    total, Hq, d = q.shape
+    B = int(seq_lens.shape[0])
+    if q_start.shape[0] != B + 1:
+        raise ValueError("q_start must have num_seqs + 1 entries")
+    desc = _desc(k_cache, None)
+    mbps = int(block_tables.shape[1])
+    if max_seq_len is None:
+        max_seq_len = mbps * desc.block_size
+    if max_q is None:
+        max_q = int((q_start[1:] - q_start[:-1]).max().item()) if B else 0
+    nbytes = multi_workspace_bytes(B, total, max_q, Hq, desc.num_kv_heads, d)
+    if workspace is None:
+        dev = q.device.index if q.device.index is not None else torch.cuda.current_device()
+        workspace = _default_ws.setdefault(dev, DecodeWorkspace(q.device))
+    ws = workspace.get(nbytes)
+    qdt = F32 if q.dtype == torch.float32 else BF16
+    _check(library().pkv_paged_attention_multi(
+        _ptr(out), _ptr(q), qdt, _ptr(q_start), B, total, int(max_q), Hq, _ptr(k_cache), _ptr(v_cache),
+        ctypes.byref(desc), _ptr(block_tables), mbps, _ptr(seq_lens), int(max_seq_len), float(scale),
+        float(kv_scale), _ptr(ws), ws.numel(), _stream(stream)), "paged_attention_multi")
     return out
 
 

@@ -4,11 +4,11 @@
 namespace pkv {
 bool find_prefix_bf16(int head_dim, int block_size, PrefixKernel* out) {
   if (head_dim == 128) {
-    if (block_size == 16) { *out = prefix_kernel_info<CacheBF16, 128, 16>(); return true; }
-    if (block_size == 8) { *out = prefix_kernel_info<CacheBF16, 128, 8>(); return true; }
-    if (block_size == 32) { *out = prefix_kernel_info<CacheBF16, 128, 32>(); return true; }
+    if (block_size == 16) { *out = prefix_kernel_info<CacheBF16, 128, 16, false>(); return true; }
+    if (block_size == 8) { *out = prefix_kernel_info<CacheBF16, 128, 8, false>(); return true; }
+    if (block_size == 32) { *out = prefix_kernel_info<CacheBF16, 128, 32, false>(); return true; }
   }
-  if (head_dim == 64 && block_size == 16) { *out = prefix_kernel_info<CacheBF16, 64, 16>(); return true; }
+  if (head_dim == 64 && block_size == 16) { *out = prefix_kernel_info<CacheBF16, 64, 16, false>(); return true; }
   return false;
 }
 }  // namespace pkv

@@ -114,18 +114,25 @@ inline bool find_decode(pkv_dtype dt, int D, int BS, int G, bool balanced, bool 
 struct PrefixKernel {
   const void* fn = nullptr;  // __global__ entry, parameters (PrefixArgs, TmaMaps)
   size_t smem = 0;
+  int warps = kPrefixWarps;  // warps per CTA
 };
 
-template <class CT, int D, int BS>
+// MULTI: the same kernel for several query tokens per sequence
+// (pkv_paged_attention_multi).
+template <class CT, int D, int BS, bool MULTI, int PW = kPrefixWarps>
 PrefixKernel prefix_kernel_info() {
   PrefixKernel k;
-  k.fn = reinterpret_cast<const void*>(&prefix_attention_kernel<CT, D, BS>);
+  k.fn = reinterpret_cast<const void*>(&prefix_attention_kernel<CT, D, BS, MULTI, PW>);
   k.smem = PrefixSmem<CT, D, BS>::kBytes;
+  k.warps = PW;
   return k;
 }
 
 bool find_prefix_bf16(int head_dim, int block_size, PrefixKernel* out);
 bool find_prefix_fp8(int head_dim, int block_size, PrefixKernel* out);
+// one_warp: the one-warp-per-CTA instance (at most 16 rows per sequence and kv head)
+bool find_multi_bf16(int head_dim, int block_size, bool one_warp, PrefixKernel* out);
+bool find_multi_fp8(int head_dim, int block_size, bool one_warp, PrefixKernel* out);
 
 // The engine set by pkv_set_decode_engine (pkv_api.cu).
 bool decode_on_tensor_cores();

@@ -1,4 +1,15 @@
-// decode_prefix.cuh -- the shared-prefix half of cascade decode.
+// decode_prefix.cuh -- attention of blocks of 16 query rows over paged K/V
+// on the tensor cores, in two modes:
+//
+//  - the shared-prefix half of cascade decode (MULTI false), below;
+//  - several query tokens per sequence (MULTI true): a prefill chunk, or the
+//    tokens a speculative step verifies ("PagedAttention por dentro",
+//    section "Chunked prefill integrado con paged KV"; "Componentes Internos
+//    de Servicio de vLLM", section "Chunked prefill protege la cola del
+//    TTFT").  The rows of a warp are (query token, query head) pairs of one
+//    sequence and kv head; query token i of a chunk of T sits at position
+//    L - T + i and attends positions 0 .. L - T + i (causal inside the
+//    chunk), so each row has its own token limit, as the prefix rows do.
 //
 // When every sequence of a batch starts with the same prefix blocks (a
 // shared system prompt: "La despensa por casilleros", section "Prefix
@@ -28,7 +39,7 @@ namespace pkv {
 
 struct PrefixArgs {
   unsigned int* err;
-  const void* q;                 // [B, Hq, D]
+  const void* q;                 // [B, Hq, D]; MULTI: [total_q, Hq, D]
   const int32_t* block_tables;   // the first prefix_blocks entries of every row are the prefix
   int64_t table_stride;
   const int32_t* seq_lens;
@@ -41,11 +52,20 @@ struct PrefixArgs {
   float* pre;                    // [B * Hq] rows of pre_row_floats(D): o, m, l (the result)
   float* scratch;                // [splits, B * Hq] rows of the same: one per piece (splits > 1)
   int* counters;                 // [Hkv * row_blocks], zero between calls (splits > 1)
+  // MULTI only
+  const int32_t* q_start;        // [B + 1]: sequence s owns query rows q_start[s] .. q_start[s+1]-1
+  int total_q;                   // query rows in all
+  int max_rb;                    // 16-row blocks per (sequence, kv head) the grid covers
+  void* out;                     // [total_q, Hq, D] in the query type, normalised
+  float out_scale;               // 1 (kv_scale for fp8 caches)
 };
 
-// Warps per CTA: the PW warps of a CTA take 16 rows each of the same kv head
-// and piece, and share one ring of prefix tiles (one tensor copy per tile
-// for all of them).
+// Warps per CTA (PW): the PW warps of a CTA take 16 rows each of the same kv
+// head [and sequence] and piece, and share one ring of tiles (one tensor
+// copy per tile for all of them).  Four for the prefix pass and for
+// multi-token queries with more than 16 rows per (sequence, kv head); one
+// for at most 16 (a speculative step's few tokens), so that no warp slot
+// idles.  Either way 12 warps fit per SM (168 registers).
 constexpr int kPrefixWarps = 4;
 
 template <class CT, int D, int BS>
@@ -57,8 +77,8 @@ struct PrefixSmem {
   static constexpr size_t kBytes = kEmpty + (size_t)GE::NSW * 8;
 };
 
-template <class CT, int D, int BS>
-__global__ void __launch_bounds__(32 * kPrefixWarps, 12 / kPrefixWarps)
+template <class CT, int D, int BS, bool MULTI, int PW>
+__global__ void __launch_bounds__(32 * PW, 12 / PW)
     prefix_attention_kernel(const __grid_constant__ PrefixArgs a, const __grid_constant__ TmaMaps maps) {
   using GE = TcGeo<CT, D, BS, 1>;
   using SM = PrefixSmem<CT, D, BS>;
@@ -69,7 +89,6 @@ __global__ void __launch_bounds__(32 * kPrefixWarps, 12 / kPrefixWarps)
 
   extern __shared__ __align__(1024) uint8_t pf_smem[];
   uint8_t* const stages = pf_smem + SM::kStages;
-  constexpr int PW = kPrefixWarps;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
   if (smem_addr(stages) & 1023u) {
@@ -79,40 +98,70 @@ __global__ void __launch_bounds__(32 * kPrefixWarps, 12 / kPrefixWarps)
   const uint32_t stages_s = smem_addr(stages);
   uint64_t* bars = reinterpret_cast<uint64_t*>(pf_smem + SM::kFull);
   uint64_t* empty = reinterpret_cast<uint64_t*>(pf_smem + SM::kEmpty);
+
+  // CTA -> (piece of the K/V range, kv head [, sequence], PW blocks of 16
+  // rows); warp -> one of those blocks
+  const int piece = blockIdx.x % a.splits, cg = blockIdx.x / a.splits;
+  int h, rb, nrb;             // kv head, this warp's row block, row blocks in all
+  int ms = 0, mq0 = 0, mT = 0, mL = 0;  // MULTI: sequence, its first query row, T, its length
+  if constexpr (!MULTI) {
+    const int groups = (a.row_blocks + PW - 1) / PW;
+    h = cg / groups;
+    rb = (cg % groups) * PW + w;
+    nrb = a.row_blocks;
+  } else {
+    const int groups = (a.max_rb + PW - 1) / PW;
+    const int sh = cg / groups;
+    ms = sh / a.num_kv_heads;
+    h = sh % a.num_kv_heads;
+    rb = (cg % groups) * PW + w;
+    mq0 = __ldg(a.q_start + ms);
+    mT = __ldg(a.q_start + ms + 1) - mq0;
+    mL = __ldg(a.seq_lens + ms);
+    const bool bad = mL < 0 || mL > a.len_clip || mT < 0 || mT > mL || mq0 < 0 || mq0 + mT > a.total_q ||
+                     mT * a.group > a.max_rb * 16;
+    if (bad) {  // flagged once per sequence; its rows are left alone
+      if (threadIdx.x == 0 && h == 0 && piece == 0 && cg % groups == 0) raise_error(a.err, PKV_DEVERR_BAD_SEQ_LEN);
+      mT = 0;
+    }
+    nrb = (mT * a.group + 15) / 16;
+  }
+  // warps past the last row block have nothing to do: they leave before the
+  // ring starts, and the "empty" barriers count only the warps that stay
+  const int nact = min(PW, max(0, nrb - (rb - w)));
+  if (nact == 0) return;  // the whole CTA (uniform)
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int i = 0; i < NSW; ++i) {
       mbar_init(&bars[i], 1);
-      mbar_init(&empty[i], PW);
+      mbar_init(&empty[i], nact);
     }
     fence_mbar_init();
   }
   __syncthreads();
-
-  // CTA -> (piece of the prefix, kv head, PW blocks of 16 rows); warp -> one
-  // of those blocks (past the last one a warp has no rows but still keeps
-  // the ring's pace)
-  const int groups = (a.row_blocks + PW - 1) / PW;
-  const int piece = blockIdx.x % a.splits, cg = blockIdx.x / a.splits;
-  const int h = cg / groups, rb = (cg % groups) * PW + w;
-  const bool has_rows = rb < a.row_blocks;
-  const int hr = h * a.row_blocks + rb;
-  const int jb = piece * a.split_blocks;
-  const int je = min(a.prefix_blocks, jb + a.split_blocks);
+  if (w >= nact) return;
+  const int hr = MULTI ? (ms * a.num_kv_heads + h) * a.max_rb + rb : h * a.row_blocks + rb;
+  // the lane's two rows (g, g + 8): the query row they read (the sequence's
+  // row for the prefix; the token's row of q for MULTI), query head, tokens
+  // attended (positions below rlim), validity
+  int rrow[2], rq[2], rlim[2];
+  bool rv[2];
   const int ptok = a.prefix_blocks * BS;
-  // the lane's two rows (g, g + 8): sequence, query head, prefix tokens attended
-  int rs[2], rq[2], rlim[2];
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     const int R = rb * 16 + g + 8 * r;
-    rs[r] = R / a.group;
     rq[r] = h * a.group + R % a.group;
-    if (rs[r] < a.num_seqs) {
-      int L = __ldg(a.seq_lens + rs[r]);
+    if constexpr (!MULTI) {
+      rrow[r] = R / a.group;
+      rv[r] = rrow[r] < a.num_seqs;
+      int L = rv[r] ? __ldg(a.seq_lens + rrow[r]) : 0;
       L = L < 0 ? 0 : (L > a.len_clip ? a.len_clip : L);
       rlim[r] = L < ptok ? L : ptok;
     } else {
-      rlim[r] = 0;
+      const int i = R / a.group;  // query token of the chunk
+      rv[r] = R < mT * a.group;
+      rrow[r] = mq0 + (rv[r] ? i : 0);
+      rlim[r] = rv[r] ? mL - mT + i + 1 : 0;
     }
   }
   // tokens no row of this warp attends are zeroed in V (they may be unwritten)
@@ -120,10 +169,22 @@ __global__ void __launch_bounds__(32 * kPrefixWarps, 12 / kPrefixWarps)
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) lim_all = max(lim_all, __shfl_xor_sync(0xffffffffu, lim_all, off));
 
+  // blocks of this piece: the prefix's, or (MULTI) the sequence's up to the
+  // last position any row of the CTA attends; the table row they are read from
+  const int32_t* table = a.block_tables;
+  int nb_all = a.prefix_blocks;
+  if constexpr (MULTI) {
+    table = a.block_tables + (size_t)ms * a.table_stride;
+    const int last_row = min(mT * a.group, (rb - w + nact) * 16) - 1;  // the CTA's last row
+    nb_all = (mL - mT + last_row / a.group + 1 + BS - 1) / BS;
+  }
+  const int jb = piece * a.split_blocks;
+  const int je = min(nb_all, jb + a.split_blocks);
+
   // the prefix blocks a sequence attends must be those of sequence 0's table
   // (checked once, by kv head 0; entries past a short sequence's end are not
   // read by plain decode either, so they are not compared)
-  if (h == 0 && piece == 0) {
+  if (!MULTI && h == 0 && piece == 0) {
     const int s_lo = rb * 16 / a.group, s_hi = min(a.num_seqs, (rb * 16 + 15) / a.group + 1);
     for (int s = s_lo; s < s_hi; ++s) {
       int L = __ldg(a.seq_lens + s);
@@ -142,13 +203,13 @@ __global__ void __launch_bounds__(32 * kPrefixWarps, 12 / kPrefixWarps)
     const QT* qrow[2];
 #pragma unroll
     for (int r = 0; r < 2; ++r)
-      qrow[r] = reinterpret_cast<const QT*>(a.q) + ((size_t)(rs[r] < a.num_seqs ? rs[r] : 0) * a.num_q_heads + rq[r]) * D;
+      qrow[r] = reinterpret_cast<const QT*>(a.q) + ((size_t)(rv[r] ? rrow[r] : 0) * a.num_q_heads + rq[r]) * D;
     if constexpr (!F8) {
 #pragma unroll
       for (int kk = 0; kk < KS; ++kk)
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-          const bool live = rs[r] < a.num_seqs;
+          const bool live = rv[r];
           qa[kk][r] = live ? *reinterpret_cast<const uint32_t*>(qrow[r] + 16 * kk + 2 * t) : 0u;
           qa[kk][2 + r] = live ? *reinterpret_cast<const uint32_t*>(qrow[r] + 16 * kk + 2 * t + 8) : 0u;
         }
@@ -161,7 +222,7 @@ __global__ void __launch_bounds__(32 * kPrefixWarps, 12 / kPrefixWarps)
       for (int kk = 0; kk < KS; ++kk)
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-          const bool live = rs[r] < a.num_seqs;
+          const bool live = rv[r];
           const uint2 raw = live ? *reinterpret_cast<const uint2*>(qrow[r] + 16 * kk + 4 * t) : make_uint2(0u, 0u);
           const float2 lo = bf16x2_to_f2(raw.x), hi = bf16x2_to_f2(raw.y);
           qv[kk][r][0] = lo.x;
@@ -195,7 +256,7 @@ __global__ void __launch_bounds__(32 * kPrefixWarps, 12 / kPrefixWarps)
     if (jb + issued >= je) return;
     const int st = issued % NSW;
     if (w == 0 && lane == 0) {
-      const int32_t id = __ldg(a.block_tables + jb + issued);
+      const int32_t id = __ldg(table + jb + issued);
       uint8_t* dst = stages + (size_t)st * STAGE;
       if (id >= 0 && id < a.num_blocks) {
         mbar_arrive_expect_tx(&bars[st], STAGE);
@@ -259,7 +320,7 @@ __global__ void __launch_bounds__(32 * kPrefixWarps, 12 / kPrefixWarps)
       if (!mbar_wait_bounded(&bars[st], (i / NSW) & 1, a.err)) alive = false;
       waited = i + 1;
     }
-    const int32_t id = __ldg(a.block_tables + j);
+    const int32_t id = __ldg(table + j);
     const bool ok = alive && id >= 0 && id < a.num_blocks;
 #pragma unroll
     for (int step = 0; step < GE::STEPS; ++step) {
@@ -451,27 +512,46 @@ __global__ void __launch_bounds__(32 * kPrefixWarps, 12 / kPrefixWarps)
   }
 
   // ---------------------------------------------------------------- partials
+  // One piece: the result (the prefix partial, or MULTI's normalised
+  // output).  Several: this piece's partial, merged below.
   constexpr int PRF = pre_row_floats(D);
-  const size_t rows = (size_t)a.num_seqs * a.num_q_heads;
+  const size_t rows = MULTI ? (size_t)a.total_q * a.num_q_heads : (size_t)a.num_seqs * a.num_q_heads;
   float* base = a.splits == 1 ? a.pre : a.scratch + (size_t)piece * rows * PRF;
   auto odim = [&](int n, int e) -> int { return F8 ? GE::VPL * (2 * t + e) + n : 8 * n + 2 * t + e; };
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     float l_row = l_run[r] + __shfl_xor_sync(0xffffffffu, l_run[r], 1);
     l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
-    if (rs[r] < a.num_seqs) {
-      float* dst = base + ((size_t)rs[r] * a.num_q_heads + rq[r]) * PRF;
+    if (!rv[r]) continue;
+    const size_t orow = (size_t)rrow[r] * a.num_q_heads + rq[r];
+    if (MULTI && a.splits == 1) {
+      QT* dst = reinterpret_cast<QT*>(a.out) + orow * D;
+      const float inv = l_row > 0.f ? a.out_scale / l_row : 0.f;
+      if constexpr (F8) {  // dims n, n + 1 of column 2t + e are adjacent
 #pragma unroll
-      for (int n = 0; n < NTO; ++n)
+        for (int e = 0; e < 2; ++e)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) dst[odim(n, e)] = o[n][2 * r + e];
-      if (t == 0) {
-        dst[D] = m_run[r];
-        dst[D + 1] = l_row;
+          for (int n = 0; n < NTO; n += 2)
+            *reinterpret_cast<uint32_t*>(dst + odim(n, e)) =
+                pack_bf16x2(o[n][2 * r + e] * inv, o[n + 1][2 * r + e] * inv);
+      } else {
+#pragma unroll
+        for (int n = 0; n < NTO; ++n)
+          *reinterpret_cast<uint32_t*>(dst + odim(n, 0)) = pack_bf16x2(o[n][2 * r] * inv, o[n][2 * r + 1] * inv);
       }
+      continue;
+    }
+    float* dst = base + orow * PRF;
+#pragma unroll
+    for (int n = 0; n < NTO; ++n)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) dst[odim(n, e)] = o[n][2 * r + e];
+    if (t == 0) {
+      dst[D] = m_run[r];
+      dst[D + 1] = l_row;
     }
   }
-  if (a.splits > 1 && has_rows) {
+  if (a.splits > 1) {
     // the last piece of this (kv head, row block) to finish merges them all
     __threadfence();
     __syncwarp();
@@ -491,9 +571,15 @@ __global__ void __launch_bounds__(32 * kPrefixWarps, 12 / kPrefixWarps)
         float mk[4], lk[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int R = rb * 16 + r0 + u, s = R / a.group;
-          live[u] = s < a.num_seqs;
-          row[u] = live[u] ? (size_t)s * a.num_q_heads + h * a.group + R % a.group : 0;
+          const int R = rb * 16 + r0 + u;
+          if constexpr (!MULTI) {
+            const int s = R / a.group;
+            live[u] = s < a.num_seqs;
+            row[u] = live[u] ? (size_t)s * a.num_q_heads + h * a.group + R % a.group : 0;
+          } else {
+            live[u] = R < mT * a.group;
+            row[u] = live[u] ? (size_t)(mq0 + R / a.group) * a.num_q_heads + h * a.group + R % a.group : 0;
+          }
           mk[u] = -CUDART_INF_F;
           lk[u] = 0.f;
           if (live[u] && lane < a.splits) {
@@ -535,11 +621,19 @@ __global__ void __launch_bounds__(32 * kPrefixWarps, 12 / kPrefixWarps)
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           if (!live[u]) continue;
-          float* dst = a.pre + row[u] * PRF;
-          if (4 * lane < D) reinterpret_cast<float4*>(dst)[lane] = acc[u];
-          if (lane == 0) {
-            dst[D] = M[u];
-            dst[D + 1] = den[u];
+          if constexpr (MULTI) {  // the normalised output row
+            const float inv = den[u] > 0.f ? a.out_scale / den[u] : 0.f;
+            QT* dst = reinterpret_cast<QT*>(a.out) + row[u] * D;
+            if (4 * lane < D)
+              *reinterpret_cast<uint2*>(dst + 4 * lane) =
+                  make_uint2(pack_bf16x2(acc[u].x * inv, acc[u].y * inv), pack_bf16x2(acc[u].z * inv, acc[u].w * inv));
+          } else {
+            float* dst = a.pre + row[u] * PRF;
+            if (4 * lane < D) reinterpret_cast<float4*>(dst)[lane] = acc[u];
+            if (lane == 0) {
+              dst[D] = M[u];
+              dst[D + 1] = den[u];
+            }
           }
         }
       }

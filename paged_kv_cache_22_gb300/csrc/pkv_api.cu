@@ -522,6 +522,47 @@ bool cascade_layout(int num_seqs, int num_q_heads, int num_kv_heads, int D, int 
   return true;
 }
 
+// Multi-token queries: pieces of the K/V range.  Sequence lengths differ and
+// the host knows only the longest, so a piece is short enough that the
+// (sequence, kv head, 16-row block, piece) work items number about twice
+// the resident warps (kPrefixWarpsPerSm per SM): the pieces of short
+// sequences past their end are empty and end at once.  nb_max < 0 gives the
+// bound the workspace is sized by.
+int multi_pieces(int sms, int num_seqs, int num_kv_heads, int max_rb, int nb_max) {
+  const int64_t units = (int64_t)num_seqs * num_kv_heads * max_rb;
+  if (units <= 0) return 1;
+  const int64_t slots = (int64_t)sms * kPrefixWarpsPerSm * 2;
+  int64_t S = (slots + units - 1) / units;
+  if (nb_max >= 0) S = std::min<int64_t>(S, nb_max / kMinPieceBlocks);
+  return (int)std::max<int64_t>(1, std::min<int64_t>(S, kMaxPieces));
+}
+
+// Workspace of pkv_paged_attention_multi: merge counters (one per sequence,
+// kv head and 16-row block) at the bottom of the zeroed 1 MiB counter region,
+// then one partial row per (query row, query head) and piece when the K/V
+// range is cut.
+struct MultiLayout {
+  size_t scratch, total;
+  int max_rb, pieces;
+};
+
+bool multi_layout(int num_seqs, int total_q, int max_q, int num_q_heads, int num_kv_heads, int D, MultiLayout* L) {
+  if (num_seqs < 0 || total_q < 0 || max_q < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      num_q_heads % num_kv_heads || (D != 64 && D != 128))
+    return false;
+  const int dev = current_device();
+  const int sms = dev < 0 ? 0 : sm_count(dev);
+  if (sms <= 0) return false;
+  const int group = num_q_heads / num_kv_heads;
+  L->max_rb = (int)(((int64_t)max_q * group + 15) / 16);
+  if ((int64_t)num_seqs * num_kv_heads * L->max_rb * sizeof(int) > kCounterRegionMin) return false;
+  L->pieces = multi_pieces(sms, num_seqs, num_kv_heads, L->max_rb, -1);
+  const size_t row_bytes = (size_t)total_q * num_q_heads * pre_row_floats(D) * sizeof(float);
+  L->scratch = kCounterRegionMin;
+  L->total = L->scratch + (L->pieces > 1 ? align_up(L->pieces * row_bytes) : 0);
+  return true;
+}
+
 }  // namespace pkv
 
 extern "C" {
@@ -609,6 +650,87 @@ pkv_status pkv_cascade_decode(void* out, const void* q, pkv_dtype q_dtype, int32
   return decode_impl(out, q, q_dtype, num_seqs, num_q_heads, k_cache, v_cache, cache, block_tables,
                      max_blocks_per_seq, seq_lens, max_seq_len, scale, kv_scale, 0, workspace, dec, stream, false,
                      false, ex);
+}
+
+size_t pkv_multi_workspace_bytes(int32_t num_seqs, int32_t total_q, int32_t max_q, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t head_dim) {
+  MultiLayout L;
+  return multi_layout(num_seqs, total_q, max_q, num_q_heads, num_kv_heads, head_dim, &L) ? L.total : 0;
+}
+
+pkv_status pkv_paged_attention_multi(void* out, const void* q, pkv_dtype q_dtype, const int32_t* q_start,
+                                     int32_t num_seqs, int32_t total_q, int32_t max_q, int32_t num_q_heads,
+                                     const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
+                                     const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                     const int32_t* seq_lens, int32_t max_seq_len, float scale, float kv_scale,
+                                     void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+  if (num_seqs < 0 || total_q < 0 || max_q < 0 || !valid_cache_desc(cache)) return PKV_ERR_INVALID_ARG;
+  if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return PKV_ERR_INVALID_ARG;
+  if (max_blocks_per_seq <= 0 || max_seq_len < 0 || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (cache->dtype == PKV_FP8_E4M3 && !(kv_scale > 0.f && std::isfinite(kv_scale))) return PKV_ERR_INVALID_ARG;
+  if (cache->dtype == PKV_F32 || q_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;  // tensor cores: bf16 / fp8
+  if (num_seqs == 0 || total_q == 0) return PKV_OK;
+  if (max_q == 0) return PKV_ERR_INVALID_ARG;
+  if (!out || !q || !q_start || !k_cache || !v_cache || !block_tables || !seq_lens) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_INVALID_ARG;
+  const int D = cache->head_dim, BS = cache->block_size;
+  MultiLayout lay;
+  if (!multi_layout(num_seqs, total_q, max_q, num_q_heads, cache->num_kv_heads, D, &lay)) return PKV_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < lay.total) return PKV_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return PKV_ERR_INVALID_ARG;
+  PrefixKernel pk;
+  const bool one_warp = lay.max_rb == 1;
+  const bool found = cache->dtype == PKV_BF16 ? find_multi_bf16(D, BS, one_warp, &pk)
+                                              : find_multi_fp8(D, BS, one_warp, &pk);
+  if (!found) return PKV_ERR_UNSUPPORTED;
+  const int dev = current_device();
+  const int sms = dev < 0 ? 0 : sm_count(dev);
+  unsigned int* err = dev < 0 ? nullptr : error_word(dev);
+  if (!err || sms <= 0) return PKV_ERR_CUDA;
+  const int64_t table_tokens = (int64_t)max_blocks_per_seq * BS;
+  const int len_clip = (int)(table_tokens < max_seq_len ? table_tokens : max_seq_len);
+  const int nb_max = (len_clip + BS - 1) / BS;
+  int S = multi_pieces(sms, num_seqs, cache->num_kv_heads, lay.max_rb, nb_max);
+  const int SB = nb_max > 0 ? (nb_max + S - 1) / S : 1;
+  S = nb_max > 0 ? (nb_max + SB - 1) / SB : 1;  // no empty piece
+  const int groups = (lay.max_rb + pk.warps - 1) / pk.warps;
+  const int64_t ctas = (int64_t)num_seqs * cache->num_kv_heads * groups * S;
+  if (ctas > 0x7FFFFFFF) return PKV_ERR_UNSUPPORTED;
+  if (cudaFuncSetAttribute(pk.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pk.smem) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  DecodeKernel tk;
+  tk.tensor_maps = true;
+  TmaMaps maps{};
+  if (!encode_cache_maps(tk, cache, k_cache, v_cache, &maps)) return PKV_ERR_CUDA;
+  char* ws = static_cast<char*>(workspace);
+  PrefixArgs pa{};
+  pa.err = err;
+  pa.q = q;
+  pa.block_tables = block_tables;
+  pa.table_stride = max_blocks_per_seq;
+  pa.seq_lens = seq_lens;
+  pa.num_seqs = num_seqs;
+  pa.num_q_heads = num_q_heads;
+  pa.num_kv_heads = cache->num_kv_heads;
+  pa.group = num_q_heads / cache->num_kv_heads;
+  pa.num_blocks = cache->num_blocks;
+  pa.len_clip = len_clip;
+  pa.splits = S;
+  pa.split_blocks = SB;
+  const bool fp8 = cache->dtype == PKV_FP8_E4M3;
+  pa.qk_scale = scale * 1.4426950408889634f * (fp8 ? kv_scale : 1.f);
+  pa.scratch = reinterpret_cast<float*>(ws + lay.scratch);
+  pa.counters = reinterpret_cast<int*>(ws);
+  pa.q_start = q_start;
+  pa.total_q = total_q;
+  pa.max_rb = lay.max_rb;
+  pa.out = out;
+  pa.out_scale = fp8 ? kv_scale : 1.f;
+  void* args[] = {&pa, &maps};
+  if (cudaLaunchKernel(pk.fn, dim3((unsigned)ctas), dim3(32 * pk.warps), args, pk.smem,
+                       reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  return PKV_OK;
 }
 
 pkv_status pkv_decode_step(const void* k, const void* v, pkv_dtype src_dtype, int32_t num_new_tokens,

@@ -105,3 +105,31 @@ def cascade_bytes(seq_lens: Iterable[int], prefix_tokens: int, num_q_heads: int,
     tables = 4 * (blocks_for_tokens(pre, block_size)
                   + sum(max(blocks_for_tokens(L, block_size) - pb, 0) for L in lens))
     return kv + qo + tables + 4 * len(lens)
+
+
+def multi_bytes(seq_lens: Iterable[int], q_lens: Iterable[int], num_q_heads: int, num_kv_heads: int,
+                head_dim: int, cache_dtype: str, q_dtype: str, block_size: int) -> int:
+    """Algorithmic bytes of one multi-token attention call: each sequence's K
+    and V up to its last position once per kv head (the chunk's last token
+    attends all of them), q and out of every query row, the table entries
+    read, seq_lens and the query offsets."""
+    lens = [int(x) for x in seq_lens]
+    rows = sum(int(t) for t in q_lens)
+    e_c, e_q = ELEM_BYTES[cache_dtype], ELEM_BYTES[q_dtype]
+    kv = sum(lens) * kv_bytes_per_token(1, num_kv_heads, head_dim, e_c)
+    qo = 2 * rows * num_q_heads * head_dim * e_q
+    tables = 4 * sum(blocks_for_tokens(L, block_size) for L in lens)
+    return kv + qo + tables + 4 * len(lens) + 4 * (len(lens) + 1)
+
+
+def multi_flops(seq_lens: Iterable[int], q_lens: Iterable[int], num_q_heads: int, head_dim: int) -> int:
+    """Multiply-add work of one multi-token attention call, 2 FLOP each: q.K
+    and P.V over the positions every query row attends (query token i of a
+    chunk of T attends L - T + i + 1 positions): 4 * d FLOP per (row, head,
+    position)."""
+    total = 0
+    for L, T in zip(seq_lens, q_lens):
+        L, T = int(L), int(T)
+        attended = T * (L - T) + T * (T + 1) // 2  # sum over i of (L - T + i + 1)
+        total += attended
+    return 4 * head_dim * num_q_heads * total

@@ -131,3 +131,28 @@ def test_cascade_rejects_bad_prefix_before_launch(lib):
     st = lib.pkv_cascade_decode(p, p, 0, 2, 8, p, p, ctypes.byref(desc), p, 4, p, 64, 2, 0.125, 1.0,
                                 p, 1 << 24, None)
     assert st == UNSUPPORTED
+
+
+def test_multi_rejects_bad_arguments_before_launch(lib):
+    from paged_kv_cache_22_gb300 import CacheDesc
+    INVALID, UNSUPPORTED = 1, 2
+    p = ctypes.c_void_p(256)
+    desc = CacheDesc(num_blocks=8, block_size=16, num_kv_heads=2, head_dim=64, dtype=1)
+    # negative sizes
+    assert lib.pkv_paged_attention_multi(p, p, 1, p, -1, 4, 2, 8, p, p, ctypes.byref(desc), p, 4, p, 64,
+                                         0.125, 1.0, p, 1 << 24, None) == INVALID
+    assert lib.pkv_paged_attention_multi(p, p, 1, p, 2, 4, -1, 8, p, p, ctypes.byref(desc), p, 4, p, 64,
+                                         0.125, 1.0, p, 1 << 24, None) == INVALID
+    # rows but no bound on rows per sequence
+    assert lib.pkv_paged_attention_multi(p, p, 1, p, 2, 4, 0, 8, p, p, ctypes.byref(desc), p, 4, p, 64,
+                                         0.125, 1.0, p, 1 << 24, None) == INVALID
+    # no query rows: nothing to do
+    assert lib.pkv_paged_attention_multi(p, p, 1, p, 2, 0, 0, 8, p, p, ctypes.byref(desc), p, 4, p, 64,
+                                         0.125, 1.0, p, 1 << 24, None) == 0
+    # fp32 caches / fp32 q: the products run on the tensor cores
+    desc.dtype = 0
+    assert lib.pkv_paged_attention_multi(p, p, 0, p, 2, 4, 2, 8, p, p, ctypes.byref(desc), p, 4, p, 64,
+                                         0.125, 1.0, p, 1 << 24, None) == UNSUPPORTED
+    desc.dtype = 1
+    assert lib.pkv_paged_attention_multi(p, p, 0, p, 2, 4, 2, 8, p, p, ctypes.byref(desc), p, 4, p, 64,
+                                         0.125, 1.0, p, 1 << 24, None) == UNSUPPORTED

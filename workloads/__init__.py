@@ -266,6 +266,33 @@ def chunk_queries(w: Workload, q_lens: Sequence[int], seed: int = 0):
     return q, q_start
 
 
+# ------------------------------------------------------------------ multi-token configs
+def verify4_llama3_8b(seed: int = 1301):
+    """Speculative verification on the Llama-3-8B-shaped batch: 64
+    sequences, L ~ U[128, 2048], the last 4 positions of each are query
+    tokens (3 drafted + 1)."""
+    w = llama3_8b(seed=seed)
+    q, q_start = chunk_queries(w, [4] * w.num_seqs, seed=seed + 1)
+    return w, q, q_start
+
+
+def prefill_chunk512(seed: int = 1302, num_seqs: int = 8):
+    """Chunked prefill at the default chunk size: 8 sequences of Llama-3-8B
+    heads whose next 512-token chunk lands at L ~ U[1024, 4096] (the chunk is
+    the last 512 positions, already in the cache)."""
+    gen = torch.Generator().manual_seed(seed)
+    lens = torch.randint(1024, 4097, (num_seqs,), generator=gen).tolist()
+    w = make_workload("prefill_chunk512", lens, 32, 8, 128, 16, "bf16", seed=seed)
+    q, q_start = chunk_queries(w, [512] * num_seqs, seed=seed + 1)
+    return w, q, q_start
+
+
+MULTI_CONFIGS = {
+    "verify4_llama3_8b": verify4_llama3_8b,
+    "prefill_chunk512": prefill_chunk512,
+}
+
+
 def poison_bits(cache_dtype: str) -> int:
     """Byte pattern that fills a fresh cache: a NaN in every float type, so a
     reader of a never-written slot poisons its result."""
