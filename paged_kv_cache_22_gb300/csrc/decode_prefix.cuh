@@ -178,8 +178,12 @@ __global__ void __launch_bounds__(32 * PW, 12 / PW)
     const int last_row = min(mT * a.group, (rb - w + nact) * 16) - 1;  // the CTA's last row
     nb_all = (mL - mT + last_row / a.group + 1 + BS - 1) / BS;
   }
-  const int jb = piece * a.split_blocks;
-  const int je = min(nb_all, jb + a.split_blocks);
+  // MULTI: each sequence's own range is cut into `splits` equal pieces
+  // (lengths differ, so pieces sized by the longest would leave the short
+  // sequences' pieces empty and the long ones' long)
+  const int sb = MULTI ? (nb_all + a.splits - 1) / a.splits : a.split_blocks;
+  const int jb = piece * sb;
+  const int je = min(nb_all, jb + sb);
 
   // the prefix blocks a sequence attends must be those of sequence 0's table
   // (checked once, by kv head 0; entries past a short sequence's end are not

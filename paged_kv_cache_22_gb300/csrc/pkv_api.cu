@@ -484,7 +484,7 @@ namespace pkv {
 // Pieces the cascade's prefix pass cuts the prefix into: enough warps (kv
 // heads x blocks of 16 query rows x pieces) for one resident wave of
 // kPrefixWarpsPerSm per SM, each piece at least kMinPieceBlocks blocks long.
-constexpr int kPrefixWarpsPerSm = 12, kMinPieceBlocks = 4, kMaxPieces = 32;
+constexpr int kPrefixWarpsPerSm = 12, kMinPieceBlocks = 4, kMaxPieces = 32, kMultiItemsPerSlot = 2;
 
 int prefix_pieces(int sms, int num_seqs, int group, int num_kv_heads, int prefix_blocks) {
   const int64_t pairs = (int64_t)num_kv_heads * (((int64_t)num_seqs * group + 15) / 16);
@@ -522,16 +522,16 @@ bool cascade_layout(int num_seqs, int num_q_heads, int num_kv_heads, int D, int 
   return true;
 }
 
-// Multi-token queries: pieces of the K/V range.  Sequence lengths differ and
-// the host knows only the longest, so a piece is short enough that the
-// (sequence, kv head, 16-row block, piece) work items number about twice
-// the resident warps (kPrefixWarpsPerSm per SM): the pieces of short
-// sequences past their end are empty and end at once.  nb_max < 0 gives the
-// bound the workspace is sized by.
+// Multi-token queries: pieces of the K/V range.  Each sequence's own range
+// is cut into S equal pieces (in the kernel), S chosen so that the
+// (sequence, kv head, 16-row block, piece) work items number about
+// kMultiItemsPerSlot times the resident warps (kPrefixWarpsPerSm per SM):
+// 2 measured faster than 1 (a ragged last wave) and 4 (more pieces to
+// merge).  nb_max < 0 gives the bound the workspace is sized by.
 int multi_pieces(int sms, int num_seqs, int num_kv_heads, int max_rb, int nb_max) {
   const int64_t units = (int64_t)num_seqs * num_kv_heads * max_rb;
   if (units <= 0) return 1;
-  const int64_t slots = (int64_t)sms * kPrefixWarpsPerSm * 2;
+  const int64_t slots = (int64_t)sms * kPrefixWarpsPerSm * kMultiItemsPerSlot;
   int64_t S = (slots + units - 1) / units;
   if (nb_max >= 0) S = std::min<int64_t>(S, nb_max / kMinPieceBlocks);
   return (int)std::max<int64_t>(1, std::min<int64_t>(S, kMaxPieces));
