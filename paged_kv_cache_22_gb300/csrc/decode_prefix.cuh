@@ -74,7 +74,8 @@ struct PrefixSmem {
   static constexpr size_t kStages = 0;  // 1024-byte aligned
   static constexpr size_t kFull = (size_t)GE::NSW * GE::STAGE;  // tile landed
   static constexpr size_t kEmpty = kFull + (size_t)GE::NSW * 8;  // every warp done with it
-  static constexpr size_t kBytes = kEmpty + (size_t)GE::NSW * 8;
+  static constexpr size_t kOk = kEmpty + (size_t)GE::NSW * 8;     // the stage's block id was valid
+  static constexpr size_t kBytes = kOk + (size_t)GE::NSW * 4;
 };
 
 template <class CT, int D, int BS, bool MULTI, int PW>
@@ -98,6 +99,7 @@ __global__ void __launch_bounds__(32 * PW, 12 / PW)
   const uint32_t stages_s = smem_addr(stages);
   uint64_t* bars = reinterpret_cast<uint64_t*>(pf_smem + SM::kFull);
   uint64_t* empty = reinterpret_cast<uint64_t*>(pf_smem + SM::kEmpty);
+  int* stage_ok = reinterpret_cast<int*>(pf_smem + SM::kOk);
 
   // CTA -> (piece of the K/V range, kv head [, sequence], PW blocks of 16
   // rows); warp -> one of those blocks
@@ -256,22 +258,38 @@ __global__ void __launch_bounds__(32 * PW, 12 / PW)
   // ---------------------------------------------------------------- issue side
   // Producer: lane 0 of warp 0 starts every tile copy of the CTA.
   int issued = 0;  // blocks of this piece whose copy was started
+  // The producer warp reads the piece's block ids 32 at a time (one
+  // coalesced load) and hands each to lane 0 by shuffle; whether a stage's
+  // id was valid goes to shared memory with the stage, so that no warp waits
+  // on a global load per block.
+  int id_chunk = -1;
+  int32_t id_reg = 0;
   auto issue_next = [&]() {
     if (jb + issued >= je) return;
     const int st = issued % NSW;
-    if (w == 0 && lane == 0) {
-      const int32_t id = __ldg(table + jb + issued);
+    if (w == 0) {
+      if ((issued >> 5) != id_chunk) {
+        id_chunk = issued >> 5;
+        const int jj = jb + (id_chunk << 5) + lane;
+        id_reg = jj < je ? __ldg(table + jj) : -1;
+      }
+      const int32_t id = __shfl_sync(0xffffffffu, id_reg, issued & 31);
       uint8_t* dst = stages + (size_t)st * STAGE;
-      if (id >= 0 && id < a.num_blocks) {
-        mbar_arrive_expect_tx(&bars[st], STAGE);
+      const bool valid = id >= 0 && id < a.num_blocks;
+      if (lane == 0) {
+        if (valid) {
+          stage_ok[st] = 1;
+          mbar_arrive_expect_tx(&bars[st], STAGE);
 #pragma unroll
-        for (int bx = 0; bx < GE::NBX; ++bx) {
-          tma_load_3d(dst + bx * GE::BOX, &maps.k, bx * (GE::IB / GE::E), h * BS, id, &bars[st]);
-          tma_load_3d(dst + TILE + bx * GE::BOX, &maps.v, bx * (GE::IB / GE::E), h * BS, id, &bars[st]);
+          for (int bx = 0; bx < GE::NBX; ++bx) {
+            tma_load_3d(dst + bx * GE::BOX, &maps.k, bx * (GE::IB / GE::E), h * BS, id, &bars[st]);
+            tma_load_3d(dst + TILE + bx * GE::BOX, &maps.v, bx * (GE::IB / GE::E), h * BS, id, &bars[st]);
+          }
+        } else {
+          raise_error(a.err, PKV_DEVERR_BAD_BLOCK_ID);
+          stage_ok[st] = 0;
+          mbar_arrive(&bars[st]);
         }
-      } else {
-        raise_error(a.err, PKV_DEVERR_BAD_BLOCK_ID);
-        mbar_arrive(&bars[st]);
       }
     }
     ++issued;
@@ -324,8 +342,7 @@ __global__ void __launch_bounds__(32 * PW, 12 / PW)
       if (!mbar_wait_bounded(&bars[st], (i / NSW) & 1, a.err)) alive = false;
       waited = i + 1;
     }
-    const int32_t id = __ldg(table + j);
-    const bool ok = alive && id >= 0 && id < a.num_blocks;
+    const bool ok = alive && stage_ok[st] != 0;
 #pragma unroll
     for (int step = 0; step < GE::STEPS; ++step) {
       const uint32_t kt = stages_s + (uint32_t)(st * STAGE + step * TB * GE::IB);
