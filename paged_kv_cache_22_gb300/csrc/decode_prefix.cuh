@@ -280,11 +280,8 @@ __global__ void __launch_bounds__(32 * PW, 12 / PW)
         if (valid) {
           stage_ok[st] = 1;
           mbar_arrive_expect_tx(&bars[st], STAGE);
-#pragma unroll
-          for (int bx = 0; bx < GE::NBX; ++bx) {
-            tma_load_3d(dst + bx * GE::BOX, &maps.k, bx * (GE::IB / GE::E), h * BS, id, &bars[st]);
-            tma_load_3d(dst + TILE + bx * GE::BOX, &maps.v, bx * (GE::IB / GE::E), h * BS, id, &bars[st]);
-          }
+          tma_load_tile<GE>(dst, &maps.k, h * BS, id, &bars[st]);
+          tma_load_tile<GE>(dst + TILE, &maps.v, h * BS, id, &bars[st]);
         } else {
           raise_error(a.err, PKV_DEVERR_BAD_BLOCK_ID);
           stage_ok[st] = 0;

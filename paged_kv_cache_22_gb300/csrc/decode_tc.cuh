@@ -60,6 +60,14 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const TmaMap* map, int x,
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(void* dst, const TmaMap* map, int x, int y, int z, int w, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_addr(bar))
+      : "memory");
+}
+
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -186,6 +194,18 @@ struct TcSmem {
   static constexpr size_t kBytes = kPBar + (size_t)W * 8;
 };
 
+// One (block, kv head) tile of a cache into `dst`: row-wide boxes with one
+// copy each (3-D map), or, for rows wider than the swizzle span, every span
+// of the tile in one copy (4-D map); the layout is the same, span by span.
+template <class GE>
+__device__ __forceinline__ void tma_load_tile(void* dst, const TmaMap* map, int row0, int block, uint64_t* bar) {
+  if constexpr (GE::NBX == 1) {
+    tma_load_3d(dst, map, 0, row0, block, bar);
+  } else {
+    tma_load_4d(dst, map, 0, row0, 0, block, bar);
+  }
+}
+
 // Byte offset, within a tile, of 16-byte chunk c of token row `row` as the
 // swizzled tensor copy lays it out: chunk index XOR the 128-byte line index
 // (bits 4..6 ^= bits 7..9; for 64-byte spans bits 4..5 ^= bits 7..8).
@@ -264,11 +284,8 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
       if (next_id >= 0 && next_id < a.num_blocks) {
         stage_ok[st] = 1;
         mbar_arrive_expect_tx(bar, STAGE);
-#pragma unroll
-        for (int bx = 0; bx < GE::NBX; ++bx) {
-          tma_load_3d(dst + bx * GE::BOX, &maps.k, bx * (GE::IB / GE::E), kvh * BS, next_id, bar);
-          tma_load_3d(dst + TILE + bx * GE::BOX, &maps.v, bx * (GE::IB / GE::E), kvh * BS, next_id, bar);
-        }
+        tma_load_tile<GE>(dst, &maps.k, kvh * BS, next_id, bar);
+        tma_load_tile<GE>(dst + TILE, &maps.v, kvh * BS, next_id, bar);
       } else {
         raise_error(a.err, PKV_DEVERR_BAD_BLOCK_ID);
         stage_ok[st] = 0;

@@ -160,18 +160,30 @@ bool encode_cache_map(const pkv_cache_desc* c, const void* base, TmaMap* out) {
   const int E = elem_bytes(c->dtype);
   const int row = c->head_dim * E;
   const int ib = tma_box_bytes(row);
-  const cuuint64_t dims[3] = {(cuuint64_t)c->head_dim, (cuuint64_t)c->num_kv_heads * c->block_size,
-                              (cuuint64_t)c->num_blocks};
-  const cuuint64_t strides[2] = {(cuuint64_t)row, (cuuint64_t)row * c->num_kv_heads * c->block_size};
-  const cuuint32_t box[3] = {(cuuint32_t)(ib / E), (cuuint32_t)c->block_size, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
+  const cuuint64_t rows = (cuuint64_t)c->num_kv_heads * c->block_size;
   const CUtensorMapDataType dt = c->dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const CUtensorMapSwizzle sw = ib == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   static_assert(sizeof(TmaMap) == sizeof(CUtensorMap), "opaque tensor map size");
-  if (fn(reinterpret_cast<CUtensorMap*>(out), dt, 3, const_cast<void*>(base), dims, strides, box, estr,
-         CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return false;
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult rc;
+  if (row == ib) {
+    // (elements of a row, rows of a block, blocks): one box per tile
+    const cuuint64_t dims[3] = {(cuuint64_t)c->head_dim, rows, (cuuint64_t)c->num_blocks};
+    const cuuint64_t strides[2] = {(cuuint64_t)row, (cuuint64_t)row * rows};
+    const cuuint32_t box[3] = {(cuuint32_t)(ib / E), (cuuint32_t)c->block_size, 1};
+    rc = fn(reinterpret_cast<CUtensorMap*>(out), dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    // rows wider than the swizzle span: (elements of a span, rows of a block,
+    // spans of a row, blocks), so that one copy brings a whole tile, laid
+    // out span by span (the span stride is smaller than the row stride)
+    const cuuint64_t dims[4] = {(cuuint64_t)(ib / E), rows, (cuuint64_t)(row / ib), (cuuint64_t)c->num_blocks};
+    const cuuint64_t strides[3] = {(cuuint64_t)row, (cuuint64_t)ib, (cuuint64_t)row * rows};
+    const cuuint32_t box[4] = {(cuuint32_t)(ib / E), (cuuint32_t)c->block_size, (cuuint32_t)(row / ib), 1};
+    rc = fn(reinterpret_cast<CUtensorMap*>(out), dt, 4, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  if (rc != CUDA_SUCCESS) return false;
   Memo& m = memo[next];
   next ^= 1;
   m.base = base;
