@@ -496,7 +496,7 @@ namespace pkv {
 // Pieces the cascade's prefix pass cuts the prefix into: enough warps (kv
 // heads x blocks of 16 query rows x pieces) for one resident wave of
 // kPrefixWarpsPerSm per SM, each piece at least kMinPieceBlocks blocks long.
-constexpr int kPrefixWarpsPerSm = 12, kMinPieceBlocks = 4, kMaxPieces = 32, kMultiItemsPerSlot = 2;
+constexpr int kPrefixWarpsPerSm = 12, kMinPieceBlocks = 4, kMaxPieces = 32, kMultiItemsPerSlot = 1;
 
 int prefix_pieces(int sms, int num_seqs, int group, int num_kv_heads, int prefix_blocks) {
   const int64_t pairs = (int64_t)num_kv_heads * (((int64_t)num_seqs * group + 15) / 16);
@@ -538,8 +538,9 @@ bool cascade_layout(int num_seqs, int num_q_heads, int num_kv_heads, int D, int 
 // is cut into S equal pieces (in the kernel), S chosen so that the
 // (sequence, kv head, 16-row block, piece) work items number about
 // kMultiItemsPerSlot times the resident warps (kPrefixWarpsPerSm per SM):
-// 2 measured faster than 1 (a ragged last wave) and 4 (more pieces to
-// merge).  nb_max < 0 gives the bound the workspace is sized by.
+// on speculative verify one item per slot measured faster than two, three
+// or four (every extra piece is one more partial to write and merge).
+// nb_max < 0 gives the bound the workspace is sized by.
 int multi_pieces(int sms, int num_seqs, int num_kv_heads, int max_rb, int nb_max) {
   const int64_t units = (int64_t)num_seqs * num_kv_heads * max_rb;
   if (units <= 0) return 1;
