@@ -17,20 +17,22 @@
 // prefix's K and V once per sequence although the tiles are the same.  The
 // cascade splits the work: this kernel attends every query row of the batch
 // to the prefix once per 16 rows, and the decode kernel then walks each
-// sequence's own blocks past the prefix and folds this partial result in by
-// log-sum-exp.  The output is that of plain decode.
+// sequence's own blocks past the prefix and starts each segment's online
+// softmax from this partial result.  The output is that of plain decode.
 //
-// Design (GB300): one warp per (kv head, block of 16 query rows, piece of
-// the prefix); the 16 rows are (sequence, query head) pairs of that kv head,
-// so all 16 rows of the m16n8k16 operand are real and each prefix tile feeds
-// 16 rows instead of G.  The prefix is cut into pieces so that the grid fills
-// every SM; the last warp of a (kv head, row block) to finish merges the
-// pieces' partials by log-sum-exp into the one partial the decode reads.
-// Tiles come by TMA tensor copies into a per-warp ring, swizzled for
-// ldmatrix, as in the decode kernel; P keeps a head and a remainder of the
-// operand type (two MMAs per n-tile).  Partials are unnormalised:
-// o = sum_t 2^(s_t - m) v_t, m = max_t s_t (log2 units of the scaled score),
-// l = sum_t 2^(s_t - m), over the prefix tokens t < seq_len of the row.
+// Design (GB300): one warp per (kv head [, sequence], block of 16 query
+// rows, piece of the K/V range); the 16 rows are (sequence or query token,
+// query head) pairs of that kv head, so all 16 rows of the m16n8k16 operand
+// are real and each tile feeds 16 rows instead of G.  The PW warps of a CTA
+// share one ring of tiles: lane 0 of warp 0 starts each TMA tensor copy
+// (swizzled for ldmatrix, as in the decode kernel) and refills a stage once
+// every warp has arrived on its "empty" barrier.  The range is cut into
+// pieces so that the grid fills every SM; the last warp of a row block to
+// finish merges the pieces' partials by log-sum-exp.  P keeps a head and a
+// remainder of the operand type (two MMAs per n-tile).  Partials are
+// unnormalised: o = sum_t 2^(s_t - m) v_t, m = max_t s_t (log2 units of the
+// scaled score), l = sum_t 2^(s_t - m), over the tokens t below the row's
+// limit.
 #pragma once
 
 #include "decode_tc.cuh"
