@@ -254,8 +254,8 @@ size_t pkv_cascade_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_
  *      result per row (unnormalised output, running maximum, running sum) in
  *      the workspace;
  *   2. the decode kernel attends each sequence over its own blocks after the
- *      prefix and folds the prefix partial in with the log-sum-exp merge of
- *      split-KV decoding.
+ *      prefix, starting each sequence's online softmax from the prefix
+ *      partial (the log-sum-exp algebra of split-KV decoding).
  *
  * A sequence shorter than the prefix attends only its first seq_lens[i]
  * tokens of it, as in plain decoding.
