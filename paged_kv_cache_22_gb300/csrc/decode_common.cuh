@@ -248,6 +248,8 @@ __device__ __forceinline__ bool plan_warp(const DecodeArgs& a, int64_t gw, int64
     // warps): zero, or in a cascade the shared prefix's result alone
     for (int64_t s = gw; s < a.num_seqs; s += NW) {
       if (seq_blocks<BS>(a, (int)s) == 0) {
+        // a cascade's prefix partial comes from the grid this one may depend on
+        if (a.pre) asm volatile("griddepcontrol.wait;" ::: "memory");
         QT* o = reinterpret_cast<QT*>(a.out) + (size_t)s * a.num_q_heads * D;
         for (int i = lane; i < a.num_q_heads * D; i += 32) {
           float v = 0.f;

@@ -143,6 +143,9 @@ __global__ void __launch_bounds__(32 * PW, 12 / PW)
     fence_mbar_init();
   }
   __syncthreads();
+  // the cascade's suffix decode may start its prologue on SMs this grid frees
+  // (it waits for the whole grid before it reads any partial)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (w >= nact) return;
   const int hr = MULTI ? (ms * a.num_kv_heads + h) * a.max_rb + rb : h * a.row_blocks + rb;
   // the lane's two rows (g, g + 8): the query row they read (the sequence's

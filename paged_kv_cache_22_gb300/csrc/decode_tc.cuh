@@ -319,16 +319,17 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
 
   Walker qlook = wk0;
   if (lane == 0) issue_q(wk0, 0);
+  // Everything above reads only the step's inputs (lengths, tables, q).  When
+  // this grid is the programmatic dependent of the cache write (or of a
+  // cascade's prefix pass), the K/V tiles and the prefix partials must wait
+  // for that grid; on an ordinary launch this returns at once.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if constexpr (REMAP) {
     if (a.pre && wk0.jb == 0) {
       if (lane == 0) issue_pre(wk0);
       ++pre_issued;
     }
   }
-  // Everything above reads only the step's inputs (lengths, tables, q).  When
-  // this grid is the programmatic dependent of the cache write, the K/V tiles
-  // must wait for that grid; on an ordinary launch this returns at once.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
 #pragma unroll 1
   for (int i = 0; i < NSW; ++i) issue_next();
 

@@ -660,8 +660,11 @@ pkv_status pkv_cascade_decode(void* out, const void* q, pkv_dtype q_dtype, int32
   void* args[] = {&pa, &maps};
   if (cudaLaunchKernel(pk.fn, dim3((unsigned)ctas), dim3(32 * kPrefixWarps), args, pk.smem, cs) != cudaSuccess)
     return PKV_ERR_CUDA;
+  // the suffix decode is the prefix pass's programmatic dependent: its
+  // prologue overlaps the pass's tail, and it waits for the pass before it
+  // reads a partial
   return decode_impl(out, q, q_dtype, num_seqs, num_q_heads, k_cache, v_cache, cache, block_tables,
-                     max_blocks_per_seq, seq_lens, max_seq_len, scale, kv_scale, 0, workspace, dec, stream, false,
+                     max_blocks_per_seq, seq_lens, max_seq_len, scale, kv_scale, 0, workspace, dec, stream, true,
                      false, ex);
 }
 
