@@ -151,6 +151,15 @@ def _desc(k_cache: torch.Tensor, cache_dtype: Optional[int]) -> CacheDesc:
     return CacheDesc(nb, bs, hkv, d, dt)
 
 
+def _same_layout(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor) -> None:
+    """The library writes `out` in q's type and shape and reads both caches
+    with one descriptor: catch mismatches before anything is enqueued."""
+    if out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError(f"out must match q: got {tuple(out.shape)} {out.dtype}, q is {tuple(q.shape)} {q.dtype}")
+    if v_cache.shape != k_cache.shape or v_cache.dtype != k_cache.dtype:
+        raise ValueError("k_cache and v_cache must have the same shape and dtype")
+
+
 def _check(status: int, what: str) -> None:
     if status != 0:
         raise PkvError(status, what)
@@ -244,6 +253,7 @@ def paged_attention_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Te
     its first ``sinks`` tokens (blocks outside them are never read)."""
     if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
         raise TypeError("block_tables and seq_lens must be int32")
+    _same_layout(out, q, k_cache, v_cache)
     B, Hq, d = q.shape
     desc = _desc(k_cache, None)
     mbps = int(block_tables.shape[1])
@@ -288,6 +298,7 @@ def cascade_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_
     partial results are merged (bf16 and fp8 caches)."""
     if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
         raise TypeError("block_tables and seq_lens must be int32")
+    _same_layout(out, q, k_cache, v_cache)
     B, Hq, d = q.shape
     desc = _desc(k_cache, None)
     mbps = int(block_tables.shape[1])
@@ -328,6 +339,7 @@ def paged_attention_multi(out: torch.Tensor, q: torch.Tensor, q_start: torch.Ten
     omitted)."""
     if q_start.dtype != torch.int32 or block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
         raise TypeError("q_start, block_tables and seq_lens must be int32")
+    _same_layout(out, q, k_cache, v_cache)
     total, Hq, d = q.shape
     B = int(seq_lens.shape[0])
     if q_start.shape[0] != B + 1:
@@ -365,6 +377,7 @@ def decode_step(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, ou
         raise TypeError("k and v must both be float32 or bfloat16")
     if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
         raise TypeError("block_tables and seq_lens must be int32")
+    _same_layout(out, q, k_cache, v_cache)
     B, Hq, d = q.shape
     desc = _desc(k_cache, None)
     mbps = int(block_tables.shape[1])

@@ -156,3 +156,26 @@ def test_multi_rejects_bad_arguments_before_launch(lib):
     desc.dtype = 1
     assert lib.pkv_paged_attention_multi(p, p, 0, p, 2, 4, 2, 8, p, p, ctypes.byref(desc), p, 4, p, 64,
                                          0.125, 1.0, p, 1 << 24, None) == UNSUPPORTED
+
+
+def test_bindings_reject_mismatched_out_and_caches_before_any_device_work():
+    """The Python entry points check that out matches q and that the two
+    caches agree, before anything touches the device (CPU tensors here)."""
+    import torch
+
+    import paged_kv_cache_22_gb300 as pkv
+    kc = torch.zeros((8, 2, 16, 64), dtype=torch.bfloat16)
+    q = torch.zeros((2, 8, 64), dtype=torch.bfloat16)
+    tables = torch.zeros((2, 4), dtype=torch.int32)
+    lens = torch.ones(2, dtype=torch.int32)
+    bad_outs = [torch.zeros((2, 8, 64), dtype=torch.float32), torch.zeros((2, 8, 32), dtype=torch.bfloat16)]
+    for out in bad_outs:
+        with pytest.raises(ValueError):
+            pkv.paged_attention_decode(out, q, kc, kc, tables, lens, 0.125)
+        with pytest.raises(ValueError):
+            pkv.cascade_decode(out, q, kc, kc, tables, lens, 1, 0.125)
+        with pytest.raises(ValueError):
+            pkv.paged_attention_multi(out, q, torch.tensor([0, 1, 2], dtype=torch.int32), kc, kc, tables, lens,
+                                      0.125, max_q=1)
+    with pytest.raises(ValueError):  # V cache of another type
+        pkv.paged_attention_decode(q.clone(), q, kc, kc.to(torch.uint8), tables, lens, 0.125)
