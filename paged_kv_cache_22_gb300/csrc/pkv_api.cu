@@ -626,8 +626,13 @@ pkv_status pkv_cascade_decode(void* out, const void* q, pkv_dtype q_dtype, int32
   PrefixKernel pk;
   const bool found = cache->dtype == PKV_BF16 ? find_prefix_bf16(D, BS, &pk) : find_prefix_fp8(D, BS, &pk);
   if (!found) return PKV_ERR_UNSUPPORTED;
-  if (cudaFuncSetAttribute(pk.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pk.smem) != cudaSuccess)
-    return PKV_ERR_CUDA;
+  {  // opt into the dynamic shared memory once per kernel and device
+    DecodeKernel pkd;
+    pkd.fn = pk.fn;
+    pkd.threads = 32 * pk.warps;
+    pkd.smem = pk.smem;
+    if (prepare_kernel(pkd, dev) <= 0) return PKV_ERR_CUDA;
+  }
   DecodeKernel tk;  // the tensor maps both kernels read the caches through
   tk.tensor_maps = true;
   TmaMaps maps{};
@@ -712,8 +717,13 @@ pkv_status pkv_paged_attention_multi(void* out, const void* q, pkv_dtype q_dtype
   const int groups = (lay.max_rb + pk.warps - 1) / pk.warps;
   const int64_t ctas = (int64_t)num_seqs * cache->num_kv_heads * groups * S;
   if (ctas > 0x7FFFFFFF) return PKV_ERR_UNSUPPORTED;
-  if (cudaFuncSetAttribute(pk.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pk.smem) != cudaSuccess)
-    return PKV_ERR_CUDA;
+  {  // opt into the dynamic shared memory once per kernel and device
+    DecodeKernel pkd;
+    pkd.fn = pk.fn;
+    pkd.threads = 32 * pk.warps;
+    pkd.smem = pk.smem;
+    if (prepare_kernel(pkd, dev) <= 0) return PKV_ERR_CUDA;
+  }
   DecodeKernel tk;
   tk.tensor_maps = true;
   TmaMaps maps{};
