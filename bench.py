@@ -630,6 +630,9 @@ def run_multi(args):
     write is the decode step's cache-write kernel)."""
     import paged_kv_cache_22_gb300 as pkv
     ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     pkv.library()
@@ -745,6 +748,8 @@ def run_multi(args):
         line["cpu_baseline"] = cpu_baseline_multi(w, q_cpu, qs_cpu, args.cpu_seconds, compute)
     if rank == 0:
         print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
 
 
 def cpu_baseline_multi(w, q_cpu, qs_cpu, seconds: float, compute: bool):
