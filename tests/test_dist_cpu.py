@@ -57,3 +57,23 @@ def test_single_process_is_identity():
     import bench
     assert bench.max_over_ranks(3.5, torch.device("cpu")) == 3.5
     assert bench.job_throughput(1, 4_000_000_000, 1000.0) == pytest.approx(4.0)
+
+
+def test_reference_arm_under_torchrun_prints_one_line_from_rank_zero():
+    """`bench.py --impl reference` launched by torchrun with two ranks on the
+    CPU: rank 0 alone runs the oracle and prints one JSON line, rank 1 exits 0
+    without work."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py",
+           "--impl", "reference", "--gpus", "2", "--steps", "3", "--warmup", "3", "--ref-seqs", "2"]
+    res = subprocess.run(cmd, cwd=root, capture_output=True, text=True, timeout=600)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [l for l in res.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
