@@ -146,13 +146,16 @@ size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
  *               that many tokens (a multiple of block_size), merged by
  *               pkv_split_kv_reduce inside this call (two launches)
  *   workspace   device, >= pkv_decode_workspace_bytes(...) bytes, 256-byte
- *               aligned.  The merge counters at its start must be zero when a
- *               balanced call starts; every completed call leaves them zero
- *               and no call writes partials into the counter region, so a
- *               workspace zero-filled once serves any sequence of calls of
- *               either mode while num_seqs * units stays <= 262144 (a larger
- *               batch grows the region: zero it again then).  Calls sharing
- *               one workspace must not overlap on the GPU.
+ *               aligned.  Zero-fill it once before its first use; after that
+ *               it serves any sequence of calls of either mode (and of
+ *               pkv_cascade_decode and pkv_paged_attention_multi): every
+ *               completed call leaves the merge counters of the first 1 MiB
+ *               zero and no call writes partials there, and a balanced call
+ *               whose counter region is larger (num_seqs * units > 262144)
+ *               clears that region itself (an asynchronous memset on
+ *               `stream`, before the decode) because an earlier call may
+ *               have left partials in it.  Calls sharing one workspace must
+ *               not overlap on the GPU.
  */
 pkv_status pkv_paged_attention_decode(void* out, const void* q, pkv_dtype q_dtype,
                                       int32_t num_seqs, int32_t num_q_heads, const void* k_cache,
@@ -179,10 +182,11 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, pkv_dtype q_dtyp
  *
  * Arguments are those of pkv_paged_attention_decode without
  * partition_tokens, workspace and workspace_bytes; layouts, supported shapes
- * and error behaviour are the same.  A problem whose counters and partials
- * need more than the fixed scratch (many (sequence, kv-head) segments, or an
- * unusually large grid) is refused with PKV_ERR_WORKSPACE before anything
- * is enqueued.
+ * and error behaviour are the same.  When the partial-result slots of a full
+ * grid do not fit beside the merge counters, the call runs on fewer thread
+ * blocks (same result).  A problem whose counters alone leave no room for
+ * one thread block's slots (about four million (sequence, kv-head unit)
+ * segments) is refused with PKV_ERR_WORKSPACE before anything is enqueued.
  *
  * The first call on a device looks up the scratch array's device address
  * (once per device, with that device current); make that first call before
@@ -453,6 +457,22 @@ pkv_status pkv_copy_blocks(void* k_dst, void* v_dst, const pkv_cache_desc* dst, 
  */
 pkv_status pkv_get_device_error(uint32_t* code_out, pkv_stream_t stream);
 
+/*
+ * pkv_selftest_wait_timeout -- exercise the failure path of the bounded
+ * waits (no counterpart on the source pages: a diagnostic of this library).
+ *
+ * Every kernel that waits for an asynchronous copy waits with an iteration
+ * limit of about a second, after which it sets PKV_DEVERR_WAIT_TIMEOUT,
+ * stops issuing copies and returns, so that a lost copy cannot hang the
+ * GPU.  This call launches one thread that arms an mbarrier for 16 bytes of
+ * transactions no copy will deliver (it issues none, so nothing is left in
+ * flight) and waits on it with that same bounded wait: the wait gives up,
+ * the bit is set in the device error word and the kernel returns, leaving
+ * the context usable.  Takes up to about a second of GPU time.
+ * Asynchronous on `stream`; read the bit with pkv_get_device_error.
+ */
+pkv_status pkv_selftest_wait_timeout(pkv_stream_t stream);
+
 /* Human-readable name of a status; never NULL. */
 const char* pkv_status_string(pkv_status status);
 
@@ -483,6 +503,29 @@ typedef enum { PKV_ENGINE_TENSOR_CORES = 0, PKV_ENGINE_CUDA_CORES = 1 } pkv_deco
 
 pkv_status pkv_set_decode_engine(pkv_decode_engine engine);
 pkv_decode_engine pkv_get_decode_engine(void);
+
+/*
+ * The tcgen05 kernels of pkv_paged_attention_multi and of the prefix pass of
+ * pkv_cascade_decode (bf16 caches, and fp8-e4m3 caches with head_dim 128).
+ *
+ *   enable != 0 (default)  a call whose tiles can hold 128 query rows -- a
+ *       (sequence, kv head) with max_q * Hq / Hkv >= 128, or a cascade batch
+ *       with num_seqs * Hq / Hkv >= 128 -- runs the tcgen05 kernel: 128 rows
+ *       per CTA, q.K and P.V as 5th-generation tensor-core MMAs with both
+ *       accumulators in tensor memory, K/V tiles by tensor copy (fp8 codes
+ *       widened exactly to fp16 in shared memory). Smaller calls keep the
+ *       mma.sync kernels, except for cache shapes those have no instance of
+ *       (fp8 caches with 8- or 32-token blocks), which the tcgen05 kernel
+ *       serves at any size.
+ *   enable == 0            every call runs the mma.sync kernels (fp8 caches
+ *       with 8- or 32-token blocks are then PKV_ERR_UNSUPPORTED).
+ *
+ * Both give the same results within the tolerances of their cache type; the
+ * switch exists to compare them. Process-wide, for calls issued after it
+ * returns.
+ */
+void pkv_set_tcgen05(int32_t enable);
+int32_t pkv_get_tcgen05(void);
 
 #ifdef __cplusplus
 }

@@ -20,7 +20,10 @@ Entry points (same names as the C ABI, without the ``pkv_`` prefix):
 * :func:`decode_workspace_bytes`, :func:`get_device_error`;
 * :func:`set_decode_engine` / :func:`get_decode_engine` (and the
   :func:`decode_engine` context manager) -- tensor cores (default) or CUDA
-  cores for the contractions of bf16 and fp8 decodes.
+  cores for the contractions of bf16 and fp8 decodes;
+* :func:`set_tcgen05` / :func:`get_tcgen05` (and the :func:`tcgen05`
+  context manager) -- whether multi-token calls and cascade prefix passes
+  with 128-row tiles take the tcgen05 kernels.
 """
 from __future__ import annotations
 
@@ -40,6 +43,7 @@ __all__ = [
     "DecodeWorkspace", "F32", "BF16", "FP8_E4M3", "DEVERR_BAD_BLOCK_ID", "DEVERR_BAD_SLOT",
     "DEVERR_BAD_SEQ_LEN", "DEVERR_WAIT_TIMEOUT", "DEVERR_SMEM_ALIGN", "set_decode_engine",
     "get_decode_engine", "decode_engine", "ENGINE_TENSOR_CORES", "ENGINE_CUDA_CORES",
+    "set_tcgen05", "get_tcgen05", "tcgen05", "selftest_wait_timeout",
 ]
 
 F32, BF16, FP8_E4M3 = 0, 1, 2
@@ -104,6 +108,8 @@ def library() -> ctypes.CDLL:
             "pkv_device_sm_count": [],
             "pkv_set_decode_engine": [ctypes.c_int],
             "pkv_get_decode_engine": [],
+            "pkv_get_tcgen05": [],
+            "pkv_selftest_wait_timeout": [vp],
         }
         for name, args in sigs.items():
             fn = getattr(lib, name)
@@ -113,6 +119,8 @@ def library() -> ctypes.CDLL:
         lib.pkv_cascade_workspace_bytes.restype = sz
         lib.pkv_multi_workspace_bytes.restype = sz
         lib.pkv_status_string.restype = ctypes.c_char_p
+        lib.pkv_set_tcgen05.argtypes = [i32]
+        lib.pkv_set_tcgen05.restype = None
         _lib = lib
         return lib
 
@@ -190,6 +198,29 @@ def decode_engine(engine):
         set_decode_engine(prev)
 
 
+def set_tcgen05(enable: bool) -> None:
+    """Let :func:`paged_attention_multi` and the prefix pass of
+    :func:`cascade_decode` run the tcgen05 kernels when their tiles can hold
+    128 query rows (default True), or keep every call on the mma.sync
+    kernels; process-wide."""
+    library().pkv_set_tcgen05(1 if enable else 0)
+
+
+def get_tcgen05() -> bool:
+    return bool(library().pkv_get_tcgen05())
+
+
+@contextlib.contextmanager
+def tcgen05(enable: bool):
+    """Temporarily set :func:`set_tcgen05`."""
+    prev = get_tcgen05()
+    set_tcgen05(enable)
+    try:
+        yield
+    finally:
+        set_tcgen05(prev)
+
+
 def kv_reshape_and_cache(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor,
                          v_cache: torch.Tensor, slot_mapping: torch.Tensor,
                          kv_scale: float = 1.0, stream=None) -> None:
@@ -216,22 +247,17 @@ def decode_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, h
 class DecodeWorkspace:
     """A device workspace (torch-allocated) that grows on demand.
 
-    It is zero-filled when (re)allocated; the library keeps its merge counters
-    zero between calls.  A batch whose counter region outgrows every earlier
-    one gets a fresh zeroed buffer, since the larger region may cover bytes
-    that held partials."""
-
-    COUNTER_REGION_MIN = 1 << 20
+    It is zero-filled when (re)allocated.  The library keeps it valid from
+    then on: every call leaves its merge counters zero, and a call whose
+    counter region reaches past the part that is always kept zero clears
+    that region itself."""
 
     def __init__(self, device=None):
         self.device = device
         self.buf: Optional[torch.Tensor] = None
-        self.counter_bytes = self.COUNTER_REGION_MIN
 
-    def get(self, nbytes: int, counter_bytes: int = 0) -> torch.Tensor:
-        grow = self.buf is None or self.buf.numel() < nbytes or counter_bytes > self.counter_bytes
-        if grow:
-            self.counter_bytes = max(self.counter_bytes, counter_bytes)
+    def get(self, nbytes: int) -> torch.Tensor:
+        if self.buf is None or self.buf.numel() < nbytes:
             self.buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=self.device or "cuda")
         return self.buf
 
@@ -263,10 +289,7 @@ def paged_attention_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Te
     if workspace is None:
         dev = q.device.index if q.device.index is not None else torch.cuda.current_device()
         workspace = _default_ws.setdefault(dev, DecodeWorkspace(q.device))
-    g = Hq // desc.num_kv_heads
-    heads = next(G for G in (8, 4, 2, 1) if g % G == 0)
-    units = desc.num_kv_heads * (g // heads)
-    ws = workspace.get(nbytes, (B * units * 4 + 255) // 256 * 256)
+    ws = workspace.get(nbytes)
     qdt = F32 if q.dtype == torch.float32 else BF16
     if window:
         _check(library().pkv_paged_attention_decode_window(
@@ -308,10 +331,7 @@ def cascade_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_
     if workspace is None:
         dev = q.device.index if q.device.index is not None else torch.cuda.current_device()
         workspace = _default_ws.setdefault(dev, DecodeWorkspace(q.device))
-    g = Hq // desc.num_kv_heads
-    heads = next(G for G in (8, 4, 2, 1) if g % G == 0)
-    units = desc.num_kv_heads * (g // heads)
-    ws = workspace.get(nbytes, (B * units * 4 + 255) // 256 * 256)
+    ws = workspace.get(nbytes)
     qdt = F32 if q.dtype == torch.float32 else BF16
     _check(library().pkv_cascade_decode(
         _ptr(out), _ptr(q), qdt, B, Hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc),
@@ -387,10 +407,7 @@ def decode_step(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, ou
     if workspace is None:
         dev = q.device.index if q.device.index is not None else torch.cuda.current_device()
         workspace = _default_ws.setdefault(dev, DecodeWorkspace(q.device))
-    g = Hq // desc.num_kv_heads
-    heads = next(G for G in (8, 4, 2, 1) if g % G == 0)
-    units = desc.num_kv_heads * (g // heads)
-    ws = workspace.get(nbytes, (B * units * 4 + 255) // 256 * 256)
+    ws = workspace.get(nbytes)
     qdt = F32 if q.dtype == torch.float32 else BF16
     _check(library().pkv_decode_step(
         _ptr(k), _ptr(v), _dt(k), int(k.shape[0]), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
@@ -454,6 +471,13 @@ def copy_blocks(k_dst: torch.Tensor, v_dst: torch.Tensor, k_src: torch.Tensor, v
     _check(library().pkv_copy_blocks(_addr(k_dst), _addr(v_dst), ctypes.byref(dd), _addr(k_src), _addr(v_src),
                                      ctypes.byref(sd), _addr(block_pairs), int(block_pairs.shape[0]),
                                      _stream(stream)), "copy_blocks")
+
+
+def selftest_wait_timeout(stream=None) -> None:
+    """Run the library's bounded-wait failure path once (an mbarrier armed for
+    bytes no copy delivers): afterwards :func:`get_device_error` reports
+    ``DEVERR_WAIT_TIMEOUT``.  Takes up to about a second of GPU time."""
+    _check(library().pkv_selftest_wait_timeout(_stream(stream)), "selftest_wait_timeout")
 
 
 def get_device_error(stream=None) -> int:

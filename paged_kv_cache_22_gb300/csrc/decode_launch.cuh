@@ -4,6 +4,7 @@
 #include "decode.cuh"
 #include "decode_tc.cuh"
 #include "decode_prefix.cuh"
+#include "attn_tc05.cuh"
 
 namespace pkv {
 
@@ -133,6 +134,27 @@ bool find_prefix_fp8(int head_dim, int block_size, PrefixKernel* out);
 // one_warp: the one-warp-per-CTA instance (at most 16 rows per sequence and kv head)
 bool find_multi_bf16(int head_dim, int block_size, bool one_warp, PrefixKernel* out);
 bool find_multi_fp8(int head_dim, int block_size, bool one_warp, PrefixKernel* out);
+
+// The tcgen05 kernels (attn_tc05.cuh): 128 query rows per CTA, parameters
+// (Tc05Args, TmaMaps). bf16 caches: the maps view each cache as (D, Hkv * BS,
+// num_blocks) with a box of one 128-byte span (64, BS, 1); fp8 caches
+// (head_dim 128): the decode kernels' map, a box of whole rows (128, BS, 1).
+struct Tc05Kernel {
+  const void* fn = nullptr;
+  size_t smem = 0;
+  int threads = 0;
+};
+template <int D, int BS, bool F8, bool PREFIX>
+Tc05Kernel tc05_kernel_info() {
+  Tc05Kernel k;
+  k.fn = reinterpret_cast<const void*>(&attn_tc05_kernel<D, BS, F8, PREFIX>);
+  k.smem = tc05::Layout<D, F8>::kBytes;
+  k.threads = tc05::threads(F8);
+  return k;
+}
+// prefix: the cascade's shared-prefix pass; otherwise several query tokens per sequence
+bool find_tc05_bf16(int head_dim, int block_size, bool prefix, Tc05Kernel* out);
+bool find_tc05_fp8(int head_dim, int block_size, bool prefix, Tc05Kernel* out);
 
 // The engine set by pkv_set_decode_engine (pkv_api.cu).
 bool decode_on_tensor_cores();

@@ -196,4 +196,24 @@ cudaError_t launch_split_kv_reduce(const ReduceArgs& a, int out_is_bf16, cudaStr
   return cudaGetLastError();
 }
 
+// ----------------------------------------------------------------------------
+// Self-test of the failure path every pipelined kernel shares: one thread
+// arms an mbarrier for 16 bytes of transactions that no copy will ever
+// deliver (none is issued, so nothing is in flight), then waits on it with
+// the same bounded wait the attention kernels use.  The wait gives up after
+// its probe limit, raises PKV_DEVERR_WAIT_TIMEOUT and the kernel returns.
+// ----------------------------------------------------------------------------
+__global__ void wait_timeout_selftest_kernel(unsigned int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  mbar_arrive_expect_tx(&bar, 16);
+  mbar_wait_bounded(&bar, 0, err);
+}
+
+cudaError_t launch_wait_timeout_selftest(unsigned int* err, cudaStream_t stream) {
+  wait_timeout_selftest_kernel<<<1, 1, 0, stream>>>(err);
+  return cudaGetLastError();
+}
+
 }  // namespace pkv

@@ -64,5 +64,6 @@ cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t stream);
 cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, int src_is_bf16, cudaStream_t stream);
 cudaError_t launch_gather_kv(const GatherArgs& a, int max_seq_len, cudaStream_t stream);
 cudaError_t launch_split_kv_reduce(const ReduceArgs& a, int out_is_bf16, cudaStream_t stream);
+cudaError_t launch_wait_timeout_selftest(unsigned int* err, cudaStream_t stream);
 
 }  // namespace pkv

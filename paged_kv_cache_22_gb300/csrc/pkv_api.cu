@@ -192,6 +192,42 @@ bool encode_cache_map(const pkv_cache_desc* c, const void* base, TmaMap* out) {
   return true;
 }
 
+// The cache [num_blocks, Hkv, BS, D] (bf16) as the 3-D tensor (D, Hkv * BS,
+// num_blocks) with a box of one 128-byte span of one (block, kv head) tile:
+// (64, BS, 1), swizzled over the span. The tcgen05 kernel for several query
+// tokens stacks the spans of 64 / BS blocks into one operand per span.
+bool encode_span_map(const pkv_cache_desc* c, const void* base, TmaMap* out) {
+  auto fn = tensor_map_encoder();
+  if (!fn || c->dtype != PKV_BF16 || c->head_dim % 64) return false;
+  const cuuint64_t rows = (cuuint64_t)c->num_kv_heads * c->block_size;
+  const cuuint64_t dims[3] = {(cuuint64_t)c->head_dim, rows, (cuuint64_t)c->num_blocks};
+  const cuuint64_t strides[2] = {(cuuint64_t)c->head_dim * 2, (cuuint64_t)c->head_dim * 2 * rows};
+  const cuuint32_t box[3] = {64, (cuuint32_t)c->block_size, 1}, estr[3] = {1, 1, 1};
+  return fn(reinterpret_cast<CUtensorMap*>(out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The tensor maps of the tcgen05 kernels: bf16, one span box per copy;
+// fp8 (rows of one span), the decode kernels' whole-row box.
+bool encode_tc05_maps(const pkv_cache_desc* c, const void* k, const void* v, TmaMaps* maps) {
+  if (c->dtype == PKV_BF16) return encode_span_map(c, k, &maps->k) && encode_span_map(c, v, &maps->v);
+  return encode_cache_map(c, k, &maps->k) && encode_cache_map(c, v, &maps->v);
+}
+
+int prepare_tc05(const Tc05Kernel& k, int dev) {
+  DecodeKernel kd;
+  kd.fn = k.fn;
+  kd.threads = k.threads;
+  kd.smem = k.smem;
+  return prepare_kernel(kd, dev);
+}
+
+// Whether pkv_paged_attention_multi and the cascade's prefix pass may take
+// the tcgen05 kernels (the default); tests switch them off to compare with
+// the mma.sync kernels.
+std::atomic<int> g_tc05{1};
+
 }  // namespace
 
 // The current device's error word, for entry points defined in other
@@ -232,6 +268,10 @@ pkv_status pkv_set_decode_engine(pkv_decode_engine engine) {
 pkv_decode_engine pkv_get_decode_engine(void) {
   return static_cast<pkv_decode_engine>(g_engine.load(std::memory_order_relaxed));
 }
+
+void pkv_set_tcgen05(int32_t enable) { g_tc05.store(enable != 0, std::memory_order_relaxed); }
+
+int32_t pkv_get_tcgen05(void) { return g_tc05.load(std::memory_order_relaxed); }
 
 int32_t pkv_device_sm_count(void) {
   const int dev = current_device();
@@ -422,6 +462,11 @@ pkv_status decode_impl(void* out, const void* q, pkv_dtype q_dtype, int32_t num_
     const int64_t tiles_hint = (int64_t)num_seqs * a.units * ((a.len_clip + BS - 1) / BS);
     if (tiles_hint < grid) grid = tiles_hint > 0 ? tiles_hint : 1;
     if (dry_run) return PKV_OK;
+    // A counter region beyond the fixed minimum may cover bytes that an
+    // earlier call with fewer segments used for partials: clear it here, so
+    // that a workspace zero-filled once serves any sequence of calls.
+    const size_t region = counter_region(num_seqs, a.units);
+    if (region > kCounterRegionMin && cudaMemsetAsync(workspace, 0, region, st) != cudaSuccess) return PKV_ERR_CUDA;
     return from_cuda(launch_decode_grid(k, dim3((unsigned)grid), args, st, programmatic));
   }
   // fixed partitions, then the log-sum-exp reduce
@@ -623,9 +668,59 @@ pkv_status pkv_cascade_decode(void* out, const void* q, pkv_dtype q_dtype, int32
                               max_blocks_per_seq, seq_lens, max_seq_len, scale, kv_scale, 0, workspace, dec, stream,
                               false, /*dry_run=*/true, ex);
   if (st != PKV_OK) return st;
+  const int64_t prefix_rows = (int64_t)num_seqs * group;
+  Tc05Kernel t5;
+  const bool fp8c = cache->dtype == PKV_FP8_E4M3;
   PrefixKernel pk;
-  const bool found = cache->dtype == PKV_BF16 ? find_prefix_bf16(D, BS, &pk) : find_prefix_fp8(D, BS, &pk);
-  if (!found) return PKV_ERR_UNSUPPORTED;
+  const bool have_pk = fp8c ? find_prefix_fp8(D, BS, &pk) : find_prefix_bf16(D, BS, &pk);
+  // the tcgen05 kernel once a kv head has a full 128-row tile, or where the
+  // mma.sync kernel has no instance for this cache shape
+  if (g_tc05.load(std::memory_order_relaxed) && (prefix_rows >= tc05::kRows || !have_pk) &&
+      cache->num_kv_heads <= 65535 && (fp8c ? find_tc05_fp8(D, BS, true, &t5) : find_tc05_bf16(D, BS, true, &t5))) {
+    // the prefix pass on the tcgen05 kernel: 128 rows per CTA, the prefix cut
+    // into as many pieces as fill one wave (bounded by the pieces the
+    // workspace holds)
+    const int64_t tiles = (prefix_rows + tc05::kRows - 1) / tc05::kRows;
+    if (tiles > 65535) return PKV_ERR_UNSUPPORTED;
+    int64_t S = std::max<int64_t>(1, sms / (tiles * cache->num_kv_heads));
+    S = std::min<int64_t>(S, std::max(1, prefix_blocks / kMinPieceBlocks));
+    S = std::min<int64_t>(S, prefix_pieces(sms, num_seqs, group, cache->num_kv_heads, -1));
+    const int SB = (int)((prefix_blocks + S - 1) / S);
+    S = (prefix_blocks + SB - 1) / SB;  // no empty piece
+    TmaMaps tmaps{};
+    if (!encode_tc05_maps(cache, k_cache, v_cache, &tmaps)) return PKV_ERR_CUDA;
+    if (prepare_tc05(t5, dev) <= 0) return PKV_ERR_CUDA;
+    Tc05Args ta{};
+    ta.err = err;
+    ta.q = static_cast<const __nv_bfloat16*>(q);
+    ta.block_tables = block_tables;
+    ta.table_stride = max_blocks_per_seq;
+    ta.seq_lens = seq_lens;
+    ta.num_seqs = num_seqs;
+    ta.num_q_heads = num_q_heads;
+    ta.num_kv_heads = cache->num_kv_heads;
+    ta.group = group;
+    ta.num_blocks = cache->num_blocks;
+    const int64_t tt = (int64_t)max_blocks_per_seq * BS;
+    ta.len_clip = (int)(tt < max_seq_len ? tt : max_seq_len);
+    ta.prefix_blocks = prefix_blocks;
+    ta.row_tiles = (int)tiles;
+    ta.splits = (int)S;
+    ta.split_blocks = SB;
+    ta.qk_scale = scale * 1.4426950408889634f * (fp8c ? kv_scale : 1.f);
+    ta.out_scale = 1.f;
+    ta.pre = pre;
+    ta.scratch = reinterpret_cast<float*>(ws + lay.scratch);
+    ta.counters = reinterpret_cast<int*>(ws + lay.counters);
+    void* targs[] = {&ta, &tmaps};
+    if (cudaLaunchKernel(t5.fn, dim3((unsigned)S, (unsigned)tiles, (unsigned)cache->num_kv_heads), dim3(t5.threads),
+                         targs, t5.smem, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    return decode_impl(out, q, q_dtype, num_seqs, num_q_heads, k_cache, v_cache, cache, block_tables,
+                       max_blocks_per_seq, seq_lens, max_seq_len, scale, kv_scale, 0, workspace, dec, stream, true,
+                       false, ex);
+  }
+  if (!have_pk) return PKV_ERR_UNSUPPORTED;
   {  // opt into the dynamic shared memory once per kernel and device
     DecodeKernel pkd;
     pkd.fn = pk.fn;
@@ -699,17 +794,57 @@ pkv_status pkv_paged_attention_multi(void* out, const void* q, pkv_dtype q_dtype
   if (!multi_layout(num_seqs, total_q, max_q, num_q_heads, cache->num_kv_heads, D, &lay)) return PKV_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < lay.total) return PKV_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return PKV_ERR_INVALID_ARG;
+  const int64_t table_tokens = (int64_t)max_blocks_per_seq * BS;
+  const int len_clip = (int)(table_tokens < max_seq_len ? table_tokens : max_seq_len);
+  const int group = num_q_heads / cache->num_kv_heads;
+  const int64_t rows_max = (int64_t)max_q * group;  // rows of the largest (sequence, kv head)
+  const bool fp8 = cache->dtype == PKV_FP8_E4M3;
   PrefixKernel pk;
   const bool one_warp = lay.max_rb == 1;
-  const bool found = cache->dtype == PKV_BF16 ? find_multi_bf16(D, BS, one_warp, &pk)
-                                              : find_multi_fp8(D, BS, one_warp, &pk);
-  if (!found) return PKV_ERR_UNSUPPORTED;
+  const bool have_pk = cache->dtype == PKV_BF16 ? find_multi_bf16(D, BS, one_warp, &pk)
+                                                 : find_multi_fp8(D, BS, one_warp, &pk);
+  // the tcgen05 kernel once a (sequence, kv head) fills a 128-row tile, or
+  // where the mma.sync kernel has no instance for this cache shape
+  if (g_tc05.load(std::memory_order_relaxed) && (rows_max >= tc05::kRows || !have_pk) && num_seqs <= 65535 &&
+      cache->num_kv_heads <= 65535) {
+    Tc05Kernel tk;
+    if (fp8 ? find_tc05_fp8(D, BS, false, &tk) : find_tc05_bf16(D, BS, false, &tk)) {
+      const int dev = current_device();
+      unsigned int* err = dev < 0 ? nullptr : error_word(dev);
+      if (!err) return PKV_ERR_CUDA;
+      TmaMaps maps{};
+      if (!encode_tc05_maps(cache, k_cache, v_cache, &maps)) return PKV_ERR_CUDA;
+      if (prepare_tc05(tk, dev) <= 0) return PKV_ERR_CUDA;
+      Tc05Args ta{};
+      ta.err = err;
+      ta.q = static_cast<const __nv_bfloat16*>(q);
+      ta.q_start = q_start;
+      ta.block_tables = block_tables;
+      ta.table_stride = max_blocks_per_seq;
+      ta.seq_lens = seq_lens;
+      ta.num_seqs = num_seqs;
+      ta.total_q = total_q;
+      ta.num_q_heads = num_q_heads;
+      ta.num_kv_heads = cache->num_kv_heads;
+      ta.group = group;
+      ta.num_blocks = cache->num_blocks;
+      ta.len_clip = len_clip;
+      ta.max_q = max_q;
+      ta.qk_scale = scale * 1.4426950408889634f * (fp8 ? kv_scale : 1.f);
+      ta.out_scale = fp8 ? kv_scale : 1.f;
+      ta.out = static_cast<__nv_bfloat16*>(out);
+      const dim3 grid((unsigned)((rows_max + tc05::kRows - 1) / tc05::kRows), (unsigned)cache->num_kv_heads,
+                      (unsigned)num_seqs);
+      void* args[] = {&ta, &maps};
+      return from_cuda(cudaLaunchKernel(tk.fn, grid, dim3(tk.threads), args, tk.smem,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+    }
+  }
+  if (!have_pk) return PKV_ERR_UNSUPPORTED;
   const int dev = current_device();
   const int sms = dev < 0 ? 0 : sm_count(dev);
   unsigned int* err = dev < 0 ? nullptr : error_word(dev);
   if (!err || sms <= 0) return PKV_ERR_CUDA;
-  const int64_t table_tokens = (int64_t)max_blocks_per_seq * BS;
-  const int len_clip = (int)(table_tokens < max_seq_len ? table_tokens : max_seq_len);
   const int nb_max = (len_clip + BS - 1) / BS;
   int S = multi_pieces(sms, num_seqs, cache->num_kv_heads, lay.max_rb, nb_max);
   const int SB = nb_max > 0 ? (nb_max + S - 1) / S : 1;
@@ -743,7 +878,6 @@ pkv_status pkv_paged_attention_multi(void* out, const void* q, pkv_dtype q_dtype
   pa.len_clip = len_clip;
   pa.splits = S;
   pa.split_blocks = SB;
-  const bool fp8 = cache->dtype == PKV_FP8_E4M3;
   pa.qk_scale = scale * 1.4426950408889634f * (fp8 ? kv_scale : 1.f);
   pa.scratch = reinterpret_cast<float*>(ws + lay.scratch);
   pa.counters = reinterpret_cast<int*>(ws);
@@ -840,6 +974,13 @@ pkv_status pkv_copy_blocks(void* k_dst, void* v_dst, const pkv_cache_desc* dst, 
   a.pairs = block_pairs;
   a.num_pairs = num_pairs;
   return from_cuda(launch_copy_blocks(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_selftest_wait_timeout(pkv_stream_t stream) {
+  const int dev = current_device();
+  unsigned int* err = dev < 0 ? nullptr : error_word(dev);
+  if (!err) return PKV_ERR_CUDA;
+  return from_cuda(launch_wait_timeout_selftest(err, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 pkv_status pkv_get_device_error(uint32_t* code_out, pkv_stream_t stream) {

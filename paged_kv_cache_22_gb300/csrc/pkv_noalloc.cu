@@ -26,8 +26,10 @@
 // segment) and two partial-result slots per warp of the balanced grid.  On a
 // 152-SM GB300 the grids these kernels run at need at most ~10 MB of slots
 // (8 query heads per unit, head_dim 128: 1216 one-warp CTAs x 2 x 4160 bytes),
-// which leaves room for about a million segments.  A call that needs more is
-// refused.
+// which leaves room for about a million segments.  Where the slots of a full
+// grid do not fit beside the counters, the grid is cut to what fits (the
+// balanced split works with any grid); a call whose counters leave no room
+// for even one warp's slots is refused.
 #define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[PKV_NOALLOC_SCRATCH_BYTES];
@@ -140,8 +142,10 @@ extern "C" pkv_status pkv_paged_attention_decode_noalloc(
 
   // scratch layout: [merge counters][two partial slots per warp]
   const size_t counter_bytes = round256((size_t)num_seqs * a.units * sizeof(int));
-  const size_t need = counter_bytes + (size_t)2 * grid * kDecodeWarps * (G * D + 2 * G) * sizeof(float);
-  if (need > PKV_NOALLOC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;  // beyond the fixed scratch
+  const size_t cta_bytes = (size_t)2 * kDecodeWarps * (G * D + 2 * G) * sizeof(float);
+  if (counter_bytes + cta_bytes > PKV_NOALLOC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;  // beyond the fixed scratch
+  const int64_t grid_fit = (int64_t)((PKV_NOALLOC_SCRATCH_BYTES - counter_bytes) / cta_bytes);
+  if (grid > grid_fit) grid = grid_fit;
 
   TmaMaps maps{};
   if (!encode_cache_maps(k, cache, k_cache, v_cache, &maps)) return PKV_ERR_CUDA;

@@ -179,3 +179,14 @@ def test_bindings_reject_mismatched_out_and_caches_before_any_device_work():
                                       0.125, max_q=1)
     with pytest.raises(ValueError):  # V cache of another type
         pkv.paged_attention_decode(q.clone(), q, kc, kc.to(torch.uint8), tables, lens, 0.125)
+
+
+def test_multi_kernel_switch_without_a_device(lib):
+    """The tcgen05 kernels (multi-token calls, cascade prefix pass) are on by default; the
+    switch only records the choice (no device work)."""
+    import paged_kv_cache_22_gb300 as pkv
+    assert pkv.get_tcgen05()
+    with pkv.tcgen05(False):
+        assert not pkv.get_tcgen05()
+        assert lib.pkv_get_tcgen05() == 0
+    assert pkv.get_tcgen05()

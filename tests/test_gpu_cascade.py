@@ -59,7 +59,23 @@ CASES = [
     ("bf16_long_prefix", [3, 50], 32, 8, 128, 16, "bf16", 1024),
     ("fp8_odd_prefix", [7, 20, 1], 32, 8, 128, 16, "fp8_e4m3", 37 * 16),
     ("bf16_bs8_odd_prefix", [5], 16, 2, 128, 8, "bf16", 29 * 8),
+    # at least 128 rows (sequences x g) per kv head: the prefix pass runs on
+    # the tcgen05 kernel (128-row tiles, pieces merged by the last one)
+    ("bf16_rows160", [int(x) for x in np.random.default_rng(5).integers(1, 60, 40)], 32, 8, 128, 16, "bf16",
+     256),
+    ("bf16_rows300_g8_bs8", [int(x) for x in np.random.default_rng(6).integers(1, 40, 40)], 64, 8, 128, 8,
+     "bf16", 37 * 8),
+    ("bf16_rows_d64", [int(x) for x in np.random.default_rng(7).integers(1, 50, 33)], 16, 4, 64, 16,
+     "bf16", 96),
+    ("fp8_rows160", [int(x) for x in np.random.default_rng(8).integers(1, 80, 40)], 32, 8, 128, 16, "fp8_e4m3",
+     512),
+    ("fp8_rows_long_prefix", [int(x) for x in np.random.default_rng(9).integers(1, 30, 32)], 32, 8, 128, 16,
+     "fp8_e4m3", 2048),
 ]
+
+# cascade batches with at least 128 rows per kv head run the prefix pass on
+# the tcgen05 kernel unless it is switched off; every case runs both ways
+KERNELS = ["tcgen05", "mma_sync"]
 
 
 def make_case(case, seed):
@@ -68,40 +84,49 @@ def make_case(case, seed):
     return workloads.make_workload(name, lens, Hq, Hkv, d, bs, dt, seed=seed, prefix_tokens=ptok)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
-def test_cascade_matches_plain_decode(pkv, case):
+def test_cascade_matches_plain_decode(pkv, case, kernel):
     w = make_case(case, 71)
     kc, vc = gpu_caches(pkv, w)
     okc, ovc = oracle_caches(w)
     ref = plain_ref(w, okc, ovc)
     P = w.shared_prefix_blocks
     # the whole shared prefix, a part of it, and none (plain decode)
-    for pb in sorted({P, max(P // 2, 1), 1, 0}):
-        got = run_cascade(pkv, w, kc, vc, pb)
-        assert_close(got, ref, TOL[w.cache_dtype], f"{case[0]} prefix_blocks={pb}")
+    with pkv.tcgen05(kernel == "tcgen05"):
+        for pb in sorted({P, max(P // 2, 1), 1, 0}):
+            got = run_cascade(pkv, w, kc, vc, pb)
+            assert_close(got, ref, TOL[w.cache_dtype], f"{case[0]} prefix_blocks={pb}")
     assert pkv.get_device_error() == 0
 
 
-def test_sequences_shorter_than_the_prefix(pkv):
+# sequence counts of the edge-case tests: a few rows (mma.sync prefix pass)
+# and, repeating the lengths, at least 128 rows per kv head (tcgen05)
+REPEATS = [1, 32]
+
+
+@pytest.mark.parametrize("repeat", REPEATS)
+def test_sequences_shorter_than_the_prefix(pkv, repeat):
     """Sequences that end inside the prefix, at its end or are empty attend
     only their own tokens of it; their suffix is empty, so their row is the
     prefix partial alone."""
-    w = make_case(("short", [5, 9, 1, 30, 2], 32, 8, 128, 16, "bf16", 128), 72)
-    lens = torch.tensor([3, 128, 0, 77, 129], dtype=torch.int32)
+    w = make_case(("short", [5, 9, 1, 30, 2] * repeat, 32, 8, 128, 16, "bf16", 128), 72)
+    lens = torch.tensor([3, 128, 0, 77, 129] * repeat, dtype=torch.int32)
     kc, vc = gpu_caches(pkv, w)
     okc, ovc = oracle_caches(w)
     got = run_cascade(pkv, w, kc, vc, w.shared_prefix_blocks, seq_lens=lens)
     ref = plain_ref(w, okc, ovc, seq_lens=lens)
     assert_close(got, ref, TOL["bf16"], "short sequences")
-    assert np.all(got[2] == 0.0)
+    assert np.all(got[2::5] == 0.0)
     assert pkv.get_device_error() == 0
 
 
-def test_prefix_tail_nobody_attends_is_never_used(pkv):
+@pytest.mark.parametrize("repeat", REPEATS)
+def test_prefix_tail_nobody_attends_is_never_used(pkv, repeat):
     """Every sequence ends inside the prefix: the prefix tokens past the
     longest one are NaN in both caches and must not reach any output."""
-    w = make_case(("tail", [4, 4, 4], 16, 4, 128, 16, "bf16", 96), 73)
-    lens = torch.tensor([20, 51, 7], dtype=torch.int32)
+    w = make_case(("tail", [4, 4, 4] * repeat, 16, 4, 128, 16, "bf16", 96), 73)
+    lens = torch.tensor([20, 51, 7] * repeat, dtype=torch.int32)
     kc, vc = gpu_caches(pkv, w)
     okc, ovc = oracle_caches(w)
     bs = w.block_size
@@ -116,14 +141,15 @@ def test_prefix_tail_nobody_attends_is_never_used(pkv):
     assert pkv.get_device_error() == 0
 
 
-def test_table_that_disagrees_on_the_prefix_is_flagged(pkv):
+@pytest.mark.parametrize("repeat", REPEATS)
+def test_table_that_disagrees_on_the_prefix_is_flagged(pkv, repeat):
     """A sequence whose table names another block for a prefix block it
     attends is flagged; entries past a short sequence's end are not
     compared."""
-    w = make_case(("mismatch", [10, 20, 30], 32, 8, 128, 16, "bf16", 64), 74)
+    w = make_case(("mismatch", [10, 20, 30] * repeat, 32, 8, 128, 16, "bf16", 64), 74)
     kc, vc = gpu_caches(pkv, w)
     okc, ovc = oracle_caches(w)
-    lens = torch.tensor([74, 20, 94], dtype=torch.int32)  # sequence 1 ends in prefix block 1
+    lens = torch.tensor([74, 20, 94] * repeat, dtype=torch.int32)  # sequence 1 ends in prefix block 1
     tables = w.block_tables.clone()
     tables[1, 2] = workloads.UNUSED_TABLE_ENTRY  # past its end: not read, not compared
     tables[1, 3] = workloads.UNUSED_TABLE_ENTRY
@@ -176,8 +202,11 @@ def test_prefix_fp8_full_size(pkv):
     prefix): every output row against the oracle's plain decode."""
     w = workloads.CONFIGS["prefix_fp8"]()
     kc, vc = gpu_caches(pkv, w)
-    got = run_cascade(pkv, w, kc, vc, w.shared_prefix_blocks)
     okc, ovc = oracle_caches(w)
     ref = oracle_decode(w, okc, ovc, threads=os.cpu_count() or 4)
+    got = run_cascade(pkv, w, kc, vc, w.shared_prefix_blocks)  # the prefix pass the benchmark times (tcgen05)
     assert_close(got, ref, TOL[w.cache_dtype], "prefix_fp8 cascade")
+    with pkv.tcgen05(False):
+        got = run_cascade(pkv, w, kc, vc, w.shared_prefix_blocks)
+    assert_close(got, ref, TOL[w.cache_dtype], "prefix_fp8 cascade (mma.sync prefix pass)")
     assert pkv.get_device_error() == 0

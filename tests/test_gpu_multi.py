@@ -52,22 +52,40 @@ CASES = [
     ("bf16_g8_bs8", [9, 130], [2, 33], 16, 2, 128, 8, "bf16"),
     ("bf16_g1_bs32", [31, 77, 150], [5, 1, 64], 4, 4, 128, 32, "bf16"),
     ("bf16_g8_long", [3000, 2500], [3, 16], 64, 8, 128, 16, "bf16"),
+    ("fp8_chunks_d128", [700, 90, 300], [200, 90, 1], 32, 8, 128, 16, "fp8_e4m3"),
+    ("fp8_bs8_chunk", [130, 77], [64, 40], 16, 2, 128, 8, "fp8_e4m3"),
+    # fewer than 128 rows per (sequence, kv head), blocks of 32: only the
+    # tcgen05 kernel has an fp8 instance, so it serves the call
+    ("fp8_bs32_small", [70, 33, 5], [3, 9, 5], 32, 8, 128, 32, "fp8_e4m3"),
 ]
 
 
+# calls with at least 128 rows per (sequence, kv head) run the tcgen05 kernel
+# (bf16, and fp8 with head_dim 128) unless it is switched off; every case runs
+# both ways
+KERNELS = ["tcgen05", "mma_sync"]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
-def test_multi_matches_oracle(pkv, case):
+def test_multi_matches_oracle(pkv, case, kernel):
     name, lens, q_lens, Hq, Hkv, d, bs, dt = case
     w = workloads.make_workload(name, lens, Hq, Hkv, d, bs, dt, seed=81 + len(lens))
     q, q_start = workloads.chunk_queries(w, q_lens, seed=82)
     kc, vc = gpu_caches(pkv, w)
     okc, ovc = oracle_caches(w)
     ref = multi_ref(w, okc, ovc, q, q_start)
-    got = run_multi(pkv, w, kc, vc, q, q_start)
-    assert_close(got, ref, TOL[dt], name)
-    # a larger bound on the rows per sequence changes the grid, not the result
-    got2 = run_multi(pkv, w, kc, vc, q, q_start, max_q=max(q_lens) + 37)
-    assert_close(got2, ref, TOL[dt], name + " (max_q larger)")
+    if kernel == "mma_sync" and dt == "fp8_e4m3" and bs != 16:
+        # the mma.sync kernels serve fp8 caches of 16-token blocks only
+        with pkv.tcgen05(False), pytest.raises(pkv.PkvError, match="UNSUPPORTED"):
+            run_multi(pkv, w, kc, vc, q, q_start)
+        return
+    with pkv.tcgen05(kernel == "tcgen05"):
+        got = run_multi(pkv, w, kc, vc, q, q_start)
+        assert_close(got, ref, TOL[dt], name)
+        # a larger bound on the rows per sequence changes the grid, not the result
+        got2 = run_multi(pkv, w, kc, vc, q, q_start, max_q=max(q_lens) + 37)
+        assert_close(got2, ref, TOL[dt], name + " (max_q larger)")
     assert pkv.get_device_error() == 0
 
 
@@ -102,6 +120,51 @@ def test_multi_rows_beyond_the_bound_are_flagged(pkv):
     assert np.isnan(got[3:]).all()
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_multi_long_chunk_beyond_the_bound_is_flagged(pkv, kernel):
+    """The same with chunks long enough for the tcgen05 kernel (at least 128
+    rows per sequence and kv head)."""
+    w = workloads.make_workload("bad_long", [200, 300, 150], 32, 8, 128, 16, "bf16", seed=97)
+    q, q_start = workloads.chunk_queries(w, [40, 90, 33], seed=98)
+    kc, vc = gpu_caches(pkv, w)
+    okc, ovc = oracle_caches(w)
+    ref = multi_ref(w, okc, ovc, q, q_start)
+    assert pkv.get_device_error() == 0
+    with pkv.tcgen05(kernel == "tcgen05"):
+        got = run_multi(pkv, w, kc, vc, q, q_start, max_q=64)  # sequence 1 has 90 > 64
+    assert pkv.get_device_error() & pkv.DEVERR_BAD_SEQ_LEN
+    assert_close(got[:40], ref[:40], TOL["bf16"], "sequence 0")
+    assert np.isnan(got[40:130]).all()
+    assert_close(got[130:], ref[130:], TOL["bf16"], "sequence 2")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_multi_bad_block_ids_are_masked(pkv, kernel):
+    """A table entry outside the pool is flagged and its positions are left
+    out, by either kernel: the rows equal the oracle's over a table whose
+    bad block is dropped from the attended positions."""
+    w = workloads.make_workload("badid", [100, 180], 32, 8, 128, 16, "bf16", seed=99)
+    q, q_start = workloads.chunk_queries(w, [40, 64], seed=100)
+    kc, vc = gpu_caches(pkv, w)
+    tables = w.block_tables.clone()
+    tables[1, 2] = w.num_blocks + 5  # positions 32..47 of sequence 1
+    assert pkv.get_device_error() == 0
+    with pkv.tcgen05(kernel == "tcgen05"):
+        got = run_multi(pkv, w, kc, vc, q, q_start, tables=tables)
+    assert pkv.get_device_error() & pkv.DEVERR_BAD_BLOCK_ID
+    okc, ovc = oracle_caches(w)
+    ref = multi_ref(w, okc, ovc, q, q_start)
+    assert_close(got[:40], ref[:40], TOL["bf16"], "sequence 0 untouched by the bad id")
+    assert np.isfinite(got[40:]).all()
+
+
+def test_tcgen05_switch(pkv):
+    assert pkv.get_tcgen05()
+    with pkv.tcgen05(False):
+        assert not pkv.get_tcgen05()
+    assert pkv.get_tcgen05()
+
+
 def test_multi_invalid_calls(pkv):
     w = workloads.make_workload("inv", [8, 9], 8, 2, 64, 16, "f32", seed=95)
     q, q_start = workloads.chunk_queries(w, [2, 2], seed=96)
@@ -114,12 +177,17 @@ def test_multi_invalid_calls(pkv):
 
 @pytest.mark.parametrize("which", ["verify4_llama3_8b", "prefill_chunk512"])
 def test_multi_full_size(pkv, which):
-    """The multi-token workloads the benchmark times, every row against the
-    (multi-threaded) oracle."""
+    """The multi-token workloads the benchmark times (in the kernel it times:
+    tcgen05 for the prefill chunks), every row against the (multi-threaded)
+    oracle; the prefill chunks also through the mma.sync kernel."""
     w, q, q_start = workloads.MULTI_CONFIGS[which]()
     kc, vc = gpu_caches(pkv, w)
     okc, ovc = oracle_caches(w)
-    got = run_multi(pkv, w, kc, vc, q, q_start)
     ref = multi_ref(w, okc, ovc, q, q_start, threads=os.cpu_count() or 4)
+    got = run_multi(pkv, w, kc, vc, q, q_start)
     assert_close(got, ref, TOL[w.cache_dtype], which)
+    if which == "prefill_chunk512":
+        with pkv.tcgen05(False):
+            got = run_multi(pkv, w, kc, vc, q, q_start)
+        assert_close(got, ref, TOL[w.cache_dtype], which + " (mma.sync)")
     assert pkv.get_device_error() == 0

@@ -495,3 +495,18 @@ def test_sliding_window_never_reads_blocks_left_out(pkv, engine, pt):
                                max_seq_len=w.max_seq_len, partition_tokens=pt, window=window, sinks=sinks)
     assert pkv.get_device_error() == 0
     assert_close(out.float().cpu().numpy().astype(np.float64), ref, TOL["bf16"], "window with freed blocks")
+
+
+# ------------------------------------------------------------------ failure path of the bounded waits
+def test_bounded_wait_gives_up_and_the_context_stays_usable(pkv):
+    """A wait on an mbarrier whose bytes never arrive (no copy is issued, so
+    none is left in flight) gives up after its probe limit, sets
+    DEVERR_WAIT_TIMEOUT and returns; the next decode still matches the
+    oracle and raises nothing."""
+    assert pkv.get_device_error() == 0
+    pkv.selftest_wait_timeout()
+    assert pkv.get_device_error() == pkv.DEVERR_WAIT_TIMEOUT
+    w = workloads.make_workload("after_timeout", [1, 40, 300], 32, 8, 128, 16, "bf16", seed=111)
+    kc, vc = gpu_caches(pkv, w)
+    assert_close(run_decode(pkv, w, kc, vc), oracle_decode(w), TOL["bf16"], "decode after the timeout")
+    assert pkv.get_device_error() == 0

@@ -1,10 +1,14 @@
 """The allocation-free decode entry point, through the C ABI.
 
 pkv_paged_attention_decode_noalloc serves callers that cannot allocate
-device memory (it keeps its scratch in a fixed array the library reserves
-per GPU).  It must give what pkv_paged_attention_decode gives with a
-caller-provided workspace, call after call: the scratch keeps the previous
-call's contents, so two calls in a row are checked.  This file is collected
+device memory: a plugin inside a serving runtime that has reserved all of
+the GPU's memory for its own pool, plain C code that is handed tensor
+pointers but no allocator, or a latency-critical loop that must not touch
+one.  It keeps its scratch in a fixed array the library reserves on each GPU,
+and that array keeps the previous call's contents.  Every output is compared
+with the oracle, call after call, in an order where a later call's merge
+counters lie on bytes where an earlier call left partial results (so the
+clearing at the start of each call is exercised).  This file is collected
 last so that a stop-at-first-failure run has already run everything else.
 """
 from __future__ import annotations
@@ -16,6 +20,7 @@ import pytest
 import torch
 
 import workloads
+from tests._util import oracle_caches, oracle_decode
 
 pytestmark = pytest.mark.gpu
 
@@ -42,36 +47,43 @@ def _setup(pkv, w):
     return kc, vc
 
 
-@pytest.mark.parametrize("name,lens,Hq,Hkv,d,dt", [
-    ("gqa4_bf16", [1, 17, 300, 1200, 2048, 64], 32, 8, 128, "bf16"),
-    ("gqa8_fp8", [5, 700, 1500], 64, 8, 128, "fp8_e4m3"),
-    ("mha_f32", [1, 17, 33, 100], 4, 4, 64, "f32"),
-])
-def test_noalloc_matches_workspace_entry_point_twice(name, lens, Hq, Hkv, d, dt):
+# In this order on the one scratch array: "long" cuts its 16 segments between
+# most warps of the grid, so partial slots fill the scratch from byte 256 on;
+# "wide" has 32,000 segments, whose counters (128,000 bytes) cover those
+# slots, and its cut segments are among the last ones.
+CASES = [
+    ("long_gqa4_bf16", [6000, 5000], 32, 8, 128, 16, "bf16"),
+    ("wide_gqa4_bf16", [1] * 3700 + [48] * 300, 32, 8, 64, 16, "bf16"),
+    ("gqa8_fp8", [5, 700, 1500], 64, 8, 128, 16, "fp8_e4m3"),
+    ("mha_f32", [1, 17, 33, 100], 4, 4, 64, 16, "f32"),
+    ("long_again", [6000, 5000], 32, 8, 128, 16, "bf16"),
+]
+
+
+def test_noalloc_matches_oracle_call_after_call():
     import paged_kv_cache_22_gb300 as pkv
     fn = _noalloc_fn(pkv)
-    w = workloads.make_workload(name, lens, Hq, Hkv, d, 16, dt, seed=99)
-    kc, vc = _setup(pkv, w)
-    q, tables, seq_lens = w.q.to(DEV), w.block_tables.to(DEV), w.seq_lens.to(DEV)
-    ref = torch.empty_like(q)
-    pkv.paged_attention_decode(ref, q, kc, vc, tables, seq_lens, w.scale, w.kv_scale,
-                               max_seq_len=w.max_seq_len, partition_tokens=0)
-    desc = pkv.CacheDesc(w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim,
-                         {"f32": 0, "bf16": 1, "fp8_e4m3": 2}[dt])
-    qdt = 0 if dt == "f32" else 1
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    for call in range(2):
-        out = torch.full_like(q, float("nan"))
-        st = fn(out.data_ptr(), q.data_ptr(), qdt, w.num_seqs, w.num_q_heads, kc.data_ptr(),
-                vc.data_ptr(), ctypes.byref(desc), tables.data_ptr(), w.max_blocks_per_seq,
-                seq_lens.data_ptr(), w.max_seq_len, w.scale, w.kv_scale, stream)
-        assert st == 0, f"call {call}: status {st}"
-        torch.cuda.synchronize()
-        got = out.float().cpu().numpy()
-        want = ref.float().cpu().numpy()
-        assert np.isfinite(got).all(), f"call {call}: unwritten output"
-        err = float(np.abs(got - want).max())
-        assert err <= TOL[dt], f"call {call}: max |noalloc - workspace| = {err}"
+    for i, (name, lens, Hq, Hkv, d, bs, dt) in enumerate(CASES):
+        w = workloads.make_workload(name, lens, Hq, Hkv, d, bs, dt, seed=99 + i)
+        kc, vc = _setup(pkv, w)
+        okc, ovc = oracle_caches(w)
+        ref = oracle_decode(w, okc, ovc, threads=4)
+        q, tables, seq_lens = w.q.to(DEV), w.block_tables.to(DEV), w.seq_lens.to(DEV)
+        desc = pkv.CacheDesc(w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim,
+                             {"f32": 0, "bf16": 1, "fp8_e4m3": 2}[dt])
+        qdt = 0 if dt == "f32" else 1
+        for call in range(2):
+            out = torch.full_like(q, float("nan"))
+            st = fn(out.data_ptr(), q.data_ptr(), qdt, w.num_seqs, w.num_q_heads, kc.data_ptr(),
+                    vc.data_ptr(), ctypes.byref(desc), tables.data_ptr(), w.max_blocks_per_seq,
+                    seq_lens.data_ptr(), w.max_seq_len, w.scale, w.kv_scale, stream)
+            assert st == 0, f"{name} call {call}: status {st}"
+            torch.cuda.synchronize()
+            got = out.float().cpu().numpy().astype(np.float64)
+            assert np.isfinite(got).all(), f"{name} call {call}: unwritten output"
+            err = float(np.abs(got - ref).max())
+            assert err <= TOL[dt], f"{name} call {call}: max |noalloc - oracle| = {err}"
     assert pkv.get_device_error() == 0
 
 
