@@ -87,6 +87,16 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def tensor_peak():
+    """Dense bf16 tensor-core peak (TFLOP/s): the measured cuBLAS burst figure."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (cuBLAS bf16 burst)"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -312,6 +322,7 @@ def run_gpu(args):
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(pkv, w, kc, vc, dev, pt, max(10, min(K, 200)), flush, win, sinks, pblocks)
     e2e["ms_per_step"] = max_over_ranks(e2e["ms_per_step"], dev)
+    e2e["host_ms_per_step"] = max_over_ranks(e2e["host_ms_per_step"], dev)
     e2e_value = job_throughput(ws, dec_b + rc_b, e2e["ms_per_step"])
 
     traffic = None
@@ -319,6 +330,11 @@ def run_gpu(args):
             and args.engine == "tensor_cores" and not win and not pblocks):
         traffic = TRAFFIC["bytes_per_launch"]
 
+    # the kernel of the cascade's prefix pass (tcgen05 once a kv head has 128 rows)
+    prefix_kernel = ("attn_tc05_kernel (tcgen05.mma, S and O in TMEM)"
+                     if pblocks and pkv.get_tcgen05() and w.head_dim == 128
+                     and w.num_seqs * (w.num_q_heads // w.num_kv_heads) >= 128
+                     else "prefix_attention_kernel")
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -343,7 +359,7 @@ def run_gpu(args):
             **({"window": win, "sinks": sinks,
                 "step_launches": "kv_reshape_and_cache, then the windowed decode"} if win else {}),
             **({"cascade": {"prefix_blocks": pblocks,
-                            "step_launches": "kv_reshape_and_cache, prefix_attention_kernel, decode_tc_kernel",
+                            "step_launches": f"kv_reshape_and_cache, {prefix_kernel}, decode_tc_kernel",
                             "metric_bytes": "logical: every sequence's prefix counted (as plain decode reads it)",
                             "roofline_bytes": "unique: the shared prefix once"}} if pblocks else {}),
             "engine": ("cuda_cores" if w.cache_dtype == "f32" else args.engine)
@@ -363,23 +379,168 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": ("prefix_attention_kernel + decode_tc_kernel (cascade, both launches)"
+                     "kernel": (f"{prefix_kernel} + decode_tc_kernel (cascade, both launches)"
                                 if pblocks else
                                 ("decode_tc_kernel" if w.cache_dtype != "f32" and args.engine == "tensor_cores"
                                  else "decode_kernel")
                                 + (" (balanced split)" if pt == 0 else " (partitions)"))},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-                "ms_per_step": round(e2e["ms_per_step"], 6)},
+                "ms_per_step": round(e2e["ms_per_step"], 6),
+                "host_wall": {"ms_per_step": round(e2e["host_ms_per_step"], 6),
+                              "value": round(job_throughput(ws, dec_b + rc_b, e2e["host_ms_per_step"]), 1),
+                              "what": "host clock from the first call of a step until its output "
+                                      "is on the host (binding, C ABI, launches, copies, GPU time)"}},
         "gpu_launches": K * (3 if pblocks else (2 if pt == 0 else 3)),
         "clocks": clocks,
     }
+    if (ws == 1 and args.config == "llama3_8b" and pt == 0 and not win and not pblocks
+            and args.engine == "tensor_cores" and not args.no_per_config):
+        line["per_config"] = per_config(pkv, dev, flush, min(K, 50), dec_avg_ms)
+        if pkv.get_device_error():
+            raise RuntimeError("device error in the per-config measurements")
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, win, sinks)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+def time_calls(fn, flush, stream, K: int, warmup: int = 3) -> float:
+    """Mean device time (ms) of `fn` over K calls, each after an L2 flush,
+    with CUDA events on the launching stream."""
+    for i in range(warmup):
+        flush(i)
+        fn()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for i in range(K):
+        flush(i)
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return sum(e[0].elapsed_time(e[1]) for e in ev) / K
+
+
+def per_config(pkv, dev, flush, K: int, main_decode_ms: float):
+    """Decode-only figures of the other workloads, measured in this process
+    with the same flush and events: each entry gives the time per call, the
+    algorithmic GB/s (TFLOP/s for prefill chunks) and its fraction of the
+    measured and nominal peaks.  Also the paged-vs-contiguous control
+    (identity block tables) and block sizes 8 and 32 on the Llama-3-8B-shaped
+    batch, and the multi-token workloads on both of their kernels."""
+    stream = torch.cuda.current_stream()
+    hbm_peak, _ = measured_peak()
+    tc_peak = tensor_peak()[0]
+    res = {}
+
+    def caches(w):
+        shape = workloads.cache_shape(w)
+        cdt = workloads.cache_torch_dtype(w.cache_dtype)
+        kc = torch.zeros(shape, dtype=cdt, device=dev)
+        vc = torch.zeros(shape, dtype=cdt, device=dev)
+        k, v, sl = w.all_tokens()
+        pkv.kv_reshape_and_cache(k.to(dev), v.to(dev), kc, vc, sl.to(dev), w.kv_scale)
+        return kc, vc
+
+    def hbm_entry(ms, nbytes, kernel, extra=None):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        e = {"ms": round(ms, 6), "bytes": nbytes, "gbs": round(gbs, 1),
+             "frac_of_measured": round(gbs / hbm_peak, 4), "frac_of_8TBs": round(gbs / NOMINAL_HBM_GBS, 4),
+             "kernel": kernel}
+        e.update(extra or {})
+        return e
+
+    def decode_entries(name, w, variants):
+        kc, vc = caches(w)
+        q = w.q.to(dev)
+        out = torch.empty_like(q)
+        tables, lens = w.block_tables.to(dev), w.seq_lens.to(dev)
+        wsp = pkv.DecodeWorkspace(dev)
+        lens_l = w.seq_lens.tolist()
+        for tag, pt, win, sinks, pblocks in variants:
+            def call():
+                if pblocks:
+                    pkv.cascade_decode(out, q, kc, vc, tables, lens, pblocks, w.scale, w.kv_scale,
+                                       max_seq_len=w.max_seq_len, workspace=wsp)
+                else:
+                    pkv.paged_attention_decode(out, q, kc, vc, tables, lens, w.scale, w.kv_scale,
+                                               max_seq_len=w.max_seq_len, partition_tokens=pt,
+                                               workspace=wsp, window=win, sinks=sinks)
+            ms = time_calls(call, flush, stream, K)
+            nbytes = metrics.decode_bytes(lens_l, w.num_q_heads, w.num_kv_heads, w.head_dim, w.cache_dtype,
+                                          w.q_dtype, w.block_size, win, sinks)
+            extra = {"tok_s_per_layer": round(w.num_seqs / (ms * 1e-3), 1)}
+            if pblocks:
+                ub = metrics.cascade_bytes(lens_l, pblocks * w.block_size, w.num_q_heads, w.num_kv_heads,
+                                           w.head_dim, w.cache_dtype, w.q_dtype, w.block_size)
+                ugbs = ub / (ms * 1e-3) / 1e9
+                e = {"ms": round(ms, 6), "bytes": nbytes, "logical_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                     "unique_bytes": ub, "unique_gbs": round(ugbs, 1),
+                     "unique_frac_of_measured": round(ugbs / hbm_peak, 4),
+                     "kernel": "prefix pass (attn_tc05_kernel once a kv head has >= 128 rows, else "
+                               "prefix_attention_kernel) + decode_tc_kernel", **extra}
+            else:
+                kern = "decode_kernel (CUDA cores)" if w.cache_dtype == "f32" else "decode_tc_kernel"
+                kern += " + split_kv_reduce_kernel (fixed partitions)" if pt else " (balanced split)"
+                e = hbm_entry(ms, nbytes, kern, extra)
+            if win:
+                e["window"], e["sinks"] = win, sinks
+            res[name + tag] = e
+        del kc, vc
+        torch.cuda.empty_cache()
+
+    decode_entries("llama70b_128", workloads.llama70b_128(seed=1236), [("", 0, 0, 0, 0)])
+    decode_entries("long_split_kv", workloads.long_split_kv(seed=1237),
+                   [("", 0, 0, 0, 0), ("_partitions512", 512, 0, 0, 0), ("_window4096_sinks4", 0, 4096, 4, 0)])
+    pf = workloads.prefix_fp8(seed=1238)
+    decode_entries("prefix_fp8", pf, [("", 0, 0, 0, 0), ("_cascade", 0, 0, 0, pf.shared_prefix_blocks)])
+    decode_entries("tiny_mha", workloads.tiny_mha(seed=1234), [("", 0, 0, 0, 0)])
+    decode_entries("llama3_8b_identity_tables", workloads.llama3_8b(seed=1235, identity_tables=True),
+                   [("", 0, 0, 0, 0)])
+    for bsz in (8, 32):
+        decode_entries(f"llama3_8b_block{bsz}", workloads.llama3_8b(seed=1235, block_size=bsz), [("", 0, 0, 0, 0)])
+    ident = res["llama3_8b_identity_tables"]["ms"]
+    res["paged_vs_contiguous"] = {
+        "shuffled_ms": round(main_decode_ms, 6), "identity_ms": ident,
+        "ratio": round(main_decode_ms / ident, 4),
+        "what": "the llama3_8b decode over a shuffled pool vs the same batch with block tables dealt in order"}
+
+    for mname in ("verify4_llama3_8b", "prefill_chunk512"):
+        w, q_cpu, qs_cpu = workloads.MULTI_CONFIGS[mname](seed=1301 + list(workloads.MULTI_CONFIGS).index(mname))
+        kc, vc = caches(w)
+        q, qs = q_cpu.to(dev), qs_cpu.to(dev)
+        out = torch.empty_like(q)
+        tables, lens = w.block_tables.to(dev), w.seq_lens.to(dev)
+        q_lens = (qs_cpu[1:] - qs_cpu[:-1]).tolist()
+        max_q = max(q_lens)
+        wsp = pkv.DecodeWorkspace(dev)
+        lens_l = w.seq_lens.tolist()
+        nbytes = metrics.multi_bytes(lens_l, q_lens, w.num_q_heads, w.num_kv_heads, w.head_dim, w.cache_dtype,
+                                     w.q_dtype, w.block_size)
+        flops = metrics.multi_flops(lens_l, q_lens, w.num_q_heads, w.head_dim)
+        rows = max_q * (w.num_q_heads // w.num_kv_heads)
+
+        def call():
+            pkv.paged_attention_multi(out, q, qs, kc, vc, tables, lens, w.scale, w.kv_scale, max_q=max_q,
+                                      max_seq_len=w.max_seq_len, workspace=wsp)
+        # both kernels where the tcgen05 one applies (a (sequence, kv head) of >= 128 rows)
+        for tag, tc in (("", True), ("_mma_sync", False)) if rows >= 128 else (("", False),):
+            with pkv.tcgen05(tc):
+                ms = time_calls(call, flush, stream, K)
+            kern = ("attn_tc05_kernel (tcgen05.mma, S and O in TMEM)" if tc
+                    else "prefix_attention_kernel (MULTI, mma.sync m16n8k16)")
+            if mname == "prefill_chunk512":
+                tf = flops / (ms * 1e-3) / 1e12
+                res[mname + tag] = {"ms": round(ms, 6), "flop": flops, "tflops": round(tf, 2),
+                                    "frac_of_bf16_peak": round(tf / tc_peak, 4), "kernel": kern}
+            else:
+                res[mname + tag] = hbm_entry(ms, nbytes, kern)
+        del kc, vc
+        torch.cuda.empty_cache()
+    return res
 
 
 class StagedInputs:
@@ -440,16 +601,19 @@ def run_e2e(pkv, w, kc, vc, dev, pt, steps, flush, window=0, sinks=0, prefix_blo
     for _ in range(3):
         one()
     torch.cuda.synchronize()
-    tot = 0.0
+    tot, host = 0.0, 0.0
     for i in range(steps):
         flush(i)
+        torch.cuda.synchronize()  # the flush is not part of the host-side time either
+        t0 = time.perf_counter()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         one()
         b.record(stream)
         b.synchronize()
+        host += time.perf_counter() - t0
         tot += a.elapsed_time(b)
-    return {"ms_per_step": tot / steps, "h2d": h2d, "d2h": d2h}
+    return {"ms_per_step": tot / steps, "host_ms_per_step": host * 1e3 / steps, "h2d": h2d, "d2h": d2h}
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -478,24 +642,32 @@ def oracle_sample(w, max_seqs=None):
 
 def cpu_baseline(w, seconds: float, window: int = 0, sinks: int = 0):
     """The oracle, as it stands, timed on this host's cores: repeated full
-    decode steps (cache write of the new tokens + attention) for ~`seconds`."""
+    decode steps (cache write of the new tokens + attention) for ~`seconds`
+    on every core, then for ~`seconds` / 2 on one thread."""
     import oracle
     q, kc, vc, tables, lens, nk, nv, ns, B = oracle_sample(w)
-    threads = os.cpu_count() or 1
     dec_b, rc_b = step_bytes(w, window, sinks)
-    reps, t0 = 0, time.perf_counter()
-    while True:
-        oracle.reshape_and_cache(nk, nv, kc, vc, ns, w.kv_scale)
-        oracle.paged_attention_decode(q, kc, vc, tables, lens, w.scale, w.kv_scale, threads,
-                                      window=window, sinks=sinks)
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= seconds or reps >= 1000:
-            break
+
+    def timed(threads, budget):
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            oracle.reshape_and_cache(nk, nv, kc, vc, ns, w.kv_scale)
+            oracle.paged_attention_decode(q, kc, vc, tables, lens, w.scale, w.kv_scale, threads,
+                                          window=window, sinks=sinks)
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= budget or reps >= 1000:
+                return reps, el
+
+    threads = os.cpu_count() or 1
+    reps, el = timed(threads, seconds)
+    reps1, el1 = timed(1, seconds / 2)
     return {"value": round(reps * (dec_b + rc_b) / el / 1e9, 3), "unit": "GB/s", "cores": threads,
             "kind": "oracle",
             "sample": f"{reps} full decode steps of the same workload ({B} seqs), fp64 C loops, "
-                      f"{el:.1f} s wall"}
+                      f"{el:.1f} s wall",
+            "single_thread": {"value": round(reps1 * (dec_b + rc_b) / el1 / 1e9, 3), "unit": "GB/s", "cores": 1,
+                              "sample": f"{reps1} full decode steps on one thread, {el1:.1f} s wall"}}
 
 
 def run_reference(args):
@@ -649,6 +821,11 @@ def run_multi(args):
     tables, lens = w.block_tables.to(dev), w.seq_lens.to(dev)
     q_lens = (qs_cpu[1:] - qs_cpu[:-1]).tolist()
     max_q = max(q_lens)
+    # the kernel pkv_paged_attention_multi runs on this workload
+    tc05 = (pkv.get_tcgen05() and (w.cache_dtype == "bf16" or w.head_dim == 128)
+            and max_q * (w.num_q_heads // w.num_kv_heads) >= 128)
+    multi_kernel = ("attn_tc05_kernel (tcgen05.mma, S and O in TMEM)" if tc05
+                    else "prefix_attention_kernel (MULTI), mma.sync m16n8k16")
     out = torch.empty_like(q)
     workspace = pkv.DecodeWorkspace(dev)
     flush = L2Flush(dev)
@@ -711,11 +888,7 @@ def run_multi(args):
     e2e_ms = max_over_ranks(tot / n_e2e, dev)
 
     hbm_peak, hbm_src = measured_peak()
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            tc_peak, tc_src = float(json.load(f)["bf16_tflops"]), "measured (cuBLAS bf16 burst)"
-    except (OSError, KeyError, ValueError):
-        tc_peak, tc_src = 1900.0, "fallback"
+    tc_peak, tc_src = tensor_peak()
     unit = "TFLOP/s" if compute else "GB/s"
     value = tflops if compute else gbs
     e2e_value = (ws * flops / (e2e_ms * 1e-3) / 1e12) if compute else (ws * nbytes / (e2e_ms * 1e-3) / 1e9)
@@ -736,10 +909,10 @@ def run_multi(args):
         "gbs": round(gbs, 1), "tflops": round(tflops, 3),
         "roofline": ({"bound": "tensor", "achieved": round(tflops, 2), "peak": tc_peak, "peak_source": tc_src,
                       "unit": "TFLOP/s", "frac": round(tflops / tc_peak, 4), "traffic": None,
-                      "kernel": "prefix_attention_kernel (MULTI), mma.sync m16n8k16"} if compute else
+                      "kernel": multi_kernel} if compute else
                      {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "peak_source": hbm_src,
                       "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "traffic": None,
-                      "kernel": "prefix_attention_kernel (MULTI)"}),
+                      "kernel": multi_kernel}),
         "e2e": {"value": round(e2e_value, 2 if compute else 1), "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 6)},
         "gpu_launches": K, "clocks": clocks,
@@ -790,6 +963,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seqs", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the other workloads' decode-only figures of the default run")
     ap.add_argument("--engine", choices=["tensor_cores", "cuda_cores"], default="tensor_cores",
                     help="units that run q.K and P.V for bf16 / fp8 caches")
     ap.add_argument("--window", type=int, default=0,

@@ -199,12 +199,16 @@ def tiny_mha(seed: int = 1234) -> Workload:
                          num_blocks=64)
 
 
-def llama3_8b(seed: int = 1235, num_seqs: int = 64) -> Workload:
+def llama3_8b(seed: int = 1235, num_seqs: int = 64, block_size: int = 16,
+              identity_tables: bool = False) -> Workload:
     """Llama-3-8B-shaped decode layer: 32 q / 8 kv heads, head_dim 128, bf16,
-    seq_lens uniform in [128, 2048], 16384-block shuffled pool."""
+    seq_lens uniform in [128, 2048], 16384-block shuffled pool.  Other block
+    sizes keep the pool's token capacity (262,144 tokens); identity tables
+    deal the pool in order (the contiguous control)."""
     gen = torch.Generator().manual_seed(seed + 100_000)
     lens = torch.randint(128, 2049, (num_seqs,), generator=gen).tolist()
-    return make_workload("llama3_8b", lens, 32, 8, 128, 16, "bf16", seed=seed, num_blocks=16384)
+    return make_workload("llama3_8b", lens, 32, 8, 128, block_size, "bf16", seed=seed,
+                         num_blocks=16384 * 16 // block_size, identity_tables=identity_tables)
 
 
 def llama70b_128(seed: int = 1236, num_seqs: int = 128, sigma: float = 1.0) -> Workload:
