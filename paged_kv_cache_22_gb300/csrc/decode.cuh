@@ -69,7 +69,7 @@ struct Geo {
   static constexpr int PPL = (TB / 2) / TG;            // token pairs per lane per step
   static constexpr int NSW0 = 16384 / (2 * TILE);
   static constexpr int NSW = NSW0 < 2 ? 2 : (NSW0 > 8 ? 8 : NSW0);  // stages per warp
-  static constexpr int SLOT = G * D + 2 * G;           // floats of one partial result
+  static constexpr int SLOT = partial_slot_floats(G, D);  // floats of one partial result
   static_assert(D % DL == 0 && 32 % C == 0 && R <= TB && TB % R == 0, "lane layout");
   static_assert(DL % VE == 0 && VE % 2 == 0, "vector layout");
   static_assert(TILE % 16 == 0, "bulk copies move multiples of 16 bytes");

@@ -51,7 +51,7 @@ struct DecodeArgs {
   float out_scale;   // 1 (kv_scale for fp8 caches)
   // balanced split
   int* counters;     // [num_seqs * units], zero between calls
-  float* partials;   // [2 * warps][G * D + 2 * G]
+  float* partials;   // [2 * warps][partial_slot_floats(G, D)]
   // fixed partitions
   int partition_blocks;
   int max_partitions;
@@ -146,6 +146,11 @@ inline bool remaps_blocks(int window, int skip_blocks) { return window > 0 || sk
 // Floats per row of a cascade's prefix partial: D of o, m, l, two of padding
 // (rows stay 16-byte aligned for bulk copies).
 __host__ __device__ constexpr int pre_row_floats(int D) { return D + 4; }
+
+// Floats of one balanced-split partial result: acc[G][D], m[G], l[G], padded
+// to a multiple of four so that every slot starts 16-byte aligned (the merge
+// reads the accumulators as float4).
+__host__ __device__ constexpr int partial_slot_floats(int G, int D) { return (G * D + 2 * G + 3) / 4 * 4; }
 
 // Logical block of the j-th block a sequence of length L reads.
 template <int BS>
@@ -338,7 +343,7 @@ __device__ __forceinline__ int unit_first_head(const DecodeArgs& a, const Walker
 template <int G, int D>
 __device__ __forceinline__ float* partial_slot(const DecodeArgs& a, const Walker& wk, int64_t gw, int64_t u0) {
   const int64_t slot = (wk.seg_u + wk.jb == u0) ? 2 * gw : 2 * gw + 1;
-  return a.partials + (size_t)slot * (G * D + 2 * G);
+  return a.partials + (size_t)slot * partial_slot_floats(G, D);
 }
 
 // ----------------------------------------------------------------------------
@@ -362,7 +367,7 @@ __device__ __forceinline__ CutPiece cut_piece_of(const Walker& wk) { return CutP
 template <class QT, int G, int D>
 __device__ __forceinline__ void merge_segment(const DecodeArgs& a, const CutPiece& cp, int64_t T, int64_t NW,
                                               int lane) {
-  constexpr int SLOT = G * D + 2 * G, DV = 4, SL = D / DV;
+  constexpr int SLOT = partial_slot_floats(G, D), DV = 4, SL = D / DV;
   constexpr int NB = G <= 2 ? 8 : (G == 4 ? 4 : 2);  // pieces loaded per round trip
   const int d0 = (lane % SL) * DV;
   // pieces sit on warps w_first..w_last; the first one's slot depends on

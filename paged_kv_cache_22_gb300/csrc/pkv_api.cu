@@ -117,7 +117,7 @@ size_t counter_region(int B, int units) {
 
 // Two partial-result slots per warp of the largest balanced grid.
 size_t balanced_workspace(int B, int units, int G, int D, int grid_max) {
-  return counter_region(B, units) + (size_t)2 * grid_max * kDecodeWarps * (G * D + 2 * G) * sizeof(float);
+  return counter_region(B, units) + (size_t)2 * grid_max * kDecodeWarps * partial_slot_floats(G, D) * sizeof(float);
 }
 
 size_t partition_workspace(int B, int Hq, int units, int D, int P) {

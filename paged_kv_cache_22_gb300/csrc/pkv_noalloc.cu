@@ -142,7 +142,7 @@ extern "C" pkv_status pkv_paged_attention_decode_noalloc(
 
   // scratch layout: [merge counters][two partial slots per warp]
   const size_t counter_bytes = round256((size_t)num_seqs * a.units * sizeof(int));
-  const size_t cta_bytes = (size_t)2 * kDecodeWarps * (G * D + 2 * G) * sizeof(float);
+  const size_t cta_bytes = (size_t)2 * kDecodeWarps * partial_slot_floats(G, D) * sizeof(float);
   if (counter_bytes + cta_bytes > PKV_NOALLOC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;  // beyond the fixed scratch
   const int64_t grid_fit = (int64_t)((PKV_NOALLOC_SCRATCH_BYTES - counter_bytes) / cta_bytes);
   if (grid > grid_fit) grid = grid_fit;

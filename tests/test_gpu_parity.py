@@ -510,3 +510,18 @@ def test_bounded_wait_gives_up_and_the_context_stays_usable(pkv):
     kc, vc = gpu_caches(pkv, w)
     assert_close(run_decode(pkv, w, kc, vc), oracle_decode(w), TOL["bf16"], "decode after the timeout")
     assert pkv.get_device_error() == 0
+
+
+@pytest.mark.parametrize("Hq,Hkv,dt", [(8, 8, "bf16"), (24, 8, "bf16"), (8, 8, "fp8_e4m3"), (4, 4, "f32"),
+                                       (40, 8, "bf16")])
+def test_one_head_units_with_cut_segments(pkv, engine, Hq, Hkv, dt):
+    """Group sizes whose units hold one query head (g = 1, 3, 5): a few long
+    sequences, so most segments are cut between warps and merged from their
+    partial slots."""
+    d = 64 if dt == "f32" else 128
+    w = workloads.make_workload(f"g{Hq // Hkv}_{dt}", [6000, 3000, 17, 4500], Hq, Hkv, d, 16, dt, seed=121)
+    kc, vc = gpu_caches(pkv, w)
+    okc, ovc = oracle_caches(w)
+    ref = oracle_decode(w, okc, ovc, threads=4)
+    assert_close(run_decode(pkv, w, kc, vc), ref, TOL[dt], f"g={Hq // Hkv} {dt}")
+    assert pkv.get_device_error() == 0
