@@ -26,18 +26,23 @@
 //   O += P V         M 128, N = D, K = 64    TMEM columns 128 .. 128 + D
 // Warp 4 starts the tile copies (tensor maps, 128-byte swizzle) into a
 // two-stage ring; warp 5 issues the MMAs, S of step j + 1 while the softmax
-// warps work on step j. O is rescaled lazily: only when a row's running
-// maximum grows by more than 2^8 (probabilities stay below 2^8).
+// warps work on step j, and P.V of step j while they write P of step j + 1
+// (P is double-buffered). O is rescaled lazily: only when a row's running
+// maximum grows by more than 2^8 (probabilities stay below 2^8).  The score
+// scale is folded into the exponent's FMA; only the steps that cross a row's
+// causal limit or a bad block are masked.
 //
-// bf16 caches: the tiles land in the operand layout; P is a bf16 head plus a
-// bf16 remainder (two P.V passes), keeping ~16 significant bits as the decode
-// kernels do. fp8-e4m3 caches: the codes land raw and four converter warps
+// bf16 caches: the tiles land in the operand layout and P is one bf16
+// operand (8 significant bits, each probability rounded once; the sums stay
+// fp32).  fp8-e4m3 caches: the codes land raw and four converter warps
 // (6..9) widen them exactly to fp16 operand tiles; q is fp16, scaled by a
 // power of two per CTA so that it cannot overflow (the factor moves to the
 // fp32 score scale); P is one fp16 operand (11 significant bits).
 #pragma once
 
 #include <math_constants.h>
+
+#include <type_traits>
 
 #include "decode_tc.cuh"
 
@@ -83,10 +88,9 @@ struct Layout {
   static constexpr int kRawTile = F8 ? kStepTok * D : 0;         // fp8: [64 pos][D B] as copied
   static constexpr int kRawK = kV + kStages * kTile;
   static constexpr int kRawV = kRawK + kStages * kRawTile;
-  static constexpr int kPHead = kRawV + kStages * kRawTile;      // [128 rows][64 pos], 16-bit
-  static constexpr int kPRem = kPHead + kRows * kSpan;           // bf16 only
-  static constexpr int kBar = kPRem + (F8 ? 0 : kRows * kSpan);
-  static constexpr int kNumBars = 4 * kStages + 5;
+  static constexpr int kP = kRawV + kStages * kRawTile;          // [2][128 rows][64 pos], 16-bit
+  static constexpr int kBar = kP + 2 * kRows * kSpan;
+  static constexpr int kNumBars = 4 * kStages + 7;
   static constexpr int kMisc = kBar + 8 * kNumBars;              // int max_lim, int merge flag, float max|q|
   static constexpr int kTmemSlot = kMisc + 16;
   static constexpr int kBytes = kTmemSlot + 16;
@@ -246,10 +250,10 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
   uint64_t* empty = full + kStages;                             // operand tiles free (P.V done)
   uint64_t* raw_free = empty + kStages;                         // fp8: raw codes read
   uint64_t* op_full = raw_free + kStages;                       // fp8: operand tiles written
-  uint64_t* s_ready = op_full + kStages;                        // [2]
-  uint64_t* p_ready = s_ready + 2;
-  uint64_t* pv_done = p_ready + 1;
-  uint64_t* drain = pv_done + 1;
+  uint64_t* s_ready = op_full + kStages;                        // [2] S buffers
+  uint64_t* p_ready = s_ready + 2;                              // [2] P buffers written
+  uint64_t* pv_done = p_ready + 2;                              // [2] P.V of a P buffer done
+  uint64_t* drain = pv_done + 2;
   int* max_lim_s = reinterpret_cast<int*>(sm + SM::kMisc);
   int* last_s = max_lim_s + 1;
   unsigned* maxq_s = reinterpret_cast<unsigned*>(max_lim_s + 2);
@@ -262,10 +266,11 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
       mbar_init(&raw_free[i], 4 * 32);
       mbar_init(&op_full[i], 4 * 32);
     }
-    mbar_init(&s_ready[0], 1);
-    mbar_init(&s_ready[1], 1);
-    mbar_init(p_ready, 4 * 32);
-    mbar_init(pv_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_ready[i], 1);
+      mbar_init(&p_ready[i], 4 * 32);
+      mbar_init(&pv_done[i], 1);
+    }
     mbar_init(drain, 1);
     *max_lim_s = 0;
     *last_s = 0;
@@ -340,6 +345,9 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
     const int sh = e > 15 ? (e - 15 < 100 ? e - 15 : 100) : 0;
     q_down = ldexpf(1.f, -sh);
   }
+  // a negative scale moves its sign into q (exact), so that the largest raw
+  // score is also the largest scaled one
+  const uint32_t q_sign = a.qk_scale < 0.f ? 0x80008000u : 0u;
   for (int i = tid; i < kRows * (D / 8); i += NT) {
     int r, c;
     uint4 v = q_chunk(i, r, c);
@@ -348,18 +356,22 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
       v = make_uint4(pack_f16x2(f0.x * q_down, f0.y * q_down), pack_f16x2(f1.x * q_down, f1.y * q_down),
                      pack_f16x2(f2.x * q_down, f2.y * q_down), pack_f16x2(f3.x * q_down, f3.y * q_down));
     }
+    v.x ^= q_sign;
+    v.y ^= q_sign;
+    v.z ^= q_sign;
+    v.w ^= q_sign;
     const int sp = c / 8, cc = c % 8;
     *reinterpret_cast<uint4*>(sm + SM::kQ + sp * (kRows * kSpan) + r * kSpan + ((cc ^ (r & 7)) << 4)) = v;
   }
   // the operand ring (and the raw ring) start zeroed: a slot no block fills
   // holds finite values, which zero probabilities then multiply
-  for (int i = tid; i < (SM::kPHead - SM::kK) / 16; i += NT) reinterpret_cast<uint4*>(sm + SM::kK)[i] = make_uint4(0, 0, 0, 0);
+  for (int i = tid; i < (SM::kP - SM::kK) / 16; i += NT) reinterpret_cast<uint4*>(sm + SM::kK)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = *tslot;
-  const float qk_mul = a.qk_scale / q_down;
+  const float qk_mul = fabsf(a.qk_scale) / q_down;
   // positions at or past max_lim are attended by no row of the tile: their V
   // rows are zeroed before P.V (they may be unwritten)
   const int max_lim = *max_lim_s;
@@ -458,23 +470,20 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
       bool ok = steps == 0 || issue_s(0);
       for (int j = 0; ok && j < steps; ++j) {
         if (j + 1 < steps && !(ok = issue_s(j + 1))) break;
-        if (!(ok = mbar_wait_bounded(p_ready, j & 1, a.err))) break;
+        const int pb = j & 1;  // P buffer of this step
+        if (!(ok = mbar_wait_bounded(&p_ready[pb], (j >> 1) & 1, a.err))) break;
         fence_after_sync();
         const int st = j % kStages;
 #pragma unroll
-        for (int half = 0; half < (F8 ? 1 : 2); ++half) {
-          const int poff = half ? SM::kPRem : SM::kPHead;
-#pragma unroll
-          for (int k = 0; k < kStepTok / 16; ++k) {  // 16 positions per MMA: +32 B in P, +16 rows in V
-            const uint64_t da = sw128_desc(smem_addr(sm + poff + k * 32), 16, 1024);
-            // V is MN-major: 64-element spans of D kStepTok rows apart, 8-row groups 1024 B apart
-            const uint64_t db =
-                sw128_desc(smem_addr(sm + SM::kV + st * SM::kTile + k * 16 * kSpan), kStepTok * kSpan, 1024);
-            mma_bf16(tmem + 2 * kStepTok, da, db, id_o, (j > 0 || half > 0 || k > 0) ? 1u : 0u);
-          }
+        for (int k = 0; k < kStepTok / 16; ++k) {  // 16 positions per MMA: +32 B in P, +16 rows in V
+          const uint64_t da = sw128_desc(smem_addr(sm + SM::kP + pb * (kRows * kSpan) + k * 32), 16, 1024);
+          // V is MN-major: 64-element spans of D kStepTok rows apart, 8-row groups 1024 B apart
+          const uint64_t db =
+              sw128_desc(smem_addr(sm + SM::kV + st * SM::kTile + k * 16 * kSpan), kStepTok * kSpan, 1024);
+          mma_bf16(tmem + 2 * kStepTok, da, db, id_o, (j > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit(&empty[st]);
-        mma_commit(pv_done);
+        mma_commit(&pv_done[pb]);
       }
       // every MMA issued has completed before TMEM is released
       mma_commit(drain);
@@ -486,37 +495,59 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
     const uint32_t lane_base = tmem + ((uint32_t)(w * 32) << 16);
     float m_used = -CUDART_INF_F, l = 0.f;
     bool ok = true;
+    constexpr uint32_t kAllBlocks = (1u << NB) - 1;
     for (int j = 0; j < steps; ++j) {
-      const int st = j % kStages;
+      const int st = j % kStages, pb = j & 1;
       int ids[NB];
       const uint32_t okb = step_blocks<BS>(table, jb, je, j, a.num_blocks, ids);
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s_ready[j & 1], (j >> 1) & 1, a.err)))) break;
+      const int t0 = (jb + j * NB) * BS;
+      // a step where every position of every row of this warp is kept needs no mask
+      const bool interior = __all_sync(0xffffffffu, t0 + kStepTok <= my_lim && okb == kAllBlocks);
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s_ready[pb], (j >> 1) & 1, a.err)))) break;
       fence_after_sync();
       float sc[2][32];
-      tmem_ld32(lane_base + (uint32_t)(j & 1) * kStepTok, sc[0]);
-      tmem_ld32(lane_base + (uint32_t)(j & 1) * kStepTok + 32, sc[1]);
-      const int t0 = (jb + j * NB) * BS;
-      float mt = -CUDART_INF_F;
+      tmem_ld32(lane_base + (uint32_t)pb * kStepTok, sc[0]);
+      tmem_ld32(lane_base + (uint32_t)pb * kStepTok + 32, sc[1]);
+      // the largest raw score (qk_mul >= 0), four independent chains; on a
+      // boundary step `keep` marks the positions this row attends
+      float mx[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+      uint64_t keep = ~0ull;
+      if (interior) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int pos = h * 32 + c;
-          const bool valid = t0 + pos < my_lim && (okb >> (pos / BS) & 1);
-          sc[h][c] = valid ? sc[h][c] * qk_mul : -CUDART_INF_F;
-          mt = fmaxf(mt, sc[h][c]);
-        }
-      // P(j - 1).V must be done before P is overwritten or O rescaled
-      if (j > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait_bounded(pv_done, (j - 1) & 1, a.err)))) break;
-      fence_after_sync();
+          for (int c = 0; c < 32; ++c) mx[c & 3] = fmaxf(mx[c & 3], sc[h][c]);
+      } else {
+        const int lim = min(max(my_lim - t0, 0), kStepTok);
+        keep = lim >= 64 ? ~0ull : ((1ull << lim) - 1);
+#pragma unroll
+        for (int b = 0; b < NB; ++b)
+          if (!(okb >> b & 1)) keep &= ~(((1ull << BS) - 1) << (b * BS));
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (keep >> (h * 32 + c) & 1) mx[c & 3] = fmaxf(mx[c & 3], sc[h][c]);
+      }
+      const float mraw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      const float mt = mraw == -CUDART_INF_F ? -CUDART_INF_F : mraw * qk_mul;
       float factor = 1.f;
       if (mt > m_used + kRescaleSlack) {
         factor = m_used == -CUDART_INF_F ? 0.f : fast_exp2(m_used - mt);
         m_used = mt;
         l *= factor;
       }
-      // a warp rescales its rows of O together (tcgen05.ld / st are warp-wide)
-      if (j > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
+      // P buffer pb is free once the P.V of two steps ago is done; a rescale
+      // of O needs the previous step's P.V done as well (rare: the maximum
+      // must grow by more than the slack)
+      const bool rescale = j > 0 && __any_sync(0xffffffffu, factor != 1.f);
+      if (j >= 2 && !(ok = __all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[pb], ((j - 2) >> 1) & 1, a.err))))
+        break;
+      if (rescale &&
+          !(ok = __all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[pb ^ 1], ((j - 1) >> 1) & 1, a.err))))
+        break;
+      fence_after_sync();
+      if (rescale) {  // a warp rescales its rows of O together (tcgen05.ld / st are warp-wide)
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           float o[32];
@@ -527,29 +558,38 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
-      const float mref = m_used == -CUDART_INF_F ? 0.f : m_used;  // a row with nothing valid yet: all p zero
+      // p = 2^(s * qk_mul - m): a row with nothing kept yet (m = -inf) has
+      // only masked scores, which give 0
+      const float nm = m_used == -CUDART_INF_F ? 0.f : -m_used;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      uint8_t* prow = sm + SM::kP + pb * (kRows * kSpan) + r * kSpan;
+      auto emit_p = [&](auto masked) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-          uint32_t hi[4], lo[4];
+          for (int c8 = 0; c8 < 4; ++c8) {
+            uint32_t pk[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float p0 = fast_exp2(sc[h][c8 * 8 + 2 * e] - mref), p1 = fast_exp2(sc[h][c8 * 8 + 2 * e + 1] - mref);
-            l += p0 + p1;
-            if constexpr (F8) {
-              hi[e] = pack_f16x2(p0, p1);
-            } else {
-              hi[e] = pack_bf16x2(p0, p1);
-              const float2 hv = bf16x2_to_f2(hi[e]);
-              lo[e] = pack_bf16x2(p0 - hv.x, p1 - hv.y);
+            for (int e = 0; e < 4; ++e) {
+              const int c = c8 * 8 + 2 * e;
+              float p0 = fast_exp2(fmaf(sc[h][c], qk_mul, nm));
+              float p1 = fast_exp2(fmaf(sc[h][c + 1], qk_mul, nm));
+              if constexpr (decltype(masked)::value) {
+                p0 = keep >> (h * 32 + c) & 1 ? p0 : 0.f;
+                p1 = keep >> (h * 32 + c + 1) & 1 ? p1 : 0.f;
+              }
+              ls[e] += p0 + p1;
+              pk[e] = F8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
             }
+            *reinterpret_cast<uint4*>(prow + (((h * 4 + c8) ^ (r & 7)) << 4)) =
+                make_uint4(pk[0], pk[1], pk[2], pk[3]);
           }
-          const int off = r * kSpan + (((h * 4 + c8) ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4*>(sm + SM::kPHead + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          if constexpr (!F8)
-            *reinterpret_cast<uint4*>(sm + SM::kPRem + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
+      };
+      if (interior)
+        emit_p(std::false_type{});
+      else
+        emit_p(std::true_type{});
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       if constexpr (!F8) {
         // V rows of positions no row attends (the tile's last step) become zero
         const int z0 = max(0, max_lim - t0);
@@ -563,9 +603,13 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
       }
       fence_proxy_async_smem();
       fence_before_sync();
-      mbar_arrive(p_ready);
+      mbar_arrive(&p_ready[pb]);
     }
-    if (ok && steps > 0) ok = __all_sync(0xffffffffu, mbar_wait_bounded(pv_done, (steps - 1) & 1, a.err));
+    // every P.V issued has completed before O is read
+    if (ok && steps > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[(steps - 1) & 1], ((steps - 1) >> 1) & 1, a.err));
+    if (ok && steps > 1)
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[(steps - 2) & 1], ((steps - 2) >> 1) & 1, a.err));
     fence_after_sync();
     // ---- epilogue
     const float inv_l = l > 0.f ? 1.f / l : 0.f;
