@@ -72,31 +72,89 @@ namespace tc05 {
 
 constexpr int kRows = 128;     // query rows per CTA (TMEM lanes)
 constexpr int kStepTok = 64;   // positions per step
-constexpr int kStages = 2;
 constexpr int kSpan = 128;     // bytes of one 128-byte swizzle span
 constexpr float kRescaleSlack = 8.f;
 
 __host__ __device__ constexpr int threads(bool f8) { return f8 ? 320 : 192; }
 
+// Shared memory per CTA: one CTA per SM for head_dim 128, two for 64 (each
+// keeps 1 KiB of the SM's 228 KiB for the system).
+constexpr int kSmemPerSm = 233472;
+__host__ __device__ constexpr int smem_budget(int D) { return kSmemPerSm / (D == 64 ? 2 : 1) - 1024 - 512; }
+
 template <int D, bool F8>
 struct Layout {
   static constexpr int kSpans = D / 64;                          // 64 16-bit elements per span
-  static constexpr int kQ = 0;                                   // [span][128 rows][128 B]
+  static constexpr int kQBytes = kSpans * kRows * kSpan;
+  static constexpr int kPBytes = 2 * kRows * kSpan;
   static constexpr int kTile = kSpans * kStepTok * kSpan;        // one cache's operand tile of a step
-  static constexpr int kK = kQ + kSpans * kRows * kSpan;         // [stage][span][64 pos][128 B]
-  static constexpr int kV = kK + kStages * kTile;
   static constexpr int kRawTile = F8 ? kStepTok * D : 0;         // fp8: [64 pos][D B] as copied
-  static constexpr int kRawK = kV + kStages * kTile;
-  static constexpr int kRawV = kRawK + kStages * kRawTile;
-  static constexpr int kP = kRawV + kStages * kRawTile;          // [2][128 rows][64 pos], 16-bit
-  static constexpr int kBar = kP + 2 * kRows * kSpan;
-  static constexpr int kNumBars = 4 * kStages + 7;
+  // The copies must run several steps ahead of the MMAs (a tensor copy
+  // takes microseconds; a step a few hundred cycles): as many K/V stages as
+  // shared memory holds.  fp8: two operand stages and a deep ring of raw
+  // codes (half the bytes), which the converter warps widen just in time.
+  static constexpr int kFree = smem_budget(D) - kQBytes - kPBytes;
+  static constexpr int kOpStagesFit = F8 ? 2 : kFree / (2 * kTile);
+  static constexpr int kOpStages = kOpStagesFit > 6 ? 6 : kOpStagesFit;
+  static constexpr int kRawStagesFit = F8 ? (kFree - 2 * kOpStages * kTile) / (2 * kRawTile) : 0;
+  static constexpr int kRawStages = kRawStagesFit > 8 ? 8 : kRawStagesFit;
+  static constexpr int kLandStages = F8 ? kRawStages : kOpStages;  // stages the tensor copies fill
+  static constexpr int kQ = 0;                                   // [span][128 rows][128 B]
+  static constexpr int kK = kQ + kQBytes;                        // [stage][span][64 pos][128 B]
+  static constexpr int kV = kK + kOpStages * kTile;
+  static constexpr int kRawK = kV + kOpStages * kTile;
+  static constexpr int kRawV = kRawK + kRawStages * kRawTile;
+  static constexpr int kP = kRawV + kRawStages * kRawTile;       // [2][128 rows][64 pos], 16-bit
+  static constexpr int kBar = kP + kPBytes;
+  static constexpr int kNumBars = 2 * kLandStages + 2 * kOpStages + 7;
   static constexpr int kMisc = kBar + 8 * kNumBars;              // int max_lim, int merge flag, float max|q|
   static constexpr int kTmemSlot = kMisc + 16;
   static constexpr int kBytes = kTmemSlot + 16;
   static constexpr uint32_t kTmemCols = 256;                     // S double buffer + O, a power of two
   static_assert(kTmemCols >= 2 * kStepTok + D, "TMEM columns");
   static_assert(!F8 || D == 128, "fp8 rows of one swizzle span");
+  static_assert(kOpStages >= 2 && (!F8 || kRawStages >= 2), "at least double buffering");
+  static_assert(kBytes <= smem_budget(D) + 512, "shared memory");
+};
+
+// Table ids of the blocks of a step, read 32 entries at a time across a
+// warp (lane i holds entry 32c + i of the range) with the next 32 already in
+// flight, so that no step waits on a table read.
+template <int NB>
+struct StepIds {
+  const int32_t* table;
+  int jb, nblk, lane, chunk;
+  int32_t cur, nxt;
+  __device__ __forceinline__ int32_t load(int c) const {
+    const int i = 32 * c + lane;
+    return i < nblk ? __ldg(table + jb + i) : -1;
+  }
+  __device__ __forceinline__ void init(const int32_t* t, int jb_, int je_, int lane_) {
+    table = t;
+    jb = jb_;
+    nblk = je_ - jb_;
+    lane = lane_;
+    chunk = 0;
+    cur = load(0);
+    nxt = load(1);
+  }
+  // bit b set when block j * NB + b of the range exists and its id is in the
+  // pool; ids[b] the id.  Called by every lane of the warp, steps in order.
+  __device__ __forceinline__ uint32_t step(int j, int num_blocks, int (&ids)[NB]) {
+    const int first = j * NB;
+    if (first / 32 != chunk) {
+      cur = nxt;
+      ++chunk;
+      nxt = load(chunk + 1);
+    }
+    uint32_t ok = 0;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      ids[b] = __shfl_sync(0xffffffffu, cur, (first % 32) + b);
+      if (first + b < nblk && ids[b] >= 0 && ids[b] < num_blocks) ok |= 1u << b;
+    }
+    return ok;
+  }
 };
 
 // Shared-memory matrix descriptor, 128-byte swizzle: start >> 4, leading
@@ -174,21 +232,6 @@ __device__ __forceinline__ void tma_span_tile(void* dst, const void* map, int x,
       : "memory");
 }
 
-// Bit b set when block jb + j * (64 / BS) + b is below je and its id lies in
-// the pool; ids[b] the id (or -1).
-template <int BS>
-__device__ __forceinline__ uint32_t step_blocks(const int32_t* table, int jb, int je, int j, int num_blocks,
-                                                int (&ids)[kStepTok / BS]) {
-  uint32_t ok = 0;
-#pragma unroll
-  for (int b = 0; b < kStepTok / BS; ++b) {
-    const int idx = jb + j * (kStepTok / BS) + b;
-    ids[b] = idx < je ? __ldg(table + idx) : -1;
-    if (idx < je && ids[b] >= 0 && ids[b] < num_blocks) ok |= 1u << b;
-  }
-  return ok;
-}
-
 // Widen 16 e4m3 codes of a raw row chunk into 16 fp16 (two 16-byte chunks).
 __device__ __forceinline__ void e4m3x16_to_f16(uint4 raw, uint4& lo, uint4& hi) {
   e4m3x4_to_f16x2x2(raw.x, lo.x, lo.y);
@@ -246,11 +289,12 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
     if (tid == 0) raise_error(a.err, PKV_DEVERR_SMEM_ALIGN);
     return;
   }
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + SM::kBar);  // tiles (bf16) / raw codes (fp8) landed
-  uint64_t* empty = full + kStages;                             // operand tiles free (P.V done)
-  uint64_t* raw_free = empty + kStages;                         // fp8: raw codes read
-  uint64_t* op_full = raw_free + kStages;                       // fp8: operand tiles written
-  uint64_t* s_ready = op_full + kStages;                        // [2] S buffers
+  constexpr int OPS = SM::kOpStages, LS = SM::kLandStages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + SM::kBar);  // [LS] tiles (bf16) / raw codes (fp8) landed
+  uint64_t* raw_free = full + LS;                               // [LS] fp8: raw codes read
+  uint64_t* empty = raw_free + LS;                              // [OPS] operand tiles free (P.V done)
+  uint64_t* op_full = empty + OPS;                              // [OPS] fp8: operand tiles written
+  uint64_t* s_ready = op_full + OPS;                            // [2] S buffers
   uint64_t* p_ready = s_ready + 2;                              // [2] P buffers written
   uint64_t* pv_done = p_ready + 2;                              // [2] P.V of a P buffer done
   uint64_t* drain = pv_done + 2;
@@ -260,10 +304,12 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SM::kTmemSlot);
 
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < LS; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
       mbar_init(&raw_free[i], 4 * 32);
+    }
+    for (int i = 0; i < OPS; ++i) {
+      mbar_init(&empty[i], 1);
       mbar_init(&op_full[i], 4 * 32);
     }
     for (int i = 0; i < 2; ++i) {
@@ -383,16 +429,19 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
 
   if (w == 4) {
     // ---- producer: per block of a step, one tensor copy per cache and span
-    // (bf16: into the operand tiles; fp8: one 128-byte row box into the raw ring)
-    if (lane == 0) {
-      uint64_t* freed = F8 ? raw_free : empty;
-      int armed = 0;
-      for (int j = 0; j < steps; ++j) {
-        const int st = j % kStages;
-        if (!mbar_wait_bounded(&freed[st], ((j / kStages) & 1) ^ 1, a.err)) break;
-        armed = j + 1;
-        int ids[NB];
-        const uint32_t ok = step_blocks<BS>(table, jb, je, j, a.num_blocks, ids);
+    // (bf16: into the operand tiles; fp8: one 128-byte row box into the raw
+    // ring).  The whole warp reads the table; lane 0 waits and copies.
+    uint64_t* freed = F8 ? raw_free : empty;
+    StepIds<NB> sid;
+    sid.init(table, jb, je, lane);
+    int armed = 0;
+    for (int j = 0; j < steps; ++j) {
+      const int st = j % LS;
+      int ids[NB];
+      const uint32_t ok = sid.step(j, a.num_blocks, ids);
+      if (!__all_sync(0xffffffffu, lane != 0 || mbar_wait_bounded(&freed[st], ((j / LS) & 1) ^ 1, a.err))) break;
+      armed = j + 1;
+      if (lane == 0) {
         const int left = je - jb - j * NB;
         const uint32_t want = left >= NB ? (1u << NB) - 1 : (1u << left) - 1;
         if (ok != want) raise_error(a.err, PKV_DEVERR_BAD_BLOCK_ID);
@@ -412,19 +461,21 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
           }
         }
       }
-      // no copy may land after the CTA is gone: wait (bounded) for the last
-      // copies of every stage, consumed or not
-      for (int j = max(0, armed - kStages); j < armed; ++j)
-        if (!mbar_wait_bounded(&full[j % kStages], (j / kStages) & 1, a.err)) break;
+      __syncwarp();
     }
+    // no copy may land after the CTA is gone: wait (bounded) for the last
+    // copies of every stage, consumed or not
+    if (lane == 0)
+      for (int j = max(0, armed - LS); j < armed; ++j)
+        if (!mbar_wait_bounded(&full[j % LS], (j / LS) & 1, a.err)) break;
   } else if (F8 && w >= 6) {
     // ---- converters (fp8): raw e4m3 rows -> fp16 operand tiles, exact; V
     // rows at positions no row attends become zero
     const int ct = tid - 6 * 32;
     for (int j = 0; j < steps; ++j) {
-      const int st = j % kStages;
-      const bool got = mbar_wait_bounded(&full[st], (j / kStages) & 1, a.err) &&
-                       mbar_wait_bounded(&empty[st], ((j / kStages) & 1) ^ 1, a.err);
+      const int rs = j % LS, st = j % OPS;
+      const bool got = mbar_wait_bounded(&full[rs], (j / LS) & 1, a.err) &&
+                       mbar_wait_bounded(&empty[st], ((j / OPS) & 1) ^ 1, a.err);
       if (!__all_sync(0xffffffffu, got)) break;
       const int t0 = (jb + j * NB) * BS;  // first position of the step
       // 16-byte raw chunk k of a row: codes 16k .. 16k + 15 -> operand span k / 4, chunks 2 (k % 4), + 1
@@ -432,7 +483,7 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
       for (int i = ct; i < 2 * kStepTok * (D / 16); i += 4 * 32) {
         const int cache = i / (kStepTok * (D / 16)), rem = i % (kStepTok * (D / 16));
         const int p = rem / (D / 16), k = rem % (D / 16);
-        const uint8_t* raw = sm + (cache ? SM::kRawV : SM::kRawK) + st * SM::kRawTile;
+        const uint8_t* raw = sm + (cache ? SM::kRawV : SM::kRawK) + rs * SM::kRawTile;
         uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
         if (!cache || t0 + p < max_lim)
           e4m3x16_to_f16(*reinterpret_cast<const uint4*>(raw + p * D + ((k ^ (p & 7)) << 4)), lo, hi);
@@ -442,7 +493,7 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
         *reinterpret_cast<uint4*>(op + (((c0 + 1) ^ (p & 7)) << 4)) = hi;
       }
       fence_proxy_async_smem();
-      mbar_arrive(&raw_free[st]);
+      mbar_arrive(&raw_free[rs]);
       mbar_arrive(&op_full[st]);
     }
   } else if (w == 5) {
@@ -452,8 +503,8 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
       constexpr uint32_t id_o = idesc_f16kind(kRows, D, !F8, true);
       uint64_t* ready = F8 ? op_full : full;
       auto issue_s = [&](int j) -> bool {
-        const int st = j % kStages;
-        if (!mbar_wait_bounded(&ready[st], (j / kStages) & 1, a.err)) return false;
+        const int st = j % OPS;
+        if (!mbar_wait_bounded(&ready[st], (j / OPS) & 1, a.err)) return false;
         fence_after_sync();
         const uint32_t dst = tmem + (uint32_t)(j & 1) * kStepTok;
 #pragma unroll
@@ -473,7 +524,7 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
         const int pb = j & 1;  // P buffer of this step
         if (!(ok = mbar_wait_bounded(&p_ready[pb], (j >> 1) & 1, a.err))) break;
         fence_after_sync();
-        const int st = j % kStages;
+        const int st = j % OPS;
 #pragma unroll
         for (int k = 0; k < kStepTok / 16; ++k) {  // 16 positions per MMA: +32 B in P, +16 rows in V
           const uint64_t da = sw128_desc(smem_addr(sm + SM::kP + pb * (kRows * kSpan) + k * 32), 16, 1024);
@@ -496,10 +547,12 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
     float m_used = -CUDART_INF_F, l = 0.f;
     bool ok = true;
     constexpr uint32_t kAllBlocks = (1u << NB) - 1;
+    StepIds<NB> sid;
+    sid.init(table, jb, je, lane);
     for (int j = 0; j < steps; ++j) {
-      const int st = j % kStages, pb = j & 1;
+      const int st = j % OPS, pb = j & 1;
       int ids[NB];
-      const uint32_t okb = step_blocks<BS>(table, jb, je, j, a.num_blocks, ids);
+      const uint32_t okb = sid.step(j, a.num_blocks, ids);
       const int t0 = (jb + j * NB) * BS;
       // a step where every position of every row of this warp is kept needs no mask
       const bool interior = __all_sync(0xffffffffu, t0 + kStepTok <= my_lim && okb == kAllBlocks);
