@@ -22,20 +22,25 @@
 //
 // Per step of 64 positions:
 //   S = Q K^T        M 128, N 64, K = D      TMEM columns 0..63 / 64..127
-//   P = 2^(S - m)    four softmax warps, one row per thread, into shared memory
+//   P = 2^(S - m)    eight softmax warps, two threads per row (32 columns
+//                    each), into shared memory
 //   O += P V         M 128, N = D, K = 64    TMEM columns 128 .. 128 + D
-// Warp 4 starts the tile copies (tensor maps, 128-byte swizzle) into a
-// two-stage ring; warp 5 issues the MMAs, S of step j + 1 while the softmax
-// warps work on step j, and P.V of step j while they write P of step j + 1
-// (P is double-buffered). O is rescaled lazily: only when a row's running
-// maximum grows by more than 2^8 (probabilities stay below 2^8).  The score
-// scale is folded into the exponent's FMA; only the steps that cross a row's
-// causal limit or a bad block are masked.
+// Producer warps start the tile copies (tensor maps, 128-byte swizzle) into
+// a ring of as many stages as shared memory holds, reading the block table
+// 32 entries at a time one chunk ahead; one warp issues the MMAs, S of step
+// j + 1
+// while the softmax warps work on step j, and P.V of step j while they write
+// P of step j + 1 (P is double-buffered).  The two threads of a row swap
+// their half's maximum through shared memory each step, so that two softmax
+// warps share every SM sub-partition.  O is rescaled lazily: only when a
+// row's running maximum grows by more than 2^8 (probabilities stay below
+// 2^8).  The score scale is folded into the exponent's FMA; only the steps
+// that cross a row's causal limit or a bad block are masked.
 //
 // bf16 caches: the tiles land in the operand layout and P is one bf16
 // operand (8 significant bits, each probability rounded once; the sums stay
-// fp32).  fp8-e4m3 caches: the codes land raw and four converter warps
-// (6..9) widen them exactly to fp16 operand tiles; q is fp16, scaled by a
+// fp32).  fp8-e4m3 caches: the codes land raw and two converter warps
+// widen them exactly to fp16 operand tiles; q is fp16, scaled by a
 // power of two per CTA so that it cannot overflow (the factor moves to the
 // fp32 score scale); P is one fp16 operand (11 significant bits).
 #pragma once
@@ -75,12 +80,23 @@ constexpr int kStepTok = 64;   // positions per step
 constexpr int kSpan = 128;     // bytes of one 128-byte swizzle span
 constexpr float kRescaleSlack = 8.f;
 
-__host__ __device__ constexpr int threads(bool f8) { return f8 ? 320 : 192; }
+// Warps: 0-7 softmax (two per row of the tile); then the tensor-copy
+// producers: two for bf16 caches (K and V: a copy costs its issuing thread
+// about a hundred cycles, and a step needs up to 32 of them), one for fp8
+// caches (half the copies); then the MMA issuer; then, for fp8 caches, two
+// converter warps.  At most three warps share an SM sub-partition, so that
+// each thread may hold 168 registers.
+constexpr int kConvWarps = 2;
+__host__ __device__ constexpr int prod_warps(bool f8) { return f8 ? 1 : 2; }
+__host__ __device__ constexpr int mma_warp(bool f8) { return 8 + prod_warps(f8); }
+__host__ __device__ constexpr int threads(bool f8) { return (mma_warp(f8) + 1 + (f8 ? kConvWarps : 0)) * 32; }
 
-// Shared memory per CTA: one CTA per SM for head_dim 128, two for 64 (each
-// keeps 1 KiB of the SM's 228 KiB for the system).
+// Shared memory per CTA: one CTA per SM (the 320-448 threads' registers
+// fill the SM's file), which keeps 1 KiB of the SM's 228 KiB for the system;
+// less the barriers, the row-maximum exchange and a few words.
 constexpr int kSmemPerSm = 233472;
-__host__ __device__ constexpr int smem_budget(int D) { return kSmemPerSm / (D == 64 ? 2 : 1) - 1024 - 512; }
+constexpr int kSmemReserve = 2560;
+__host__ __device__ constexpr int smem_budget(int) { return kSmemPerSm - 1024 - kSmemReserve; }
 
 template <int D, bool F8>
 struct Layout {
@@ -107,14 +123,15 @@ struct Layout {
   static constexpr int kP = kRawV + kRawStages * kRawTile;       // [2][128 rows][64 pos], 16-bit
   static constexpr int kBar = kP + kPBytes;
   static constexpr int kNumBars = 2 * kLandStages + 2 * kOpStages + 7;
-  static constexpr int kMisc = kBar + 8 * kNumBars;              // int max_lim, int merge flag, float max|q|
+  static constexpr int kXch = (kBar + 8 * kNumBars + 15) / 16 * 16;  // [2][2][128] floats: row maxima, sums
+  static constexpr int kMisc = kXch + 4 * kRows * 4;             // int max_lim, int merge flag, float max|q|
   static constexpr int kTmemSlot = kMisc + 16;
   static constexpr int kBytes = kTmemSlot + 16;
   static constexpr uint32_t kTmemCols = 256;                     // S double buffer + O, a power of two
   static_assert(kTmemCols >= 2 * kStepTok + D, "TMEM columns");
   static_assert(!F8 || D == 128, "fp8 rows of one swizzle span");
   static_assert(kOpStages >= 2 && (!F8 || kRawStages >= 2), "at least double buffering");
-  static_assert(kBytes <= smem_budget(D) + 512, "shared memory");
+  static_assert(kBytes <= smem_budget(D) + kSmemReserve, "shared memory");
 };
 
 // Table ids of the blocks of a step, read 32 entries at a time across a
@@ -305,16 +322,16 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
 
   if (tid == 0) {
     for (int i = 0; i < LS; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&raw_free[i], 4 * 32);
+      mbar_init(&full[i], prod_warps(F8));  // every producer warp arrives
+      mbar_init(&raw_free[i], kConvWarps * 32);
     }
     for (int i = 0; i < OPS; ++i) {
       mbar_init(&empty[i], 1);
-      mbar_init(&op_full[i], 4 * 32);
+      mbar_init(&op_full[i], kConvWarps * 32);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_ready[i], 1);
-      mbar_init(&p_ready[i], 4 * 32);
+      mbar_init(&p_ready[i], 8 * 32);
       mbar_init(&pv_done[i], 1);
     }
     mbar_init(drain, 1);
@@ -357,9 +374,9 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
   };
   int my_qrow = 0, my_qhead = 0, my_lim = 0;
   bool my_valid = false;
-  if (tid < kRows) {
-    my_valid = row_of(tid, my_qrow, my_qhead, my_lim);
-    atomicMax(max_lim_s, my_lim);
+  if (tid < 2 * kRows) {  // the softmax threads: row tid % 128
+    my_valid = row_of(tid & (kRows - 1), my_qrow, my_qhead, my_lim);
+    if (tid < kRows) atomicMax(max_lim_s, my_lim);
   }
   // the query tile, K-major with the 128-byte swizzle: 16-byte chunk c of row
   // r at r * 128 + ((c ^ (r % 8)) * 16) of its span; padding rows zero. fp8
@@ -427,10 +444,13 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
   // frees (it waits for the whole grid before it reads a partial)
   if constexpr (PREFIX) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  if (w == 4) {
-    // ---- producer: per block of a step, one tensor copy per cache and span
-    // (bf16: into the operand tiles; fp8: one 128-byte row box into the raw
-    // ring).  The whole warp reads the table; lane 0 waits and copies.
+  if (w >= 8 && w < mma_warp(F8)) {
+    // ---- producers (K then V, or both from one warp): per block of a
+    // step, one tensor copy per span (bf16: into the operand tiles; fp8: one
+    // 128-byte row box into the raw ring).  The whole warp reads the table;
+    // lane 0 waits and copies.
+    constexpr int PW = prod_warps(F8);
+    const int c_lo = (w - 8) * 2 / PW, c_hi = (w - 8 + 1) * 2 / PW;  // caches of this warp: 0 K, 1 V
     uint64_t* freed = F8 ? raw_free : empty;
     StepIds<NB> sid;
     sid.init(table, jb, je, lane);
@@ -444,19 +464,20 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
       if (lane == 0) {
         const int left = je - jb - j * NB;
         const uint32_t want = left >= NB ? (1u << NB) - 1 : (1u << left) - 1;
-        if (ok != want) raise_error(a.err, PKV_DEVERR_BAD_BLOCK_ID);
-        mbar_arrive_expect_tx(&full[st], (uint32_t)(__popc(ok) * 2 * BS * D * (F8 ? 1 : 2)));
-        for (int b = 0; b < NB; ++b) {
-          if (!(ok >> b & 1)) continue;
-          if constexpr (F8) {
-            const int off = st * SM::kRawTile + b * (BS * D);
-            tma_span_tile(sm + SM::kRawK + off, &maps.k, 0, kvh * BS, ids[b], &full[st]);
-            tma_span_tile(sm + SM::kRawV + off, &maps.v, 0, kvh * BS, ids[b], &full[st]);
-          } else {
-            for (int sp = 0; sp < SPANS; ++sp) {
-              const int off = st * SM::kTile + sp * (kStepTok * kSpan) + b * (BS * kSpan);
-              tma_span_tile(sm + SM::kK + off, &maps.k, sp * 64, kvh * BS, ids[b], &full[st]);
-              tma_span_tile(sm + SM::kV + off, &maps.v, sp * 64, kvh * BS, ids[b], &full[st]);
+        if (ok != want && c_lo == 0) raise_error(a.err, PKV_DEVERR_BAD_BLOCK_ID);
+        mbar_arrive_expect_tx(&full[st], (uint32_t)(__popc(ok) * (c_hi - c_lo) * BS * D * (F8 ? 1 : 2)));
+        for (int c = c_lo; c < c_hi; ++c) {
+          const TmaMap* map = c ? &maps.v : &maps.k;
+          for (int b = 0; b < NB; ++b) {
+            if (!(ok >> b & 1)) continue;
+            if constexpr (F8) {
+              const int off = st * SM::kRawTile + b * (BS * D);
+              tma_span_tile(sm + (c ? SM::kRawV : SM::kRawK) + off, map, 0, kvh * BS, ids[b], &full[st]);
+            } else {
+              for (int sp = 0; sp < SPANS; ++sp) {
+                const int off = st * SM::kTile + sp * (kStepTok * kSpan) + b * (BS * kSpan);
+                tma_span_tile(sm + (c ? SM::kV : SM::kK) + off, map, sp * 64, kvh * BS, ids[b], &full[st]);
+              }
             }
           }
         }
@@ -468,10 +489,10 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
     if (lane == 0)
       for (int j = max(0, armed - LS); j < armed; ++j)
         if (!mbar_wait_bounded(&full[j % LS], (j / LS) & 1, a.err)) break;
-  } else if (F8 && w >= 6) {
+  } else if (F8 && w > mma_warp(F8)) {
     // ---- converters (fp8): raw e4m3 rows -> fp16 operand tiles, exact; V
     // rows at positions no row attends become zero
-    const int ct = tid - 6 * 32;
+    const int ct = tid - (mma_warp(F8) + 1) * 32;
     for (int j = 0; j < steps; ++j) {
       const int rs = j % LS, st = j % OPS;
       const bool got = mbar_wait_bounded(&full[rs], (j / LS) & 1, a.err) &&
@@ -480,7 +501,7 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
       const int t0 = (jb + j * NB) * BS;  // first position of the step
       // 16-byte raw chunk k of a row: codes 16k .. 16k + 15 -> operand span k / 4, chunks 2 (k % 4), + 1
 #pragma unroll 2
-      for (int i = ct; i < 2 * kStepTok * (D / 16); i += 4 * 32) {
+      for (int i = ct; i < 2 * kStepTok * (D / 16); i += kConvWarps * 32) {
         const int cache = i / (kStepTok * (D / 16)), rem = i % (kStepTok * (D / 16));
         const int p = rem / (D / 16), k = rem % (D / 16);
         const uint8_t* raw = sm + (cache ? SM::kRawV : SM::kRawK) + rs * SM::kRawTile;
@@ -496,7 +517,7 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
       mbar_arrive(&raw_free[rs]);
       mbar_arrive(&op_full[st]);
     }
-  } else if (w == 5) {
+  } else if (w == mma_warp(F8)) {
     // ---- MMA issue: S(j + 1) = Q K(j + 1)^T while the softmax warps work on step j
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_f16kind(kRows, kStepTok, !F8, false);
@@ -540,49 +561,54 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
       mma_commit(drain);
       mbar_wait_bounded(drain, 0, a.err);
     }
-  } else if (w < 4) {
-    // ---- softmax: thread t owns row t of the tile (TMEM lane t)
-    const int r = tid;
-    const uint32_t lane_base = tmem + ((uint32_t)(w * 32) << 16);
+  } else if (w < 8) {
+    // ---- softmax: two threads per row of the tile (TMEM lane r).  Warp w
+    // takes the column half h = w / 4 of every step's S and the same half of
+    // O's columns, so that two warps share each SM sub-partition; the two
+    // threads of a row exchange their half's maximum in shared memory.
+    const int r = tid & (kRows - 1), h = w >> 2;
+    const uint32_t lane_base = tmem + ((uint32_t)((w & 3) * 32) << 16);
+    float* xch = reinterpret_cast<float*>(sm + SM::kXch);  // [2 steps][2 halves][128 rows]
+    constexpr int HC = kStepTok / 2;                       // columns of a half
+    constexpr int HB = HC / BS;                            // blocks of a half
+    constexpr int OC = D / 64;                             // 32-column chunks of O per half
+    const uint32_t half_blocks = ((1u << HB) - 1) << (h * HB);
     float m_used = -CUDART_INF_F, l = 0.f;
     bool ok = true;
-    constexpr uint32_t kAllBlocks = (1u << NB) - 1;
     StepIds<NB> sid;
     sid.init(table, jb, je, lane);
     for (int j = 0; j < steps; ++j) {
       const int st = j % OPS, pb = j & 1;
       int ids[NB];
       const uint32_t okb = sid.step(j, a.num_blocks, ids);
-      const int t0 = (jb + j * NB) * BS;
-      // a step where every position of every row of this warp is kept needs no mask
-      const bool interior = __all_sync(0xffffffffu, t0 + kStepTok <= my_lim && okb == kAllBlocks);
+      const int t0 = (jb + j * NB) * BS, th = t0 + h * HC;  // first position of the step, of this half
+      // a half-step where every position of every row of this warp is kept needs no mask
+      const bool interior = __all_sync(0xffffffffu, th + HC <= my_lim && (okb & half_blocks) == half_blocks);
       if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s_ready[pb], (j >> 1) & 1, a.err)))) break;
       fence_after_sync();
-      float sc[2][32];
-      tmem_ld32(lane_base + (uint32_t)pb * kStepTok, sc[0]);
-      tmem_ld32(lane_base + (uint32_t)pb * kStepTok + 32, sc[1]);
-      // the largest raw score (qk_mul >= 0), four independent chains; on a
-      // boundary step `keep` marks the positions this row attends
+      float sc[HC];
+      tmem_ld32(lane_base + (uint32_t)(pb * kStepTok + h * HC), sc);
+      // the largest raw score of this half (qk_mul >= 0), four independent
+      // chains; on a boundary step `keep` marks the positions the row attends
       float mx[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
-      uint64_t keep = ~0ull;
+      uint32_t keep = 0xFFFFFFFFu;
       if (interior) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int c = 0; c < 32; ++c) mx[c & 3] = fmaxf(mx[c & 3], sc[h][c]);
+        for (int c = 0; c < HC; ++c) mx[c & 3] = fmaxf(mx[c & 3], sc[c]);
       } else {
-        const int lim = min(max(my_lim - t0, 0), kStepTok);
-        keep = lim >= 64 ? ~0ull : ((1ull << lim) - 1);
+        const int lim = min(max(my_lim - th, 0), HC);
+        keep = lim >= 32 ? 0xFFFFFFFFu : ((1u << lim) - 1);
 #pragma unroll
-        for (int b = 0; b < NB; ++b)
-          if (!(okb >> b & 1)) keep &= ~(((1ull << BS) - 1) << (b * BS));
+        for (int b = 0; b < HB; ++b)
+          if (!(okb >> (h * HB + b) & 1)) keep &= ~((BS >= 32 ? 0xFFFFFFFFu : ((1u << BS) - 1)) << (b * BS));
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (keep >> (h * 32 + c) & 1) mx[c & 3] = fmaxf(mx[c & 3], sc[h][c]);
+        for (int c = 0; c < HC; ++c)
+          if (keep >> c & 1) mx[c & 3] = fmaxf(mx[c & 3], sc[c]);
       }
-      const float mraw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      const float mine = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      xch[(j & 1) * 2 * kRows + h * kRows + r] = mine;
+      asm volatile("bar.sync 2, 256;" ::: "memory");
+      const float mraw = fmaxf(mine, xch[(j & 1) * 2 * kRows + (h ^ 1) * kRows + r]);
       const float mt = mraw == -CUDART_INF_F ? -CUDART_INF_F : mraw * qk_mul;
       float factor = 1.f;
       if (mt > m_used + kRescaleSlack) {
@@ -600,14 +626,15 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
           !(ok = __all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[pb ^ 1], ((j - 1) >> 1) & 1, a.err))))
         break;
       fence_after_sync();
-      if (rescale) {  // a warp rescales its rows of O together (tcgen05.ld / st are warp-wide)
+      if (rescale) {  // a warp rescales its rows' half of O together (tcgen05.ld / st are warp-wide)
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < OC; ++c) {
           float o[32];
-          tmem_ld32(lane_base + 2 * kStepTok + c * 32, o);
+          const uint32_t col = 2 * kStepTok + (uint32_t)((h * OC + c) * 32);
+          tmem_ld32(lane_base + col, o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] *= factor;
-          tmem_st32(lane_base + 2 * kStepTok + c * 32, o);
+          tmem_st32(lane_base + col, o);
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
@@ -618,25 +645,23 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
       uint8_t* prow = sm + SM::kP + pb * (kRows * kSpan) + r * kSpan;
       auto emit_p = [&](auto masked) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+        for (int c8 = 0; c8 < HC / 8; ++c8) {
+          uint32_t pk[4];
 #pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c = c8 * 8 + 2 * e;
-              float p0 = fast_exp2(fmaf(sc[h][c], qk_mul, nm));
-              float p1 = fast_exp2(fmaf(sc[h][c + 1], qk_mul, nm));
-              if constexpr (decltype(masked)::value) {
-                p0 = keep >> (h * 32 + c) & 1 ? p0 : 0.f;
-                p1 = keep >> (h * 32 + c + 1) & 1 ? p1 : 0.f;
-              }
-              ls[e] += p0 + p1;
-              pk[e] = F8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+          for (int e = 0; e < 4; ++e) {
+            const int c = c8 * 8 + 2 * e;
+            float p0 = fast_exp2(fmaf(sc[c], qk_mul, nm));
+            float p1 = fast_exp2(fmaf(sc[c + 1], qk_mul, nm));
+            if constexpr (decltype(masked)::value) {
+              p0 = keep >> c & 1 ? p0 : 0.f;
+              p1 = keep >> (c + 1) & 1 ? p1 : 0.f;
             }
-            *reinterpret_cast<uint4*>(prow + (((h * 4 + c8) ^ (r & 7)) << 4)) =
-                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            ls[e] += p0 + p1;
+            pk[e] = F8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
           }
+          *reinterpret_cast<uint4*>(prow + (((h * (HC / 8) + c8) ^ (r & 7)) << 4)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
       };
       if (interior)
         emit_p(std::false_type{});
@@ -647,7 +672,7 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
         // V rows of positions no row attends (the tile's last step) become zero
         const int z0 = max(0, max_lim - t0);
         if (z0 < kStepTok) {
-          for (int i = r; i < (kStepTok - z0) * SPANS * 8; i += kRows) {
+          for (int i = tid; i < (kStepTok - z0) * SPANS * 8; i += 2 * kRows) {
             const int p = z0 + i / (SPANS * 8), sp = (i / 8) % SPANS, c = i % 8;
             *reinterpret_cast<uint4*>(sm + SM::kV + st * SM::kTile + sp * (kStepTok * kSpan) + p * kSpan + (c << 4)) =
                 make_uint4(0, 0, 0, 0);
@@ -664,18 +689,25 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
     if (ok && steps > 1)
       ok = __all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[(steps - 2) & 1], ((steps - 2) >> 1) & 1, a.err));
     fence_after_sync();
-    // ---- epilogue
+    // the row's sum: both halves' shares, through the exchange area (every
+    // read of the last step's maxima is done once all 256 threads are here)
+    asm volatile("bar.sync 2, 256;" ::: "memory");
+    xch[h * kRows + r] = l;
+    asm volatile("bar.sync 2, 256;" ::: "memory");
+    l += xch[(h ^ 1) * kRows + r];
+    // ---- epilogue: each thread its half of the row's columns
     const float inv_l = l > 0.f ? 1.f / l : 0.f;
     if constexpr (!PREFIX) {
       if (ok) {
         __nv_bfloat16* orow = a.out + ((size_t)my_qrow * a.num_q_heads + my_qhead) * D;
         const float sc_out = inv_l * a.out_scale;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < OC; ++c) {
           float o[32];
-          tmem_ld32(lane_base + 2 * kStepTok + c * 32, o);
+          const int cc = h * OC + c;
+          tmem_ld32(lane_base + 2 * kStepTok + cc * 32, o);
           if (my_valid) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+            uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
 #pragma unroll
             for (int v = 0; v < 4; ++v)
               dst[v] = make_uint4(pack_bf16x2(o[8 * v] * sc_out, o[8 * v + 1] * sc_out),
@@ -694,10 +726,11 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
       const bool have = ok && steps > 0;
       float* dst = (a.splits == 1 ? a.pre : a.scratch + (size_t)piece * all_rows * PRF) + orow * PRF;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < OC; ++c) {
         float o[32];
+        const int cc = h * OC + c;
         if (have) {
-          tmem_ld32(lane_base + 2 * kStepTok + c * 32, o);
+          tmem_ld32(lane_base + 2 * kStepTok + cc * 32, o);
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = 0.f;
@@ -705,24 +738,25 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
         if (my_valid) {
 #pragma unroll
           for (int v = 0; v < 8; ++v)
-            reinterpret_cast<float4*>(dst + c * 32)[v] = make_float4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+            reinterpret_cast<float4*>(dst + cc * 32)[v] = make_float4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
         }
       }
-      if (my_valid) {
+      if (my_valid && h == 0) {
         dst[D] = have ? m_used : -CUDART_INF_F;
         dst[D + 1] = have ? l : 0.f;
       }
       if (a.splits > 1) {
-        // the last piece of this (kv head, tile) to finish merges them all
+        // the last piece of this (kv head, tile) to finish merges them all,
+        // each thread its half of the row's columns
         __threadfence();
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+        asm volatile("bar.sync 1, 256;" ::: "memory");
         if (tid == 0) {
           int* ctr = a.counters + (size_t)kvh * a.row_tiles + tile;
           const int last = atomicAdd(ctr, 1) == a.splits - 1;
           if (last) *ctr = 0;  // ready for the next call
           *last_s = last;
         }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+        asm volatile("bar.sync 1, 256;" ::: "memory");
         if (*last_s && my_valid) {
           __threadfence();
           float M = -CUDART_INF_F;
@@ -735,7 +769,8 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
           }
           float* out = a.pre + orow * PRF;
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {  // 32 dims at a time
+          for (int c = 0; c < OC; ++c) {  // 32 dims at a time
+            const int cc = h * OC + c;
             float4 acc[8];
 #pragma unroll
             for (int v = 0; v < 8; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -744,7 +779,7 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
               const float wk = fast_exp2(__ldcg(pk + D) - Mc);
 #pragma unroll
               for (int v = 0; v < 8; ++v) {
-                const float4 x = __ldcg(reinterpret_cast<const float4*>(pk + c * 32) + v);
+                const float4 x = __ldcg(reinterpret_cast<const float4*>(pk + cc * 32) + v);
                 acc[v].x += wk * x.x;
                 acc[v].y += wk * x.y;
                 acc[v].z += wk * x.z;
@@ -752,16 +787,18 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
               }
             }
 #pragma unroll
-            for (int v = 0; v < 8; ++v) reinterpret_cast<float4*>(out + c * 32)[v] = acc[v];
+            for (int v = 0; v < 8; ++v) reinterpret_cast<float4*>(out + cc * 32)[v] = acc[v];
           }
-          out[D] = M;
-          out[D + 1] = den;
+          if (h == 0) {
+            out[D] = M;
+            out[D + 1] = den;
+          }
         }
       }
       // the prefix blocks a sequence attends must be those of sequence 0's
       // table (checked once, by kv head 0 and piece 0; entries past a short
       // sequence's end are not read by plain decode either)
-      if (kvh == 0 && piece == 0 && my_valid && (row0 + r) % g == 0) {
+      if (kvh == 0 && piece == 0 && my_valid && h == 0 && (row0 + r) % g == 0) {
         const int nb = min(a.prefix_blocks, (my_lim + BS - 1) / BS);
         const int32_t* mine = a.block_tables + (size_t)my_qrow * a.table_stride;
 #pragma unroll 8
