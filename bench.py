@@ -51,8 +51,8 @@ L2_FLUSH_BYTES = 256 << 20
 
 # DRAM traffic of one decode launch on the default workload, from an ncu
 # capture, valid only for the kernel sources it was taken on.
-TRAFFIC = {"sources_sha256": "c53984008431e87a14284c518f0039ef0545b829f719e839a829f6a11a4dd27f",
-           "bytes_per_launch": 322227200}  # 317.659392 MB read + 4.567808 MB written
+TRAFFIC = {"sources_sha256": "18b3c2532a96fae41aaff179ac9267f64c03b10b684cdb3e4576ad242b130710",
+           "bytes_per_launch": 320088832}  # mean of two launches: 317.65 MB read + 2.44 MB written
 
 WORKLOAD_TEXT = {
     "llama3_8b": "Llama-3-8B-shaped decode layer: 64 seqs, L~U[128,2048], 32 q / 8 kv heads, "

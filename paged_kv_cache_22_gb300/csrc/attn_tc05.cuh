@@ -523,18 +523,25 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
       constexpr uint32_t id_s = idesc_f16kind(kRows, kStepTok, !F8, false);
       constexpr uint32_t id_o = idesc_f16kind(kRows, D, !F8, true);
       uint64_t* ready = F8 ? op_full : full;
+      // Descriptors of the operand bases; an operand at byte offset x from
+      // its base adds x >> 4 to the start-address field (shared addresses
+      // stay below 256 KiB, so the 14-bit field never carries).
+      const uint64_t dq = sw128_desc(smem_addr(sm + SM::kQ), 16, 1024);
+      const uint64_t dk = sw128_desc(smem_addr(sm + SM::kK), 16, 1024);
+      const uint64_t dp = sw128_desc(smem_addr(sm + SM::kP), 16, 1024);
+      // V is MN-major: 64-element spans of D kStepTok rows apart, 8-row groups 1024 B apart
+      const uint64_t dv = sw128_desc(smem_addr(sm + SM::kV), kStepTok * kSpan, 1024);
       auto issue_s = [&](int j) -> bool {
         const int st = j % OPS;
         if (!mbar_wait_bounded(&ready[st], (j / OPS) & 1, a.err)) return false;
         fence_after_sync();
         const uint32_t dst = tmem + (uint32_t)(j & 1) * kStepTok;
+        const uint64_t dks = dk + (uint64_t)((st * SM::kTile) >> 4);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {  // 16 dims per MMA: +32 B inside a span
           const int sp = k / 4, ko = (k % 4) * 32;
-          const uint64_t da = sw128_desc(smem_addr(sm + SM::kQ + sp * (kRows * kSpan) + ko), 16, 1024);
-          const uint64_t db =
-              sw128_desc(smem_addr(sm + SM::kK + st * SM::kTile + sp * (kStepTok * kSpan) + ko), 16, 1024);
-          mma_bf16(dst, da, db, id_s, k > 0);
+          mma_bf16(dst, dq + (uint64_t)((sp * (kRows * kSpan) + ko) >> 4),
+                   dks + (uint64_t)((sp * (kStepTok * kSpan) + ko) >> 4), id_s, k > 0);
         }
         mma_commit(&s_ready[j & 1]);
         return true;
@@ -546,14 +553,12 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
         if (!(ok = mbar_wait_bounded(&p_ready[pb], (j >> 1) & 1, a.err))) break;
         fence_after_sync();
         const int st = j % OPS;
+        const uint64_t dps = dp + (uint64_t)((pb * (kRows * kSpan)) >> 4);
+        const uint64_t dvs = dv + (uint64_t)((st * SM::kTile) >> 4);
 #pragma unroll
-        for (int k = 0; k < kStepTok / 16; ++k) {  // 16 positions per MMA: +32 B in P, +16 rows in V
-          const uint64_t da = sw128_desc(smem_addr(sm + SM::kP + pb * (kRows * kSpan) + k * 32), 16, 1024);
-          // V is MN-major: 64-element spans of D kStepTok rows apart, 8-row groups 1024 B apart
-          const uint64_t db =
-              sw128_desc(smem_addr(sm + SM::kV + st * SM::kTile + k * 16 * kSpan), kStepTok * kSpan, 1024);
-          mma_bf16(tmem + 2 * kStepTok, da, db, id_o, (j > 0 || k > 0) ? 1u : 0u);
-        }
+        for (int k = 0; k < kStepTok / 16; ++k)  // 16 positions per MMA: +32 B in P, +16 rows in V
+          mma_bf16(tmem + 2 * kStepTok, dps + (uint64_t)((k * 32) >> 4), dvs + (uint64_t)((k * 16 * kSpan) >> 4), id_o,
+                   (j > 0 || k > 0) ? 1u : 0u);
         mma_commit(&empty[st]);
         mma_commit(&pv_done[pb]);
       }
@@ -796,14 +801,20 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
         }
       }
       // the prefix blocks a sequence attends must be those of sequence 0's
-      // table (checked once, by kv head 0 and piece 0; entries past a short
-      // sequence's end are not read by plain decode either)
-      if (kvh == 0 && piece == 0 && my_valid && h == 0 && (row0 + r) % g == 0) {
-        const int nb = min(a.prefix_blocks, (my_lim + BS - 1) / BS);
-        const int32_t* mine = a.block_tables + (size_t)my_qrow * a.table_stride;
-#pragma unroll 8
-        for (int jj = 0; jj < nb; ++jj)
-          if (__ldg(mine + jj) != __ldg(a.block_tables + jj)) raise_error(a.err, PKV_DEVERR_BAD_BLOCK_ID);
+      // table: kv head 0's CTAs check the sequences of their rows over their
+      // piece, one (sequence, block) pair per thread at a time (entries past
+      // a short sequence's end are not read by plain decode either)
+      if (kvh == 0) {
+        const int s_lo = row0 / g, s_hi = min(a.num_seqs, (min(row0 + kRows, rows) - 1) / g + 1);
+        const int nblk = je_cap - jb;
+        for (int i = tid; i < (s_hi - s_lo) * nblk; i += 2 * kRows) {
+          const int sq = s_lo + i / nblk, jj = jb + i % nblk;
+          int Ls = __ldg(a.seq_lens + sq);
+          Ls = Ls < 0 ? 0 : (Ls > a.len_clip ? a.len_clip : Ls);
+          if (jj < (Ls + BS - 1) / BS &&
+              __ldg(a.block_tables + (size_t)sq * a.table_stride + jj) != __ldg(a.block_tables + jj))
+            raise_error(a.err, PKV_DEVERR_BAD_BLOCK_ID);
+        }
       }
     }
   }

@@ -7,6 +7,8 @@
 
 namespace pkv {
 
+constexpr int kReduceThreads = 256;  // split-KV reduce: threads per (sequence, query head)
+
 // ----------------------------------------------------------------------------
 // reshape_and_cache: "PagedAttention por dentro" (section "La tabla de páginas
 // (block table)") -- the new token of a sequence goes to the free position of
@@ -150,13 +152,17 @@ cudaError_t launch_gather_kv(const GatherArgs& a, int max_seq_len, cudaStream_t 
 
 // ----------------------------------------------------------------------------
 // split-KV reduce: log-sum-exp merge of per-partition partials.  One CTA per
-// (sequence, query head), one thread per head dimension.
+// (sequence, query head) of 256 threads: 256 / head_dim groups of one
+// thread per head dimension, each group summing every groups-th partition
+// with four independent chains (a row has up to hundreds of partitions, and
+// a single chain per thread left the reduce bound by load latency).
 // ----------------------------------------------------------------------------
 template <class OT>
-__global__ void split_kv_reduce_kernel(ReduceArgs a) {
+__global__ void __launch_bounds__(kReduceThreads) split_kv_reduce_kernel(ReduceArgs a) {
   const int row = blockIdx.x;  // s * Hq + qh
   const int s = row / a.num_q_heads;
-  const int d = threadIdx.x;
+  const int tid = threadIdx.x, D = a.head_dim;
+  const int groups = kReduceThreads / D, grp = tid / D, d = tid % D;
   const int L = a.seq_lens[s];
   int np = L <= 0 ? 0 : (L + a.partition_tokens - 1) / a.partition_tokens;
   if (a.window > 0 && L > a.window) {
@@ -167,32 +173,63 @@ __global__ void split_kv_reduce_kernel(ReduceArgs a) {
     const int pb = a.partition_tokens / bs;
     np = (nb + pb - 1) / pb;
   }
-  OT* out = reinterpret_cast<OT*>(a.out) + (int64_t)row * a.head_dim;
-  if (np > a.max_partitions) {
-    if (d == 0) raise_error(a.err, PKV_DEVERR_BAD_SEQ_LEN);
-  }
+  OT* out = reinterpret_cast<OT*>(a.out) + (int64_t)row * D;
+  if (np > a.max_partitions && tid == 0) raise_error(a.err, PKV_DEVERR_BAD_SEQ_LEN);
   const int n = np < a.max_partitions ? np : a.max_partitions;
   const float* m = a.m_part + (int64_t)row * a.max_partitions;
   const float* l = a.l_part + (int64_t)row * a.max_partitions;
-  const float* o = a.o_part + (int64_t)row * a.max_partitions * a.head_dim;
+  const float* o = a.o_part + (int64_t)row * a.max_partitions * D;
+  __shared__ float red[kReduceThreads / 32];
+  __shared__ float part[kReduceThreads];  // [group][dim] numerators, then [group] denominators
+  // the largest partition maximum, over all threads
   float M = -CUDART_INF_F;
-  for (int p = 0; p < n; ++p) M = fmaxf(M, m[p]);
-  float num = 0.f, den = 0.f;
-  for (int p = 0; p < n; ++p) {
-    const float wgt = l[p] * expf(m[p] - M);
-    den += wgt;
-    num += wgt * o[(int64_t)p * a.head_dim + d];
+  for (int p = tid; p < n; p += kReduceThreads) M = fmaxf(M, m[p]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  if ((tid & 31) == 0) red[tid >> 5] = M;
+  __syncthreads();
+  M = red[0];
+#pragma unroll
+  for (int i = 1; i < kReduceThreads / 32; ++i) M = fmaxf(M, red[i]);
+  // group grp sums the partitions p = grp (mod groups), four independent
+  // chains so that several partitions' loads are in flight at once
+  float num[4] = {0.f, 0.f, 0.f, 0.f}, den[4] = {0.f, 0.f, 0.f, 0.f};
+  int p = grp;
+  for (; p + 3 * groups < n; p += 4 * groups) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int q = p + k * groups;
+      const float wgt = l[q] * expf(m[q] - M);
+      den[k] += wgt;
+      num[k] += wgt * o[(int64_t)q * D + d];
+    }
   }
-  if (d < a.head_dim) out[d] = from_f32<OT>(den > 0.f ? num / den : 0.f);
+  for (; p < n; p += groups) {
+    const float wgt = l[p] * expf(m[p] - M);
+    den[0] += wgt;
+    num[0] += wgt * o[(int64_t)p * D + d];
+  }
+  __syncthreads();  // red[] is read by every thread above
+  part[tid] = (num[0] + num[1]) + (num[2] + num[3]);
+  if (d == 0) red[grp] = (den[0] + den[1]) + (den[2] + den[3]);
+  __syncthreads();
+  if (grp == 0) {
+    float nu = 0.f, de = 0.f;
+    for (int g2 = 0; g2 < groups; ++g2) {
+      nu += part[g2 * D + d];
+      de += red[g2];
+    }
+    out[d] = from_f32<OT>(de > 0.f ? nu / de : 0.f);
+  }
 }
 
 cudaError_t launch_split_kv_reduce(const ReduceArgs& a, int out_is_bf16, cudaStream_t stream) {
   if (a.num_seqs == 0) return cudaSuccess;
   const unsigned rows = (unsigned)a.num_seqs * a.num_q_heads;
   if (out_is_bf16)
-    split_kv_reduce_kernel<__nv_bfloat16><<<rows, a.head_dim, 0, stream>>>(a);
+    split_kv_reduce_kernel<__nv_bfloat16><<<rows, kReduceThreads, 0, stream>>>(a);
   else
-    split_kv_reduce_kernel<float><<<rows, a.head_dim, 0, stream>>>(a);
+    split_kv_reduce_kernel<float><<<rows, kReduceThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
