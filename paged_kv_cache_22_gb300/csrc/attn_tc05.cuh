@@ -83,13 +83,17 @@ constexpr float kRescaleSlack = 8.f;
 // Warps: 0-7 softmax (two per row of the tile); then the tensor-copy
 // producers: two for bf16 caches (K and V: a copy costs its issuing thread
 // about a hundred cycles, and a step needs up to 32 of them), one for fp8
-// caches (half the copies); then the MMA issuer; then, for fp8 caches, two
-// converter warps.  At most three warps share an SM sub-partition, so that
-// each thread may hold 168 registers.
+// caches (half the copies); then the MMA issuers: for bf16 caches one for
+// S = Q K^T and one for O += P V (an MMA costs its issuing thread tens of
+// cycles, and a step has twelve), one for both with fp8 caches; then, for
+// fp8 caches, two converter warps.  Twelve warps either way: at most three
+// share an SM sub-partition, so that each thread may hold 168 registers.
 constexpr int kConvWarps = 2;
 __host__ __device__ constexpr int prod_warps(bool f8) { return f8 ? 1 : 2; }
+__host__ __device__ constexpr int mma_warps(bool f8) { return f8 ? 1 : 2; }
 __host__ __device__ constexpr int mma_warp(bool f8) { return 8 + prod_warps(f8); }
-__host__ __device__ constexpr int threads(bool f8) { return (mma_warp(f8) + 1 + (f8 ? kConvWarps : 0)) * 32; }
+__host__ __device__ constexpr int conv_warp(bool f8) { return mma_warp(f8) + mma_warps(f8); }
+__host__ __device__ constexpr int threads(bool f8) { return (conv_warp(f8) + (f8 ? kConvWarps : 0)) * 32; }
 
 // Shared memory per CTA: one CTA per SM (the 320-448 threads' registers
 // fill the SM's file), which keeps 1 KiB of the SM's 228 KiB for the system;
@@ -323,18 +327,18 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
   if (tid == 0) {
     for (int i = 0; i < LS; ++i) {
       mbar_init(&full[i], prod_warps(F8));  // every producer warp arrives
-      mbar_init(&raw_free[i], kConvWarps * 32);
+      mbar_init(&raw_free[i], kConvWarps);  // lane 0 of every converter warp
     }
     for (int i = 0; i < OPS; ++i) {
       mbar_init(&empty[i], 1);
-      mbar_init(&op_full[i], kConvWarps * 32);
+      mbar_init(&op_full[i], kConvWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_ready[i], 1);
-      mbar_init(&p_ready[i], 8 * 32);
+      mbar_init(&p_ready[i], 8);  // lane 0 of every softmax warp
       mbar_init(&pv_done[i], 1);
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, mma_warps(F8));
     *max_lim_s = 0;
     *last_s = 0;
     *maxq_s = 0u;
@@ -489,10 +493,10 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
     if (lane == 0)
       for (int j = max(0, armed - LS); j < armed; ++j)
         if (!mbar_wait_bounded(&full[j % LS], (j / LS) & 1, a.err)) break;
-  } else if (F8 && w > mma_warp(F8)) {
+  } else if (F8 && w >= conv_warp(F8)) {
     // ---- converters (fp8): raw e4m3 rows -> fp16 operand tiles, exact; V
     // rows at positions no row attends become zero
-    const int ct = tid - (mma_warp(F8) + 1) * 32;
+    const int ct = tid - conv_warp(F8) * 32;
     for (int j = 0; j < steps; ++j) {
       const int rs = j % LS, st = j % OPS;
       const bool got = mbar_wait_bounded(&full[rs], (j / LS) & 1, a.err) &&
@@ -514,11 +518,15 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
         *reinterpret_cast<uint4*>(op + (((c0 + 1) ^ (p & 7)) << 4)) = hi;
       }
       fence_proxy_async_smem();
-      mbar_arrive(&raw_free[rs]);
-      mbar_arrive(&op_full[st]);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&raw_free[rs]);
+        mbar_arrive(&op_full[st]);
+      }
     }
-  } else if (w == mma_warp(F8)) {
-    // ---- MMA issue: S(j + 1) = Q K(j + 1)^T while the softmax warps work on step j
+  } else if (w >= mma_warp(F8) && w < conv_warp(F8)) {
+    // ---- MMA issue: S(j + 1) = Q K(j + 1)^T while the softmax warps work on
+    // step j, O += P(j) V(j) once they have written P(j)
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_f16kind(kRows, kStepTok, !F8, false);
       constexpr uint32_t id_o = idesc_f16kind(kRows, D, !F8, true);
@@ -546,11 +554,11 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
         mma_commit(&s_ready[j & 1]);
         return true;
       };
-      bool ok = steps == 0 || issue_s(0);
-      for (int j = 0; ok && j < steps; ++j) {
-        if (j + 1 < steps && !(ok = issue_s(j + 1))) break;
+      // O += P(j) V(j) once the softmax warps have written P(j); the K/V
+      // stage is free after it (S(j) completed before P(j) could be written)
+      auto issue_pv = [&](int j) -> bool {
         const int pb = j & 1;  // P buffer of this step
-        if (!(ok = mbar_wait_bounded(&p_ready[pb], (j >> 1) & 1, a.err))) break;
+        if (!mbar_wait_bounded(&p_ready[pb], (j >> 1) & 1, a.err)) return false;
         fence_after_sync();
         const int st = j % OPS;
         const uint64_t dps = dp + (uint64_t)((pb * (kRows * kSpan)) >> 4);
@@ -561,6 +569,24 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
                    (j > 0 || k > 0) ? 1u : 0u);
         mma_commit(&empty[st]);
         mma_commit(&pv_done[pb]);
+        return true;
+      };
+      if constexpr (mma_warps(F8) == 1) {
+        bool ok = steps == 0 || issue_s(0);
+        for (int j = 0; ok && j < steps; ++j) {
+          if (j + 1 < steps && !(ok = issue_s(j + 1))) break;
+          ok = issue_pv(j);
+        }
+      } else if (w == mma_warp(F8)) {
+        // S(j) goes into S buffer j & 1 once the softmax warps have read
+        // S(j - 2) out of it (they arrive on P(j - 2) after that)
+        for (int j = 0; j < steps; ++j) {
+          if (j >= 2 && !mbar_wait_bounded(&p_ready[j & 1], ((j - 2) >> 1) & 1, a.err)) break;
+          if (!issue_s(j)) break;
+        }
+      } else {
+        for (int j = 0; j < steps; ++j)
+          if (!issue_pv(j)) break;
       }
       // every MMA issued has completed before TMEM is released
       mma_commit(drain);
@@ -686,7 +712,8 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
       }
       fence_proxy_async_smem();
       fence_before_sync();
-      mbar_arrive(&p_ready[pb]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_ready[pb]);
     }
     // every P.V issued has completed before O is read
     if (ok && steps > 0)
