@@ -78,6 +78,11 @@ namespace tc05 {
 constexpr int kRows = 128;     // query rows per CTA (TMEM lanes)
 constexpr int kStepTok = 64;   // positions per step
 constexpr int kSpan = 128;     // bytes of one 128-byte swizzle span
+// S buffers in tensor memory: S(j) is computed while the softmax warps still
+// work on S(j - 1) and S(j - 2), so that the issue and the latency of its
+// MMAs stay off their critical path; O follows the S buffers.
+constexpr int kSBuf = 3;
+constexpr int kOCol = kSBuf * kStepTok;
 constexpr float kRescaleSlack = 8.f;
 
 // Warps: 0-7 softmax (two per row of the tile); then the tensor-copy
@@ -126,13 +131,13 @@ struct Layout {
   static constexpr int kRawV = kRawK + kRawStages * kRawTile;
   static constexpr int kP = kRawV + kRawStages * kRawTile;       // [2][128 rows][64 pos], 16-bit
   static constexpr int kBar = kP + kPBytes;
-  static constexpr int kNumBars = 2 * kLandStages + 2 * kOpStages + 7;
+  static constexpr int kNumBars = 2 * kLandStages + 2 * kOpStages + 2 * kSBuf + 5;
   static constexpr int kXch = (kBar + 8 * kNumBars + 15) / 16 * 16;  // [2][2][128] floats: row maxima, sums
   static constexpr int kMisc = kXch + 4 * kRows * 4;             // int max_lim, int merge flag, float max|q|
   static constexpr int kTmemSlot = kMisc + 16;
   static constexpr int kBytes = kTmemSlot + 16;
-  static constexpr uint32_t kTmemCols = 256;                     // S double buffer + O, a power of two
-  static_assert(kTmemCols >= 2 * kStepTok + D, "TMEM columns");
+  static constexpr uint32_t kTmemCols = 512;                     // S buffers + O, a power of two
+  static_assert(kTmemCols >= kSBuf * kStepTok + D, "TMEM columns");
   static_assert(!F8 || D == 128, "fp8 rows of one swizzle span");
   static_assert(kOpStages >= 2 && (!F8 || kRawStages >= 2), "at least double buffering");
   static_assert(kBytes <= smem_budget(D) + kSmemReserve, "shared memory");
@@ -202,6 +207,15 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
                : "memory");
+}
+
+// One lane of a converged warp (the lowest active one), chosen by the hardware.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
 }
 
 __device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -315,8 +329,9 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
   uint64_t* raw_free = full + LS;                               // [LS] fp8: raw codes read
   uint64_t* empty = raw_free + LS;                              // [OPS] operand tiles free (P.V done)
   uint64_t* op_full = empty + OPS;                              // [OPS] fp8: operand tiles written
-  uint64_t* s_ready = op_full + OPS;                            // [2] S buffers
-  uint64_t* p_ready = s_ready + 2;                              // [2] P buffers written
+  uint64_t* s_ready = op_full + OPS;                            // [kSBuf] S computed
+  uint64_t* s_free = s_ready + kSBuf;                           // [kSBuf] S read by the softmax warps
+  uint64_t* p_ready = s_free + kSBuf;                           // [2] P buffers written
   uint64_t* pv_done = p_ready + 2;                              // [2] P.V of a P buffer done
   uint64_t* drain = pv_done + 2;
   int* max_lim_s = reinterpret_cast<int*>(sm + SM::kMisc);
@@ -333,9 +348,12 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
       mbar_init(&empty[i], 1);
       mbar_init(&op_full[i], kConvWarps);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSBuf; ++i) {
       mbar_init(&s_ready[i], 1);
-      mbar_init(&p_ready[i], 8);  // lane 0 of every softmax warp
+      mbar_init(&s_free[i], 8);  // lane 0 of every softmax warp
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&p_ready[i], 8);
       mbar_init(&pv_done[i], 1);
     }
     mbar_init(drain, mma_warps(F8));
@@ -463,11 +481,12 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
       const int st = j % LS;
       int ids[NB];
       const uint32_t ok = sid.step(j, a.num_blocks, ids);
-      if (!__all_sync(0xffffffffu, lane != 0 || mbar_wait_bounded(&freed[st], ((j / LS) & 1) ^ 1, a.err))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&freed[st], ((j / LS) & 1) ^ 1, a.err))) break;
       armed = j + 1;
-      if (lane == 0) {
-        const int left = je - jb - j * NB;
-        const uint32_t want = left >= NB ? (1u << NB) - 1 : (1u << left) - 1;
+      const int left = je - jb - j * NB;
+      const uint32_t want = left >= NB ? (1u << NB) - 1 : (1u << left) - 1;
+      // every value above is the same on all lanes: one elected lane issues
+      if (elect_one()) {
         if (ok != want && c_lo == 0) raise_error(a.err, PKV_DEVERR_BAD_BLOCK_ID);
         mbar_arrive_expect_tx(&full[st], (uint32_t)(__popc(ok) * (c_hi - c_lo) * BS * D * (F8 ? 1 : 2)));
         for (int c = c_lo; c < c_hi; ++c) {
@@ -490,9 +509,8 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
     }
     // no copy may land after the CTA is gone: wait (bounded) for the last
     // copies of every stage, consumed or not
-    if (lane == 0)
-      for (int j = max(0, armed - LS); j < armed; ++j)
-        if (!mbar_wait_bounded(&full[j % LS], (j / LS) & 1, a.err)) break;
+    for (int j = max(0, armed - LS); j < armed; ++j)
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[j % LS], (j / LS) & 1, a.err))) break;
   } else if (F8 && w >= conv_warp(F8)) {
     // ---- converters (fp8): raw e4m3 rows -> fp16 operand tiles, exact; V
     // rows at positions no row attends become zero
@@ -525,73 +543,83 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
       }
     }
   } else if (w >= mma_warp(F8) && w < conv_warp(F8)) {
-    // ---- MMA issue: S(j + 1) = Q K(j + 1)^T while the softmax warps work on
-    // step j, O += P(j) V(j) once they have written P(j)
-    if (lane == 0) {
-      constexpr uint32_t id_s = idesc_f16kind(kRows, kStepTok, !F8, false);
-      constexpr uint32_t id_o = idesc_f16kind(kRows, D, !F8, true);
-      uint64_t* ready = F8 ? op_full : full;
-      // Descriptors of the operand bases; an operand at byte offset x from
-      // its base adds x >> 4 to the start-address field (shared addresses
-      // stay below 256 KiB, so the 14-bit field never carries).
-      const uint64_t dq = sw128_desc(smem_addr(sm + SM::kQ), 16, 1024);
-      const uint64_t dk = sw128_desc(smem_addr(sm + SM::kK), 16, 1024);
-      const uint64_t dp = sw128_desc(smem_addr(sm + SM::kP), 16, 1024);
-      // V is MN-major: 64-element spans of D kStepTok rows apart, 8-row groups 1024 B apart
-      const uint64_t dv = sw128_desc(smem_addr(sm + SM::kV), kStepTok * kSpan, 1024);
-      auto issue_s = [&](int j) -> bool {
-        const int st = j % OPS;
-        if (!mbar_wait_bounded(&ready[st], (j / OPS) & 1, a.err)) return false;
-        fence_after_sync();
-        const uint32_t dst = tmem + (uint32_t)(j & 1) * kStepTok;
-        const uint64_t dks = dk + (uint64_t)((st * SM::kTile) >> 4);
+    // ---- MMA issue: S(j) = Q K(j)^T into S buffer j % kSBuf ahead of the
+    // softmax warps, O += P(j) V(j) once they have written P(j).  The whole
+    // warp runs the loop (its values stay warp-uniform); one elected lane
+    // issues each group of MMAs and their commit.
+    constexpr uint32_t id_s = idesc_f16kind(kRows, kStepTok, !F8, false);
+    constexpr uint32_t id_o = idesc_f16kind(kRows, D, !F8, true);
+    uint64_t* ready = F8 ? op_full : full;
+    // Descriptors of the operand bases; an operand at byte offset x from
+    // its base adds x >> 4 to the start-address field (shared addresses
+    // stay below 256 KiB, so the 14-bit field never carries).
+    const uint64_t dq = sw128_desc(smem_addr(sm + SM::kQ), 16, 1024);
+    const uint64_t dk = sw128_desc(smem_addr(sm + SM::kK), 16, 1024);
+    const uint64_t dp = sw128_desc(smem_addr(sm + SM::kP), 16, 1024);
+    // V is MN-major: 64-element spans of D kStepTok rows apart, 8-row groups 1024 B apart
+    const uint64_t dv = sw128_desc(smem_addr(sm + SM::kV), kStepTok * kSpan, 1024);
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, a.err));
+    };
+    // S(j): its buffer is free once the softmax warps have read S(j - kSBuf)
+    auto issue_s = [&](int j) -> bool {
+      const int sb = j % kSBuf, st = j % OPS;
+      if (j >= kSBuf && !wait_all(&s_free[sb], ((j / kSBuf) - 1) & 1)) return false;
+      if (!wait_all(&ready[st], (j / OPS) & 1)) return false;
+      fence_after_sync();
+      const uint32_t dst = tmem + (uint32_t)(sb * kStepTok);
+      const uint64_t dks = dk + (uint64_t)((st * SM::kTile) >> 4);
+      if (elect_one()) {
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {  // 16 dims per MMA: +32 B inside a span
           const int sp = k / 4, ko = (k % 4) * 32;
           mma_bf16(dst, dq + (uint64_t)((sp * (kRows * kSpan) + ko) >> 4),
                    dks + (uint64_t)((sp * (kStepTok * kSpan) + ko) >> 4), id_s, k > 0);
         }
-        mma_commit(&s_ready[j & 1]);
-        return true;
-      };
-      // O += P(j) V(j) once the softmax warps have written P(j); the K/V
-      // stage is free after it (S(j) completed before P(j) could be written)
-      auto issue_pv = [&](int j) -> bool {
-        const int pb = j & 1;  // P buffer of this step
-        if (!mbar_wait_bounded(&p_ready[pb], (j >> 1) & 1, a.err)) return false;
-        fence_after_sync();
-        const int st = j % OPS;
-        const uint64_t dps = dp + (uint64_t)((pb * (kRows * kSpan)) >> 4);
-        const uint64_t dvs = dv + (uint64_t)((st * SM::kTile) >> 4);
+        mma_commit(&s_ready[sb]);
+      }
+      __syncwarp();
+      return true;
+    };
+    // O += P(j) V(j) once the softmax warps have written P(j); the K/V
+    // stage is free after it (S(j) completed before P(j) could be written)
+    auto issue_pv = [&](int j) -> bool {
+      const int pb = j & 1;  // P buffer of this step
+      if (!wait_all(&p_ready[pb], (j >> 1) & 1)) return false;
+      fence_after_sync();
+      const int st = j % OPS;
+      const uint64_t dps = dp + (uint64_t)((pb * (kRows * kSpan)) >> 4);
+      const uint64_t dvs = dv + (uint64_t)((st * SM::kTile) >> 4);
+      if (elect_one()) {
 #pragma unroll
         for (int k = 0; k < kStepTok / 16; ++k)  // 16 positions per MMA: +32 B in P, +16 rows in V
-          mma_bf16(tmem + 2 * kStepTok, dps + (uint64_t)((k * 32) >> 4), dvs + (uint64_t)((k * 16 * kSpan) >> 4), id_o,
+          mma_bf16(tmem + kOCol, dps + (uint64_t)((k * 32) >> 4), dvs + (uint64_t)((k * 16 * kSpan) >> 4), id_o,
                    (j > 0 || k > 0) ? 1u : 0u);
         mma_commit(&empty[st]);
         mma_commit(&pv_done[pb]);
-        return true;
-      };
-      if constexpr (mma_warps(F8) == 1) {
-        bool ok = steps == 0 || issue_s(0);
-        for (int j = 0; ok && j < steps; ++j) {
-          if (j + 1 < steps && !(ok = issue_s(j + 1))) break;
-          ok = issue_pv(j);
-        }
-      } else if (w == mma_warp(F8)) {
-        // S(j) goes into S buffer j & 1 once the softmax warps have read
-        // S(j - 2) out of it (they arrive on P(j - 2) after that)
-        for (int j = 0; j < steps; ++j) {
-          if (j >= 2 && !mbar_wait_bounded(&p_ready[j & 1], ((j - 2) >> 1) & 1, a.err)) break;
-          if (!issue_s(j)) break;
-        }
-      } else {
-        for (int j = 0; j < steps; ++j)
-          if (!issue_pv(j)) break;
       }
-      // every MMA issued has completed before TMEM is released
-      mma_commit(drain);
-      mbar_wait_bounded(drain, 0, a.err);
+      __syncwarp();
+      return true;
+    };
+    bool ok = true;
+    if constexpr (mma_warps(F8) == 1) {
+      // S runs LA steps ahead of P.V, no further than the S buffers allow
+      // nor than the operand stages: S(j) needs stage j % OPS, which only
+      // P.V(j - OPS) frees, and this loop issues that after S(j - OPS + LA)
+      constexpr int LA = (kSBuf < OPS ? kSBuf : OPS) - 1;
+      for (int j = 0; ok && j < steps + LA; ++j) {
+        if (j < steps) ok = issue_s(j);
+        if (ok && j >= LA) ok = issue_pv(j - LA);
+      }
+    } else if (w == mma_warp(F8)) {
+      for (int j = 0; ok && j < steps; ++j) ok = issue_s(j);
+    } else {
+      for (int j = 0; ok && j < steps; ++j) ok = issue_pv(j);
     }
+    // every MMA issued has completed before TMEM is released
+    if (elect_one()) mma_commit(drain);
+    __syncwarp();
+    wait_all(drain, 0);
   } else if (w < 8) {
     // ---- softmax: two threads per row of the tile (TMEM lane r).  Warp w
     // takes the column half h = w / 4 of every step's S and the same half of
@@ -615,10 +643,15 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
       const int t0 = (jb + j * NB) * BS, th = t0 + h * HC;  // first position of the step, of this half
       // a half-step where every position of every row of this warp is kept needs no mask
       const bool interior = __all_sync(0xffffffffu, th + HC <= my_lim && (okb & half_blocks) == half_blocks);
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s_ready[pb], (j >> 1) & 1, a.err)))) break;
+      const int sb = j % kSBuf;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s_ready[sb], (j / kSBuf) & 1, a.err)))) break;
       fence_after_sync();
       float sc[HC];
-      tmem_ld32(lane_base + (uint32_t)(pb * kStepTok + h * HC), sc);
+      tmem_ld32(lane_base + (uint32_t)(sb * kStepTok + h * HC), sc);
+      // S buffer sb may take S(j + kSBuf) now
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[sb]);
       // the largest raw score of this half (qk_mul >= 0), four independent
       // chains; on a boundary step `keep` marks the positions the row attends
       float mx[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
@@ -661,7 +694,7 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
 #pragma unroll
         for (int c = 0; c < OC; ++c) {
           float o[32];
-          const uint32_t col = 2 * kStepTok + (uint32_t)((h * OC + c) * 32);
+          const uint32_t col = kOCol + (uint32_t)((h * OC + c) * 32);
           tmem_ld32(lane_base + col, o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] *= factor;
@@ -737,7 +770,7 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
         for (int c = 0; c < OC; ++c) {
           float o[32];
           const int cc = h * OC + c;
-          tmem_ld32(lane_base + 2 * kStepTok + cc * 32, o);
+          tmem_ld32(lane_base + kOCol + cc * 32, o);
           if (my_valid) {
             uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
 #pragma unroll
@@ -762,7 +795,7 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
         float o[32];
         const int cc = h * OC + c;
         if (have) {
-          tmem_ld32(lane_base + 2 * kStepTok + cc * 32, o);
+          tmem_ld32(lane_base + kOCol + cc * 32, o);
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = 0.f;
