@@ -76,13 +76,16 @@ struct Tc05Args {
 namespace tc05 {
 
 constexpr int kRows = 128;     // query rows per CTA (TMEM lanes)
-constexpr int kStepTok = 64;   // positions per step
+// Positions per step: 128 for bf16 caches (fewer steps, so the fixed costs of
+// a step -- barrier waits, table ids, the row-maximum exchange -- are spread
+// over more work), 64 for fp8 caches (whose raw and operand rings would not
+// fit shared memory at 128).
+__host__ __device__ constexpr int step_tok(bool f8) { return f8 ? 64 : 128; }
 constexpr int kSpan = 128;     // bytes of one 128-byte swizzle span
 // S buffers in tensor memory: S(j) is computed while the softmax warps still
 // work on S(j - 1) and S(j - 2), so that the issue and the latency of its
 // MMAs stay off their critical path; O follows the S buffers.
 constexpr int kSBuf = 3;
-constexpr int kOCol = kSBuf * kStepTok;
 constexpr float kRescaleSlack = 8.f;
 
 // Warps: 0-7 softmax (two per row of the tile); then the tensor-copy
@@ -109,11 +112,14 @@ __host__ __device__ constexpr int smem_budget(int) { return kSmemPerSm - 1024 - 
 
 template <int D, bool F8>
 struct Layout {
+  static constexpr int kStepTok = step_tok(F8);
+  static constexpr int kOCol = kSBuf * kStepTok;                 // TMEM column of O
   static constexpr int kSpans = D / 64;                          // 64 16-bit elements per span
   static constexpr int kQBytes = kSpans * kRows * kSpan;
-  static constexpr int kPBytes = 2 * kRows * kSpan;
+  static constexpr int kPBuf = kRows * kStepTok * 2;             // one P buffer: [pos span][128 rows][128 B]
+  static constexpr int kPBytes = 2 * kPBuf;
   static constexpr int kTile = kSpans * kStepTok * kSpan;        // one cache's operand tile of a step
-  static constexpr int kRawTile = F8 ? kStepTok * D : 0;         // fp8: [64 pos][D B] as copied
+  static constexpr int kRawTile = F8 ? kStepTok * D : 0;         // fp8: [step pos][D B] as copied
   // The copies must run several steps ahead of the MMAs (a tensor copy
   // takes microseconds; a step a few hundred cycles): as many K/V stages as
   // shared memory holds.  fp8: two operand stages and a deep ring of raw
@@ -125,11 +131,11 @@ struct Layout {
   static constexpr int kRawStages = kRawStagesFit > 8 ? 8 : kRawStagesFit;
   static constexpr int kLandStages = F8 ? kRawStages : kOpStages;  // stages the tensor copies fill
   static constexpr int kQ = 0;                                   // [span][128 rows][128 B]
-  static constexpr int kK = kQ + kQBytes;                        // [stage][span][64 pos][128 B]
+  static constexpr int kK = kQ + kQBytes;                        // [stage][span][step pos][128 B]
   static constexpr int kV = kK + kOpStages * kTile;
   static constexpr int kRawK = kV + kOpStages * kTile;
   static constexpr int kRawV = kRawK + kRawStages * kRawTile;
-  static constexpr int kP = kRawV + kRawStages * kRawTile;       // [2][128 rows][64 pos], 16-bit
+  static constexpr int kP = kRawV + kRawStages * kRawTile;       // [2][pos span][128 rows][64 pos], 16-bit
   static constexpr int kBar = kP + kPBytes;
   static constexpr int kNumBars = 2 * kLandStages + 2 * kOpStages + 2 * kSBuf + 5;
   static constexpr int kXch = (kBar + 8 * kNumBars + 15) / 16 * 16;  // [2][2][128] floats: row maxima, sums
@@ -282,6 +288,7 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
     attn_tc05_kernel(const __grid_constant__ Tc05Args a, const __grid_constant__ TmaMaps maps) {
   using namespace tc05;
   using SM = Layout<D, F8>;
+  constexpr int kStepTok = SM::kStepTok, kOCol = SM::kOCol;
   constexpr int NB = kStepTok / BS;  // blocks per step
   constexpr int SPANS = SM::kSpans;
   constexpr int NT = threads(F8);
@@ -588,13 +595,13 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
       if (!wait_all(&p_ready[pb], (j >> 1) & 1)) return false;
       fence_after_sync();
       const int st = j % OPS;
-      const uint64_t dps = dp + (uint64_t)((pb * (kRows * kSpan)) >> 4);
+      const uint64_t dps = dp + (uint64_t)((pb * SM::kPBuf) >> 4);
       const uint64_t dvs = dv + (uint64_t)((st * SM::kTile) >> 4);
       if (elect_one()) {
 #pragma unroll
         for (int k = 0; k < kStepTok / 16; ++k)  // 16 positions per MMA: +32 B in P, +16 rows in V
-          mma_bf16(tmem + kOCol, dps + (uint64_t)((k * 32) >> 4), dvs + (uint64_t)((k * 16 * kSpan) >> 4), id_o,
-                   (j > 0 || k > 0) ? 1u : 0u);
+          mma_bf16(tmem + kOCol, dps + (uint64_t)(((k / 4) * (kRows * kSpan) + (k % 4) * 32) >> 4),
+                   dvs + (uint64_t)((k * 16 * kSpan) >> 4), id_o, (j > 0 || k > 0) ? 1u : 0u);
         mma_commit(&empty[st]);
         mma_commit(&pv_done[pb]);
       }
@@ -646,8 +653,10 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
       const int sb = j % kSBuf;
       if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s_ready[sb], (j / kSBuf) & 1, a.err)))) break;
       fence_after_sync();
-      float sc[HC];
-      tmem_ld32(lane_base + (uint32_t)(sb * kStepTok + h * HC), sc);
+      float sc2[HC / 32][32];
+#pragma unroll
+      for (int c = 0; c < HC / 32; ++c) tmem_ld32(lane_base + (uint32_t)(sb * kStepTok + h * HC + 32 * c), sc2[c]);
+      auto sc = [&](int c) -> float& { return sc2[c / 32][c % 32]; };
       // S buffer sb may take S(j + kSBuf) now
       fence_before_sync();
       __syncwarp();
@@ -655,19 +664,19 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
       // the largest raw score of this half (qk_mul >= 0), four independent
       // chains; on a boundary step `keep` marks the positions the row attends
       float mx[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
-      uint32_t keep = 0xFFFFFFFFu;
+      uint64_t keep = ~0ull;
       if (interior) {
 #pragma unroll
-        for (int c = 0; c < HC; ++c) mx[c & 3] = fmaxf(mx[c & 3], sc[c]);
+        for (int c = 0; c < HC; ++c) mx[c & 3] = fmaxf(mx[c & 3], sc(c));
       } else {
         const int lim = min(max(my_lim - th, 0), HC);
-        keep = lim >= 32 ? 0xFFFFFFFFu : ((1u << lim) - 1);
+        keep = lim >= 64 ? ~0ull : ((1ull << lim) - 1);
 #pragma unroll
         for (int b = 0; b < HB; ++b)
-          if (!(okb >> (h * HB + b) & 1)) keep &= ~((BS >= 32 ? 0xFFFFFFFFu : ((1u << BS) - 1)) << (b * BS));
+          if (!(okb >> (h * HB + b) & 1)) keep &= ~(((1ull << BS) - 1) << (b * BS));
 #pragma unroll
         for (int c = 0; c < HC; ++c)
-          if (keep >> c & 1) mx[c & 3] = fmaxf(mx[c & 3], sc[c]);
+          if (keep >> c & 1) mx[c & 3] = fmaxf(mx[c & 3], sc(c));
       }
       const float mine = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       xch[(j & 1) * 2 * kRows + h * kRows + r] = mine;
@@ -706,7 +715,10 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
       // only masked scores, which give 0
       const float nm = m_used == -CUDART_INF_F ? 0.f : -m_used;
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
-      uint8_t* prow = sm + SM::kP + pb * (kRows * kSpan) + r * kSpan;
+      // this half's positions within P: span (h * HC) / 64, 16-byte chunks
+      // from ((h * HC) % 64) / 8 on
+      uint8_t* prow = sm + SM::kP + pb * SM::kPBuf + ((h * HC) / 64) * (kRows * kSpan) + r * kSpan;
+      const int c0 = ((h * HC) % 64) / 8;
       auto emit_p = [&](auto masked) {
 #pragma unroll
         for (int c8 = 0; c8 < HC / 8; ++c8) {
@@ -714,8 +726,8 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int c = c8 * 8 + 2 * e;
-            float p0 = fast_exp2(fmaf(sc[c], qk_mul, nm));
-            float p1 = fast_exp2(fmaf(sc[c + 1], qk_mul, nm));
+            float p0 = fast_exp2(fmaf(sc(c), qk_mul, nm));
+            float p1 = fast_exp2(fmaf(sc(c + 1), qk_mul, nm));
             if constexpr (decltype(masked)::value) {
               p0 = keep >> c & 1 ? p0 : 0.f;
               p1 = keep >> (c + 1) & 1 ? p1 : 0.f;
@@ -723,8 +735,7 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
             ls[e] += p0 + p1;
             pk[e] = F8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
           }
-          *reinterpret_cast<uint4*>(prow + (((h * (HC / 8) + c8) ^ (r & 7)) << 4)) =
-              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(prow + (((c0 + c8) ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
       };
       if (interior)
