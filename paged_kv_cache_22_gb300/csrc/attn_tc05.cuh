@@ -170,6 +170,23 @@ struct StepIds {
     cur = load(0);
     nxt = load(1);
   }
+  // The same bits without the ids (the softmax warps need only these): one
+  // ballot per chunk of 32 entries.  Called by every lane, steps in order.
+  uint32_t valid = 0;
+  int valid_chunk = -1;
+  __device__ __forceinline__ uint32_t bits(int j, int num_blocks) {
+    const int first = j * NB;
+    if (first / 32 != valid_chunk) {
+      if (first / 32 != chunk) {
+        cur = nxt;
+        ++chunk;
+        nxt = load(chunk + 1);
+      }
+      valid_chunk = chunk;
+      valid = __ballot_sync(0xffffffffu, 32 * chunk + lane < nblk && cur >= 0 && cur < num_blocks);
+    }
+    return (valid >> (first % 32)) & ((1u << NB) - 1);
+  }
   // bit b set when block j * NB + b of the range exists and its id is in the
   // pool; ids[b] the id.  Called by every lane of the warp, steps in order.
   __device__ __forceinline__ uint32_t step(int j, int num_blocks, int (&ids)[NB]) {
@@ -645,8 +662,7 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
     sid.init(table, jb, je, lane);
     for (int j = 0; j < steps; ++j) {
       const int st = j % OPS, pb = j & 1;
-      int ids[NB];
-      const uint32_t okb = sid.step(j, a.num_blocks, ids);
+      const uint32_t okb = sid.bits(j, a.num_blocks);
       const int t0 = (jb + j * NB) * BS, th = t0 + h * HC;  // first position of the step, of this half
       // a half-step where every position of every row of this warp is kept needs no mask
       const bool interior = __all_sync(0xffffffffu, th + HC <= my_lim && (okb & half_blocks) == half_blocks);
