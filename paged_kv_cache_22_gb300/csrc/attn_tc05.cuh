@@ -669,30 +669,32 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
       const int sb = j % kSBuf;
       if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s_ready[sb], (j / kSBuf) & 1, a.err)))) break;
       fence_after_sync();
-      float sc2[HC / 32][32];
-#pragma unroll
-      for (int c = 0; c < HC / 32; ++c) tmem_ld32(lane_base + (uint32_t)(sb * kStepTok + h * HC + 32 * c), sc2[c]);
-      auto sc = [&](int c) -> float& { return sc2[c / 32][c % 32]; };
-      // S buffer sb may take S(j + kSBuf) now
-      fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[sb]);
+      // S is read twice, 32 columns at a time: once for the maximum, once
+      // for the exponentials, so that only 32 scores are live at a time
+      const uint32_t s_col = lane_base + (uint32_t)(sb * kStepTok + h * HC);
       // the largest raw score of this half (qk_mul >= 0), four independent
       // chains; on a boundary step `keep` marks the positions the row attends
       float mx[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
       uint64_t keep = ~0ull;
-      if (interior) {
-#pragma unroll
-        for (int c = 0; c < HC; ++c) mx[c & 3] = fmaxf(mx[c & 3], sc(c));
-      } else {
+      if (!interior) {
         const int lim = min(max(my_lim - th, 0), HC);
         keep = lim >= 64 ? ~0ull : ((1ull << lim) - 1);
 #pragma unroll
         for (int b = 0; b < HB; ++b)
           if (!(okb >> (h * HB + b) & 1)) keep &= ~(((1ull << BS) - 1) << (b * BS));
+      }
 #pragma unroll
-        for (int c = 0; c < HC; ++c)
-          if (keep >> c & 1) mx[c & 3] = fmaxf(mx[c & 3], sc(c));
+      for (int cc = 0; cc < HC / 32; ++cc) {
+        float sc[32];
+        tmem_ld32(s_col + 32 * cc, sc);
+        if (interior) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) mx[c & 3] = fmaxf(mx[c & 3], sc[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (keep >> (32 * cc + c) & 1) mx[c & 3] = fmaxf(mx[c & 3], sc[c]);
+        }
       }
       const float mine = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       xch[(j & 1) * 2 * kRows + h * kRows + r] = mine;
@@ -737,27 +739,37 @@ __global__ void __launch_bounds__(tc05::threads(F8), 1)
       const int c0 = ((h * HC) % 64) / 8;
       auto emit_p = [&](auto masked) {
 #pragma unroll
-        for (int c8 = 0; c8 < HC / 8; ++c8) {
-          uint32_t pk[4];
+        for (int cc = 0; cc < HC / 32; ++cc) {
+          float sc[32];
+          tmem_ld32(s_col + 32 * cc, sc);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = c8 * 8 + 2 * e;
-            float p0 = fast_exp2(fmaf(sc(c), qk_mul, nm));
-            float p1 = fast_exp2(fmaf(sc(c + 1), qk_mul, nm));
-            if constexpr (decltype(masked)::value) {
-              p0 = keep >> c & 1 ? p0 : 0.f;
-              p1 = keep >> (c + 1) & 1 ? p1 : 0.f;
+          for (int c4 = 0; c4 < 4; ++c4) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int c = c4 * 8 + 2 * e;
+              float p0 = fast_exp2(fmaf(sc[c], qk_mul, nm));
+              float p1 = fast_exp2(fmaf(sc[c + 1], qk_mul, nm));
+              if constexpr (decltype(masked)::value) {
+                p0 = keep >> (32 * cc + c) & 1 ? p0 : 0.f;
+                p1 = keep >> (32 * cc + c + 1) & 1 ? p1 : 0.f;
+              }
+              ls[e] += p0 + p1;
+              pk[e] = F8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
             }
-            ls[e] += p0 + p1;
-            pk[e] = F8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+            *reinterpret_cast<uint4*>(prow + (((c0 + 4 * cc + c4) ^ (r & 7)) << 4)) =
+                make_uint4(pk[0], pk[1], pk[2], pk[3]);
           }
-          *reinterpret_cast<uint4*>(prow + (((c0 + c8) ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
       };
       if (interior)
         emit_p(std::false_type{});
       else
         emit_p(std::true_type{});
+      // S buffer sb may take S(j + kSBuf) now
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[sb]);
       l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       if constexpr (!F8) {
         // V rows of positions no row attends (the tile's last step) become zero
