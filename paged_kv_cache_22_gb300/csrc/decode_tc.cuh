@@ -277,20 +277,26 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
   auto issue_next = [&]() {
     if (cw.done) return;
     const int st = issued % NSW;
-    if (lane == 0) {
+    {
+      // every value here is the same on all lanes of the (converged) warp:
+      // one elected lane starts the copies
       const int kvh = cw.unit / a.units_per_kv;
       uint8_t* dst = stages + (size_t)st * STAGE;
       uint64_t* bar = &bars[st];
-      if (next_id >= 0 && next_id < a.num_blocks) {
-        stage_ok[st] = 1;
-        mbar_arrive_expect_tx(bar, STAGE);
-        tma_load_tile<GE>(dst, &maps.k, kvh * BS, next_id, bar);
-        tma_load_tile<GE>(dst + TILE, &maps.v, kvh * BS, next_id, bar);
-      } else {
-        raise_error(a.err, PKV_DEVERR_BAD_BLOCK_ID);
-        stage_ok[st] = 0;
-        mbar_arrive(bar);
+      const bool valid = next_id >= 0 && next_id < a.num_blocks;
+      if (elect_one()) {
+        if (valid) {
+          stage_ok[st] = 1;
+          mbar_arrive_expect_tx(bar, STAGE);
+          tma_load_tile<GE>(dst, &maps.k, kvh * BS, next_id, bar);
+          tma_load_tile<GE>(dst + TILE, &maps.v, kvh * BS, next_id, bar);
+        } else {
+          raise_error(a.err, PKV_DEVERR_BAD_BLOCK_ID);
+          stage_ok[st] = 0;
+          mbar_arrive(bar);
+        }
       }
+      __syncwarp();
     }
     ++issued;
     if (++cj >= cw.je) {

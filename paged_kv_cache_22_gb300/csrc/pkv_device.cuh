@@ -184,6 +184,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
+// One lane of a converged warp (the lowest active one), chosen by the hardware.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // Order this thread's earlier generic-proxy shared-memory accesses before
 // later async-proxy (bulk copy) writes to the same buffer.
 __device__ __forceinline__ void fence_proxy_async_smem() {
