@@ -424,6 +424,22 @@ def time_calls(fn, flush, stream, K: int, warmup: int = 3) -> float:
     return sum(e[0].elapsed_time(e[1]) for e in ev) / K
 
 
+MULTI_KERNEL_LABELS = {
+    "tcgen05": "attn_tc05_kernel (tcgen05.mma, S and O in TMEM)",
+    "multi_query_decode": "decode_tc_kernel (multi-query: 16 (token, head) rows per unit, balanced split, "
+                          "mma.sync m16n8k16)",
+    "mma_sync": "prefix_attention_kernel (MULTI, mma.sync m16n8k16)",
+}
+
+
+def multi_kernel_label(pkv, w, max_q: int) -> str:
+    """The kernel pkv_paged_attention_multi launches for this workload, as the
+    library decides it under the current tcgen05 setting."""
+    k = pkv.multi_kernel_for(w.num_seqs, max_q, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
+                             w.cache_dtype, w.num_blocks)
+    return MULTI_KERNEL_LABELS.get(k, "none")
+
+
 def per_config(pkv, dev, flush, K: int, main_decode_ms: float):
     """Decode-only figures of the other workloads, measured in this process
     with the same flush and events: each entry gives the time per call, the
@@ -530,8 +546,7 @@ def per_config(pkv, dev, flush, K: int, main_decode_ms: float):
         for tag, tc in (("", True), ("_mma_sync", False)) if rows >= 128 else (("", False),):
             with pkv.tcgen05(tc):
                 ms = time_calls(call, flush, stream, K)
-            kern = ("attn_tc05_kernel (tcgen05.mma, S and O in TMEM)" if tc
-                    else "prefix_attention_kernel (MULTI, mma.sync m16n8k16)")
+                kern = multi_kernel_label(pkv, w, max_q)
             if mname == "prefill_chunk512":
                 tf = flops / (ms * 1e-3) / 1e12
                 res[mname + tag] = {"ms": round(ms, 6), "flop": flops, "tflops": round(tf, 2),
@@ -821,11 +836,8 @@ def run_multi(args):
     tables, lens = w.block_tables.to(dev), w.seq_lens.to(dev)
     q_lens = (qs_cpu[1:] - qs_cpu[:-1]).tolist()
     max_q = max(q_lens)
-    # the kernel pkv_paged_attention_multi runs on this workload
-    tc05 = (pkv.get_tcgen05() and (w.cache_dtype == "bf16" or w.head_dim == 128)
-            and max_q * (w.num_q_heads // w.num_kv_heads) >= 128)
-    multi_kernel = ("attn_tc05_kernel (tcgen05.mma, S and O in TMEM)" if tc05
-                    else "prefix_attention_kernel (MULTI), mma.sync m16n8k16")
+    # the kernel pkv_paged_attention_multi runs on this workload (the library's own choice)
+    multi_kernel = multi_kernel_label(pkv, w, max_q)
     out = torch.empty_like(q)
     workspace = pkv.DecodeWorkspace(dev)
     flush = L2Flush(dev)

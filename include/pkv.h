@@ -350,6 +350,37 @@ pkv_status pkv_paged_attention_multi(void* out, const void* q, pkv_dtype q_dtype
                                      void* workspace, size_t workspace_bytes, pkv_stream_t stream);
 
 /*
+ * pkv_multi_kernel_for -- the kernel pkv_paged_attention_multi launches for a
+ * call of this shape under the current pkv_set_tcgen05 setting.  Host only:
+ * nothing is enqueued and no device is needed.  The three kernels compute the
+ * same attention; they differ in how the rows are tiled.
+ *
+ *   PKV_MULTI_TCGEN05       128-row tiles on the tcgen05 tensor cores: a
+ *                           (sequence, kv head) with max_q * Hq / Hkv >= 128,
+ *                           or a cache shape the mma.sync kernel has no
+ *                           instance of
+ *   PKV_MULTI_QUERY_DECODE  the balanced decode kernel with 16 (token, head)
+ *                           rows per unit, each row limited to the positions
+ *                           up to its token: max_q * Hq / Hkv <= 32, Hq / Hkv
+ *                           a power of two up to 16, and an instance for the
+ *                           cache (bf16: head_dim 128 with blocks of 8, 16 or
+ *                           32, head_dim 64 with 16; fp8-e4m3: blocks of 16)
+ *   PKV_MULTI_MMA_SYNC      16-row tiles on mma.sync (every other call)
+ *   PKV_MULTI_NONE          the shape is invalid (num_seqs < 0, max_q <= 0, a
+ *                           bad cache descriptor, Hq not a multiple of Hkv)
+ *                           or no kernel serves it (PKV_ERR_UNSUPPORTED)
+ */
+typedef enum {
+  PKV_MULTI_NONE = 0,
+  PKV_MULTI_TCGEN05 = 1,
+  PKV_MULTI_QUERY_DECODE = 2,
+  PKV_MULTI_MMA_SYNC = 3
+} pkv_multi_kernel;
+
+pkv_multi_kernel pkv_multi_kernel_for(int32_t num_seqs, int32_t max_q, int32_t num_q_heads,
+                                      const pkv_cache_desc* cache);
+
+/*
  * pkv_decode_step -- one decode step of one layer: pkv_kv_reshape_and_cache of
  * the step's new tokens, then pkv_paged_attention_decode, on `stream`.
  *

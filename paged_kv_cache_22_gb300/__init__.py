@@ -38,7 +38,7 @@ import torch
 __all__ = [
     "PkvError", "CacheDesc", "kv_reshape_and_cache", "paged_attention_decode", "decode_step",
     "split_kv_reduce", "cascade_decode", "cascade_workspace_bytes", "paged_attention_multi",
-    "multi_workspace_bytes",
+    "multi_workspace_bytes", "multi_kernel_for", "MULTI_KERNELS",
     "gather_kv", "copy_blocks", "decode_workspace_bytes", "get_device_error", "library", "library_path",
     "DecodeWorkspace", "F32", "BF16", "FP8_E4M3", "DEVERR_BAD_BLOCK_ID", "DEVERR_BAD_SLOT",
     "DEVERR_BAD_SEQ_LEN", "DEVERR_WAIT_TIMEOUT", "DEVERR_SMEM_ALIGN", "set_decode_engine",
@@ -110,6 +110,7 @@ def library() -> ctypes.CDLL:
             "pkv_get_decode_engine": [],
             "pkv_get_tcgen05": [],
             "pkv_selftest_wait_timeout": [vp],
+            "pkv_multi_kernel_for": [i32, i32, i32, desc],
         }
         for name, args in sigs.items():
             fn = getattr(lib, name)
@@ -344,6 +345,21 @@ def multi_workspace_bytes(num_seqs: int, total_q: int, max_q: int, num_q_heads: 
                           head_dim: int) -> int:
     return int(library().pkv_multi_workspace_bytes(num_seqs, total_q, max_q, num_q_heads, num_kv_heads,
                                                    head_dim))
+
+
+MULTI_KERNELS = {0: None, 1: "tcgen05", 2: "multi_query_decode", 3: "mma_sync"}
+
+
+def multi_kernel_for(num_seqs: int, max_q: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                     block_size: int, cache_dtype: str, num_blocks: int = 1) -> str | None:
+    """The kernel :func:`paged_attention_multi` runs for a call of this shape
+    under the current :func:`set_tcgen05` setting: "tcgen05" (128-row
+    tcgen05 tiles), "multi_query_decode" (the balanced decode kernel, 16
+    (token, head) rows per unit), "mma_sync" (16-row mma.sync tiles), or None
+    for a shape no kernel serves.  Host only."""
+    dt = {"f32": F32, "bf16": BF16, "fp8_e4m3": FP8_E4M3}[cache_dtype]
+    desc = CacheDesc(num_blocks, block_size, num_kv_heads, head_dim, dt)
+    return MULTI_KERNELS[library().pkv_multi_kernel_for(num_seqs, max_q, num_q_heads, ctypes.byref(desc))]
 
 
 def paged_attention_multi(out: torch.Tensor, q: torch.Tensor, q_start: torch.Tensor, k_cache: torch.Tensor,

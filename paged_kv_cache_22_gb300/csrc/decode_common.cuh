@@ -49,6 +49,14 @@ struct DecodeArgs {
   const float* pre;
   float qk_scale;    // scale * log2(e) (* kv_scale for fp8 caches)
   float out_scale;   // 1 (kv_scale for fp8 caches)
+  // several query tokens per sequence (the multi-query instances): sequence
+  // s owns query rows q_start[s] .. q_start[s + 1] - 1 of q and out ([rows,
+  // Hq, D]), its last positions; a unit is (kv head, group of mq_tpu
+  // tokens), its G rows (token, head) = (r / group, r % group) of the group
+  const int32_t* q_start;
+  int mq_tpu;        // tokens per unit (G / group); 0 for one token per sequence
+  int max_q;         // host bound of the query rows per sequence
+  int total_q;       // query rows in all
   // balanced split
   int* counters;     // [num_seqs * units], zero between calls
   float* partials;   // [2 * warps][partial_slot_floats(G, D)]
@@ -251,7 +259,7 @@ __device__ __forceinline__ bool plan_warp(const DecodeArgs& a, int64_t gw, int64
   if constexpr (BALANCED) {
     // sequences with no block to read get their row here (spread over the
     // warps): zero, or in a cascade the shared prefix's result alone
-    for (int64_t s = gw; s < a.num_seqs; s += NW) {
+    for (int64_t s = gw; s < a.num_seqs && !a.q_start; s += NW) {
       if (seq_blocks<BS>(a, (int)s) == 0) {
         // a cascade's prefix partial comes from the grid this one may depend on
         if (a.pre) asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -337,6 +345,24 @@ __device__ __forceinline__ int unit_first_head(const DecodeArgs& a, const Walker
   return kvh * a.group + chunk * G;
 }
 
+// Multi-query: the query rows of sequence s (first row of q, token count);
+// a count beyond the sequence, the host bound or the rows given is flagged
+// and taken as 0 (the sequence's rows are left alone).
+struct MqRows {
+  int q0, T;
+};
+__device__ __forceinline__ MqRows mq_rows(const DecodeArgs& a, int s) {
+  MqRows r;
+  r.q0 = __ldg(a.q_start + s);
+  r.T = __ldg(a.q_start + s + 1) - r.q0;
+  const int L = seq_len_clipped(a, s);
+  if (r.T < 0 || r.T > L || r.T > a.max_q || r.q0 < 0 || r.q0 + r.T > a.total_q) {
+    raise_error(a.err, PKV_DEVERR_BAD_SEQ_LEN);
+    r.T = 0;
+  }
+  return r;
+}
+
 // The partial-result slot of the piece a walker stands on: two per warp, the
 // first for a piece that starts exactly at the warp's range (the tail of a
 // segment begun by earlier warps), the second for any later piece.
@@ -368,7 +394,7 @@ template <class QT, int G, int D>
 __device__ __forceinline__ void merge_segment(const DecodeArgs& a, const CutPiece& cp, int64_t T, int64_t NW,
                                               int lane) {
   constexpr int SLOT = partial_slot_floats(G, D), DV = 4, SL = D / DV;
-  constexpr int NB = G <= 2 ? 8 : (G == 4 ? 4 : 2);  // pieces loaded per round trip
+  constexpr int NB = G <= 2 ? 8 : (G == 4 ? 4 : (G <= 8 ? 2 : 1));  // pieces loaded per round trip
   const int d0 = (lane % SL) * DV;
   // pieces sit on warps w_first..w_last; the first one's slot depends on
   // whether the segment starts exactly at that warp's range
@@ -478,13 +504,21 @@ __device__ __forceinline__ void merge_segment(const DecodeArgs& a, const CutPiec
       for (int off = 16; off > 0; off >>= 1) den[h] += __shfl_xor_sync(0xffffffffu, den[h], off);
   }
   const int kvh = cp.unit / a.units_per_kv, chunk = cp.unit % a.units_per_kv;
-  QT* out = reinterpret_cast<QT*>(a.out) + ((size_t)cp.s * a.num_q_heads + kvh * a.group + chunk * G) * D;
 #pragma unroll
   for (int h = 0; h < G; ++h) {
+    QT* out;
+    if (a.q_start) {  // multi-query: row h is (token chunk * tpu + h / group, head h % group)
+      const MqRows mr = mq_rows(a, cp.s);
+      const int tok = chunk * a.mq_tpu + h / a.group;
+      if (tok >= mr.T) continue;
+      out = reinterpret_cast<QT*>(a.out) + ((size_t)(mr.q0 + tok) * a.num_q_heads + kvh * a.group + h % a.group) * D;
+    } else {
+      out = reinterpret_cast<QT*>(a.out) + ((size_t)cp.s * a.num_q_heads + kvh * a.group + chunk * G + h) * D;
+    }
     if (lane < SL) {
       const float inv = den[h] > 0.f ? a.out_scale / den[h] : 0.f;
 #pragma unroll
-      for (int d = 0; d < DV; ++d) out[h * D + d0 + d] = from_f32<QT>(num[h][d] * inv);
+      for (int d = 0; d < DV; ++d) out[d0 + d] = from_f32<QT>(num[h][d] * inv);
     }
   }
 }

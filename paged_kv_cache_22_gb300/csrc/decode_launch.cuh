@@ -39,6 +39,23 @@ DecodeKernel decode_kernel_info() {
   return k;
 }
 
+// The multi-query instance (several query tokens per sequence; balanced,
+// no remap, 16 rows per unit) on the tensor cores.
+constexpr int kMqRows = 16;
+template <class CT, int D, int BS>
+DecodeKernel decode_mq_kernel_info() {
+  DecodeKernel k;
+  k.fn = reinterpret_cast<const void*>(&decode_tc_kernel<CT, D, BS, kMqRows, kDecodeWarps, true, false, true>);
+  k.smem = TcSmem<CT, D, BS, kMqRows, kDecodeWarps, false>::kBytes;
+  k.tensor_maps = true;
+  k.threads = kDecodeWarps * 32;
+  k.heads_per_unit = kMqRows;
+  return k;
+}
+// bf16 caches: head_dim 128 with blocks of 8, 16, 32, head_dim 64 with 16;
+// fp8 caches: head_dim 64 or 128 with blocks of 16.
+bool find_decode_mq(pkv_dtype dt, int head_dim, int block_size, DecodeKernel* out);
+
 // Fill the tensor maps a kernel reads the caches through (pkv_api.cu); true
 // when the kernel needs none or both were encoded.
 bool encode_cache_maps(const DecodeKernel& k, const pkv_cache_desc* cache, const void* k_cache,

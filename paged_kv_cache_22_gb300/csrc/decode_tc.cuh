@@ -34,6 +34,12 @@
 //    fills rows 0..7 of the m16 operand, the remainder rows 8..15, one MMA
 //    per n-tile serves both, and the two row halves of the accumulator are
 //    summed when the piece ends.
+//  * Several query tokens per sequence (speculative verify, short chunks):
+//    a unit is 16 rows, (token, head) pairs of one kv head, so that rows g
+//    and g + 8 of both m16 operands are query rows.  A lane then keeps two
+//    rows' softmax state, P is one operand of the MMA type (its weights keep
+//    8 significant bits for bf16, 11 for fp16), and each row attends the
+//    positions up to its own token.
 //  * bf16 caches: V arrives through ldmatrix.trans.  fp8 caches: K and V
 //    codes widen exactly to fp16 (cvt e4m3x2 -> f16x2); q is fp16,
 //    pre-scaled by a power of two chosen per piece so that it cannot
@@ -172,7 +178,7 @@ struct TcGeo {
   static constexpr int VPL = D / 8;              // fp8 V: bytes of a token row per lane
   static constexpr int NSW0 = 16384 / STAGE;
   static constexpr int NSW = NSW0 < 2 ? 2 : (NSW0 > 8 ? 8 : NSW0);  // stages per warp
-  static_assert(G >= 1 && G <= 8, "at most 8 query heads per m16 row block");
+  static_assert((G >= 1 && G <= 8) || G == 16, "up to 8 query rows (P head + remainder) or 16");
   static_assert(IB == 128 || IB == 64, "swizzle span");
   static_assert(ROW % IB == 0 && KS % 2 == 0, "tile shape");
   static_assert(!F8 || TB == 16, "fp8 caches: 16-token steps");
@@ -220,9 +226,20 @@ __device__ __forceinline__ uint32_t swz(int row, int c) {
 // ----------------------------------------------------------------------------
 // The kernel.
 // ----------------------------------------------------------------------------
-template <class CT, int D, int BS, int G, int W, bool BALANCED, bool REMAP>
+// MQ: several query tokens per sequence (balanced split, no remap): a unit
+// is (kv head, group of a.mq_tpu tokens) and its G = a.mq_tpu * group rows
+// are (token, head) pairs, each with its own causal limit (G = 16: two rows
+// per lane).
+template <class CT, int D, int BS, int G, int W, bool BALANCED, bool REMAP, bool MQ = false>
 __global__ void __launch_bounds__(W * 32, 8 / W)
     decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ TmaMaps maps) {
+  static_assert(!MQ || (BALANCED && !REMAP), "multi-query: balanced split, no remap");
+  // 16-row units (multi-query): rows g and g + 8 of the m16 operands are both
+  // query rows, and P is a single operand of the MMA type (no remainder)
+  constexpr bool R16 = G == 16;
+  constexpr int RPL = R16 ? 2 : 1;  // query rows per lane: g (and g + 8)
+  constexpr int RE = 2 * RPL;       // score / accumulator entries per n-tile and lane
+  static_assert(!R16 || MQ, "16-row units: multi-query only");
   using GE = TcGeo<CT, D, BS, G>;
   using SM = TcSmem<CT, D, BS, G, W, REMAP>;
   using QT = typename CT::QType;
@@ -307,9 +324,22 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
   };
 
   auto issue_q = [&](const Walker& pw, int slot) {
-    const QT* src = reinterpret_cast<const QT*>(a.q) + ((size_t)pw.s * a.num_q_heads + unit_first_head(a, pw, G)) * D;
-    mbar_arrive_expect_tx(&qbars[slot], G * D * sizeof(QT));
-    bulk_g2s(qbuf + (size_t)slot * G * D, src, G * D * sizeof(QT), &qbars[slot]);
+    if constexpr (MQ) {
+      // the group's heads of each of the unit's tokens: one contiguous run per token
+      const MqRows mr = mq_rows(a, pw.s);
+      const int kvh = pw.unit / a.units_per_kv, tok0 = (pw.unit % a.units_per_kv) * a.mq_tpu;
+      const int nt = max(0, min(a.mq_tpu, mr.T - tok0));
+      const uint32_t run = (uint32_t)(a.group * D * sizeof(QT));
+      mbar_arrive_expect_tx(&qbars[slot], nt * run);
+      for (int i = 0; i < nt; ++i)
+        bulk_g2s(qbuf + (size_t)slot * G * D + (size_t)i * a.group * D,
+                 reinterpret_cast<const QT*>(a.q) + ((size_t)(mr.q0 + tok0 + i) * a.num_q_heads + kvh * a.group) * D,
+                 run, &qbars[slot]);
+    } else {
+      const QT* src = reinterpret_cast<const QT*>(a.q) + ((size_t)pw.s * a.num_q_heads + unit_first_head(a, pw, G)) * D;
+      mbar_arrive_expect_tx(&qbars[slot], G * D * sizeof(QT));
+      bulk_g2s(qbuf + (size_t)slot * G * D, src, G * D * sizeof(QT), &qbars[slot]);
+    }
   };
 
   // cascade: the prefix partial of the G rows of a piece that starts a
@@ -376,16 +406,26 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
     voff8[3] = swz<GE>(2 * t + 9, c) + b;
   }
 
+  // q.K of one k-step into one n-tile's score entries of this lane's rows
+  auto qk_mma = [](float (&c)[RE], const uint32_t (&qk)[RE], uint32_t b0, uint32_t b1) {
+    if constexpr (R16) {
+      mma_k16_rows16<F8>(c, qk[0], qk[1], qk[2], qk[3], b0, b1);
+    } else {
+      mma_k16<F8>(c[0], c[1], qk[0], qk[1], b0, b1);
+    }
+  };
+
   // ---------------------------------------------------------------- consume side
   Walker wk = wk0;
   int consumed = 0, waited = 0, piece = 0;
   CutPiece cut0{}, cut1{};  // this warp's cut pieces (its first and last at most)
   int ncut = 0;
   bool alive = true;
-  uint32_t qa[KS][2];     // q.K A operand: row g, (a0, a2) per k-step
-  float o[NTO][4];        // accumulators, columns 2t, 2t+1 of each n-tile: [0..1] the
-                          // P-head part (row g), [2..3] the P-remainder part (row g+8)
-  float m_run, l_run;     // row g's running max (log2 units) and this lane's share of its sum
+  uint32_t qa[KS][RE];    // q.K A operand per k-step: (a0, a2) of row g, or (a0, a1, a2, a3)
+                          // of rows g and g + 8 (16-row units)
+  float o[NTO][4];        // accumulators, columns 2t, 2t+1 of each n-tile: [0..1] row g,
+                          // [2..3] row g + 8 (16-row units) or the P-remainder part of row g
+  float m_run[RPL], l_run[RPL];  // running max (log2 units) and this lane's share of the sum
 
 #pragma unroll 1
   while (!wk.done) {
@@ -401,29 +441,54 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
     }
     if (!mbar_wait_bounded(&qbars[qslot], (piece >> 1) & 1, a.err)) alive = false;
     float qk_mul = a.qk_scale;
+    // this lane's rows g (+ 8): valid, and (MQ) the positions each attends (below row_lim)
+    bool row_ok[RPL];
+    int row_lim[RPL];
+    MqRows mr{0, 0};
+    if constexpr (MQ) mr = mq_rows(a, wk.s);
+#pragma unroll
+    for (int i = 0; i < RPL; ++i) {
+      row_ok[i] = g + 8 * i < G;
+      row_lim[i] = 0x7FFFFFFF;
+      if constexpr (MQ) {
+        const int tok = (wk.unit % a.units_per_kv) * a.mq_tpu + (g + 8 * i) / a.group;
+        row_ok[i] = row_ok[i] && tok < mr.T;
+        row_lim[i] = seq_len_clipped(a, wk.s) - mr.T + tok + 1;
+      }
+    }
     {
-      const QT* qs = qbuf + (size_t)qslot * G * D + (size_t)(g < G ? g : 0) * D;
+      // operand slot of row i's k pair h (h = 0: k 2t.., h = 1: k 2t + 8..)
+      auto qslot_of = [](int i, int h) { return R16 ? 2 * h + i : h; };
       if constexpr (!F8) {
 #pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-          qa[kk][0] = g < G ? *reinterpret_cast<const uint32_t*>(qs + 16 * kk + 2 * t) : 0u;
-          qa[kk][1] = g < G ? *reinterpret_cast<const uint32_t*>(qs + 16 * kk + 2 * t + 8) : 0u;
+        for (int i = 0; i < RPL; ++i) {
+          const QT* qs = qbuf + (size_t)qslot * G * D + (size_t)(row_ok[i] ? g + 8 * i : 0) * D;
+#pragma unroll
+          for (int kk = 0; kk < KS; ++kk) {
+            qa[kk][qslot_of(i, 0)] = row_ok[i] ? *reinterpret_cast<const uint32_t*>(qs + 16 * kk + 2 * t) : 0u;
+            qa[kk][qslot_of(i, 1)] = row_ok[i] ? *reinterpret_cast<const uint32_t*>(qs + 16 * kk + 2 * t + 8) : 0u;
+          }
         }
       } else {
-        // k-step kk holds dims 16kk + 4t + (0, 1) in a0 and + (2, 3) in a2,
-        // the order in which a K chunk reaches the lane through ldmatrix
-        float qv[KS][4];
+        // k-step kk holds dims 16kk + 4t + (0, 1) in the first pair and
+        // + (2, 3) in the second, the order in which a K chunk reaches the
+        // lane through ldmatrix
+        float qv[RPL][KS][4];
         float mq = 0.f;
 #pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-          const uint2 raw = *reinterpret_cast<const uint2*>(qs + 16 * kk + 4 * t);
-          const float2 lo = bf16x2_to_f2(raw.x), hi = bf16x2_to_f2(raw.y);
-          qv[kk][0] = g < G ? lo.x : 0.f;
-          qv[kk][1] = g < G ? lo.y : 0.f;
-          qv[kk][2] = g < G ? hi.x : 0.f;
-          qv[kk][3] = g < G ? hi.y : 0.f;
+        for (int i = 0; i < RPL; ++i) {
+          const QT* qs = qbuf + (size_t)qslot * G * D + (size_t)(row_ok[i] ? g + 8 * i : 0) * D;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) mq = fmaxf(mq, fabsf(qv[kk][i]));
+          for (int kk = 0; kk < KS; ++kk) {
+            const uint2 raw = *reinterpret_cast<const uint2*>(qs + 16 * kk + 4 * t);
+            const float2 lo = bf16x2_to_f2(raw.x), hi = bf16x2_to_f2(raw.y);
+            qv[i][kk][0] = row_ok[i] ? lo.x : 0.f;
+            qv[i][kk][1] = row_ok[i] ? lo.y : 0.f;
+            qv[i][kk][2] = row_ok[i] ? hi.x : 0.f;
+            qv[i][kk][3] = row_ok[i] ? hi.y : 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) mq = fmaxf(mq, fabsf(qv[i][kk][e]));
+          }
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) mq = fmaxf(mq, __shfl_xor_sync(0xffffffffu, mq, off));
@@ -434,16 +499,21 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
         const float down = ldexpf(1.f, -sh);
         qk_mul = a.qk_scale * ldexpf(1.f, sh);
 #pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-          qa[kk][0] = pack_f16x2(qv[kk][0] * down, qv[kk][1] * down);
-          qa[kk][1] = pack_f16x2(qv[kk][2] * down, qv[kk][3] * down);
-        }
+        for (int i = 0; i < RPL; ++i)
+#pragma unroll
+          for (int kk = 0; kk < KS; ++kk) {
+            qa[kk][qslot_of(i, 0)] = pack_f16x2(qv[i][kk][0] * down, qv[i][kk][1] * down);
+            qa[kk][qslot_of(i, 1)] = pack_f16x2(qv[i][kk][2] * down, qv[i][kk][3] * down);
+          }
       }
     }
 #pragma unroll
     for (int n = 0; n < NTO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    m_run = -CUDART_INF_F;
-    l_run = 0.f;
+#pragma unroll
+    for (int i = 0; i < RPL; ++i) {
+      m_run[i] = -CUDART_INF_F;
+      l_run[i] = 0.f;
+    }
     if constexpr (REMAP) {
       if (a.pre && wk.jb == 0) {
         // cascade: a segment's online softmax starts from the shared prefix's
@@ -456,8 +526,8 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
           for (int n = 0; n < NTO; ++n)
 #pragma unroll
             for (int e = 0; e < 2; ++e) o[n][e] = pr[odim(n, e)];
-          m_run = pr[D];
-          l_run = t == 0 ? pr[D + 1] : 0.f;
+          m_run[0] = pr[D];
+          l_run[0] = t == 0 ? pr[D + 1] : 0.f;
         }
       }
       if (a.pre && !qlook.done && qlook.jb == 0) {  // the next piece starts a segment
@@ -488,10 +558,10 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
         const uint32_t vt = kt + TILE;
         const int t0 = step * TB;  // first token of this step within the tile
 
-        // ---- scores: s[n][e] = q_g . K[8n + 2t + e]
-        float s[GE::NTS][2];
+        // ---- scores: s[n][2i + e] = q_(g + 8i) . K[8n + 2t + e]
+        float s[GE::NTS][RE];
         if constexpr (TB == 16) {
-          float s2[2][2][2] = {};  // even / odd k-steps, two independent chains
+          float s2[2][2][RE] = {};  // even / odd k-steps, two independent chains
           if constexpr (F8) {
 #pragma unroll
             for (int kq = 0; kq < KS / 2; ++kq) {
@@ -501,10 +571,10 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
 #pragma unroll
               for (int m = 0; m < 4; ++m) e4m3x4_to_f16x2x2(r[m], b[m][0], b[m][1]);
               // r[0]: rows 0-7, k-step 2kq; r[1]: rows 8-15, 2kq; r[2], r[3]: k-step 2kq + 1
-              mma_k16<true>(s2[0][0][0], s2[0][0][1], qa[2 * kq][0], qa[2 * kq][1], b[0][0], b[0][1]);
-              mma_k16<true>(s2[0][1][0], s2[0][1][1], qa[2 * kq][0], qa[2 * kq][1], b[1][0], b[1][1]);
-              mma_k16<true>(s2[1][0][0], s2[1][0][1], qa[2 * kq + 1][0], qa[2 * kq + 1][1], b[2][0], b[2][1]);
-              mma_k16<true>(s2[1][1][0], s2[1][1][1], qa[2 * kq + 1][0], qa[2 * kq + 1][1], b[3][0], b[3][1]);
+              qk_mma(s2[0][0], qa[2 * kq], b[0][0], b[0][1]);
+              qk_mma(s2[0][1], qa[2 * kq], b[1][0], b[1][1]);
+              qk_mma(s2[1][0], qa[2 * kq + 1], b[2][0], b[2][1]);
+              qk_mma(s2[1][1], qa[2 * kq + 1], b[3][0], b[3][1]);
             }
           } else {
 #pragma unroll
@@ -512,76 +582,97 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
               uint32_t r[4];
               ldsm_x4(frag(kt + kx, 2 * kk), r);
               // r[0], r[1]: rows 0-7 (b0, b1); r[2], r[3]: rows 8-15
-              mma_k16<false>(s2[kk & 1][0][0], s2[kk & 1][0][1], qa[kk][0], qa[kk][1], r[0], r[1]);
-              mma_k16<false>(s2[kk & 1][1][0], s2[kk & 1][1][1], qa[kk][0], qa[kk][1], r[2], r[3]);
+              qk_mma(s2[kk & 1][0], qa[kk], r[0], r[1]);
+              qk_mma(s2[kk & 1][1], qa[kk], r[2], r[3]);
             }
           }
 #pragma unroll
           for (int n = 0; n < 2; ++n)
 #pragma unroll
-            for (int e = 0; e < 2; ++e) s[n][e] = s2[0][n][e] + s2[1][n][e];
+            for (int e = 0; e < RE; ++e) s[n][e] = s2[0][n][e] + s2[1][n][e];
         } else {
-          float s2[2][2] = {};
+          float s2[2][RE] = {};
 #pragma unroll
           for (int kq = 0; kq < KS / 2; ++kq) {
             uint32_t r[4];
             ldsm_x4(frag(kt + kx, 4 * kq), r);
             // rows 0-7; r[0], r[1]: k-step 2kq; r[2], r[3]: k-step 2kq + 1
-            mma_k16<false>(s2[0][0], s2[0][1], qa[2 * kq][0], qa[2 * kq][1], r[0], r[1]);
-            mma_k16<false>(s2[1][0], s2[1][1], qa[2 * kq + 1][0], qa[2 * kq + 1][1], r[2], r[3]);
+            qk_mma(s2[0], qa[2 * kq], r[0], r[1]);
+            qk_mma(s2[1], qa[2 * kq + 1], r[2], r[3]);
           }
-          s[0][0] = s2[0][0] + s2[1][0];
-          s[0][1] = s2[0][1] + s2[1][1];
+#pragma unroll
+          for (int e = 0; e < RE; ++e) s[0][e] = s2[0][e] + s2[1][e];
         }
 
-        // ---- online softmax of row g (log2 units)
-        float mx = -CUDART_INF_F;
+        // ---- online softmax of rows g (+ 8) (log2 units)
+        float mx[RPL];
+        bool grow = false;
 #pragma unroll
-        for (int n = 0; n < GE::NTS; ++n)
+        for (int i = 0; i < RPL; ++i) {
+          const int rl = MQ ? row_lim[i] - j * BS : BS;  // (MQ) the row's positions kept in the tile
+          mx[i] = -CUDART_INF_F;
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int tok = 8 * n + 2 * t + e;
-            s[n][e] = tm.keep(t0 + tok) ? s[n][e] * qk_mul : -CUDART_INF_F;
-            mx = fmaxf(mx, s[n][e]);
+          for (int n = 0; n < GE::NTS; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int tok = 8 * n + 2 * t + e;
+              float& v = s[n][2 * i + e];
+              v = tm.keep(t0 + tok) && (!MQ || t0 + tok < rl) ? v * qk_mul : -CUDART_INF_F;
+              mx[i] = fmaxf(mx[i], v);
+            }
+          mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
+          mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
+          grow = grow || mx[i] > m_run[i];
+        }
+        if (__any_sync(0xffffffffu, grow)) {
+          float alpha[RPL];
+#pragma unroll
+          for (int i = 0; i < RPL; ++i) {
+            const float m_new = fmaxf(m_run[i], mx[i]);
+            alpha[i] = m_new > m_run[i] ? fast_exp2(m_run[i] - m_new) : 1.f;
+            l_run[i] *= alpha[i];
+            m_run[i] = m_new;
           }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m_run, mx);
-        if (__any_sync(0xffffffffu, m_new > m_run)) {
-          const float alpha = m_new > m_run ? fast_exp2(m_run - m_new) : 1.f;
-          const float2 a2 = make_float2(alpha, alpha);
+          // o[n][2..3] belong to row g + 8 (16-row units) or to row g's P remainder
+          const float2 a0 = make_float2(alpha[0], alpha[0]), a1 = make_float2(alpha[RPL - 1], alpha[RPL - 1]);
 #pragma unroll
           for (int n = 0; n < NTO; ++n) {
-            const float2 v = __fmul2_rn(make_float2(o[n][0], o[n][1]), a2);
-            const float2 u = __fmul2_rn(make_float2(o[n][2], o[n][3]), a2);
+            const float2 v = __fmul2_rn(make_float2(o[n][0], o[n][1]), a0);
+            const float2 u = __fmul2_rn(make_float2(o[n][2], o[n][3]), a1);
             o[n][0] = v.x;
             o[n][1] = v.y;
             o[n][2] = u.x;
             o[n][3] = u.y;
           }
-          l_run *= alpha;
-          m_run = m_new;
         }
-        const float m_use = m_run == -CUDART_INF_F ? 0.f : m_run;
-        float p[GE::NTS][2];
+        float p[GE::NTS][RE];
 #pragma unroll
-        for (int n = 0; n < GE::NTS; ++n)
+        for (int i = 0; i < RPL; ++i) {
+          const float m_use = m_run[i] == -CUDART_INF_F ? 0.f : m_run[i];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            p[n][e] = fast_exp2(s[n][e] - m_use);
-            l_run += p[n][e];
-          }
+          for (int n = 0; n < GE::NTS; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              p[n][2 * i + e] = fast_exp2(s[n][2 * i + e] - m_use);
+              l_run[i] += p[n][2 * i + e];
+            }
+        }
 
         // ---- P . V
         const bool full = tm.all(t0, t0 + TB);
         if constexpr (F8) {
-          // P = head + remainder, both fp16
+          // A rows 0-7 / 8-15: P of rows g / g + 8 (16-row units), or row g's
+          // P as head + remainder, all fp16
           uint32_t ph[2], pl[2];
 #pragma unroll
           for (int n = 0; n < 2; ++n) {
             ph[n] = pack_f16x2(p[n][0], p[n][1]);
-            const float2 h = f16x2_to_f2(ph[n]);
-            pl[n] = pack_f16x2(p[n][0] - h.x, p[n][1] - h.y);
+            if constexpr (R16) {
+              pl[n] = pack_f16x2(p[n][RE - 2], p[n][RE - 1]);
+            } else {
+              const float2 h = f16x2_to_f2(ph[n]);
+              pl[n] = pack_f16x2(p[n][0] - h.x, p[n][1] - h.y);
+            }
           }
           static_assert(GE::VPL == 16 || GE::VPL == 8, "fp8 V slice");
           uint32_t X[4][GE::VPL / 4];  // rows 2t, 2t+1, 2t+8, 2t+9
@@ -616,13 +707,18 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
             for (int k = 0; k < 4; ++k) mma_k16_rows16<true>(o[4 * q + k], ph[0], pl[0], ph[1], pl[1], b0[k], b1[k]);
           }
         } else {
-          // P = head + remainder, both bf16
+          // A rows 0-7 / 8-15: P of rows g / g + 8 (16-row units), or row g's
+          // P as head + remainder, all bf16
           uint32_t ph[GE::NTS], pl[GE::NTS];
 #pragma unroll
           for (int n = 0; n < GE::NTS; ++n) {
             ph[n] = pack_bf16x2(p[n][0], p[n][1]);
-            const float2 h = bf16x2_to_f2(ph[n]);
-            pl[n] = pack_bf16x2(p[n][0] - h.x, p[n][1] - h.y);
+            if constexpr (R16) {
+              pl[n] = pack_bf16x2(p[n][RE - 2], p[n][RE - 1]);
+            } else {
+              const float2 h = bf16x2_to_f2(ph[n]);
+              pl[n] = pack_bf16x2(p[n][0] - h.x, p[n][1] - h.y);
+            }
           }
           // keep-masks of this lane's token pairs (2t, 2t+1) and (2t+8, 2t+9)
           uint32_t keep0 = 0xFFFFFFFFu, keep1 = 0xFFFFFFFFu;
@@ -661,13 +757,21 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
     }
 
     // ------------------------------------------------------------ piece end
+    // row g + 8i's accumulator: o[n][2i + e]; with one row per lane the P
+    // remainder's half is added to the head's
+    if constexpr (!R16) {
 #pragma unroll
-    for (int n = 0; n < NTO; ++n) {
-      o[n][0] += o[n][2];
-      o[n][1] += o[n][3];
+      for (int n = 0; n < NTO; ++n) {
+        o[n][0] += o[n][2];
+        o[n][1] += o[n][3];
+      }
     }
-    float l_row = l_run + __shfl_xor_sync(0xffffffffu, l_run, 1);
-    l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
+    float l_row[RPL];
+#pragma unroll
+    for (int i = 0; i < RPL; ++i) {
+      l_row[i] = l_run[i] + __shfl_xor_sync(0xffffffffu, l_run[i], 1);
+      l_row[i] += __shfl_xor_sync(0xffffffffu, l_row[i], 2);
+    }
     const int qh0 = unit_first_head(a, wk, G);
     const bool whole = (wk.jb == 0 && wk.je == wk.nb);
 
@@ -675,27 +779,34 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
       if (g < G) {
         const int p = (int)(gw % a.max_partitions);
         const size_t row = ((size_t)wk.s * a.num_q_heads + qh0 + g) * a.max_partitions + p;
-        const float inv = l_row > 0.f ? a.out_scale / l_row : 0.f;
+        const float inv = l_row[0] > 0.f ? a.out_scale / l_row[0] : 0.f;
         float* dst = a.o_part + row * D;
 #pragma unroll
         for (int n = 0; n < NTO; ++n)
 #pragma unroll
           for (int e = 0; e < 2; ++e) dst[odim(n, e)] = o[n][e] * inv;
         if (t == 0) {
-          a.m_part[row] = m_run * 0.69314718055994531f;
-          a.l_part[row] = l_row;
+          a.m_part[row] = m_run[0] * 0.69314718055994531f;
+          a.l_part[row] = l_row[0];
         }
       }
     } else if (whole) {
-      if (g < G) {
-        QT* dst = reinterpret_cast<QT*>(a.out) + ((size_t)wk.s * a.num_q_heads + qh0 + g) * D;
-        const float inv = l_row > 0.f ? a.out_scale / l_row : 0.f;
+#pragma unroll
+      for (int i = 0; i < RPL; ++i) {
+        if (!row_ok[i]) continue;
+        const int r = g + 8 * i;
+        QT* dst = reinterpret_cast<QT*>(a.out) +
+                  (MQ ? ((size_t)(mr.q0 + (wk.unit % a.units_per_kv) * a.mq_tpu + r / a.group) * a.num_q_heads +
+                         (wk.unit / a.units_per_kv) * a.group + r % a.group) * D
+                      : ((size_t)wk.s * a.num_q_heads + qh0 + r) * D);
+        const float inv = l_row[i] > 0.f ? a.out_scale / l_row[i] : 0.f;
         if constexpr (F8) {
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             uint32_t pk[NTO / 2];
 #pragma unroll
-            for (int n = 0; n < NTO / 2; ++n) pk[n] = pack_bf16x2(o[2 * n][e] * inv, o[2 * n + 1][e] * inv);
+            for (int n = 0; n < NTO / 2; ++n)
+              pk[n] = pack_bf16x2(o[2 * n][2 * i + e] * inv, o[2 * n + 1][2 * i + e] * inv);
 #pragma unroll
             for (int n = 0; n < NTO / 2; n += 4)
               *reinterpret_cast<uint4*>(dst + odim(2 * n, e)) = make_uint4(pk[n], pk[n + 1], pk[n + 2], pk[n + 3]);
@@ -703,20 +814,25 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
         } else {
 #pragma unroll
           for (int n = 0; n < NTO; ++n)
-            *reinterpret_cast<uint32_t*>(dst + odim(n, 0)) = pack_bf16x2(o[n][0] * inv, o[n][1] * inv);
+            *reinterpret_cast<uint32_t*>(dst + odim(n, 0)) =
+                pack_bf16x2(o[n][2 * i] * inv, o[n][2 * i + 1] * inv);
         }
       }
     } else {
       // segment cut between warps: publish (acc, m, l) now
       float* pslot = partial_slot<G, D>(a, wk, gw, u0);
-      if (g < G) {
 #pragma unroll
-        for (int n = 0; n < NTO; ++n)
+      for (int i = 0; i < RPL; ++i) {
+        const int r = g + 8 * i;
+        if (r < G) {
 #pragma unroll
-          for (int e = 0; e < 2; ++e) pslot[g * D + odim(n, e)] = o[n][e];
-        if (t == 0) {
-          pslot[G * D + g] = m_run;
-          pslot[G * D + G + g] = l_row;
+          for (int n = 0; n < NTO; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) pslot[r * D + odim(n, e)] = o[n][2 * i + e];
+          if (t == 0) {
+            pslot[G * D + r] = m_run[i];
+            pslot[G * D + G + r] = l_row[i];
+          }
         }
       }
       // the ticket is taken when this warp's whole range is done

@@ -602,7 +602,17 @@ int multi_pieces(int sms, int num_seqs, int num_kv_heads, int max_rb, int nb_max
 struct MultiLayout {
   size_t scratch, total;
   int max_rb, pieces;
+  int mq_units;  // > 0: the multi-query decode serves the call, with this many units per sequence
 };
+
+// Multi-query decode: 16 rows per unit, a unit holding 16 / g tokens of one
+// kv head (g a power of two up to 16); used while a (sequence, kv head) has
+// at most kMqMaxRows rows, i.e. its K/V is streamed at most twice (the
+// repeat, by the second unit, mostly from L2 right after the first).
+constexpr int kMqMaxRows = 2 * kMqRows;
+int mq_tokens_per_unit(int group) {
+  return (group > 0 && group <= kMqRows && (group & (group - 1)) == 0) ? kMqRows / group : 0;
+}
 
 bool multi_layout(int num_seqs, int total_q, int max_q, int num_q_heads, int num_kv_heads, int D, MultiLayout* L) {
   if (num_seqs < 0 || total_q < 0 || max_q < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
@@ -618,7 +628,47 @@ bool multi_layout(int num_seqs, int total_q, int max_q, int num_q_heads, int num
   const size_t row_bytes = (size_t)total_q * num_q_heads * pre_row_floats(D) * sizeof(float);
   L->scratch = kCounterRegionMin;
   L->total = L->scratch + (L->pieces > 1 ? align_up(L->pieces * row_bytes) : 0);
+  // the multi-query decode (few tokens per sequence): its merge counters and
+  // two partial slots of kMqRows rows per warp of its balanced grid
+  L->mq_units = 0;
+  if (mq_tokens_per_unit(group) > 0 && (int64_t)max_q * group <= kMqMaxRows) {
+    L->mq_units = num_kv_heads * ((max_q + mq_tokens_per_unit(group) - 1) / mq_tokens_per_unit(group));
+    const size_t mq = balanced_workspace(num_seqs, L->mq_units, kMqRows, D, sms * kMaxCtasPerSm);
+    if (mq > L->total) L->total = mq;
+  }
   return true;
+}
+
+// The kernel pkv_paged_attention_multi runs for a call of this shape (host
+// only): the tcgen05 kernel once a (sequence, kv head) fills a 128-row tile,
+// or where the mma.sync kernel has no instance for the cache shape; else the
+// multi-query decode for at most kMqMaxRows rows per (sequence, kv head);
+// else the mma.sync multi-token kernel.  Fills the chosen kernel's entry.
+struct MultiChoice {
+  pkv_multi_kernel path = PKV_MULTI_NONE;
+  Tc05Kernel tk;
+  DecodeKernel mk;
+  PrefixKernel pk;
+};
+
+MultiChoice choose_multi(int num_seqs, int max_q, int group, const pkv_cache_desc* cache) {
+  MultiChoice c;
+  const int D = cache->head_dim, BS = cache->block_size;
+  const bool fp8 = cache->dtype == PKV_FP8_E4M3;
+  if (cache->dtype == PKV_F32 || group <= 0) return c;
+  const int64_t rows_max = (int64_t)max_q * group;  // rows of the largest (sequence, kv head)
+  const bool one_warp = (rows_max + 15) / 16 == 1;
+  const bool have_pk = fp8 ? find_multi_fp8(D, BS, one_warp, &c.pk) : find_multi_bf16(D, BS, one_warp, &c.pk);
+  if (g_tc05.load(std::memory_order_relaxed) && (rows_max >= tc05::kRows || !have_pk) && num_seqs <= 65535 &&
+      cache->num_kv_heads <= 65535 &&
+      (fp8 ? find_tc05_fp8(D, BS, false, &c.tk) : find_tc05_bf16(D, BS, false, &c.tk))) {
+    c.path = PKV_MULTI_TCGEN05;
+  } else if (mq_tokens_per_unit(group) > 0 && rows_max <= kMqMaxRows && find_decode_mq(cache->dtype, D, BS, &c.mk)) {
+    c.path = PKV_MULTI_QUERY_DECODE;
+  } else if (have_pk) {
+    c.path = PKV_MULTI_MMA_SYNC;
+  }
+  return c;
 }
 
 }  // namespace pkv
@@ -774,6 +824,14 @@ size_t pkv_multi_workspace_bytes(int32_t num_seqs, int32_t total_q, int32_t max_
   return multi_layout(num_seqs, total_q, max_q, num_q_heads, num_kv_heads, head_dim, &L) ? L.total : 0;
 }
 
+pkv_multi_kernel pkv_multi_kernel_for(int32_t num_seqs, int32_t max_q, int32_t num_q_heads,
+                                      const pkv_cache_desc* cache) {
+  if (num_seqs < 0 || max_q <= 0 || !valid_cache_desc(cache) || num_q_heads <= 0 ||
+      num_q_heads % cache->num_kv_heads)
+    return PKV_MULTI_NONE;
+  return choose_multi(num_seqs, max_q, num_q_heads / cache->num_kv_heads, cache).path;
+}
+
 pkv_status pkv_paged_attention_multi(void* out, const void* q, pkv_dtype q_dtype, const int32_t* q_start,
                                      int32_t num_seqs, int32_t total_q, int32_t max_q, int32_t num_q_heads,
                                      const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
@@ -799,16 +857,11 @@ pkv_status pkv_paged_attention_multi(void* out, const void* q, pkv_dtype q_dtype
   const int group = num_q_heads / cache->num_kv_heads;
   const int64_t rows_max = (int64_t)max_q * group;  // rows of the largest (sequence, kv head)
   const bool fp8 = cache->dtype == PKV_FP8_E4M3;
-  PrefixKernel pk;
-  const bool one_warp = lay.max_rb == 1;
-  const bool have_pk = cache->dtype == PKV_BF16 ? find_multi_bf16(D, BS, one_warp, &pk)
-                                                 : find_multi_fp8(D, BS, one_warp, &pk);
-  // the tcgen05 kernel once a (sequence, kv head) fills a 128-row tile, or
-  // where the mma.sync kernel has no instance for this cache shape
-  if (g_tc05.load(std::memory_order_relaxed) && (rows_max >= tc05::kRows || !have_pk) && num_seqs <= 65535 &&
-      cache->num_kv_heads <= 65535) {
-    Tc05Kernel tk;
-    if (fp8 ? find_tc05_fp8(D, BS, false, &tk) : find_tc05_bf16(D, BS, false, &tk)) {
+  const MultiChoice choice = choose_multi(num_seqs, max_q, group, cache);
+  if (choice.path == PKV_MULTI_NONE) return PKV_ERR_UNSUPPORTED;
+  if (choice.path == PKV_MULTI_TCGEN05) {
+    const Tc05Kernel& tk = choice.tk;
+    {
       const int dev = current_device();
       unsigned int* err = dev < 0 ? nullptr : error_word(dev);
       if (!err) return PKV_ERR_CUDA;
@@ -840,7 +893,54 @@ pkv_status pkv_paged_attention_multi(void* out, const void* q, pkv_dtype q_dtype
                                         reinterpret_cast<cudaStream_t>(stream)));
     }
   }
-  if (!have_pk) return PKV_ERR_UNSUPPORTED;
+  // few tokens per (sequence, kv head): the balanced decode kernel in its
+  // multi-query form (the K/V of a sequence streamed by consecutive warps,
+  // the whole batch cut into equal ranges)
+  if (choice.path == PKV_MULTI_QUERY_DECODE) {
+    const DecodeKernel& mk = choice.mk;
+    const int dev = current_device();
+    unsigned int* err = dev < 0 ? nullptr : error_word(dev);
+    const int sms = dev < 0 ? 0 : sm_count(dev);
+    const int occ = dev < 0 ? 0 : prepare_kernel(mk, dev);
+    if (!err || sms <= 0 || occ <= 0) return PKV_ERR_CUDA;
+    DecodeArgs a{};
+    a.err = err;
+    a.out = out;
+    a.q = q;
+    a.k_cache = static_cast<const uint8_t*>(k_cache);
+    a.v_cache = static_cast<const uint8_t*>(v_cache);
+    a.block_tables = block_tables;
+    a.table_stride = max_blocks_per_seq;
+    a.seq_lens = seq_lens;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = cache->num_kv_heads;
+    a.num_blocks = cache->num_blocks;
+    a.group = group;
+    a.units = lay.mq_units;
+    a.units_per_kv = lay.mq_units / cache->num_kv_heads;
+    a.len_clip = len_clip;
+    a.q_start = q_start;
+    a.mq_tpu = mq_tokens_per_unit(group);
+    a.max_q = max_q;
+    a.total_q = total_q;
+    a.qk_scale = scale * 1.4426950408889634f * (fp8 ? kv_scale : 1.f);
+    a.out_scale = fp8 ? kv_scale : 1.f;
+    const size_t region = counter_region(num_seqs, a.units);
+    a.counters = static_cast<int*>(workspace);
+    a.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + region);
+    int64_t grid = (int64_t)sms * (occ < kMaxCtasPerSm ? occ : kMaxCtasPerSm);
+    const int64_t tiles_hint = (int64_t)num_seqs * a.units * ((len_clip + BS - 1) / BS);
+    if (tiles_hint < grid) grid = tiles_hint > 0 ? tiles_hint : 1;
+    TmaMaps maps{};
+    if (!encode_cache_maps(mk, cache, k_cache, v_cache, &maps)) return PKV_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // a counter region past the fixed minimum may hold an earlier call's partials
+    if (region > kCounterRegionMin && cudaMemsetAsync(workspace, 0, region, st) != cudaSuccess) return PKV_ERR_CUDA;
+    void* args[] = {&a, &maps};
+    return from_cuda(launch_decode_grid(mk, dim3((unsigned)grid), args, st, false));
+  }
+  const PrefixKernel& pk = choice.pk;
   const int dev = current_device();
   const int sms = dev < 0 ? 0 : sm_count(dev);
   unsigned int* err = dev < 0 ? nullptr : error_word(dev);

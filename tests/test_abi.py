@@ -190,3 +190,33 @@ def test_multi_kernel_switch_without_a_device(lib):
         assert not pkv.get_tcgen05()
         assert lib.pkv_get_tcgen05() == 0
     assert pkv.get_tcgen05()
+
+
+def test_multi_kernel_choice_without_a_device(lib):
+    """Which kernel a multi-token call runs, decided on the host: 128-row tcgen05 tiles once a
+    (sequence, kv head) holds 128 query rows, the multi-query decode (16 rows per unit) for at
+    most 32 rows and a power-of-two group, the mma.sync kernel otherwise."""
+    import paged_kv_cache_22_gb300 as pkv
+
+    def k(max_q, hq, hkv=8, d=128, bs=16, dt="bf16", seqs=64):
+        return pkv.multi_kernel_for(seqs, max_q, hq, hkv, d, bs, dt)
+
+    # speculative verify on Llama-3-8B heads (g = 4): 4 tokens = 16 rows, 8 tokens = 32 rows
+    assert k(4, 32) == "multi_query_decode"
+    assert k(8, 32) == "multi_query_decode"
+    assert k(9, 32) == "mma_sync"            # 36 rows: beyond two units
+    assert k(32, 32) == "tcgen05"            # 128 rows
+    assert k(1, 8) == "multi_query_decode"   # g = 1
+    assert k(2, 128) == "multi_query_decode"  # g = 16: one token per unit
+    assert k(4, 24) == "mma_sync"            # g = 3: rows of a unit would mix kv heads' tokens
+    assert k(4, 32, d=64) == "multi_query_decode"
+    assert k(4, 32, d=64, bs=32) is None     # bf16, head_dim 64: blocks of 16 only
+    assert k(4, 32, dt="fp8_e4m3") == "multi_query_decode"
+    assert k(4, 32, dt="fp8_e4m3", bs=32) == "tcgen05"  # no mma.sync fp8 instance for 32-token blocks
+    assert k(512, 32) == "tcgen05"
+    with pkv.tcgen05(False):
+        assert k(512, 32) == "mma_sync"
+        assert k(4, 32, dt="fp8_e4m3", bs=32) is None
+        assert k(4, 32) == "multi_query_decode"
+    assert k(4, 32, dt="f32") is None        # the products run on the tensor cores
+    assert k(0, 32) is None and k(4, 30) is None  # max_q 0; Hq not a multiple of Hkv

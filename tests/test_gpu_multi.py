@@ -57,6 +57,19 @@ CASES = [
     # fewer than 128 rows per (sequence, kv head), blocks of 32: only the
     # tcgen05 kernel has an fp8 instance, so it serves the call
     ("fp8_bs32_small", [70, 33, 5], [3, 9, 5], 32, 8, 128, 32, "fp8_e4m3"),
+    # at most 32 rows per (sequence, kv head) and g a power of two up to 8:
+    # the balanced decode kernel in its multi-query form (8 rows per unit,
+    # 8 / g tokens), including token counts that leave a unit part empty,
+    # long sequences whose segments are cut between warps, and g = 3 (the
+    # mma.sync multi-token kernel)
+    ("mq_g8_t3", [1500, 40, 700], [3, 1, 2], 64, 8, 128, 16, "bf16"),
+    ("mq_g2_t5", [900, 33, 2100], [5, 2, 5], 16, 8, 128, 16, "bf16"),
+    ("mq_g1_t4_bs8", [300, 1200], [4, 3], 8, 8, 128, 8, "bf16"),
+    ("mq_d64", [400, 50, 1700], [4, 4, 2], 32, 8, 64, 16, "bf16"),
+    ("mq_fp8_d64", [300, 1000], [4, 2], 32, 8, 64, 16, "fp8_e4m3"),
+    ("mq_long_cut", [9000, 7000, 3], [4, 4, 3], 32, 8, 128, 16, "bf16"),
+    ("mq_bs32", [100, 900], [4, 4], 32, 8, 128, 32, "bf16"),
+    ("g3_small", [200, 70], [4, 3], 24, 8, 128, 16, "bf16"),
 ]
 
 
