@@ -427,7 +427,7 @@ def time_calls(fn, flush, stream, K: int, warmup: int = 3) -> float:
 MULTI_KERNEL_LABELS = {
     "tcgen05": "attn_tc05_kernel (tcgen05.mma, S and O in TMEM)",
     "multi_query_decode": "decode_tc_kernel (multi-query: 16 (token, head) rows per unit, balanced split, "
-                          "mma.sync m16n8k16)",
+                          "mma.sync m16n8k16) + merge_cut_kernel (segments cut between warps)",
     "mma_sync": "prefix_attention_kernel (MULTI, mma.sync m16n8k16)",
 }
 
@@ -927,7 +927,7 @@ def run_multi(args):
                       "kernel": multi_kernel}),
         "e2e": {"value": round(e2e_value, 2 if compute else 1), "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 6)},
-        "gpu_launches": K, "clocks": clocks,
+        "gpu_launches": K * (2 if "merge_cut_kernel" in multi_kernel else 1), "clocks": clocks,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_multi(w, q_cpu, qs_cpu, args.cpu_seconds, compute)

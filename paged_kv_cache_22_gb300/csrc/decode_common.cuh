@@ -57,6 +57,9 @@ struct DecodeArgs {
   int mq_tpu;        // tokens per unit (G / group); 0 for one token per sequence
   int max_q;         // host bound of the query rows per sequence
   int total_q;       // query rows in all
+  // balanced split: 1 = cut pieces only publish their partials; a dependent
+  // grid (merge_cut_kernel) merges the segments once this grid is done
+  int defer_merge;
   // balanced split
   int* counters;     // [num_seqs * units], zero between calls
   float* partials;   // [2 * warps][partial_slot_floats(G, D)]
@@ -252,14 +255,14 @@ __device__ __forceinline__ void walker_next_piece(Walker& wk, const DecodeArgs& 
 // empty sequences are zeroed on the way.  Fixed-partition mode: warp gw takes
 // partition gw % P of segment gw / P.  False when the warp has nothing to do.
 // ----------------------------------------------------------------------------
-template <class QT, int D, int BS, bool BALANCED>
+template <class QT, int D, int BS, bool BALANCED, bool ZERO_EMPTY = true>
 __device__ __forceinline__ bool plan_warp(const DecodeArgs& a, int64_t gw, int64_t NW, int lane, Walker& wk0,
                                           int64_t& u0, int64_t& u1, int64_t& T) {
   T = 0;
   if constexpr (BALANCED) {
     // sequences with no block to read get their row here (spread over the
     // warps): zero, or in a cascade the shared prefix's result alone
-    for (int64_t s = gw; s < a.num_seqs && !a.q_start; s += NW) {
+    for (int64_t s = gw; ZERO_EMPTY && s < a.num_seqs && !a.q_start; s += NW) {
       if (seq_blocks<BS>(a, (int)s) == 0) {
         // a cascade's prefix partial comes from the grid this one may depend on
         if (a.pre) asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -385,9 +388,129 @@ __device__ __forceinline__ float* partial_slot(const DecodeArgs& a, const Walker
 struct CutPiece {
   int s, unit, nb;
   int64_t seg_u;  // linear index of the segment's first tile
+  int q0, qT;     // multi-query: the sequence's first query row and row count
 };
 
-__device__ __forceinline__ CutPiece cut_piece_of(const Walker& wk) { return CutPiece{wk.s, wk.unit, wk.nb, wk.seg_u}; }
+__device__ __forceinline__ CutPiece cut_piece_of(const Walker& wk, int q0 = 0, int qT = 0) {
+  return CutPiece{wk.s, wk.unit, wk.nb, wk.seg_u, q0, qT};
+}
+
+// Draw the ticket of cut piece `cp` ahead of the range's end, behind a fence
+// over this warp's partial-slot stores (issued a tile earlier, so the fence
+// finds them landed).  The atomic's result is read only when the range is
+// done: lane 0 holds it, the other lanes get -1.
+__device__ __forceinline__ int draw_ticket(const DecodeArgs& a, const CutPiece& cp, int lane, bool async_readers) {
+  if (async_readers) asm volatile("fence.proxy.async.global;" ::: "memory");
+  __threadfence();
+  __syncwarp();
+  int t = -1;
+  if (lane == 0) t = atomicAdd(a.counters + ((int64_t)cp.s * a.units + cp.unit), 1);
+  return t;
+}
+
+// The output rows of a merged segment: lanes < D / 4 write dims 4 * lane ..
+// 4 * lane + 3 of every row, num / den scaled by out_scale.
+template <class QT, int G, int D>
+__device__ __forceinline__ void write_merged(const DecodeArgs& a, const CutPiece& cp, int lane, const float (&den)[G],
+                                             const float (&num)[G][4]) {
+  constexpr int DV = 4, SL = D / DV;
+  const int d0 = (lane % SL) * DV;
+  const int kvh = cp.unit / a.units_per_kv, chunk = cp.unit % a.units_per_kv;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    QT* out;
+    if (a.q_start) {  // multi-query: row h is (token chunk * tpu + h / group, head h % group)
+      const int tok = chunk * a.mq_tpu + h / a.group;
+      if (tok >= cp.qT) continue;
+      out = reinterpret_cast<QT*>(a.out) + ((size_t)(cp.q0 + tok) * a.num_q_heads + kvh * a.group + h % a.group) * D;
+    } else {
+      out = reinterpret_cast<QT*>(a.out) + ((size_t)cp.s * a.num_q_heads + kvh * a.group + chunk * G + h) * D;
+    }
+    if (lane < SL) {
+      const float inv = den[h] > 0.f ? a.out_scale / den[h] : 0.f;
+#pragma unroll
+      for (int d = 0; d < DV; ++d) out[d0 + d] = from_f32<QT>(num[h][d] * inv);
+    }
+  }
+}
+
+// Shared memory a warp lends to its merges once its own range is done: room
+// for `cap` partial slots at `buf`, filled by bulk copies that complete on
+// `bar` (`phase` = its completed phases).  buf == nullptr: merge through
+// registers.
+struct MergeStage {
+  float* buf = nullptr;
+  int cap = 0;
+  uint64_t* bar = nullptr;
+  uint32_t phase = 0;
+};
+
+// Merge all pieces of segment `cp` through shared memory: rounds of up to
+// `cap` slots, each slot one bulk copy (accumulators, maxima and sums
+// together), the rows combined online by log-sum-exp across rounds.  Every
+// lane reads every piece (lanes < D / 4 own 4 dims, the maxima and sums are
+// broadcast reads), so no cross-lane reduction follows.  False when a copy
+// did not land in time (the error word is set; nothing is written).
+template <class QT, int G, int D>
+__device__ __forceinline__ bool merge_segment_staged(const DecodeArgs& a, const CutPiece& cp, int64_t T, int64_t NW,
+                                                     int lane, MergeStage& ms) {
+  constexpr int SLOT = partial_slot_floats(G, D), DV = 4, SL = D / DV;
+  const int d0 = (lane % SL) * DV;
+  const int64_t w_first = owner_of(cp.seg_u, T, NW), w_last = owner_of(cp.seg_u + cp.nb - 1, T, NW);
+  const int64_t n = w_last - w_first + 1;
+  const int64_t first_slot = (cp.seg_u != range_start(w_first, T, NW)) ? 2 * w_first + 1 : 2 * w_first;
+  auto slot_of = [&](int64_t i) -> const float* {
+    return a.partials + (size_t)(i == 0 ? first_slot : 2 * (w_first + i)) * SLOT;
+  };
+  float M[G], den[G], num[G][DV];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    M[h] = -CUDART_INF_F;
+    den[h] = 0.f;
+#pragma unroll
+    for (int d = 0; d < DV; ++d) num[h][d] = 0.f;
+  }
+  for (int64_t i0 = 0; i0 < n; i0 += ms.cap) {
+    const int cnt = (int)(n - i0 < ms.cap ? n - i0 : ms.cap);
+    // the other pieces' slots were written by plain stores of other warps
+    // (ordered before this warp's ticket); the copies read them through the
+    // async proxy
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    fence_proxy_async_smem();  // earlier reads of the buffer before the copies overwrite it
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive_expect_tx(ms.bar, (uint32_t)(cnt * SLOT * sizeof(float)));
+      for (int i = 0; i < cnt; ++i) bulk_g2s(ms.buf + (size_t)i * SLOT, slot_of(i0 + i), SLOT * sizeof(float), ms.bar);
+    }
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(ms.bar, ms.phase & 1, a.err));
+    ++ms.phase;
+    if (!ok) {
+      // leave no copy in flight: one more bounded wait for this round
+      mbar_wait_bounded(ms.bar, (ms.phase - 1) & 1, a.err);
+      ms.buf = nullptr;  // the buffer is no longer trusted
+      return false;
+    }
+    for (int i = 0; i < cnt; ++i) {
+      const float* pp = ms.buf + (size_t)i * SLOT;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float m = pp[G * D + h];
+        const float Mn = fmaxf(M[h], m);
+        if (Mn == -CUDART_INF_F) continue;  // nothing kept in this row yet
+        const float f_old = fast_exp2(M[h] - Mn), f_new = fast_exp2(m - Mn);
+        const float4 acc = *reinterpret_cast<const float4*>(pp + h * D + d0);
+        den[h] = fmaf(den[h], f_old, f_new * pp[G * D + G + h]);
+        num[h][0] = fmaf(num[h][0], f_old, f_new * acc.x);
+        num[h][1] = fmaf(num[h][1], f_old, f_new * acc.y);
+        num[h][2] = fmaf(num[h][2], f_old, f_new * acc.z);
+        num[h][3] = fmaf(num[h][3], f_old, f_new * acc.w);
+        M[h] = Mn;
+      }
+    }
+  }
+  write_merged<QT, G, D>(a, cp, lane, den, num);
+  return true;
+}
 
 // Merge all pieces of segment `cp` (lane-parallel; lanes < D / 4 own 4 dims).
 template <class QT, int G, int D>
@@ -503,33 +626,23 @@ __device__ __forceinline__ void merge_segment(const DecodeArgs& a, const CutPiec
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) den[h] += __shfl_xor_sync(0xffffffffu, den[h], off);
   }
-  const int kvh = cp.unit / a.units_per_kv, chunk = cp.unit % a.units_per_kv;
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    QT* out;
-    if (a.q_start) {  // multi-query: row h is (token chunk * tpu + h / group, head h % group)
-      const MqRows mr = mq_rows(a, cp.s);
-      const int tok = chunk * a.mq_tpu + h / a.group;
-      if (tok >= mr.T) continue;
-      out = reinterpret_cast<QT*>(a.out) + ((size_t)(mr.q0 + tok) * a.num_q_heads + kvh * a.group + h % a.group) * D;
-    } else {
-      out = reinterpret_cast<QT*>(a.out) + ((size_t)cp.s * a.num_q_heads + kvh * a.group + chunk * G + h) * D;
-    }
-    if (lane < SL) {
-      const float inv = den[h] > 0.f ? a.out_scale / den[h] : 0.f;
-#pragma unroll
-      for (int d = 0; d < DV; ++d) out[d0 + d] = from_f32<QT>(num[h][d] * inv);
-    }
-  }
+  write_merged<QT, G, D>(a, cp, lane, den, num);
 }
 
 // Take the tickets of this warp's cut pieces (n of them, 0..2) behind one
 // fence, then merge the segments whose last ticket this warp drew.
+// drawn0: c0's ticket was drawn ahead (draw_ticket), its value in pre0 (lane 0).
 template <class QT, int G, int D>
 __device__ __forceinline__ void finish_cut_pieces(const DecodeArgs& a, const CutPiece& c0, const CutPiece& c1,
-                                                  int n, int64_t T, int64_t NW, int lane) {
+                                                  int n, int64_t T, int64_t NW, int lane,
+                                                  MergeStage* ms = nullptr, bool drawn0 = false, int pre0 = -1) {
   if (n == 0) return;
-  __threadfence();  // this warp's partial slots before its tickets
+  if (!drawn0 || n > 1) {
+    // this warp's partial slots before its tickets (a merging warp may read
+    // them through the async proxy)
+    if (ms) asm volatile("fence.proxy.async.global;" ::: "memory");
+    __threadfence();
+  }
   __syncwarp();
   int last0 = 0, last1 = 0;
   if (lane == 0) {
@@ -540,7 +653,7 @@ __device__ __forceinline__ void finish_cut_pieces(const DecodeArgs& a, const Cut
       return (int)(owner_of(cp.seg_u + cp.nb - 1, T, NW) - owner_of(cp.seg_u, T, NW));
     };
     // both atomics in flight before either result is used
-    const int t0 = atomicAdd(take(c0), 1);
+    const int t0 = drawn0 ? pre0 : atomicAdd(take(c0), 1);
     const int t1 = n > 1 ? atomicAdd(take(c1), 1) : -1;
     last0 = t0 == pieces(c0);
     last1 = n > 1 && t1 == pieces(c1);
@@ -550,8 +663,15 @@ __device__ __forceinline__ void finish_cut_pieces(const DecodeArgs& a, const Cut
   last0 = __shfl_sync(0xffffffffu, last0, 0);
   last1 = __shfl_sync(0xffffffffu, last1, 0);
   if (last0 | last1) __threadfence();  // every other piece's slot before the reads
-  if (last0) merge_segment<QT, G, D>(a, c0, T, NW, lane);
-  if (last1) merge_segment<QT, G, D>(a, c1, T, NW, lane);
+  auto merge = [&](const CutPiece& cp) {
+    if (ms && ms->buf) {
+      merge_segment_staged<QT, G, D>(a, cp, T, NW, lane, *ms);
+    } else if (!ms) {
+      merge_segment<QT, G, D>(a, cp, T, NW, lane);
+    }
+  };
+  if (last0) merge(c0);
+  if (last1) merge(c1);
 }
 
 }  // namespace pkv

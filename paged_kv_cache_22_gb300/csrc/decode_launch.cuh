@@ -16,6 +16,10 @@ struct DecodeKernel {
   size_t smem = 0;           // dynamic shared memory bytes
   int heads_per_unit = 0;    // G
   bool tensor_maps = false;  // reads the caches through the TmaMaps parameter
+  // the deferred-merge grid that follows it (merge_cut_kernel: parameters
+  // (DecodeArgs, int64_t warps of the decode grid), one-warp CTAs), if any
+  const void* merge_fn = nullptr;
+  size_t merge_smem = 0;
 };
 
 // TC: the q.K and P.V contractions on the tensor cores (decode_tc.cuh, bf16
@@ -50,6 +54,9 @@ DecodeKernel decode_mq_kernel_info() {
   k.tensor_maps = true;
   k.threads = kDecodeWarps * 32;
   k.heads_per_unit = kMqRows;
+  constexpr int kMergeSlots = 4;  // partial slots staged per round of a merge
+  k.merge_fn = reinterpret_cast<const void*>(&merge_cut_kernel<__nv_bfloat16, kMqRows, D, BS, kMergeSlots>);
+  k.merge_smem = (size_t)kMergeSlots * partial_slot_floats(kMqRows, D) * sizeof(float) + 8;
   return k;
 }
 // bf16 caches: head_dim 128 with blocks of 8, 16, 32, head_dim 64 with 16;

@@ -197,7 +197,12 @@ struct TcSmem {
   // cascade (REMAP kernels): one warp's next prefix partial (G rows), and its barrier
   static constexpr size_t kPBuf = (kOk + (size_t)W * GE::NSW * 4 + 15) / 16 * 16;
   static constexpr size_t kPBar = kPBuf + (REMAP ? (size_t)W * G * pre_row_floats(D) * sizeof(float) : 0);
-  static constexpr size_t kBytes = kPBar + (size_t)W * 8;
+  static constexpr size_t kMBar = kPBar + (size_t)W * 8;  // the merges' bulk copies
+  static constexpr size_t kBytes = kMBar + (size_t)W * 8;
+  // partial slots a one-warp CTA's stage ring and q buffers (contiguous) hold
+  // once its range is done; its merges stage slots there
+  static constexpr int kMergeCap =
+      W == 1 ? (int)((kBars - kStages) / (partial_slot_floats(G, D) * sizeof(float))) : 0;
 };
 
 // One (block, kv head) tile of a cache into `dst`: row-wide boxes with one
@@ -262,6 +267,7 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
   int* stage_ok = reinterpret_cast<int*>(smem + SM::kOk) + w * NSW;
   float* pbuf = reinterpret_cast<float*>(smem + SM::kPBuf) + (size_t)w * G * pre_row_floats(D);
   uint64_t* pbar = reinterpret_cast<uint64_t*>(smem + SM::kPBar) + w;
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + SM::kMBar) + w;
 
   if (lane == 0) {
 #pragma unroll
@@ -269,6 +275,7 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
     mbar_init(&qbars[0], 1);
     mbar_init(&qbars[1], 1);
     mbar_init(pbar, 1);
+    mbar_init(mbar, 1);
     fence_mbar_init();
   }
   __syncthreads();  // the only block-wide barrier: warps are independent from here on
@@ -353,6 +360,9 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
   };
   int pre_issued = 0, pre_waited = 0;
 
+  // a dependent merge grid may start its own planning now; it waits for
+  // this grid to finish before it reads a partial
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   Walker qlook = wk0;
   if (lane == 0) issue_q(wk0, 0);
   // Everything above reads only the step's inputs (lengths, tables, q).  When
@@ -420,6 +430,11 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
   int consumed = 0, waited = 0, piece = 0;
   CutPiece cut0{}, cut1{};  // this warp's cut pieces (its first and last at most)
   int ncut = 0;
+  // a first cut piece that ends before the range does has its ticket drawn
+  // one tile later (after tile `early_at` is consumed), so that this warp
+  // merges at most the segment its range ends in
+  int early_at = -1, pre0 = -1;
+  bool drawn0 = false;
   bool alive = true;
   uint32_t qa[KS][RE];    // q.K A operand per k-step: (a0, a2) of row g, or (a0, a1, a2, a3)
                           // of rows g and g + 8 (16-row units)
@@ -754,6 +769,12 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
       __syncwarp();  // every lane is done with this stage before it is refilled
       ++consumed;
       if (alive) issue_next();
+      if constexpr (BALANCED) {
+        if (consumed == early_at) {
+          pre0 = draw_ticket(a, cut0, lane, SM::kMergeCap > 0);
+          drawn0 = true;
+        }
+      }
     }
 
     // ------------------------------------------------------------ piece end
@@ -836,19 +857,72 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
         }
       }
       // the ticket is taken when this warp's whole range is done
-      if (ncut == 0) cut0 = cut_piece_of(wk); else cut1 = cut_piece_of(wk);
+      if (ncut == 0) {
+        cut0 = cut_piece_of(wk, mr.q0, mr.T);
+        if (wk.seg_u + wk.je < u1 && !a.defer_merge) early_at = consumed + 1;
+      } else {
+        cut1 = cut_piece_of(wk, mr.q0, mr.T);
+      }
       ++ncut;
     }
     ++piece;
     walker_next_piece<BS>(wk, a, u1);
   }
 
-  if constexpr (BALANCED) finish_cut_pieces<QT, G, D>(a, cut0, cut1, ncut, T, NW, lane);
-
   // Leave no copy in flight: wait (bounded) for every stage this warp filled
   // but did not wait for (only possible after a timeout).
   for (int k = waited; k < issued; ++k) mbar_wait_bounded(&bars[k % NSW], (k / NSW) & 1, a.err);
   for (int k = pre_waited; k < pre_issued; ++k) mbar_wait_bounded(pbar, k & 1, a.err);
+
+  if (BALANCED && !a.defer_merge) {
+    // the merges stage partial slots in the stage ring and q buffers, free
+    // now (no copy is in flight there unless a wait timed out: then this
+    // warp merges nothing, its error already raised)
+    MergeStage ms;
+    if (SM::kMergeCap > 0 && alive) {
+      ms.buf = reinterpret_cast<float*>(smem + SM::kStages);
+      ms.cap = SM::kMergeCap;
+      ms.bar = mbar;
+    }
+    finish_cut_pieces<QT, G, D>(a, cut0, cut1, ncut, T, NW, lane, SM::kMergeCap > 0 ? &ms : nullptr, drawn0,
+                                pre0);
+  }
+}
+
+// ----------------------------------------------------------------------------
+// Deferred merges.  Warp gw of this grid (one-warp CTAs) replays the plan of
+// warp gw of a balanced decode grid of NW warps that ran with defer_merge:
+// when that warp's range starts inside a segment begun by earlier warps and
+// the segment ends within the range, the warp held the segment's last piece,
+// and this warp merges the segment's pieces (accumulators, maxima and sums
+// from their partial slots) into its output rows.  Each cut segment has one
+// such warp.  The planning runs while the decode grid is still streaming;
+// the merge waits for that grid (programmatic dependent launch).
+// ----------------------------------------------------------------------------
+template <class QT, int G, int D, int BS, int MC>
+__global__ void __launch_bounds__(32) merge_cut_kernel(const __grid_constant__ DecodeArgs a, int64_t NW) {
+  extern __shared__ __align__(16) uint8_t merge_smem[];
+  const int lane = threadIdx.x;
+  const int64_t gw = blockIdx.x;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(merge_smem + (size_t)MC * partial_slot_floats(G, D) * sizeof(float));
+  int64_t u0 = 0, u1 = 0, T = 0;
+  Walker wk0;
+  const bool mine = plan_warp<QT, D, BS, true, false>(a, gw, NW, lane, wk0, u0, u1, T) && wk0.jb > 0 &&
+                    wk0.seg_u + wk0.nb <= u1;
+  if (!mine) return;
+  MqRows mr{0, 0};
+  if (a.q_start) mr = mq_rows(a, wk0.s);
+  if (lane == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  MergeStage ms;
+  ms.buf = reinterpret_cast<float*>(merge_smem);
+  ms.cap = MC;
+  ms.bar = bar;
+  merge_segment_staged<QT, G, D>(a, cut_piece_of(wk0, mr.q0, mr.T), T, NW, lane, ms);
 }
 
 }  // namespace pkv

@@ -903,6 +903,11 @@ pkv_status pkv_paged_attention_multi(void* out, const void* q, pkv_dtype q_dtype
     const int sms = dev < 0 ? 0 : sm_count(dev);
     const int occ = dev < 0 ? 0 : prepare_kernel(mk, dev);
     if (!err || sms <= 0 || occ <= 0) return PKV_ERR_CUDA;
+    DecodeKernel merge;
+    merge.fn = mk.merge_fn;
+    merge.threads = 32;
+    merge.smem = mk.merge_smem;
+    if (!merge.fn || prepare_kernel(merge, dev) <= 0) return PKV_ERR_CUDA;
     DecodeArgs a{};
     a.err = err;
     a.out = out;
@@ -926,6 +931,10 @@ pkv_status pkv_paged_attention_multi(void* out, const void* q, pkv_dtype q_dtype
     a.total_q = total_q;
     a.qk_scale = scale * 1.4426950408889634f * (fp8 ? kv_scale : 1.f);
     a.out_scale = fp8 ? kv_scale : 1.f;
+    // segments cut between warps are merged by a dependent grid once the
+    // streaming is done (merges inside the grid would queue behind the
+    // SMs' tile copies at its tail)
+    a.defer_merge = 1;
     const size_t region = counter_region(num_seqs, a.units);
     a.counters = static_cast<int*>(workspace);
     a.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + region);
@@ -935,10 +944,13 @@ pkv_status pkv_paged_attention_multi(void* out, const void* q, pkv_dtype q_dtype
     TmaMaps maps{};
     if (!encode_cache_maps(mk, cache, k_cache, v_cache, &maps)) return PKV_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    // a counter region past the fixed minimum may hold an earlier call's partials
-    if (region > kCounterRegionMin && cudaMemsetAsync(workspace, 0, region, st) != cudaSuccess) return PKV_ERR_CUDA;
+    // (no merge counters are taken: the counter region is left as it is)
     void* args[] = {&a, &maps};
-    return from_cuda(launch_decode_grid(mk, dim3((unsigned)grid), args, st, false));
+    cudaError_t e = launch_decode_grid(mk, dim3((unsigned)grid), args, st, false);
+    if (e != cudaSuccess) return from_cuda(e);
+    int64_t nw = grid * kDecodeWarps;
+    void* margs[] = {&a, &nw};
+    return from_cuda(launch_decode_grid(merge, dim3((unsigned)nw), margs, st, true));
   }
   const PrefixKernel& pk = choice.pk;
   const int dev = current_device();
