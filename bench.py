@@ -330,6 +330,7 @@ def run_gpu(args):
             and args.engine == "tensor_cores" and not win and not pblocks):
         traffic = TRAFFIC["bytes_per_launch"]
 
+    tc_decode = w.cache_dtype != "f32" and args.engine == "tensor_cores"
     # the kernel of the cascade's prefix pass (tcgen05 once a kv head has 128 rows)
     prefix_kernel = ("attn_tc05_kernel (tcgen05.mma, S and O in TMEM)"
                      if pblocks and pkv.get_tcgen05() and w.head_dim == 128
@@ -379,11 +380,11 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": (f"{prefix_kernel} + decode_tc_kernel (cascade, both launches)"
+                     "kernel": (f"{prefix_kernel} + decode_tc_kernel + merge_cut_kernel (cascade, all launches)"
                                 if pblocks else
-                                ("decode_tc_kernel" if w.cache_dtype != "f32" and args.engine == "tensor_cores"
-                                 else "decode_kernel")
-                                + (" (balanced split)" if pt == 0 else " (partitions)"))},
+                                ("decode_tc_kernel" if tc_decode else "decode_kernel")
+                                + ((" + merge_cut_kernel (balanced split)" if tc_decode else " (balanced split)")
+                                   if pt == 0 else " + split_kv_reduce_kernel (partitions)"))},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": round(e2e["ms_per_step"], 6),
@@ -391,7 +392,9 @@ def run_gpu(args):
                               "value": round(job_throughput(ws, dec_b + rc_b, e2e["host_ms_per_step"]), 1),
                               "what": "host clock from the first call of a step until its output "
                                       "is on the host (binding, C ABI, launches, copies, GPU time)"}},
-        "gpu_launches": K * (3 if pblocks else (2 if pt == 0 else 3)),
+        # cache write, decode, then the merge grid (balanced split on the tensor cores) or the reduce
+        # (partitions); a cascade adds its prefix pass
+        "gpu_launches": K * (2 + (1 if (pt or tc_decode) else 0) + (1 if pblocks else 0)),
         "clocks": clocks,
     }
     if (ws == 1 and args.config == "llama3_8b" and pt == 0 and not win and not pblocks
@@ -497,10 +500,11 @@ def per_config(pkv, dev, flush, K: int, main_decode_ms: float):
                      "unique_bytes": ub, "unique_gbs": round(ugbs, 1),
                      "unique_frac_of_measured": round(ugbs / hbm_peak, 4),
                      "kernel": "prefix pass (attn_tc05_kernel once a kv head has >= 128 rows, else "
-                               "prefix_attention_kernel) + decode_tc_kernel", **extra}
+                               "prefix_attention_kernel) + decode_tc_kernel + merge_cut_kernel", **extra}
             else:
                 kern = "decode_kernel (CUDA cores)" if w.cache_dtype == "f32" else "decode_tc_kernel"
-                kern += " + split_kv_reduce_kernel (fixed partitions)" if pt else " (balanced split)"
+                kern += (" + split_kv_reduce_kernel (fixed partitions)" if pt else
+                         " (balanced split)" if w.cache_dtype == "f32" else " + merge_cut_kernel (balanced split)")
                 e = hbm_entry(ms, nbytes, kern, extra)
             if win:
                 e["window"], e["sinks"] = win, sinks

@@ -34,6 +34,11 @@ DecodeKernel decode_kernel_info() {
     k.fn = reinterpret_cast<const void*>(&decode_tc_kernel<CT, D, BS, G, kDecodeWarps, BAL, REMAP>);
     k.smem = TcSmem<CT, D, BS, G, kDecodeWarps, REMAP>::kBytes;
     k.tensor_maps = true;
+    if constexpr (BAL) {
+      constexpr int kMergeSlots = 8;  // partial slots staged per round of a merge
+      k.merge_fn = reinterpret_cast<const void*>(&merge_cut_kernel<__nv_bfloat16, G, D, BS, kMergeSlots>);
+      k.merge_smem = (size_t)kMergeSlots * partial_slot_floats(G, D) * sizeof(float) + 8;
+    }
   } else {
     k.fn = reinterpret_cast<const void*>(&decode_kernel<CT, D, BS, G, kDecodeWarps, BAL, REMAP>);
     k.smem = Smem<CT, D, BS, G, kDecodeWarps>::kBytes;

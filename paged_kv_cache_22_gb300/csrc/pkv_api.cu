@@ -26,6 +26,9 @@ __device__ unsigned int g_device_error_word;
 namespace {
 
 constexpr int kMaxCtasPerSm = 16;  // upper bound of the balanced grid, per SM
+// Balanced decode on the tensor cores: merge the segments cut between warps
+// in a dependent grid (true) or inside the decode grid by tickets (false).
+constexpr bool kDeferDecodeMerges = true;
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -466,6 +469,21 @@ pkv_status decode_impl(void* out, const void* q, pkv_dtype q_dtype, int32_t num_
     // earlier call with fewer segments used for partials: clear it here, so
     // that a workspace zero-filled once serves any sequence of calls.
     const size_t region = counter_region(num_seqs, a.units);
+    DecodeKernel merge;
+    merge.fn = k.merge_fn;
+    merge.threads = 32;
+    merge.smem = k.merge_smem;
+    if (kDeferDecodeMerges && merge.fn) {
+      // segments cut between warps are merged by a dependent grid once the
+      // streaming is done; no merge counter is taken
+      if (prepare_kernel(merge, dev) <= 0) return PKV_ERR_CUDA;
+      a.defer_merge = 1;
+      cudaError_t e = launch_decode_grid(k, dim3((unsigned)grid), args, st, programmatic);
+      if (e != cudaSuccess) return from_cuda(e);
+      int64_t nw = grid * kDecodeWarps;
+      void* margs[] = {&a, &nw};
+      return from_cuda(launch_decode_grid(merge, dim3((unsigned)nw), margs, st, true));
+    }
     if (region > kCounterRegionMin && cudaMemsetAsync(workspace, 0, region, st) != cudaSuccess) return PKV_ERR_CUDA;
     return from_cuda(launch_decode_grid(k, dim3((unsigned)grid), args, st, programmatic));
   }
