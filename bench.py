@@ -51,8 +51,8 @@ L2_FLUSH_BYTES = 256 << 20
 
 # DRAM traffic of one decode launch on the default workload, from an ncu
 # capture, valid only for the kernel sources it was taken on.
-TRAFFIC = {"sources_sha256": "18b3c2532a96fae41aaff179ac9267f64c03b10b684cdb3e4576ad242b130710",
-           "bytes_per_launch": 320088832}  # mean of two launches: 317.65 MB read + 2.44 MB written
+TRAFFIC = {"sources_sha256": "1408a83b3196bf17b06696e337997727709ee599e0d7de4d6bbe1177883f251b",
+           "bytes_per_launch": 321632512}  # one launch: 316.92 MB read + 4.71 MB written
 
 WORKLOAD_TEXT = {
     "llama3_8b": "Llama-3-8B-shaped decode layer: 64 seqs, L~U[128,2048], 32 q / 8 kv heads, "

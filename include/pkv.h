@@ -107,7 +107,7 @@ pkv_status pkv_kv_reshape_and_cache(const void* k, const void* v, pkv_dtype src_
  * bytes rounded up to 256) holding one merge counter per (sequence, kv-head
  * unit), then the mode's partials.  partition_tokens = 0 (balanced split):
  * the partial results of segments cut between thread blocks, two slots per
- * thread block; independent of the lengths.  partition_tokens > 0 (fixed
+ * thread block of the largest grid; independent of the lengths.  partition_tokens > 0 (fixed
  * partitions): fp32 partials [num_seqs, num_q_heads, P, head_dim] and
  * [num_seqs, num_q_heads, P] maxima and sums, P = ceil(max_seq_len /
  * partition_tokens).  Returns 0 for invalid arguments.
@@ -141,10 +141,15 @@ size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
  *   seq_lens    device int32 [num_seqs]
  *   max_seq_len host upper bound of seq_lens (sizes the fixed-partition grid;
  *               a longer sequence sets PKV_DEVERR_BAD_SEQ_LEN and is clipped)
- *   partition_tokens  0 = balanced split over all SMs with an in-kernel
- *               log-sum-exp merge (one launch); > 0 = fixed KV partitions of
- *               that many tokens (a multiple of block_size), merged by
- *               pkv_split_kv_reduce inside this call (two launches)
+ *   partition_tokens  0 = balanced split over all SMs: the tiles of all
+ *               (sequence, kv head) segments cut into equal ranges, one per
+ *               warp; a segment cut between warps is merged by log-sum-exp
+ *               in a second grid launched as the decode grid's programmatic
+ *               dependent (tensor cores: two launches), or inside the decode
+ *               grid by its last warp to finish (CUDA cores: one launch);
+ *               > 0 = fixed KV partitions of that many tokens (a multiple
+ *               of block_size), merged by pkv_split_kv_reduce inside this
+ *               call (two launches)
  *   workspace   device, >= pkv_decode_workspace_bytes(...) bytes, 256-byte
  *               aligned.  Zero-fill it once before its first use; after that
  *               it serves any sequence of calls of either mode (and of
@@ -300,7 +305,9 @@ pkv_status pkv_cascade_decode(void* out, const void* q, pkv_dtype q_dtype, int32
  * pkv_paged_attention_multi needs (0 for invalid sizes, a batch too large for
  * the counter region below, or no current device): the 1 MiB counter region,
  * then, when the K/V range is cut into pieces, one partial row of head_dim + 4
- * fp32 values per query row, query head and piece (at most 32 pieces).
+ * fp32 values per query row, query head and piece (at most 32 pieces); for
+ * calls the multi-query decode serves (pkv_multi_kernel_for), at least its
+ * balanced split's partial slots (16 rows each, two per thread block).
  *   max_q   the largest number of query tokens of one sequence
  */
 size_t pkv_multi_workspace_bytes(int32_t num_seqs, int32_t total_q, int32_t max_q, int32_t num_q_heads,
@@ -364,7 +371,8 @@ pkv_status pkv_paged_attention_multi(void* out, const void* q, pkv_dtype q_dtype
  *                           up to its token: max_q * Hq / Hkv <= 32, Hq / Hkv
  *                           a power of two up to 16, and an instance for the
  *                           cache (bf16: head_dim 128 with blocks of 8, 16 or
- *                           32, head_dim 64 with 16; fp8-e4m3: blocks of 16)
+ *                           32, head_dim 64 with 16; fp8-e4m3: blocks of 16);
+ *                           with its merge grid, two launches
  *   PKV_MULTI_MMA_SYNC      16-row tiles on mma.sync (every other call)
  *   PKV_MULTI_NONE          the shape is invalid (num_seqs < 0, max_q <= 0, a
  *                           bad cache descriptor, Hq not a multiple of Hkv)
@@ -394,7 +402,9 @@ pkv_multi_kernel pkv_multi_kernel_for(int32_t num_seqs, int32_t max_q, int32_t n
  * programmatic dependent of the cache-write grid: it reads lengths, block
  * tables and q while the cache write runs, and waits for the write to finish
  * before it reads any K/V.  So q, out, block_tables and seq_lens must not be
- * produced by the cache write, which is always the case here.
+ * produced by the cache write, which is always the case here.  (The merge
+ * grid of a balanced split on the tensor cores follows the decode grid as
+ * in pkv_paged_attention_decode.)
  *
  * Arguments: those of pkv_kv_reshape_and_cache (k, v, src_dtype,
  * num_new_tokens, slot_mapping, caches, kv_scale) and of
