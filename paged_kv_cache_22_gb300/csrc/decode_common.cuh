@@ -409,15 +409,32 @@ __device__ __forceinline__ int draw_ticket(const DecodeArgs& a, const CutPiece& 
 }
 
 // The output rows of a merged segment: lanes < D / 4 write dims 4 * lane ..
-// 4 * lane + 3 of every row, num / den scaled by out_scale.
-template <class QT, int G, int D>
-__device__ __forceinline__ void write_merged(const DecodeArgs& a, const CutPiece& cp, int lane, const float (&den)[G],
-                                             const float (&num)[G][4]) {
+// 4 * lane + 3 of every row, num / den scaled by out_scale: rows h0 .. h0 +
+// GW - 1 of the segment's G rows (held as den[hh], num[hh] for row h0 + hh).
+template <class QT>
+__device__ __forceinline__ void store4(QT* p, float x0, float x1, float x2, float x3);
+template <>
+__device__ __forceinline__ void store4<float>(float* p, float x0, float x1, float x2, float x3) {
+  *reinterpret_cast<float4*>(p) = make_float4(x0, x1, x2, x3);
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, float x0, float x1, float x2, float x3) {
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(x0, x1), hi = __floats2bfloat162_rn(x2, x3);
+  uint2 v;
+  v.x = *reinterpret_cast<const uint32_t*>(&lo);
+  v.y = *reinterpret_cast<const uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(p) = v;
+}
+
+template <class QT, int G, int D, int GW = G>
+__device__ __forceinline__ void write_merged(const DecodeArgs& a, const CutPiece& cp, int lane, const float (&den)[GW],
+                                             const float (&num)[GW][4], int h0 = 0) {
   constexpr int DV = 4, SL = D / DV;
   const int d0 = (lane % SL) * DV;
   const int kvh = cp.unit / a.units_per_kv, chunk = cp.unit % a.units_per_kv;
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
+  for (int hh = 0; hh < GW; ++hh) {
+    const int h = h0 + hh;
     QT* out;
     if (a.q_start) {  // multi-query: row h is (token chunk * tpu + h / group, head h % group)
       const int tok = chunk * a.mq_tpu + h / a.group;
@@ -427,9 +444,8 @@ __device__ __forceinline__ void write_merged(const DecodeArgs& a, const CutPiece
       out = reinterpret_cast<QT*>(a.out) + ((size_t)cp.s * a.num_q_heads + kvh * a.group + chunk * G + h) * D;
     }
     if (lane < SL) {
-      const float inv = den[h] > 0.f ? a.out_scale / den[h] : 0.f;
-#pragma unroll
-      for (int d = 0; d < DV; ++d) out[d0 + d] = from_f32<QT>(num[h][d] * inv);
+      const float inv = den[hh] > 0.f ? a.out_scale / den[hh] : 0.f;
+      store4<QT>(out + d0, num[hh][0] * inv, num[hh][1] * inv, num[hh][2] * inv, num[hh][3] * inv);
     }
   }
 }
@@ -509,6 +525,79 @@ __device__ __forceinline__ bool merge_segment_staged(const DecodeArgs& a, const 
     }
   }
   write_merged<QT, G, D>(a, cp, lane, den, num);
+  return true;
+}
+
+// A warp's share of a merge split over G / GW warps: rows h0 .. h0 + GW - 1
+// of segment `cp`.  Per piece, three bulk copies land the rows' accumulators
+// (GW x D floats) and their maxima and sums (GW floats each; GW a multiple of
+// 4 keeps every copy a multiple of 16 bytes, 16-byte aligned) in this warp's
+// buffer of `cap` pieces, completing on its own barrier `bar`; rows are
+// combined online as in merge_segment_staged.  The warps of a merge share
+// nothing.  False when a copy did not land in time (nothing is written).
+template <class QT, int G, int D, int GW>
+__device__ __forceinline__ bool merge_rows_staged(const DecodeArgs& a, const CutPiece& cp, int64_t T, int64_t NW,
+                                                  int lane, float* buf, int cap, uint64_t* bar, int h0) {
+  static_assert(GW % 4 == 0 && G % GW == 0, "row share");
+  constexpr int SLOT = partial_slot_floats(G, D), DV = 4, SL = D / DV, PIECE = GW * D + 2 * GW;
+  const int d0 = (lane % SL) * DV;
+  const int64_t w_first = owner_of(cp.seg_u, T, NW), w_last = owner_of(cp.seg_u + cp.nb - 1, T, NW);
+  const int64_t n = w_last - w_first + 1;
+  const int64_t first_slot = (cp.seg_u != range_start(w_first, T, NW)) ? 2 * w_first + 1 : 2 * w_first;
+  auto slot_of = [&](int64_t i) -> const float* {
+    return a.partials + (size_t)(i == 0 ? first_slot : 2 * (w_first + i)) * SLOT;
+  };
+  float M[GW], den[GW], num[GW][DV];
+#pragma unroll
+  for (int hh = 0; hh < GW; ++hh) {
+    M[hh] = -CUDART_INF_F;
+    den[hh] = 0.f;
+#pragma unroll
+    for (int d = 0; d < DV; ++d) num[hh][d] = 0.f;
+  }
+  uint32_t phase = 0;
+  for (int64_t i0 = 0; i0 < n; i0 += cap) {
+    const int cnt = (int)(n - i0 < cap ? n - i0 : cap);
+    // the slots were written by plain stores of the decode grid; the copies
+    // read them through the async proxy
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    fence_proxy_async_smem();  // earlier reads of the buffer before the copies overwrite it
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar, (uint32_t)(cnt * PIECE * sizeof(float)));
+      for (int i = 0; i < cnt; ++i) {
+        const float* src = slot_of(i0 + i);
+        float* dst = buf + (size_t)i * PIECE;
+        bulk_g2s(dst, src + h0 * D, GW * D * sizeof(float), bar);
+        bulk_g2s(dst + GW * D, src + G * D + h0, GW * sizeof(float), bar);
+        bulk_g2s(dst + GW * D + GW, src + G * D + G + h0, GW * sizeof(float), bar);
+      }
+    }
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar, phase & 1, a.err));
+    ++phase;
+    if (!ok) {
+      mbar_wait_bounded(bar, (phase - 1) & 1, a.err);  // leave no copy in flight
+      return false;
+    }
+    for (int i = 0; i < cnt; ++i) {
+      const float* pp = buf + (size_t)i * PIECE;
+#pragma unroll
+      for (int hh = 0; hh < GW; ++hh) {
+        const float m = pp[GW * D + hh];
+        const float Mn = fmaxf(M[hh], m);
+        if (Mn == -CUDART_INF_F) continue;  // nothing kept in this row yet
+        const float f_old = fast_exp2(M[hh] - Mn), f_new = fast_exp2(m - Mn);
+        const float4 acc = *reinterpret_cast<const float4*>(pp + hh * D + d0);
+        den[hh] = fmaf(den[hh], f_old, f_new * pp[GW * D + GW + hh]);
+        num[hh][0] = fmaf(num[hh][0], f_old, f_new * acc.x);
+        num[hh][1] = fmaf(num[hh][1], f_old, f_new * acc.y);
+        num[hh][2] = fmaf(num[hh][2], f_old, f_new * acc.z);
+        num[hh][3] = fmaf(num[hh][3], f_old, f_new * acc.w);
+        M[hh] = Mn;
+      }
+    }
+  }
+  write_merged<QT, G, D, GW>(a, cp, lane, den, num, h0);
   return true;
 }
 

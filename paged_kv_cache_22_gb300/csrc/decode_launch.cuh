@@ -20,6 +20,7 @@ struct DecodeKernel {
   // (DecodeArgs, int64_t warps of the decode grid), one-warp CTAs), if any
   const void* merge_fn = nullptr;
   size_t merge_smem = 0;
+  int merge_threads = 0;
 };
 
 // TC: the q.K and P.V contractions on the tensor cores (decode_tc.cuh, bf16
@@ -35,9 +36,10 @@ DecodeKernel decode_kernel_info() {
     k.smem = TcSmem<CT, D, BS, G, kDecodeWarps, REMAP>::kBytes;
     k.tensor_maps = true;
     if constexpr (BAL) {
-      constexpr int kMergeSlots = 8;  // partial slots staged per round of a merge
+      constexpr int kMergeSlots = 8;  // pieces staged per round of a merge (per warp)
       k.merge_fn = reinterpret_cast<const void*>(&merge_cut_kernel<__nv_bfloat16, G, D, BS, kMergeSlots>);
-      k.merge_smem = (size_t)kMergeSlots * partial_slot_floats(G, D) * sizeof(float) + 8;
+      k.merge_smem = MergeGeo<G, D, kMergeSlots>::kSmem;
+      k.merge_threads = 32 * MergeGeo<G, D, kMergeSlots>::kWarps;
     }
   } else {
     k.fn = reinterpret_cast<const void*>(&decode_kernel<CT, D, BS, G, kDecodeWarps, BAL, REMAP>);
@@ -59,9 +61,10 @@ DecodeKernel decode_mq_kernel_info() {
   k.tensor_maps = true;
   k.threads = kDecodeWarps * 32;
   k.heads_per_unit = kMqRows;
-  constexpr int kMergeSlots = 4;  // partial slots staged per round of a merge
+  constexpr int kMergeSlots = 4;  // pieces staged per round of a merge (per warp)
   k.merge_fn = reinterpret_cast<const void*>(&merge_cut_kernel<__nv_bfloat16, kMqRows, D, BS, kMergeSlots>);
-  k.merge_smem = (size_t)kMergeSlots * partial_slot_floats(kMqRows, D) * sizeof(float) + 8;
+  k.merge_smem = MergeGeo<kMqRows, D, kMergeSlots>::kSmem;
+  k.merge_threads = 32 * MergeGeo<kMqRows, D, kMergeSlots>::kWarps;
   return k;
 }
 // bf16 caches: head_dim 128 with blocks of 8, 16, 32, head_dim 64 with 16;

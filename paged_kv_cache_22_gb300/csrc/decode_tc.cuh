@@ -899,12 +899,27 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
 // such warp.  The planning runs while the decode grid is still streaming;
 // the merge waits for that grid (programmatic dependent launch).
 // ----------------------------------------------------------------------------
+// Geometry of a merge: segments of 8 or more rows are merged by G / 4 warps,
+// four rows each (a 16-row merge by one warp spent 4-9 us combining and
+// writing its rows one after the other); smaller ones by one warp.  Each
+// warp stages MC pieces of its rows.
+template <int G, int D, int MC>
+struct MergeGeo {
+  static constexpr int kWarps = G >= 8 ? G / 4 : 1;
+  static constexpr int kRows = G / kWarps;  // rows per warp
+  static constexpr int kPiece = kWarps > 1 ? kRows * D + 2 * kRows : partial_slot_floats(G, D);  // floats
+  static constexpr size_t kSmem = (size_t)kWarps * MC * kPiece * sizeof(float) + (size_t)kWarps * 8;
+};
+
 template <class QT, int G, int D, int BS, int MC>
-__global__ void __launch_bounds__(32) merge_cut_kernel(const __grid_constant__ DecodeArgs a, int64_t NW) {
+__global__ void __launch_bounds__(32 * MergeGeo<G, D, MC>::kWarps)
+    merge_cut_kernel(const __grid_constant__ DecodeArgs a, int64_t NW) {
+  using MG = MergeGeo<G, D, MC>;
   extern __shared__ __align__(16) uint8_t merge_smem[];
-  const int lane = threadIdx.x;
+  const int lane = threadIdx.x & 31, mw = threadIdx.x >> 5;
   const int64_t gw = blockIdx.x;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(merge_smem + (size_t)MC * partial_slot_floats(G, D) * sizeof(float));
+  float* buf = reinterpret_cast<float*>(merge_smem) + (size_t)mw * MC * MG::kPiece;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(merge_smem + (size_t)MG::kWarps * MC * MG::kPiece * sizeof(float)) + mw;
   int64_t u0 = 0, u1 = 0, T = 0;
   Walker wk0;
   const bool mine = plan_warp<QT, D, BS, true, false>(a, gw, NW, lane, wk0, u0, u1, T) && wk0.jb > 0 &&
@@ -918,11 +933,16 @@ __global__ void __launch_bounds__(32) merge_cut_kernel(const __grid_constant__ D
   }
   __syncwarp();
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  MergeStage ms;
-  ms.buf = reinterpret_cast<float*>(merge_smem);
-  ms.cap = MC;
-  ms.bar = bar;
-  merge_segment_staged<QT, G, D>(a, cut_piece_of(wk0, mr.q0, mr.T), T, NW, lane, ms);
+  if constexpr (MG::kWarps > 1) {
+    merge_rows_staged<QT, G, D, MG::kRows>(a, cut_piece_of(wk0, mr.q0, mr.T), T, NW, lane, buf, MC, bar,
+                                           mw * MG::kRows);
+  } else {
+    MergeStage ms;
+    ms.buf = buf;
+    ms.cap = MC;
+    ms.bar = bar;
+    merge_segment_staged<QT, G, D>(a, cut_piece_of(wk0, mr.q0, mr.T), T, NW, lane, ms);
+  }
 }
 
 }  // namespace pkv

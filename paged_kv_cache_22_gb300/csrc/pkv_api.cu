@@ -477,7 +477,7 @@ pkv_status decode_impl(void* out, const void* q, pkv_dtype q_dtype, int32_t num_
     const size_t region = counter_region(num_seqs, a.units);
     DecodeKernel merge;
     merge.fn = k.merge_fn;
-    merge.threads = 32;
+    merge.threads = k.merge_threads;
     merge.smem = k.merge_smem;
     if (kDeferDecodeMerges && merge.fn) {
       // segments cut between warps are merged by a dependent grid once the
@@ -929,7 +929,7 @@ pkv_status pkv_paged_attention_multi(void* out, const void* q, pkv_dtype q_dtype
     if (!err || sms <= 0 || occ <= 0) return PKV_ERR_CUDA;
     DecodeKernel merge;
     merge.fn = mk.merge_fn;
-    merge.threads = 32;
+    merge.threads = mk.merge_threads;
     merge.smem = mk.merge_smem;
     if (!merge.fn || prepare_kernel(merge, dev) <= 0) return PKV_ERR_CUDA;
     DecodeArgs a{};
