@@ -57,11 +57,12 @@ CASES = [
     # fewer than 128 rows per (sequence, kv head), blocks of 32: only the
     # tcgen05 kernel has an fp8 instance, so it serves the call
     ("fp8_bs32_small", [70, 33, 5], [3, 9, 5], 32, 8, 128, 32, "fp8_e4m3"),
-    # at most 32 rows per (sequence, kv head) and g a power of two up to 8:
-    # the balanced decode kernel in its multi-query form (8 rows per unit,
-    # 8 / g tokens), including token counts that leave a unit part empty,
-    # long sequences whose segments are cut between warps, and g = 3 (the
-    # mma.sync multi-token kernel)
+    # at most 32 rows per (sequence, kv head) and g a power of two up to 16:
+    # the balanced decode kernel in its multi-query form (16 rows per unit,
+    # 16 / g tokens), including token counts that leave a unit part empty,
+    # two units per kv head, long sequences whose segments are cut between
+    # warps (merged by four warps of four rows), and g = 3 (the mma.sync
+    # multi-token kernel)
     ("mq_g8_t3", [1500, 40, 700], [3, 1, 2], 64, 8, 128, 16, "bf16"),
     ("mq_g2_t5", [900, 33, 2100], [5, 2, 5], 16, 8, 128, 16, "bf16"),
     ("mq_g1_t4_bs8", [300, 1200], [4, 3], 8, 8, 128, 8, "bf16"),
@@ -69,6 +70,9 @@ CASES = [
     ("mq_fp8_d64", [300, 1000], [4, 2], 32, 8, 64, 16, "fp8_e4m3"),
     ("mq_long_cut", [9000, 7000, 3], [4, 4, 3], 32, 8, 128, 16, "bf16"),
     ("mq_bs32", [100, 900], [4, 4], 32, 8, 128, 32, "bf16"),
+    ("mq_g16_t2", [800, 2000, 5], [2, 2, 1], 32, 2, 128, 16, "bf16"),
+    ("mq_fp8_d128", [1200, 300, 60], [4, 3, 4], 32, 8, 128, 16, "fp8_e4m3"),
+    ("mq_g4_t8", [3000, 700, 9], [8, 5, 8], 32, 8, 128, 16, "bf16"),
     ("g3_small", [200, 70], [4, 3], 24, 8, 128, 16, "bf16"),
 ]
 
@@ -94,6 +98,8 @@ def test_multi_matches_oracle(pkv, case, kernel):
             run_multi(pkv, w, kc, vc, q, q_start)
         return
     with pkv.tcgen05(kernel == "tcgen05"):
+        if name.startswith("mq_"):  # the case exercises the multi-query decode
+            assert pkv.multi_kernel_for(w.num_seqs, max(q_lens), Hq, Hkv, d, bs, dt) == "multi_query_decode"
         got = run_multi(pkv, w, kc, vc, q, q_start)
         assert_close(got, ref, TOL[dt], name)
         # a larger bound on the rows per sequence changes the grid, not the result
