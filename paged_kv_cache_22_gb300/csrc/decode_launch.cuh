@@ -17,7 +17,8 @@ struct DecodeKernel {
   int heads_per_unit = 0;    // G
   bool tensor_maps = false;  // reads the caches through the TmaMaps parameter
   // the deferred-merge grid that follows it (merge_cut_kernel: parameters
-  // (DecodeArgs, int64_t warps of the decode grid), one-warp CTAs), if any
+  // (DecodeArgs, int64_t warps of the decode grid), one CTA of merge_threads
+  // threads per decode warp), if any
   const void* merge_fn = nullptr;
   size_t merge_smem = 0;
   int merge_threads = 0;

@@ -890,14 +890,14 @@ __global__ void __launch_bounds__(W * 32, 8 / W)
 }
 
 // ----------------------------------------------------------------------------
-// Deferred merges.  Warp gw of this grid (one-warp CTAs) replays the plan of
-// warp gw of a balanced decode grid of NW warps that ran with defer_merge:
-// when that warp's range starts inside a segment begun by earlier warps and
-// the segment ends within the range, the warp held the segment's last piece,
-// and this warp merges the segment's pieces (accumulators, maxima and sums
-// from their partial slots) into its output rows.  Each cut segment has one
-// such warp.  The planning runs while the decode grid is still streaming;
-// the merge waits for that grid (programmatic dependent launch).
+// Deferred merges.  CTA gw of this grid replays the plan of warp gw of a
+// balanced decode grid of NW warps that ran with defer_merge: when that
+// warp's range starts inside a segment begun by earlier warps and the
+// segment ends within the range, the warp held the segment's last piece, and
+// this CTA merges the segment's pieces (accumulators, maxima and sums from
+// their partial slots) into its output rows.  Each cut segment has one such
+// CTA.  The planning runs while the decode grid is still streaming; the
+// merge waits for that grid (programmatic dependent launch).
 // ----------------------------------------------------------------------------
 // Geometry of a merge: segments of 8 or more rows are merged by G / 4 warps,
 // four rows each (a 16-row merge by one warp spent 4-9 us combining and
