@@ -51,8 +51,8 @@ L2_FLUSH_BYTES = 256 << 20
 
 # DRAM traffic of one decode launch on the default workload, from an ncu
 # capture, valid only for the kernel sources it was taken on.
-TRAFFIC = {"sources_sha256": "17268f9bf67389d91e1331af9fb9d05c3e26d67d8cdf4dcd236d408f9b90e956",
-           "bytes_per_launch": 319060736}  # mean of two launches: 316.92 MB read + 2.14 MB written
+TRAFFIC = {"sources_sha256": "e2e92ca10a5eb5dedb6e155ad5f693c7c174ec151d02ce146ba8100d34690ea3",
+           "bytes_per_launch": 319391744}  # mean of two launches: 316.93 MB read + 2.47 MB written
 
 WORKLOAD_TEXT = {
     "llama3_8b": "Llama-3-8B-shaped decode layer: 64 seqs, L~U[128,2048], 32 q / 8 kv heads, "
