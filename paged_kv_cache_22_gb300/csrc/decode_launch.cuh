@@ -37,7 +37,11 @@ DecodeKernel decode_kernel_info() {
     k.smem = TcSmem<CT, D, BS, G, kDecodeWarps, REMAP>::kBytes;
     k.tensor_maps = true;
     if constexpr (BAL) {
-      constexpr int kMergeSlots = 8;  // pieces staged per round of a merge (per warp)
+      // pieces staged per round of a merge (per warp): 16 for one-warp merges
+      // (long segments, ~66 pieces on 32k-token sequences, need fewer round
+      // trips: +0.6 to +1.8 % on long_split_kv and its window; 32 slots cost
+      // the Llama-3-8B decode 5 %: fewer merge CTAs resident), 8 otherwise
+      constexpr int kMergeSlots = MergeGeo<G, D, 1>::kWarps > 1 ? 8 : 16;
       k.merge_fn = reinterpret_cast<const void*>(&merge_cut_kernel<__nv_bfloat16, G, D, BS, kMergeSlots>);
       k.merge_smem = MergeGeo<G, D, kMergeSlots>::kSmem;
       k.merge_threads = 32 * MergeGeo<G, D, kMergeSlots>::kWarps;
