@@ -214,6 +214,9 @@ def test_multi_kernel_choice_without_a_device(lib):
     assert k(4, 32, dt="fp8_e4m3") == "multi_query_decode"
     assert k(4, 32, dt="fp8_e4m3", bs=32) == "tcgen05"  # no mma.sync fp8 instance for 32-token blocks
     assert k(512, 32) == "tcgen05"
+    assert k(512, 32, d=64, dt="fp8_e4m3") == "mma_sync"  # tcgen05 on fp8 caches: head_dim 128 only
+    assert k(512, 32, d=64) == "tcgen05"
+    assert k(4, 32, seqs=0) == "multi_query_decode"  # an empty batch is valid (nothing is launched)
     with pkv.tcgen05(False):
         assert k(512, 32) == "mma_sync"
         assert k(4, 32, dt="fp8_e4m3", bs=32) is None
